@@ -1,0 +1,408 @@
+#!/usr/bin/env python
+"""Benchmark of the quantized MoE decode layer step on GB300.
+
+Metric: decode tokens/s per MoE layer step (one token through one layer),
+and the expert GEMVs' HBM GB/s against the measured peak.
+
+Default workload (one GPU): the single-token decode layer -- dim 4096, inter
+2048, 384 routed experts (Q2_K gate/up, Q3_K down, all resident in one HBM
+arena), top 6, bf16 router and bf16 shared expert -- stacked as 8 independent
+layers captured in one CUDA graph. A step is one replay: one token through the
+8 layers (865 MB of distinct weights, far above the 129 MB L2, so nothing is
+served from L2 between steps). value = token-layer steps per second over all
+ranks.
+
+Other workloads (--workload): batch8 (the same layers at m = 8 tokens),
+chain40 (40 stacked layers, one token, one replay = one 40-layer decode step;
+tokens/s).
+
+--impl reference times the CPU oracle (oracle/, plain C, f64) on the same
+workload and metric: each step one token through one layer, on the host cores.
+
+Multi-GPU: replicas only (the decode step does not shard here); under
+torchrun every rank runs its own replica, the time is the max over ranks and
+value = all ranks' units / that time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOADS = {
+    # name: (m, layers per step, metric, unit)
+    "decode": (1, 8, "decode tokens/s per MoE layer step (1 GB300)", "token-layer steps/s"),
+    "batch8": (8, 8, "decode tokens/s per MoE layer step (1 GB300), m=8", "token-layer steps/s"),
+    "chain40": (1, 40, "decode tokens/s, 40-layer MoE decode step (1 GB300)", "tokens/s"),
+}
+
+
+def decode_cfg(m, n_routed=384):
+    import moe_decode_quantized_gb300 as moe
+    return moe.Config(dim=4096, inter=2048, n_routed=n_routed, topk=6, norm_topk_prob=True, max_tokens=m,
+                      gate_temp=1.0, route_scale=2.5, swiglu_limit=7.0)
+
+
+# ------------------------------------------------------------------ distributed helpers
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def aggregate(units: float, seconds: float, world: int):
+    """(total units over ranks, max seconds over ranks) -- replicas: no data-path collective."""
+    if world <= 1:
+        return units, seconds
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    s = torch.tensor([seconds], dtype=torch.float64, device=dev)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    dist.all_reduce(s, op=dist.ReduceOp.MAX)
+    return float(u.item()), float(s.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, throttle reasons) while the GPU works."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.lines = []
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        out, _ = self.p.communicate(timeout=10)
+        rows = []
+        for line in out.splitlines():
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                rows.append((float(f[0]), float(f[1]), f[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        smax = max(r[1] for r in rows)
+        busy = [r for r in rows if r[0] >= 0.5 * smax] or rows
+        sm = sorted(r[0] for r in busy)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in busy for i, v in enumerate(r[2]) if v.lower().startswith("active")})
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": smax, "reasons": reasons, "samples": len(busy)}
+
+
+# ------------------------------------------------------------------ bytes (algorithmic)
+
+def algorithmic_bytes(cfg, m, ne):
+    """Bytes one layer step must move, per kernel (router, gate/up, down)."""
+    dim, inter, n, k = cfg.dim, cfg.inter, cfg.n_routed, cfg.topk
+    q2 = inter * (dim // 256) * 84
+    q3 = dim * (inter // 256) * 110
+    router = n * dim * 2 + m * dim * 2 + m * n * 4
+    gateup = 2 * ne * q2 + 2 * inter * dim * 2 + m * dim * 2 + 2 * m * k * inter * 4 + 2 * m * inter * 4
+    down = ne * q3 + dim * inter * 2 + 2 * m * k * inter * 4 + 2 * m * inter * 4 + m * k * dim * 4 \
+        + m * dim * (4 + 4 + 4 + 4 + 2)
+    return router, gateup, down
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "moe_decode_quantized_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")) and f != "moe_synth.cu":
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic():
+    """Per-launch DRAM bytes of the gate/up kernel from the committed ncu summary,
+    or None when the kernels changed since it was taken."""
+    try:
+        t = json.load(open(TRAFFIC))
+    except (OSError, ValueError):
+        return None
+    return t.get("gateup_dram_bytes_per_launch") if t.get("kernel_hash") == kernel_hash() else None
+
+
+def hbm_peak():
+    try:
+        return float(json.load(open(PEAKS))["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ CPU oracle (baseline leg)
+
+def oracle_sample(cfg, m, budget_s, seed=1000, max_steps=10 ** 9, warmup=0):
+    """The oracle as it stands, on host cores: one layer step per iteration over
+    the same synthetic decode layer. Returns (steps, seconds, threads, sample text)."""
+    import numpy as np
+    import oracle
+    from moe_decode_quantized_gb300 import synth
+
+    threads = os.cpu_count() or 1
+    shp = synth.LayerShape(cfg.dim, cfg.inter, cfg.n_routed)
+    oc = oracle.cfg(cfg.dim, cfg.inter, cfg.n_routed, cfg.topk, cfg.norm_topk_prob, cfg.gate_temp,
+                    cfg.route_scale, cfg.swiglu_limit)
+    router = synth.router_bf16(seed, 0, cfg.n_routed, cfg.dim)
+    bias = synth.bias_f32(seed, 0, cfg.n_routed)
+    shared = synth.shared_bf16(seed, 0, cfg.dim, cfg.inter)
+    cache = {}
+    done, spent, i = 0, 0.0, 0
+    while done < max_steps and (spent < budget_s or done == 0):
+        x = synth.x_bf16(seed, i, m, cfg.dim)
+        picks, _, _, _ = oracle.route(oc, oracle.router_logits(x, router), bias)
+        experts = {}
+        for e in np.unique(picks):
+            e = int(e)
+            if e not in cache:
+                if len(cache) > 64:
+                    cache.pop(next(iter(cache)))
+                cache[e] = synth.expert_bytes(seed, 0, e, shp)
+            experts[e] = cache[e]
+        t0 = time.perf_counter()
+        oracle.layer(oc, x, router, bias, experts, (shp.gate_off, shp.up_off, shp.down_off), shared,
+                     threads=threads)
+        dt = time.perf_counter() - t0
+        i += 1
+        if i <= warmup:
+            continue
+        spent += dt
+        done += 1
+    sample = (f"{done} layer steps of the {m}-token decode layer (dim {cfg.dim}, inter {cfg.inter}, "
+              f"{cfg.n_routed}x{cfg.topk}, shared expert), oracle.layer timed, {threads} threads")
+    return done, spent, threads, sample
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    from moe_decode_quantized_gb300 import build as mbuild
+    mbuild.build()
+    import moe_decode_quantized_gb300 as moe
+    from moe_decode_quantized_gb300.workload import Workload, x_tensor
+
+    m, L, metric, unit = WORKLOADS[args.workload]
+    if args.layers:
+        L = args.layers
+    cfg = decode_cfg(m, args.experts)
+    wl = Workload(cfg, n_layers=L, seed=rank, shared=True)
+    layers = [wl.layer(l) for l in range(L)]
+    x_a = x_tensor(rank, 0, m, cfg.dim)
+    x_b = torch.empty_like(x_a)
+    residual = torch.zeros((m, cfg.dim), dtype=torch.float32, device="cuda")
+    hw = moe.header_words(cfg, m)
+    headers = torch.zeros(L * hw, dtype=torch.int32, device="cuda")
+    graph = moe.Graph(cfg, layers, wl.arena, m, x_a, x_b, residual, headers, wl.ws)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        graph.launch()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.soak:  # clocks settle under load
+        for _ in range(50):
+            graph.launch()
+        torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        graph.launch()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    status = moe.read_status(wl.ws)
+    if status:
+        raise RuntimeError(f"workspace status {status:#x} after the timed region")
+    # decode / batch8: token-layer steps; chain40: tokens through the whole stack
+    units_local = float(args.steps * m * (1 if args.workload == "chain40" else L))
+    units, secs = aggregate(units_local, ms / 1e3, world)
+    value = units / secs
+
+    # distinct experts per layer step (for the algorithmic bytes): from the headers
+    h = headers.cpu().numpy()
+    po = m * (1 + 3 * cfg.topk)
+    ne_list = [int(h[l * hw + po]) for l in range(L)]
+    ne = float(np.mean(ne_list))
+
+    # e2e: the same replays through the host-buffer C-ABI call (pinned buffers,
+    # H2D of the token's x and residual, D2H of x, residual and the headers)
+    xh = x_a.cpu().pin_memory()
+    rh = residual.cpu().pin_memory()
+    hh = torch.zeros(L * hw, dtype=torch.int32).pin_memory()
+    for _ in range(max(1, args.warmup)):
+        graph.launch_host(xh, rh, xh, rh, hh)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(args.steps):
+        graph.launch_host(xh, rh, xh, rh, hh)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier(world)
+    e_units, e_secs = aggregate(units_local, max(e0.elapsed_time(e1) / 1e3, wall), world)
+    h2d = xh.numel() * xh.element_size() + rh.numel() * rh.element_size()
+    d2h = h2d + hh.numel() * 4
+
+    # per-kernel durations (router+select, gate/up, down) with CUDA events on the
+    # launching stream, kernels not overlapped, layers rotating (cold L2)
+    xp = x_tensor(rank, 7, m, cfg.dim)
+    xq = torch.empty_like(xp)
+    rp = torch.zeros_like(residual)
+    hp = torch.zeros(hw, dtype=torch.int32, device="cuda")
+    reps = max(2, min(16, args.steps // L + 1))
+    kms = []
+    for r in range(reps + 1):
+        for l in range(L):
+            t = moe.layer_step_profiled(cfg, layers[l], wl.arena, xp, rp, xq, hp, m, wl.ws)
+            xp, xq = xq, xp
+            if r > 0:
+                kms.append(t)
+    kms = np.array(kms, np.float64)
+    k_ms = kms.mean(axis=0)
+    b_router, b_gateup, b_down = algorithmic_bytes(cfg, m, ne)
+    peak, peak_kind = hbm_peak()
+    achieved = b_gateup / (k_ms[1] * 1e-3) / 1e9
+    expert_gbs = (b_gateup + b_down) / ((k_ms[1] + k_ms[2]) * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        n, spent, thr, sample = oracle_sample(cfg, m, args.cpu_budget)
+        cu = n * m / spent
+        if args.workload == "chain40":
+            cu = cu / L
+        cpu = {"value": cu, "unit": unit, "cores": thr, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        layer_bytes = b_router + b_gateup + b_down
+        out = {
+            "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "q2_k/q3_k x q8_1 int8 dot (dp4a) + bf16, f32 accumulate",
+            "data": "synthetic (seeded SplitMix64: random Q2_K/Q3_K blocks, bf16 ~N(0,0.02) router and shared expert, x ~N(0,1))",
+            "config": {
+                "workload": f"{args.workload}: MoE decode layer dim 4096, inter 2048, {cfg.n_routed} routed experts top 6 "
+                            f"(Q2_K gate/up, Q3_K down), bf16 router + bf16 shared expert, m={m}",
+                "layers_per_step": L, "tokens_per_layer_step": m, "graph": "CUDA graph, PDL-chained kernels",
+                "l2": f"inputs larger than L2: {L} distinct layers, {L * layer_bytes / 1e6:.0f} MB per step",
+                "parallelism": f"replicas x{world}",
+                "distinct_experts_per_layer_step": ne,
+                "us_per_layer_step": ms * 1e3 / (args.steps * L),
+                "layer_step_algorithmic_bytes": layer_bytes,
+                "layer_step_roofline_frac_of_measured": (layer_bytes / (ms * 1e-3 / (args.steps * L)) / 1e9) / peak,
+            },
+            "roofline": {"bound": "hbm", "kernel": "moe_gateup_kernel", "achieved": achieved, "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": measured_traffic(), "algorithmic_bytes": b_gateup,
+                         "avg_launch_us": k_ms[1] * 1e3},
+            "kernels_us": {"router_select": k_ms[0] * 1e3, "gateup": k_ms[1] * 1e3, "down": k_ms[2] * 1e3},
+            "expert_gemv_gbs": expert_gbs, "expert_gemv_frac": expert_gbs / peak,
+            "e2e": {"value": e_units / e_secs, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps * L * 3,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(out))
+    graph.close()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ reference arm (the oracle)
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return  # under torchrun only rank 0 runs the CPU reference
+    m, L, metric, unit = WORKLOADS[args.workload]
+    cfg = decode_cfg(m)
+    n, spent, thr, sample = oracle_sample(cfg, m, budget_s=0.0, max_steps=args.steps,
+                                          warmup=args.warmup)
+    value = n * m / spent
+    if args.workload == "chain40":
+        value = value / (args.layers or L)
+    out = {
+        "impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": spent * 1e3 / max(1, n),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (same seeded generator as the GPU arm)",
+        "config": {"workload": f"{args.workload}: the CPU oracle, one layer step per step, m={m}",
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": thr, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out))
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
+    ap.add_argument("--layers", type=int, default=0, help="layers per step (default: the workload's)")
+    ap.add_argument("--experts", type=int, default=384, help="routed experts per layer (384; fewer only for profiling)")
+    ap.add_argument("--soak", type=float, default=1.0, help="seconds of untimed load before timing")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,270 @@
+/*
+ * moe.h -- C ABI of libmoe.so, the GB300 (sm_103a) engine for one decode step
+ * of a DeepSeek-style mixture-of-experts layer whose routed experts stay in
+ * raw Q2_K (gate, up) and Q3_K (down) blocks.
+ *
+ * Sources (web pages of the "spark_model" crate, cited by page and item):
+ *   [moe_v41]  spark_model/layers/moe_v41.rs -- module doc (the layer's math),
+ *              struct MoeV41Cfg, struct MoeV41LayerWeights, struct Kernels,
+ *              struct MoeV41 (buffers), fn shared_side, fn softplus,
+ *              fn route_from_logits, fn bf16_bytes.
+ *   [route]    spark_model/layers/moe_v41/device_route.rs -- module doc,
+ *              fn header_words, fn arena_of, fn route_select_launch,
+ *              fn slot_table_update, fn parse_header, fn route_device_m1,
+ *              fn device_route_check.
+ *   [step_seg] spark_model/layers/deepseek_v41_layer/step_seg.rs -- module
+ *              doc (the step captured as CUDA graphs over layers).
+ *
+ * Conventions for every entry point:
+ *  - Pointers named *_dev or documented "device" are device pointers; the
+ *    caller owns every buffer (the library allocates no device memory on the
+ *    hot path). Host pointers are documented as such.
+ *  - Calls only ENQUEUE work on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and return at once; nothing synchronises implicitly.
+ *    Results are valid once the stream reaches the call.
+ *  - Return 0 (MOE_OK) or a negative MOE_E* code; moe_last_error() then
+ *    returns a message for the calling thread. Argument errors are detected
+ *    on the host before anything is enqueued.
+ *  - Calls that share a workspace must be ordered on one stream.
+ *  - bf16 tensors are passed as raw 16-bit patterns (uint16_t storage).
+ *
+ * Shapes supported: dim and inter in {256, 512, 1024, 2048, 4096, 8192};
+ * 1 <= topk <= 8; topk <= n_routed <= 1024; 1 <= m <= max_tokens <= 8;
+ * m * dim <= 32768. Other shapes return MOE_EUNSUPPORTED (or MOE_EINVAL for
+ * values that are wrong for any engine, e.g. topk = 0 or a non-multiple of 256).
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *moe_stream_t; /* == cudaStream_t */
+
+#define MOE_OK 0
+#define MOE_EINVAL (-1)       /* an argument is invalid                       */
+#define MOE_EUNSUPPORTED (-2) /* valid, but outside the shapes built here     */
+#define MOE_ECUDA (-3)        /* a CUDA call failed (message has the error)   */
+#define MOE_ECAPTURE (-4)     /* graph capture or instantiation failed        */
+
+#define MOE_SLOT_TABLE_LAYERS 64 /* rows of the slot table ([route] slot table) */
+#define MOE_MAX_TOPK 8
+#define MOE_MAX_TOKENS 8
+#define MOE_MAX_ROUTED 1024
+
+/* Status bits in word 0 of each token's header row. */
+#define MOE_HDR_MISS 1      /* a pick had slot -1: its pointers use slot 0 ([route] module doc) */
+#define MOE_HDR_NONFINITE 2 /* a logit or key of the token was NaN or infinite                  */
+
+/* Bits of the workspace status word (moe_read_status). */
+#define MOE_WS_TIMEOUT 1   /* a bounded wait inside a kernel gave up           */
+#define MOE_WS_PLAN 2      /* a plan exceeded a kernel's capacity; work skipped */
+#define MOE_WS_TRIPLE 4    /* moe_slot_table_set met a triple outside the table */
+
+/* Layer configuration ([moe_v41] struct MoeV41Cfg). norm_topk_prob is 0/1. */
+typedef struct {
+    int32_t dim, inter, n_routed, topk, norm_topk_prob, max_tokens;
+    float gate_temp, route_scale, swiglu_limit;
+} moe_cfg;
+
+/* The expert arena: expert slot s holds gate (Q2_K [inter, dim]), up (Q2_K
+ * [inter, dim]) and down (Q3_K [dim, inter]) blocks at base + s * slot_bytes
+ * + {gate,up,down}_off ([route] fn arena_of). base and the three offsets
+ * must be 16-byte aligned, slot_bytes a multiple of 16. Device memory. */
+typedef struct {
+    const void *base;
+    uint64_t slot_bytes, gate_off, up_off, down_off;
+} moe_arena;
+
+/* One layer's resident weights ([moe_v41] struct MoeV41LayerWeights), all
+ * device pointers: router_w bf16 [n_routed, dim] row-major; bias f32
+ * [n_routed]; slot_row i32 [n_routed] (this layer's slot-table row, -1 = not
+ * resident); sh_w1, sh_w3 bf16 [inter, dim] and sh_w2 bf16 [dim, inter] (the
+ * shared expert; all three NULL = no shared expert). 16-byte aligned. */
+typedef struct {
+    const void *router_w;
+    const float *bias;
+    const int32_t *slot_row;
+    const void *sh_w1, *sh_w3, *sh_w2;
+} moe_layer;
+
+/* Words (int32) of the route header for m tokens. Layout, k = topk:
+ *   row t (t < m), 1 + 3k words ([route] fn header_words, module doc):
+ *     [0] status bits (MOE_HDR_*); [1..k] picks in pick order;
+ *     [k+1..2k] the weights' f32 bit patterns, pick order; [2k+1..3k] the
+ *     slots of the token's picks in ascending expert id (-1 reported as 0)
+ *   then the plan over all m tokens (distinct picked experts, ascending id):
+ *     [m(1+3k)] ne; [+1 .. +1+m*k] pair_start[0..ne] (ne+1 used);
+ *     [+2+m*k .. +1+2*m*k] plan_expert[0..ne-1]. */
+int moe_header_words(const moe_cfg *cfg, int m);
+
+/* Bytes of the device workspace for up to cfg->max_tokens tokens. */
+int moe_workspace_bytes(const moe_cfg *cfg, size_t *bytes);
+
+/* Zeroes a workspace (its counters must start at zero). Call once after
+ * allocating it, on the stream that will use it. */
+int moe_workspace_init(void *ws_dev, size_t bytes, moe_stream_t stream);
+
+/* Router logits ([moe_v41] module doc: an f32-accumulated product of the bf16
+ * input and the bf16 gate weight; struct Kernels router_gemv):
+ *   logits[t, e] = sum_j x[t, j] * w[e, j], bf16 products exact in f32, f32
+ *   accumulation in a fixed order that does not depend on m.
+ * x_dev bf16 [m, dim]; w_dev bf16 [n_routed, dim]; logits_dev f32 [m, n_routed]. */
+int moe_router_logits(const moe_cfg *cfg, const void *x_dev, const void *w_dev,
+                      float *logits_dev, int m, moe_stream_t stream);
+
+/* q8_1 quantisation of m bf16 rows ([moe_v41] module doc: the activation
+ * quantised to q8_1; struct Kernels q8_rows): per 32 values d = amax / 127
+ * (f32), q = round-half-away(x / d), stored as f16 d, f16 d * sum q, int8
+ * q[32] (36 bytes). out_dev: m * dim / 32 blocks. */
+int moe_quantize_q8_1(const moe_cfg *cfg, const void *x_dev, int m, void *out_dev,
+                      moe_stream_t stream);
+
+/* Device selection ([moe_v41] fn route_from_logits; [route] fn
+ * route_select_launch, module doc): per token, scores s = f32(sqrt(
+ * softplus(l / temp))) (softplus(x) = x for x > 20), picks = the top k of
+ * s + bias with ties to the lower id, weights = picked scores divided by
+ * (their f32 sum in pick order + 1e-20) when norm_topk_prob and k > 1, times
+ * route_scale; then the plan, the plan weights and rows (pair-major:
+ * experts ascending, tokens ascending within one), and the pointer table
+ * ptrs[0..cap) gate, [cap..2cap) up, [2cap..3cap) down with cap = m * topk,
+ * pointer = base + slot * slot_bytes + offset, slot -1 -> slot 0 and the
+ * MOE_HDR_MISS bit. Picks are bit-identical to the definition; the score is
+ * evaluated so its f32 rounding is exact (double-checked in f64).
+ * logits_dev f32 [m, n_routed]; bias_dev f32 [n_routed]; slot_row_dev i32
+ * [n_routed]; arena by value (host struct, device base); header_dev i32
+ * [moe_header_words]; plan_w_dev f32 [m*topk]; plan_rows_dev i32 [m*topk];
+ * ptrs_dev u64 [3*m*topk]. */
+int moe_route_select(const moe_cfg *cfg, const float *logits_dev, const float *bias_dev,
+                     const int32_t *slot_row_dev, const moe_arena *arena, int m,
+                     int32_t *header_dev, float *plan_w_dev, int32_t *plan_rows_dev,
+                     uint64_t *ptrs_dev, moe_stream_t stream);
+
+/* The routed experts of one call ([moe_v41] module doc: three K-quant GEMVs
+ * per expert on the raw blocks, gate and up Q2_K, down Q3_K, q8_1 activation;
+ * struct Kernels mmvq_q2k_experts / swiglu_q8 / mmvq_q3k_experts /
+ * accumulate): for every plan expert p and each of its tokens t
+ *   g, u = Q2_K(gate_p, up_p) . q8_1(x_t);  h = silu(min(g, L)) * clamp(u, -L, L)
+ *   down = Q3_K(down_p) . q8_1(h);  acc_t = sum over t's plan, ascending id,
+ *   of w * down (f32). Reads the plan from header_dev (moe_route_select).
+ * acc_dev f32 [m, dim]; ws_dev: workspace (intermediates g, u, down stay there). */
+int moe_expert_step(const moe_cfg *cfg, const void *x_dev, const uint64_t *ptrs_dev,
+                    const float *plan_w_dev, const int32_t *plan_rows_dev,
+                    const int32_t *header_dev, int m, float *acc_dev, void *ws_dev,
+                    moe_stream_t stream);
+
+/* Clamped SwiGLU and the q8_1 of its output ([moe_v41] struct Kernels
+ * swiglu_q8): h[i] = silu(min(g, L)) * clamp(u, -L, L) in f32 (L <= 0: no
+ * clamp); h_q8 as moe_quantize_q8_1. g_dev, u_dev, h_dev f32 [rows, inter];
+ * hq8_dev rows * inter / 32 blocks (h_dev may be NULL). */
+int moe_swiglu_q8(const moe_cfg *cfg, const float *g_dev, const float *u_dev, int rows,
+                  float *h_dev, void *hq8_dev, moe_stream_t stream);
+
+/* One whole MoE layer step for m tokens ([moe_v41] module doc and fn
+ * shared_side; [route] module doc): router logits, selection, routed experts,
+ * the bf16 shared expert (gs, us = W1 x, W3 x; hs = bf16(SwiGLU); sd = W2 hs),
+ * acc = routed sum (ascending id) + sd added last, residual += acc,
+ * x_next = bf16 round-to-nearest-even of residual ([moe_v41] fn bf16_bytes).
+ * Launched as three kernels chained with programmatic dependent launch.
+ * x_dev bf16 [m, dim]; residual_dev f32 [m, dim] (in/out); x_next_dev bf16
+ * [m, dim] (may equal x_dev); header_dev i32 [moe_header_words]; acc, the
+ * plan, pointers and intermediates are left in ws_dev (moe_ws_view). */
+int moe_layer_step(const moe_cfg *cfg, const moe_layer *layer, const moe_arena *arena,
+                   const void *x_dev, float *residual_dev, void *x_next_dev,
+                   int32_t *header_dev, int m, void *ws_dev, moe_stream_t stream);
+
+/* Same step with HOST buffers: copies x (bf16 [m, dim], host) and residual
+ * (f32 [m, dim], host) in, runs moe_layer_step, copies residual, x_next and
+ * the header back to host buffers, all on `stream` (pinned host memory makes
+ * the copies asynchronous). io_dev: device scratch of
+ * moe_host_io_bytes(cfg, m) bytes. */
+int moe_host_io_bytes(const moe_cfg *cfg, int m, size_t *bytes);
+int moe_layer_step_host(const moe_cfg *cfg, const moe_layer *layer, const moe_arena *arena,
+                        const void *x_host, float *residual_host, void *x_next_host,
+                        int32_t *header_host, int m, void *io_dev, void *ws_dev,
+                        moe_stream_t stream);
+
+/* Where the intermediates of the last call live inside a workspace (device
+ * pointers into ws_dev), for inspection. */
+typedef struct {
+    float *logits;      /* [m, n_routed]                                   */
+    float *plan_w;      /* [m*topk]                                        */
+    int32_t *plan_rows; /* [m*topk]                                        */
+    uint64_t *ptrs;     /* [3*m*topk]                                      */
+    float *g, *u;       /* [m*topk, inter] per plan pair                   */
+    float *gs, *us;     /* [m, inter] shared expert                        */
+    float *down;        /* [m*topk, dim] per plan pair                     */
+    float *sd;          /* [m, dim] shared expert output                   */
+    float *acc;         /* [m, dim] routed sum + shared                    */
+    uint32_t *status;   /* one word, MOE_WS_* bits                         */
+} moe_ws_view;
+int moe_workspace_view(const moe_cfg *cfg, void *ws_dev, moe_ws_view *view);
+
+/* Reads the workspace status word (MOE_WS_* bits) to a host variable; this
+ * synchronises `stream`. */
+int moe_read_status(void *ws_dev, uint32_t *status_host, moe_stream_t stream);
+
+/* Slot-table update ([route] fn slot_table_update, struct Kernels
+ * slot_table_set): for each of n (layer, expert, slot) int32 triples,
+ * table[layer * n_routed + expert] = slot. The triples are applied in
+ * parallel, so the caller must pass at most one triple per (layer, expert)
+ * (moe_dedupe_triples gives the last-write-wins set). A triple outside
+ * [0, 64) x [0, n_routed) is skipped and sets MOE_WS_TRIPLE in
+ * *status_dev (may be NULL). table_dev i32 [64, n_routed]; triples_dev i32
+ * [n, 3]. */
+int moe_slot_table_set(int32_t *table_dev, int n_routed, const int32_t *triples_dev, int n,
+                       uint32_t *status_dev, moe_stream_t stream);
+
+/* Host helper: keeps only the last triple of each (layer, expert) key, in
+ * place, preserving the order of first appearance of the kept keys; *n_out
+ * = the count kept. Host pointer. */
+int moe_dedupe_triples(int32_t *triples_host, int n, int *n_out);
+
+/* Host helper ([route] fn parse_header): token t's status word, picks and
+ * weights out of a header copied to the host. Fails (MOE_EINVAL) when a pick
+ * lies outside 0..n_routed-1. picks_host i32 [topk], weights_host f32 [topk]. */
+int moe_parse_header(const moe_cfg *cfg, const int32_t *header_host, int m, int t,
+                     int32_t *status_host, int32_t *picks_host, float *weights_host);
+
+/* A whole-step CUDA graph ([step_seg] module doc: the step captured once and
+ * replayed, one read-back of the headers per launch): n_layers layer steps
+ * chained, layer l reading x from x_a (l even) or x_b (l odd) and writing the
+ * other, except that the last layer writes x_a, so each launch continues from
+ * the previous launch's output; residual_dev carries between layers; layer
+ * l's header lands at headers_dev + l * moe_header_words(cfg, m). layers is a
+ * host array of n_layers structs (its device pointers are baked in); every
+ * buffer must outlive the graph. */
+int moe_graph_create(const moe_cfg *cfg, const moe_layer *layers, int n_layers,
+                     const moe_arena *arena, int m, void *x_a_dev, void *x_b_dev,
+                     float *residual_dev, int32_t *headers_dev, void *ws_dev, void **graph);
+int moe_graph_launch(void *graph, moe_stream_t stream);
+int moe_graph_destroy(void *graph);
+
+/* One graph launch with HOST buffers: copies x (bf16 [m, dim]) and residual
+ * (f32 [m, dim]) from host memory into the graph's x_a / residual buffers,
+ * launches the graph, and copies the output x (x_a), the residual and every
+ * layer's header back to host memory, all on `stream` (pinned host memory
+ * makes the copies asynchronous). headers_host: n_layers * moe_header_words. */
+int moe_graph_launch_host(void *graph, const void *x_host, const float *residual_host, void *x_out_host,
+                          float *residual_out_host, int32_t *headers_host, moe_stream_t stream);
+
+/* Measurement entry point: the same layer step as moe_layer_step, but the
+ * three kernels run back to back without overlap, bracketed by CUDA events on
+ * `stream`; synchronises `stream` and writes the durations in milliseconds to
+ * ms_host[0] (router + selection), ms_host[1] (gate/up GEMVs incl. the shared
+ * W1/W3 rows), ms_host[2] (down GEMVs incl. shared W2, accumulate, residual). */
+int moe_layer_step_profiled(const moe_cfg *cfg, const moe_layer *layer, const moe_arena *arena,
+                            const void *x_dev, float *residual_dev, void *x_next_dev, int32_t *header_dev,
+                            int m, void *ws_dev, moe_stream_t stream, float *ms_host);
+
+/* Last error message of the calling thread ("" if none). */
+const char *moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

@@ -1,0 +1,247 @@
+"""GB300-native engine for one decode step of a DeepSeek-style MoE layer whose
+routed experts stay in raw Q2_K / Q3_K blocks.
+
+Thin Python binding of libmoe.so (include/moe.h): every function only turns
+torch tensors into device pointers and calls the C ABI function of the same
+name; all arithmetic runs in the CUDA kernels. Tensors must live on the
+current CUDA device; work is enqueued on the current torch stream unless a
+`stream` (torch.cuda.Stream or raw handle) is given.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass
+
+import numpy as np
+
+from . import _lib
+
+MOE_HDR_MISS = 1
+MOE_HDR_NONFINITE = 2
+MOE_WS_TIMEOUT = 1
+MOE_WS_PLAN = 2
+MOE_WS_TRIPLE = 4
+SLOT_TABLE_LAYERS = 64
+
+__all__ = ["Config", "Arena", "Layer", "MoeError", "header_words", "workspace_bytes",
+           "workspace_init", "router_logits", "quantize_q8_1", "route_select", "expert_step",
+           "swiglu_q8", "layer_step", "host_io_bytes", "layer_step_host", "workspace_view",
+           "read_status", "layer_step_profiled", "slot_table_set", "dedupe_triples", "parse_header", "Graph"]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise MoeError(rc, _lib.moe().moe_last_error().decode())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if hasattr(stream, "cuda_stream"):
+        return C.c_void_p(stream.cuda_stream)
+    return C.c_void_p(int(stream))
+
+
+def _ptr(t):
+    """Device (or host) address of a tensor / array / int; None stays NULL."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return C.c_void_p(t)
+    if isinstance(t, np.ndarray):
+        return C.c_void_p(t.ctypes.data)
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return C.c_void_p(t.data_ptr())
+
+
+@dataclass
+class Config:
+    """Layer configuration (page spark_model/layers/moe_v41.rs, struct MoeV41Cfg)."""
+    dim: int
+    inter: int
+    n_routed: int
+    topk: int
+    norm_topk_prob: bool = True
+    max_tokens: int = 1
+    gate_temp: float = 1.0
+    route_scale: float = 2.5
+    swiglu_limit: float = 7.0
+
+    def c(self) -> _lib.MoeCfg:
+        return _lib.MoeCfg(self.dim, self.inter, self.n_routed, self.topk, int(bool(self.norm_topk_prob)),
+                           self.max_tokens, self.gate_temp, self.route_scale, self.swiglu_limit)
+
+
+@dataclass
+class Arena:
+    """Device expert arena (page .../moe_v41/device_route.rs, fn arena_of)."""
+    base: object
+    slot_bytes: int
+    gate_off: int
+    up_off: int
+    down_off: int
+
+    def c(self) -> _lib.MoeArena:
+        return _lib.MoeArena(_ptr(self.base), self.slot_bytes, self.gate_off, self.up_off, self.down_off)
+
+
+@dataclass
+class Layer:
+    """One layer's resident weights (page spark_model/layers/moe_v41.rs, MoeV41LayerWeights)."""
+    router_w: object
+    bias: object
+    slot_row: object
+    sh_w1: object = None
+    sh_w3: object = None
+    sh_w2: object = None
+
+    def c(self) -> _lib.MoeLayer:
+        return _lib.MoeLayer(_ptr(self.router_w), _ptr(self.bias), _ptr(self.slot_row), _ptr(self.sh_w1),
+                             _ptr(self.sh_w3), _ptr(self.sh_w2))
+
+
+def header_words(cfg: Config, m: int) -> int:
+    n = _lib.moe().moe_header_words(C.byref(cfg.c()), m)
+    if n < 0:
+        _check(n)
+    return n
+
+
+def workspace_bytes(cfg: Config) -> int:
+    b = C.c_size_t(0)
+    _check(_lib.moe().moe_workspace_bytes(C.byref(cfg.c()), C.byref(b)))
+    return b.value
+
+
+def workspace_init(ws, stream=None):
+    _check(_lib.moe().moe_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def router_logits(cfg: Config, x, w, logits, m: int, stream=None):
+    _check(_lib.moe().moe_router_logits(C.byref(cfg.c()), _ptr(x), _ptr(w), _ptr(logits), m, _stream(stream)))
+
+
+def quantize_q8_1(cfg: Config, x, m: int, out, stream=None):
+    _check(_lib.moe().moe_quantize_q8_1(C.byref(cfg.c()), _ptr(x), m, _ptr(out), _stream(stream)))
+
+
+def route_select(cfg: Config, logits, bias, slot_row, arena: Arena, m: int, header, plan_w, plan_rows, ptrs,
+                 stream=None):
+    _check(_lib.moe().moe_route_select(C.byref(cfg.c()), _ptr(logits), _ptr(bias), _ptr(slot_row),
+                                       C.byref(arena.c()), m, _ptr(header), _ptr(plan_w), _ptr(plan_rows),
+                                       _ptr(ptrs), _stream(stream)))
+
+
+def expert_step(cfg: Config, x, ptrs, plan_w, plan_rows, header, m: int, acc, ws, stream=None):
+    _check(_lib.moe().moe_expert_step(C.byref(cfg.c()), _ptr(x), _ptr(ptrs), _ptr(plan_w), _ptr(plan_rows),
+                                      _ptr(header), m, _ptr(acc), _ptr(ws), _stream(stream)))
+
+
+def swiglu_q8(cfg: Config, g, u, rows: int, h, hq8, stream=None):
+    _check(_lib.moe().moe_swiglu_q8(C.byref(cfg.c()), _ptr(g), _ptr(u), rows, _ptr(h), _ptr(hq8),
+                                    _stream(stream)))
+
+
+def layer_step(cfg: Config, layer: Layer, arena: Arena, x, residual, x_next, header, m: int, ws, stream=None):
+    _check(_lib.moe().moe_layer_step(C.byref(cfg.c()), C.byref(layer.c()), C.byref(arena.c()), _ptr(x),
+                                     _ptr(residual), _ptr(x_next), _ptr(header), m, _ptr(ws), _stream(stream)))
+
+
+def host_io_bytes(cfg: Config, m: int) -> int:
+    b = C.c_size_t(0)
+    _check(_lib.moe().moe_host_io_bytes(C.byref(cfg.c()), m, C.byref(b)))
+    return b.value
+
+
+def layer_step_host(cfg: Config, layer: Layer, arena: Arena, x_host, residual_host, x_next_host, header_host,
+                    m: int, io, ws, stream=None):
+    """Host buffers (pinned torch CPU tensors or numpy arrays) in and out."""
+    _check(_lib.moe().moe_layer_step_host(C.byref(cfg.c()), C.byref(layer.c()), C.byref(arena.c()),
+                                          _ptr(x_host), _ptr(residual_host), _ptr(x_next_host),
+                                          _ptr(header_host), m, _ptr(io), _ptr(ws), _stream(stream)))
+
+
+def layer_step_profiled(cfg: Config, layer: Layer, arena: Arena, x, residual, x_next, header, m: int, ws,
+                        stream=None):
+    """-> [ms router+select, ms gate/up, ms down] for one layer step (kernels not overlapped)."""
+    ms = np.zeros(3, np.float32)
+    _check(_lib.moe().moe_layer_step_profiled(C.byref(cfg.c()), C.byref(layer.c()), C.byref(arena.c()), _ptr(x),
+                                              _ptr(residual), _ptr(x_next), _ptr(header), m, _ptr(ws),
+                                              _stream(stream), C.c_void_p(ms.ctypes.data)))
+    return ms
+
+
+def workspace_view(cfg: Config, ws) -> dict:
+    v = _lib.MoeWsView()
+    _check(_lib.moe().moe_workspace_view(C.byref(cfg.c()), _ptr(ws), C.byref(v)))
+    return {name: getattr(v, name) for name, _ in _lib.MoeWsView._fields_}
+
+
+def read_status(ws, stream=None) -> int:
+    s = C.c_uint32(0)
+    _check(_lib.moe().moe_read_status(_ptr(ws), C.byref(s), _stream(stream)))
+    return s.value
+
+
+def slot_table_set(table, n_routed: int, triples, n: int, status=None, stream=None):
+    _check(_lib.moe().moe_slot_table_set(_ptr(table), n_routed, _ptr(triples), n, _ptr(status),
+                                         _stream(stream)))
+
+
+def dedupe_triples(triples: np.ndarray) -> np.ndarray:
+    """Last-write-wins dedupe of (layer, expert, slot) triples (host)."""
+    t = np.ascontiguousarray(triples, dtype=np.int32).reshape(-1, 3).copy()
+    n = C.c_int(0)
+    _check(_lib.moe().moe_dedupe_triples(C.c_void_p(t.ctypes.data), t.shape[0], C.byref(n)))
+    return t[:n.value].copy()
+
+
+def parse_header(cfg: Config, header_host: np.ndarray, m: int, t: int):
+    """-> (status, picks, weights) of token t from a header copied to the host."""
+    h = np.ascontiguousarray(header_host, dtype=np.int32)
+    st = np.zeros(1, np.int32)
+    picks = np.zeros(cfg.topk, np.int32)
+    w = np.zeros(cfg.topk, np.float32)
+    _check(_lib.moe().moe_parse_header(C.byref(cfg.c()), C.c_void_p(h.ctypes.data), m, t,
+                                       C.c_void_p(st.ctypes.data), C.c_void_p(picks.ctypes.data),
+                                       C.c_void_p(w.ctypes.data)))
+    return int(st[0]), picks, w
+
+
+class Graph:
+    """A captured multi-layer step (include/moe.h, moe_graph_create)."""
+
+    def __init__(self, cfg: Config, layers, arena: Arena, m: int, x_a, x_b, residual, headers, ws):
+        arr = (_lib.MoeLayer * len(layers))(*[ly.c() for ly in layers])
+        self._keep = (layers, arena, x_a, x_b, residual, headers, ws)
+        h = C.c_void_p()
+        _check(_lib.moe().moe_graph_create(C.byref(cfg.c()), C.cast(arr, C.c_void_p), len(layers),
+                                           C.byref(arena.c()), m, _ptr(x_a), _ptr(x_b), _ptr(residual),
+                                           _ptr(headers), _ptr(ws), C.byref(h)))
+        self._h = h
+
+    def launch(self, stream=None):
+        _check(_lib.moe().moe_graph_launch(self._h, _stream(stream)))
+
+    def launch_host(self, x_host, residual_host, x_out_host, residual_out_host, headers_host, stream=None):
+        _check(_lib.moe().moe_graph_launch_host(self._h, _ptr(x_host), _ptr(residual_host), _ptr(x_out_host),
+                                                _ptr(residual_out_host), _ptr(headers_host), _stream(stream)))
+
+    def close(self):
+        if self._h:
+            _lib.moe().moe_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

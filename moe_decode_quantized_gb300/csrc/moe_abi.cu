@@ -1,0 +1,784 @@
+// moe_abi.cu -- the extern "C" entry points of libmoe.so (declared and
+// documented in include/moe.h): argument checks, workspace layout, launch
+// geometry, programmatic dependent launch between the three kernels of a
+// layer step, and CUDA-graph capture of whole multi-layer steps.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "moe_common.cuh"
+
+#include "moe_route.cuh"
+#include "moe_experts.cuh"
+#include "moe_slot.cuh"
+
+using namespace moe;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+#define CUDA_OK(expr)                                                                          \
+    do {                                                                                       \
+        cudaError_t e_ = (expr);                                                               \
+        if (e_ != cudaSuccess)                                                                 \
+            return fail(MOE_ECUDA, "%s: %s (%s)", #expr, cudaGetErrorString(e_), cudaGetErrorName(e_)); \
+    } while (0)
+
+bool pow2_in(int v, int lo, int hi)
+{
+    return v >= lo && v <= hi && (v & (v - 1)) == 0;
+}
+
+int check_cfg(const moe_cfg *c)
+{
+    if (!c)
+        return fail(MOE_EINVAL, "cfg is NULL");
+    if (c->dim <= 0 || c->inter <= 0 || c->dim % MOE_QK || c->inter % MOE_QK)
+        return fail(MOE_EINVAL, "dim (%d) and inter (%d) must be positive multiples of 256", c->dim, c->inter);
+    if (c->topk < 1 || c->n_routed < c->topk)
+        return fail(MOE_EINVAL, "need 1 <= topk (%d) <= n_routed (%d)", c->topk, c->n_routed);
+    if (c->max_tokens < 1)
+        return fail(MOE_EINVAL, "max_tokens (%d) must be >= 1", c->max_tokens);
+    if (!(c->gate_temp > 0.0f))
+        return fail(MOE_EINVAL, "gate_temp must be > 0");
+    if (!pow2_in(c->dim, 256, 8192) || !pow2_in(c->inter, 256, 8192))
+        return fail(MOE_EUNSUPPORTED, "dim (%d) and inter (%d) must be powers of two in [256, 8192]",
+                    c->dim, c->inter);
+    if (c->topk > MOE_MAX_TOPK || c->n_routed > MOE_MAX_ROUTED || c->max_tokens > MOE_MAX_TOKENS)
+        return fail(MOE_EUNSUPPORTED, "topk <= %d, n_routed <= %d, max_tokens <= %d", MOE_MAX_TOPK,
+                    MOE_MAX_ROUTED, MOE_MAX_TOKENS);
+    if ((long long)c->max_tokens * c->dim > 32768)
+        return fail(MOE_EUNSUPPORTED, "max_tokens * dim must be <= 32768");
+    return MOE_OK;
+}
+
+int check_m(const moe_cfg *c, int m)
+{
+    if (m < 0 || m > c->max_tokens)
+        return fail(MOE_EINVAL, "m (%d) must be in [0, max_tokens = %d]", m, c->max_tokens);
+    return MOE_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DevInfo {
+    int sms = 0;
+    int smem_optin = 0;
+    bool attrs = false;
+};
+
+std::mutex g_mu;
+DevInfo g_dev[64];
+
+int dev_info(DevInfo **out)
+{
+    int d = 0;
+    CUDA_OK(cudaGetDevice(&d));
+    if (d < 0 || d >= 64)
+        return fail(MOE_EUNSUPPORTED, "device ordinal %d", d);
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevInfo &I = g_dev[d];
+    if (!I.attrs) {
+        CUDA_OK(cudaDeviceGetAttribute(&I.sms, cudaDevAttrMultiProcessorCount, d));
+        CUDA_OK(cudaDeviceGetAttribute(&I.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d));
+        CUDA_OK(cudaFuncSetAttribute(moe_router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
+        CUDA_OK(cudaFuncSetAttribute(moe_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
+        CUDA_OK(cudaFuncSetAttribute(moe_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
+        I.attrs = true;
+    }
+    *out = &I;
+    return MOE_OK;
+}
+
+template <typename Args>
+int launch(void (*kernel)(Args), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl, const Args &a)
+{
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = grid;
+    lc.blockDim = block;
+    lc.dynamicSmemBytes = smem;
+    lc.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = at;
+    lc.numAttrs = pdl ? 1 : 0;
+    CUDA_OK(cudaLaunchKernelEx(&lc, kernel, a));
+    return MOE_OK;
+}
+
+// ------------------------------------------------------------------ geometry
+
+struct Geo {
+    int r_rows, r_grid;
+    size_t r_smem;
+    int g_S;
+    uint32_t g_stage;
+    size_t g_smem;
+    int d_S, d_pair_cap;
+    uint32_t d_stage;
+    size_t d_smem;
+    int grid;  // persistent grid of the expert kernels
+};
+
+size_t router_smem(int rows, int dim, int m)
+{
+    size_t main = (size_t)rows * dim * 2 + (size_t)m * dim * 2 + sizeof(float) * 8 * rows * m;
+    size_t sel = sizeof(SelectSmem);
+    return 128 + (main > sel ? main : sel);
+}
+
+int stages_fit(size_t fixed, uint32_t stage, int cap, size_t limit)
+{
+    int S = cap;
+    while (S > MOE_CONSUMER_WARPS && fixed + ring_head_bytes(S) + (size_t)S * stage + 16 > limit)
+        S -= MOE_CONSUMER_WARPS;
+    return S;
+}
+
+int geometry(const moe_cfg &c, int m, bool shared, const DevInfo &I, Geo &G)
+{
+    const int n = c.n_routed, dim = c.dim, inter = c.inter, k = c.topk;
+    const size_t limit = (size_t)I.smem_optin;
+    G.r_rows = (n + I.sms - 1) / I.sms;
+    G.r_grid = (n + G.r_rows - 1) / G.r_rows;
+    G.r_smem = router_smem(G.r_rows, dim, m);
+    G.grid = I.sms;
+    // gate/up: stages of max(one Q2_K task, one bf16 row)
+    G.g_stage = (uint32_t)align_up(std::max<size_t>((size_t)MOE_G_TASK_SB * MOE_Q2K_BYTES, (size_t)dim * 2), 128);
+    size_t g_fixed = align_up((size_t)m * act_row_bytes(dim), 128) + (shared ? align_up((size_t)m * dim * 2, 128) : 0);
+    G.g_S = stages_fit(g_fixed, G.g_stage, 2 * MOE_CONSUMER_WARPS, limit);
+    G.g_smem = g_smem_bytes(G.g_S, m, dim, shared, G.g_stage);
+    // down: stages of max(one Q3_K task, one bf16 row)
+    G.d_stage = (uint32_t)align_up(std::max<size_t>((size_t)MOE_D_TASK_SB * MOE_Q3K_BYTES, (size_t)inter * 2), 128);
+    const int tpr = dim / down_rows_per_task(inter);
+    const long long tmax = (long long)m * k * tpr + (shared ? dim : 0);
+    const long long per = (tmax + G.grid - 1) / G.grid;
+    int span = (int)((per + tpr - 1) / tpr) + 1;
+    G.d_pair_cap = std::min(m * k, span * m);
+    size_t d_fixed = 512 + align_up((size_t)G.d_pair_cap * act_row_bytes(inter), 128) +
+                     (shared ? align_up((size_t)m * inter * 2, 128) : 0);
+    G.d_S = stages_fit(d_fixed, G.d_stage, 3 * MOE_CONSUMER_WARPS, limit);
+    G.d_smem = d_smem_bytes(G.d_S, G.d_pair_cap, m, inter, shared, G.d_stage);
+    if (G.r_smem > limit || G.g_smem > limit || G.d_smem > limit)
+        return fail(MOE_EUNSUPPORTED, "shared memory: router %zu, gate/up %zu, down %zu > %zu bytes", G.r_smem,
+                    G.g_smem, G.d_smem, limit);
+    return MOE_OK;
+}
+
+// ------------------------------------------------------------------ launches
+
+struct Bufs {
+    const uint16_t *x;
+    float *logits;
+    int32_t *hdr;
+    float *plan_w;
+    int32_t *plan_rows;
+    unsigned long long *ptrs;
+    float *g, *u, *gs, *us, *down, *sd, *acc;
+    uint32_t *ctrl, *rgcnt;
+};
+
+Bufs ws_bufs(const moe_cfg &c, void *ws)
+{
+    const WsLayout L = ws_layout(c);
+    char *b = static_cast<char *>(ws);
+    Bufs B{};
+    B.ctrl = reinterpret_cast<uint32_t *>(b + L.ctrl);
+    B.rgcnt = reinterpret_cast<uint32_t *>(b + L.rgcnt);
+    B.logits = reinterpret_cast<float *>(b + L.logits);
+    B.plan_w = reinterpret_cast<float *>(b + L.plan_w);
+    B.plan_rows = reinterpret_cast<int32_t *>(b + L.plan_rows);
+    B.ptrs = reinterpret_cast<unsigned long long *>(b + L.ptrs);
+    B.g = reinterpret_cast<float *>(b + L.g);
+    B.u = reinterpret_cast<float *>(b + L.u);
+    B.gs = reinterpret_cast<float *>(b + L.gs);
+    B.us = reinterpret_cast<float *>(b + L.us);
+    B.down = reinterpret_cast<float *>(b + L.down);
+    B.sd = reinterpret_cast<float *>(b + L.sd);
+    B.acc = reinterpret_cast<float *>(b + L.acc);
+    return B;
+}
+
+RouteArgs route_args(const moe_cfg &c, int m)
+{
+    RouteArgs a{};
+    a.dim = c.dim;
+    a.n = c.n_routed;
+    a.m = m;
+    a.temp = c.gate_temp;
+    a.route_scale = c.route_scale;
+    a.norm = c.norm_topk_prob != 0;
+    a.k = c.topk;
+    return a;
+}
+
+void set_arena(RouteArgs &a, const moe_arena &ar)
+{
+    a.arena_base = static_cast<const char *>(ar.base);
+    a.slot_bytes = ar.slot_bytes;
+    a.gate_off = ar.gate_off;
+    a.up_off = ar.up_off;
+    a.down_off = ar.down_off;
+}
+
+int check_arena(const moe_arena *ar)
+{
+    if (!ar || !ar->base)
+        return fail(MOE_EINVAL, "arena or arena->base is NULL");
+    if (!aligned16(ar->base) || ar->slot_bytes % 16 || ar->gate_off % 16 || ar->up_off % 16 || ar->down_off % 16)
+        return fail(MOE_EINVAL, "arena base, slot_bytes and offsets must be 16-byte aligned");
+    return MOE_OK;
+}
+
+// the two expert kernels of one call. pdl_gateup: the gate/up kernel may start
+// before its predecessor ends -- only when that predecessor is the router
+// kernel of the same step, which triggers after x is complete (the gate/up
+// prologue reads x before its own wait).
+int launch_experts(const moe_cfg &c, int m, const Geo &G, const Bufs &B, const uint16_t *x,
+                   const unsigned long long *ptrs, const float *plan_w, const int32_t *plan_rows,
+                   const int32_t *hdr, const uint16_t *w1, const uint16_t *w3, const uint16_t *w2,
+                   float *acc, float *residual, uint16_t *x_next, cudaStream_t s, bool pdl_gateup,
+                   cudaEvent_t *ev = nullptr)
+{
+    const int k = c.topk, cap = m * k;
+    GArgs ga{};
+    ga.x = x;
+    ga.w1 = w1;
+    ga.w3 = w3;
+    ga.hdr = hdr;
+    ga.ptrs = ptrs;
+    ga.plan_rows = plan_rows;
+    ga.g = B.g;
+    ga.u = B.u;
+    ga.gs = B.gs;
+    ga.us = B.us;
+    ga.status = B.ctrl + MOE_CTRL_STATUS;
+    ga.dim = c.dim;
+    ga.inter = c.inter;
+    ga.m = m;
+    ga.k = k;
+    ga.cap = cap;
+    ga.plan_off = m * (1 + 3 * k);
+    ga.S = G.g_S;
+    ga.stage_bytes = G.g_stage;
+    int rc = launch(moe_gateup_kernel, dim3(G.grid), dim3(MOE_THREADS), G.g_smem, s, pdl_gateup, ga);
+    if (rc)
+        return rc;
+    if (ev)
+        CUDA_OK(cudaEventRecord(ev[0], s));
+    DArgs da{};
+    da.hdr = hdr;
+    da.ptrs = ptrs;
+    da.plan_rows = plan_rows;
+    da.plan_w = plan_w;
+    da.g = B.g;
+    da.u = B.u;
+    da.gs = B.gs;
+    da.us = B.us;
+    da.w2 = w2;
+    da.down = B.down;
+    da.sd = B.sd;
+    da.acc = acc;
+    da.residual = residual;
+    da.x_next = x_next;
+    da.rgcnt = B.rgcnt;
+    da.status = B.ctrl + MOE_CTRL_STATUS;
+    da.limit = c.swiglu_limit;
+    da.dim = c.dim;
+    da.inter = c.inter;
+    da.m = m;
+    da.k = k;
+    da.cap = cap;
+    da.plan_off = m * (1 + 3 * k);
+    da.S = G.d_S;
+    da.pair_cap = G.d_pair_cap;
+    da.stage_bytes = G.d_stage;
+    if ((rc = launch(moe_down_kernel, dim3(G.grid), dim3(MOE_THREADS), G.d_smem, s, ev == nullptr, da)))
+        return rc;
+    if (ev)
+        CUDA_OK(cudaEventRecord(ev[1], s));
+    return MOE_OK;
+}
+
+int layer_step(const moe_cfg &c, const moe_layer &ly, const moe_arena &ar, const void *x, float *residual,
+               void *x_next, int32_t *hdr, int m, void *ws, cudaStream_t s, cudaEvent_t *ev = nullptr)
+{
+    DevInfo *I;
+    int rc = dev_info(&I);
+    if (rc)
+        return rc;
+    const bool shared = ly.sh_w1 != nullptr;
+    Geo G;
+    if ((rc = geometry(c, m, shared, *I, G)))
+        return rc;
+    const Bufs B = ws_bufs(c, ws);
+    RouteArgs ra = route_args(c, m);
+    ra.x = static_cast<const uint16_t *>(x);
+    ra.w = static_cast<const uint16_t *>(ly.router_w);
+    ra.logits = B.logits;
+    ra.rows_per_cta = G.r_rows;
+    ra.do_select = 1;
+    ra.bias = ly.bias;
+    ra.slot_row = ly.slot_row;
+    set_arena(ra, ar);
+    ra.hdr = hdr;
+    ra.plan_w = B.plan_w;
+    ra.plan_rows = B.plan_rows;
+    ra.ptrs = B.ptrs;
+    ra.ctrl = B.ctrl;
+    const bool pdl = ev == nullptr;
+    if (ev)
+        CUDA_OK(cudaEventRecord(ev[0], s));
+    if ((rc = launch(moe_router_kernel, dim3(G.r_grid), dim3(256), G.r_smem, s, pdl, ra)))
+        return rc;
+    if (ev)
+        CUDA_OK(cudaEventRecord(ev[1], s));
+    return launch_experts(c, m, G, B, static_cast<const uint16_t *>(x), B.ptrs, B.plan_w, B.plan_rows, hdr,
+                          static_cast<const uint16_t *>(ly.sh_w1), static_cast<const uint16_t *>(ly.sh_w3),
+                          static_cast<const uint16_t *>(ly.sh_w2), B.acc, residual,
+                          static_cast<uint16_t *>(x_next), s, pdl, ev ? ev + 2 : nullptr);
+}
+
+int check_layer(const moe_cfg &c, const moe_layer *ly)
+{
+    if (!ly || !ly->router_w || !ly->bias || !ly->slot_row)
+        return fail(MOE_EINVAL, "layer, router_w, bias and slot_row must be non-NULL");
+    const bool any = ly->sh_w1 || ly->sh_w3 || ly->sh_w2, all = ly->sh_w1 && ly->sh_w3 && ly->sh_w2;
+    if (any && !all)
+        return fail(MOE_EINVAL, "shared expert: sh_w1, sh_w3 and sh_w2 must be all set or all NULL");
+    if (!aligned16(ly->router_w) || (all && (!aligned16(ly->sh_w1) || !aligned16(ly->sh_w3) || !aligned16(ly->sh_w2))))
+        return fail(MOE_EINVAL, "router and shared-expert weights must be 16-byte aligned");
+    (void)c;
+    return MOE_OK;
+}
+
+struct GraphObj {
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    void *x_a = nullptr;
+    float *residual = nullptr;
+    int32_t *headers = nullptr;
+    size_t x_bytes = 0, res_bytes = 0, hdr_bytes = 0;
+};
+
+}  // namespace
+
+// ==================================================================== C ABI
+
+extern "C" {
+
+const char *moe_last_error(void) { return g_err; }
+
+int moe_header_words(const moe_cfg *cfg, int m)
+{
+    if (!cfg || m < 0 || cfg->topk < 1)
+        return fail(MOE_EINVAL, "moe_header_words: bad arguments");
+    return header_words(m, cfg->topk);
+}
+
+int moe_workspace_bytes(const moe_cfg *cfg, size_t *bytes)
+{
+    int rc = check_cfg(cfg);
+    if (rc)
+        return rc;
+    if (!bytes)
+        return fail(MOE_EINVAL, "bytes is NULL");
+    *bytes = ws_layout(*cfg).total;
+    return MOE_OK;
+}
+
+int moe_workspace_init(void *ws, size_t bytes, moe_stream_t stream)
+{
+    if (!ws)
+        return fail(MOE_EINVAL, "ws is NULL");
+    CUDA_OK(cudaMemsetAsync(ws, 0, bytes, (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+int moe_workspace_view(const moe_cfg *cfg, void *ws, moe_ws_view *v)
+{
+    int rc = check_cfg(cfg);
+    if (rc)
+        return rc;
+    if (!ws || !v)
+        return fail(MOE_EINVAL, "ws and view must be non-NULL");
+    const Bufs B = ws_bufs(*cfg, ws);
+    v->logits = B.logits;
+    v->plan_w = B.plan_w;
+    v->plan_rows = B.plan_rows;
+    v->ptrs = reinterpret_cast<uint64_t *>(B.ptrs);
+    v->g = B.g;
+    v->u = B.u;
+    v->gs = B.gs;
+    v->us = B.us;
+    v->down = B.down;
+    v->sd = B.sd;
+    v->acc = B.acc;
+    v->status = B.ctrl + MOE_CTRL_STATUS;
+    return MOE_OK;
+}
+
+int moe_read_status(void *ws, uint32_t *status, moe_stream_t stream)
+{
+    if (!ws || !status)
+        return fail(MOE_EINVAL, "ws and status must be non-NULL");
+    CUDA_OK(cudaMemcpyAsync(status, static_cast<uint32_t *>(ws) + MOE_CTRL_STATUS, 4, cudaMemcpyDeviceToHost,
+                            (cudaStream_t)stream));
+    CUDA_OK(cudaStreamSynchronize((cudaStream_t)stream));
+    return MOE_OK;
+}
+
+int moe_router_logits(const moe_cfg *cfg, const void *x, const void *w, float *logits, int m,
+                      moe_stream_t stream)
+{
+    int rc = check_cfg(cfg);
+    if (rc || (rc = check_m(cfg, m)))
+        return rc;
+    if (m == 0)
+        return MOE_OK;
+    if (!x || !w || !logits || !aligned16(x) || !aligned16(w))
+        return fail(MOE_EINVAL, "x, w (16-byte aligned) and logits must be non-NULL");
+    DevInfo *I;
+    if ((rc = dev_info(&I)))
+        return rc;
+    Geo G;
+    if ((rc = geometry(*cfg, m, false, *I, G)))
+        return rc;
+    RouteArgs a = route_args(*cfg, m);
+    a.x = static_cast<const uint16_t *>(x);
+    a.w = static_cast<const uint16_t *>(w);
+    a.logits = logits;
+    a.rows_per_cta = G.r_rows;
+    a.do_select = 0;
+    return launch(moe_router_kernel, dim3(G.r_grid), dim3(256), G.r_smem, (cudaStream_t)stream, false, a);
+}
+
+int moe_quantize_q8_1(const moe_cfg *cfg, const void *x, int m, void *out, moe_stream_t stream)
+{
+    int rc = check_cfg(cfg);
+    if (rc || (rc = check_m(cfg, m)))
+        return rc;
+    if (m == 0)
+        return MOE_OK;
+    if (!x || !out)
+        return fail(MOE_EINVAL, "x and out must be non-NULL");
+    const int nblk = m * cfg->dim / 32;
+    const int threads = 256, grid = (nblk * 32 + threads - 1) / threads;
+    moe_quantize_q8_1_kernel<<<grid, threads, 0, (cudaStream_t)stream>>>(static_cast<const uint16_t *>(x), nblk,
+                                                                         static_cast<uint8_t *>(out));
+    CUDA_OK(cudaGetLastError());
+    return MOE_OK;
+}
+
+int moe_swiglu_q8(const moe_cfg *cfg, const float *g, const float *u, int rows, float *h, void *hq8,
+                  moe_stream_t stream)
+{
+    int rc = check_cfg(cfg);
+    if (rc)
+        return rc;
+    if (rows < 0)
+        return fail(MOE_EINVAL, "rows must be >= 0");
+    if (rows == 0)
+        return MOE_OK;
+    if (!g || !u || !hq8)
+        return fail(MOE_EINVAL, "g, u and hq8 must be non-NULL");
+    const int nblk = rows * cfg->inter / 32;
+    const int threads = 256, grid = (nblk * 32 + threads - 1) / threads;
+    moe_swiglu_q8_kernel<<<grid, threads, 0, (cudaStream_t)stream>>>(g, u, nblk, cfg->swiglu_limit, h,
+                                                                     static_cast<uint8_t *>(hq8));
+    CUDA_OK(cudaGetLastError());
+    return MOE_OK;
+}
+
+int moe_route_select(const moe_cfg *cfg, const float *logits, const float *bias, const int32_t *slot_row,
+                     const moe_arena *arena, int m, int32_t *header, float *plan_w, int32_t *plan_rows,
+                     uint64_t *ptrs, moe_stream_t stream)
+{
+    int rc = check_cfg(cfg);
+    if (rc || (rc = check_m(cfg, m)) || (rc = check_arena(arena)))
+        return rc;
+    if (m == 0)
+        return MOE_OK;
+    if (!logits || !bias || !slot_row || !header || !plan_w || !plan_rows || !ptrs)
+        return fail(MOE_EINVAL, "moe_route_select: a buffer is NULL");
+    RouteArgs a = route_args(*cfg, m);
+    a.logits = const_cast<float *>(logits);
+    a.bias = bias;
+    a.slot_row = slot_row;
+    set_arena(a, *arena);
+    a.hdr = header;
+    a.plan_w = plan_w;
+    a.plan_rows = plan_rows;
+    a.ptrs = reinterpret_cast<unsigned long long *>(ptrs);
+    return launch(moe_select_kernel, dim3(1), dim3(256), 0, (cudaStream_t)stream, false, a);
+}
+
+int moe_expert_step(const moe_cfg *cfg, const void *x, const uint64_t *ptrs, const float *plan_w,
+                    const int32_t *plan_rows, const int32_t *header, int m, float *acc, void *ws,
+                    moe_stream_t stream)
+{
+    int rc = check_cfg(cfg);
+    if (rc || (rc = check_m(cfg, m)))
+        return rc;
+    if (m == 0)
+        return MOE_OK;
+    if (!x || !ptrs || !plan_w || !plan_rows || !header || !acc || !ws || !aligned16(x))
+        return fail(MOE_EINVAL, "moe_expert_step: a buffer is NULL or x is not 16-byte aligned");
+    DevInfo *I;
+    if ((rc = dev_info(&I)))
+        return rc;
+    Geo G;
+    if ((rc = geometry(*cfg, m, false, *I, G)))
+        return rc;
+    const Bufs B = ws_bufs(*cfg, ws);
+    return launch_experts(*cfg, m, G, B, static_cast<const uint16_t *>(x),
+                          reinterpret_cast<const unsigned long long *>(ptrs), plan_w, plan_rows, header, nullptr,
+                          nullptr, nullptr, acc, nullptr, nullptr, (cudaStream_t)stream, false);
+}
+
+int moe_layer_step(const moe_cfg *cfg, const moe_layer *layer, const moe_arena *arena, const void *x,
+                   float *residual, void *x_next, int32_t *header, int m, void *ws, moe_stream_t stream)
+{
+    int rc = check_cfg(cfg);
+    if (rc || (rc = check_m(cfg, m)) || (rc = check_arena(arena)) || (rc = check_layer(*cfg, layer)))
+        return rc;
+    if (m == 0)
+        return MOE_OK;
+    if (!x || !residual || !x_next || !header || !ws || !aligned16(x))
+        return fail(MOE_EINVAL, "moe_layer_step: a buffer is NULL or x is not 16-byte aligned");
+    return layer_step(*cfg, *layer, *arena, x, residual, x_next, header, m, ws, (cudaStream_t)stream);
+}
+
+int moe_host_io_bytes(const moe_cfg *cfg, int m, size_t *bytes)
+{
+    int rc = check_cfg(cfg);
+    if (rc || (rc = check_m(cfg, m)))
+        return rc;
+    if (!bytes)
+        return fail(MOE_EINVAL, "bytes is NULL");
+    const size_t xd = align_up((size_t)m * cfg->dim * 2, 256), rd = align_up((size_t)m * cfg->dim * 4, 256);
+    *bytes = 2 * xd + rd + align_up(sizeof(int32_t) * header_words(m, cfg->topk), 256);
+    return MOE_OK;
+}
+
+int moe_layer_step_host(const moe_cfg *cfg, const moe_layer *layer, const moe_arena *arena, const void *x_host,
+                        float *residual_host, void *x_next_host, int32_t *header_host, int m, void *io,
+                        void *ws, moe_stream_t stream)
+{
+    int rc = check_cfg(cfg);
+    if (rc || (rc = check_m(cfg, m)) || (rc = check_arena(arena)) || (rc = check_layer(*cfg, layer)))
+        return rc;
+    if (m == 0)
+        return MOE_OK;
+    if (!x_host || !residual_host || !x_next_host || !header_host || !io || !ws || !aligned16(io))
+        return fail(MOE_EINVAL, "moe_layer_step_host: a buffer is NULL or io is not 16-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t xb = (size_t)m * cfg->dim * 2, rb = (size_t)m * cfg->dim * 4;
+    const size_t xd = align_up(xb, 256), rd = align_up(rb, 256);
+    char *p = static_cast<char *>(io);
+    void *x_dev = p, *xn_dev = p + xd;
+    float *res_dev = reinterpret_cast<float *>(p + 2 * xd);
+    int32_t *hdr_dev = reinterpret_cast<int32_t *>(p + 2 * xd + rd);
+    const size_t hb = sizeof(int32_t) * header_words(m, cfg->topk);
+    CUDA_OK(cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, s));
+    CUDA_OK(cudaMemcpyAsync(res_dev, residual_host, rb, cudaMemcpyHostToDevice, s));
+    if ((rc = layer_step(*cfg, *layer, *arena, x_dev, res_dev, xn_dev, hdr_dev, m, ws, s)))
+        return rc;
+    CUDA_OK(cudaMemcpyAsync(residual_host, res_dev, rb, cudaMemcpyDeviceToHost, s));
+    CUDA_OK(cudaMemcpyAsync(x_next_host, xn_dev, xb, cudaMemcpyDeviceToHost, s));
+    CUDA_OK(cudaMemcpyAsync(header_host, hdr_dev, hb, cudaMemcpyDeviceToHost, s));
+    return MOE_OK;
+}
+
+int moe_slot_table_set(int32_t *table, int n_routed, const int32_t *triples, int n, uint32_t *status,
+                       moe_stream_t stream)
+{
+    if (!table || n_routed < 1 || n_routed > MOE_MAX_ROUTED || n < 0 || (n > 0 && !triples))
+        return fail(MOE_EINVAL, "moe_slot_table_set: bad arguments");
+    if (n == 0)
+        return MOE_OK;
+    moe_slot_table_kernel<<<(n + 255) / 256, 256, 0, (cudaStream_t)stream>>>(table, n_routed, triples, n, status);
+    CUDA_OK(cudaGetLastError());
+    return MOE_OK;
+}
+
+int moe_dedupe_triples(int32_t *t, int n, int *n_out)
+{
+    if (n < 0 || (n > 0 && !t) || !n_out)
+        return fail(MOE_EINVAL, "moe_dedupe_triples: bad arguments");
+    // keep the last triple of each (layer, expert); quadratic, fine for the
+    // batch sizes a cache produces between two steps
+    std::vector<int32_t> out;
+    out.reserve((size_t)n * 3);
+    for (int i = 0; i < n; ++i) {
+        bool later = false;
+        for (int j = i + 1; j < n && !later; ++j)
+            later = t[3 * j] == t[3 * i] && t[3 * j + 1] == t[3 * i + 1];
+        if (!later) {
+            out.push_back(t[3 * i]);
+            out.push_back(t[3 * i + 1]);
+            out.push_back(t[3 * i + 2]);
+        }
+    }
+    std::memcpy(t, out.data(), out.size() * sizeof(int32_t));
+    *n_out = (int)(out.size() / 3);
+    return MOE_OK;
+}
+
+int moe_parse_header(const moe_cfg *cfg, const int32_t *hdr, int m, int t, int32_t *status, int32_t *picks,
+                     float *weights)
+{
+    if (!cfg || !hdr || t < 0 || t >= m || cfg->topk < 1)
+        return fail(MOE_EINVAL, "moe_parse_header: bad arguments");
+    const int k = cfg->topk;
+    const int32_t *h = hdr + (size_t)t * (1 + 3 * k);
+    for (int i = 0; i < k; ++i)
+        if (h[1 + i] < 0 || h[1 + i] >= cfg->n_routed)
+            return fail(MOE_EINVAL, "route header token %d: pick %d outside 0..%d", t, h[1 + i], cfg->n_routed - 1);
+    if (status)
+        *status = h[0];
+    for (int i = 0; i < k; ++i) {
+        if (picks)
+            picks[i] = h[1 + i];
+        if (weights)
+            std::memcpy(&weights[i], &h[1 + k + i], 4);
+    }
+    return MOE_OK;
+}
+
+int moe_graph_create(const moe_cfg *cfg, const moe_layer *layers, int n_layers, const moe_arena *arena, int m,
+                     void *x_a, void *x_b, float *residual, int32_t *headers, void *ws, void **graph)
+{
+    int rc = check_cfg(cfg);
+    if (rc || (rc = check_m(cfg, m)) || (rc = check_arena(arena)))
+        return rc;
+    if (!layers || n_layers < 1 || !x_a || !x_b || !residual || !headers || !ws || !graph || m < 1)
+        return fail(MOE_EINVAL, "moe_graph_create: bad arguments");
+    for (int l = 0; l < n_layers; ++l)
+        if ((rc = check_layer(*cfg, &layers[l])))
+            return rc;
+    DevInfo *I;
+    if ((rc = dev_info(&I)))
+        return rc;
+    cudaStream_t cs;
+    CUDA_OK(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking));
+    GraphObj *G = new GraphObj;
+    const int hw = header_words(m, cfg->topk);
+    cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+    if (e == cudaSuccess) {
+        for (int l = 0; l < n_layers && rc == MOE_OK; ++l) {
+            const void *xin = (l % 2 == 0) ? x_a : x_b;
+            void *xout = (l == n_layers - 1) ? x_a : ((l % 2 == 0) ? x_b : x_a);
+            rc = layer_step(*cfg, layers[l], *arena, xin, residual, xout, headers + (size_t)l * hw, m, ws, cs);
+        }
+        cudaGraph_t g = nullptr;
+        cudaError_t e2 = cudaStreamEndCapture(cs, &g);
+        if (rc == MOE_OK && e2 == cudaSuccess) {
+            G->graph = g;
+            e = cudaGraphInstantiate(&G->exec, g, 0);
+        } else {
+            if (g)
+                cudaGraphDestroy(g);
+            e = e2 != cudaSuccess ? e2 : cudaErrorUnknown;
+        }
+    }
+    cudaStreamDestroy(cs);
+    if (rc != MOE_OK || e != cudaSuccess) {
+        if (G->exec)
+            cudaGraphExecDestroy(G->exec);
+        if (G->graph)
+            cudaGraphDestroy(G->graph);
+        delete G;
+        cudaGetLastError();
+        if (rc != MOE_OK)
+            return fail(MOE_ECAPTURE, "graph capture failed: %s", g_err);
+        return fail(MOE_ECAPTURE, "graph capture failed: %s", cudaGetErrorString(e));
+    }
+    G->x_a = x_a;
+    G->residual = residual;
+    G->headers = headers;
+    G->x_bytes = (size_t)m * cfg->dim * 2;
+    G->res_bytes = (size_t)m * cfg->dim * 4;
+    G->hdr_bytes = sizeof(int32_t) * (size_t)hw * n_layers;
+    *graph = G;
+    return MOE_OK;
+}
+
+int moe_graph_launch(void *graph, moe_stream_t stream)
+{
+    if (!graph)
+        return fail(MOE_EINVAL, "graph is NULL");
+    CUDA_OK(cudaGraphLaunch(static_cast<GraphObj *>(graph)->exec, (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+int moe_graph_launch_host(void *graph, const void *x_host, const float *residual_host, void *x_out_host,
+                          float *residual_out_host, int32_t *headers_host, moe_stream_t stream)
+{
+    if (!graph || !x_host || !residual_host || !x_out_host || !residual_out_host || !headers_host)
+        return fail(MOE_EINVAL, "moe_graph_launch_host: a buffer is NULL");
+    GraphObj *G = static_cast<GraphObj *>(graph);
+    cudaStream_t s = (cudaStream_t)stream;
+    CUDA_OK(cudaMemcpyAsync(G->x_a, x_host, G->x_bytes, cudaMemcpyHostToDevice, s));
+    CUDA_OK(cudaMemcpyAsync(G->residual, residual_host, G->res_bytes, cudaMemcpyHostToDevice, s));
+    CUDA_OK(cudaGraphLaunch(G->exec, s));
+    CUDA_OK(cudaMemcpyAsync(x_out_host, G->x_a, G->x_bytes, cudaMemcpyDeviceToHost, s));
+    CUDA_OK(cudaMemcpyAsync(residual_out_host, G->residual, G->res_bytes, cudaMemcpyDeviceToHost, s));
+    CUDA_OK(cudaMemcpyAsync(headers_host, G->headers, G->hdr_bytes, cudaMemcpyDeviceToHost, s));
+    return MOE_OK;
+}
+
+int moe_layer_step_profiled(const moe_cfg *cfg, const moe_layer *layer, const moe_arena *arena, const void *x,
+                            float *residual, void *x_next, int32_t *header, int m, void *ws, moe_stream_t stream,
+                            float *ms)
+{
+    int rc = check_cfg(cfg);
+    if (rc || (rc = check_m(cfg, m)) || (rc = check_arena(arena)) || (rc = check_layer(*cfg, layer)))
+        return rc;
+    if (m < 1 || !x || !residual || !x_next || !header || !ws || !ms || !aligned16(x))
+        return fail(MOE_EINVAL, "moe_layer_step_profiled: bad arguments");
+    thread_local cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+    thread_local int ev_dev = -1;
+    int d = 0;
+    CUDA_OK(cudaGetDevice(&d));
+    if (ev_dev != d) {
+        for (int i = 0; i < 4; ++i)
+            CUDA_OK(cudaEventCreate(&ev[i]));
+        ev_dev = d;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    if ((rc = layer_step(*cfg, *layer, *arena, x, residual, x_next, header, m, ws, s, ev)))
+        return rc;
+    CUDA_OK(cudaEventSynchronize(ev[3]));
+    for (int i = 0; i < 3; ++i)
+        CUDA_OK(cudaEventElapsedTime(&ms[i], ev[i], ev[i + 1]));
+    return MOE_OK;
+}
+
+int moe_graph_destroy(void *graph)
+{
+    if (!graph)
+        return MOE_OK;
+    GraphObj *G = static_cast<GraphObj *>(graph);
+    if (G->exec)
+        cudaGraphExecDestroy(G->exec);
+    if (G->graph)
+        cudaGraphDestroy(G->graph);
+    delete G;
+    return MOE_OK;
+}
+
+}  // extern "C"

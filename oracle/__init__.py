@@ -302,3 +302,20 @@ def layer(c: Cfg, x_bf16, router_w, bias, experts: dict, offsets, shared=None, r
         raise KeyError("oracle layer: a picked expert has no host image")
     return dict(logits=logits, picks=picks, weights=weights, flags=flags, acc=acc, sd=sd,
                 residual=res, x_next=xn)
+
+
+# ------------------------------------------------------------------ tiny-layer inputs
+
+def quantised_expert_image(seed: int, layer: int, expert: int, shp) -> np.ndarray:
+    """One expert's slot image for the tiny layer: N(0, 0.02) weights from the seeded
+    generator, quantised with the oracle's Q2_K (gate, up) and Q3_K (down) quantisers."""
+    from moe_decode_quantized_gb300 import synth
+    img = np.zeros(shp.slot_bytes, np.uint8)
+    parts = ((shp.gate_off, shp.gate_bytes, quantize_q2k, 84, synth.T_GATE),
+             (shp.up_off, shp.up_bytes, quantize_q2k, 84, synth.T_UP),
+             (shp.down_off, shp.down_bytes, quantize_q3k, 110, synth.T_DOWN))
+    for off, nbytes, quant, bb, t in parts:
+        nw = nbytes // bb * 256
+        w = synth.normal_f32(synth.tensor_key(seed, layer, synth.T_F32, 16 * t + expert), nw, 0.02)
+        img[off:off + nbytes] = quant(w).ravel()
+    return img

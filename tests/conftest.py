@@ -11,3 +11,19 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built libmoe.so")
+
+
+def pytest_collection_modifyitems(config, items):
+    """GPU tests need a CUDA device; on a machine without one they are skipped
+    (the CPU suite is run with -m "not gpu"). With a device they always run."""
+    try:
+        import torch
+        has_gpu = torch.cuda.is_available()
+    except Exception:
+        has_gpu = False
+    if has_gpu:
+        return
+    skip = pytest.mark.skip(reason="no CUDA device")
+    for item in items:
+        if "gpu" in item.keywords:
+            item.add_marker(skip)

@@ -1,0 +1,139 @@
+"""Shared helpers of the GPU parity tests: configurations, tolerances, and the
+oracle run on the same seeded inputs the device workload holds."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import moe_decode_quantized_gb300 as moe
+import oracle
+from moe_decode_quantized_gb300 import synth
+from moe_decode_quantized_gb300.workload import Workload, x_tensor
+
+THREADS = max(1, min(16, os.cpu_count() or 1))
+
+# matching rules (stated for this engine): logits |d| <= 1e-5 max(|l|, rms(l));
+# picks, slots, pointers and weight bits exact; layer outputs max|d| / max|ref| <= 2e-3
+LOGIT_RTOL = 1e-5
+OUT_RTOL = 2e-3
+# intermediates that see only f32 scale arithmetic (no re-quantisation)
+GU_RTOL = 1e-5
+
+
+def tiny_cfg(m=1, **kw):
+    base = dict(dim=256, inter=256, n_routed=16, topk=2, norm_topk_prob=True, max_tokens=m,
+                gate_temp=1.0, route_scale=2.5, swiglu_limit=7.0)
+    base.update(kw)
+    return moe.Config(**base)
+
+
+def decode_cfg(m=1, **kw):
+    base = dict(dim=4096, inter=2048, n_routed=384, topk=6, norm_topk_prob=True, max_tokens=m,
+                gate_temp=1.0, route_scale=2.5, swiglu_limit=7.0)
+    base.update(kw)
+    return moe.Config(**base)
+
+
+def ocfg(cfg: moe.Config):
+    return oracle.cfg(cfg.dim, cfg.inter, cfg.n_routed, cfg.topk, cfg.norm_topk_prob, cfg.gate_temp,
+                      cfg.route_scale, cfg.swiglu_limit)
+
+
+def tiny_workload(cfg, seed=0, n_layers=1, shared=False):
+    """The tiny layer: experts quantised from N(0, 0.02) with the oracle's quantisers."""
+    wl = Workload(cfg, n_layers=n_layers, seed=seed, shared=shared, fill_experts=False)
+    wl.images = {}
+    for l in range(n_layers):
+        for e in range(cfg.n_routed):
+            img = oracle.quantised_expert_image(seed, l, e, wl.shape)
+            wl.images[(l, e)] = img
+            wl.set_expert_image(l, e, img)
+    return wl
+
+
+def expert_image(wl, l, e):
+    imgs = getattr(wl, "images", None)
+    if imgs is not None and (l, e) in imgs:
+        return imgs[(l, e)]
+    return wl.host_expert(l, e)
+
+
+def bf16_vals(bits):
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def rel_inf(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    den = np.abs(ref).max()
+    return float(np.abs(got - ref).max() / (den if den > 0 else 1.0))
+
+
+def assert_bf16_within_one_ulp(got_bits, ref_bits, slack):
+    """x_next = bf16(residual): the two residuals differ by rounding, so a value that
+    lies near a bf16 rounding boundary may land one bf16 ulp apart."""
+    got = bf16_vals(got_bits).astype(np.float64)
+    ref = bf16_vals(ref_bits).astype(np.float64)
+    mag = np.maximum(np.abs(ref), np.finfo(np.float32).tiny)
+    ulp = 2.0 ** (np.floor(np.log2(mag)) - 7)
+    bad = np.abs(got - ref) > ulp + slack
+    assert not bad.any(), (np.argwhere(bad)[:5], got[bad][:5], ref[bad][:5])
+
+
+def assert_logits_close(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    for t in range(ref.shape[0]):
+        rms = np.sqrt(np.mean(ref[t] ** 2))
+        bound = LOGIT_RTOL * np.maximum(np.abs(ref[t]), rms)
+        assert np.all(np.abs(got[t] - ref[t]) <= bound), (t, np.abs(got[t] - ref[t]).max())
+
+
+def keys_of(cfg, logits, bias):
+    """Exact-rounded keys as the oracle defines them (for near-tie detection)."""
+    _, _, scores, _ = oracle.route(ocfg(cfg), logits, bias)
+    return (scores + np.asarray(bias, np.float32)).astype(np.float32)
+
+
+def near_tie(cfg, logits, bias, t):
+    """True when token t's k-th and (k+1)-th keys are closer than the logit error
+    bound allows us to resolve (the end-to-end picks may then legitimately differ)."""
+    key = keys_of(cfg, logits[t:t + 1], bias)[0].astype(np.float64)
+    order = np.sort(key)[::-1]
+    k = cfg.topk
+    if k >= len(order):
+        return False
+    rms = np.sqrt(np.mean(np.asarray(logits[t], np.float64) ** 2))
+    eps = LOGIT_RTOL * max(float(np.abs(logits[t]).max()), rms)
+    return (order[k - 1] - order[k]) <= 2.0 * (0.5 * eps + 4e-7 * abs(order[k - 1]))
+
+
+def oracle_layer(wl, cfg, l, x_bits, residual=None):
+    """The oracle's layer step on the workload's host inputs (experts materialised
+    for every pick the oracle makes)."""
+    oc = ocfg(cfg)
+    router = wl.host_router(l)
+    bias = wl.host_bias(l)
+    logits = oracle.router_logits(x_bits, router)
+    picks, _, _, _ = oracle.route(oc, logits, bias)
+    experts = {int(e): expert_image(wl, l, int(e)) for e in np.unique(picks)}
+    out = oracle.layer(oc, x_bits, router, bias, experts,
+                       (wl.shape.gate_off, wl.shape.up_off, wl.shape.down_off), wl.host_shared(l),
+                       residual, threads=THREADS)
+    out["experts"] = experts
+    return out
+
+
+def new_header(cfg, m, n_layers=1):
+    return torch.zeros(n_layers * moe.header_words(cfg, m), dtype=torch.int32, device="cuda")
+
+
+def parse_all(cfg, hdr_np, m):
+    out = []
+    for t in range(m):
+        out.append(moe.parse_header(cfg, hdr_np, m, t))
+    return out
+
+
+gpu = pytest.mark.gpu

@@ -1,0 +1,67 @@
+"""The benchmark's multi-rank path on CPU (gloo, world size 2): replicas only,
+units summed over ranks, time = the max over ranks; the reference arm runs on
+rank 0 alone."""
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    units, secs = bench.aggregate(100.0 * (rank + 1), 0.5 + rank, world)
+    bench.barrier(world)
+    q.put((rank, units, secs))
+    dist.destroy_process_group()
+
+
+def test_aggregate_sums_units_and_takes_max_time():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = [q.get(timeout=120) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, units, secs in res:
+        assert units == 300.0 and secs == 1.5
+
+
+def test_reference_arm_exits_quietly_off_rank_zero(capsys, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"])
+    assert capsys.readouterr().out == ""
+
+
+def test_algorithmic_bytes_of_the_decode_layer():
+    sys.path.insert(0, ROOT)
+    import bench
+    r, g, d = bench.algorithmic_bytes(bench.decode_cfg(1), 1, 6)
+    # router 384 x 4096 bf16; 6 experts' Q2_K gate+up + shared W1/W3; Q3_K down + shared W2
+    assert r >= 3_145_728 and r < 3_160_000
+    assert g >= 2 * 6 * 2_752_512 + 2 * 2048 * 4096 * 2
+    assert d >= 6 * 3_604_480 + 4096 * 2048 * 2
+    assert (r + g + d) / 1e6 == pytest.approx(108.3, abs=0.4)
