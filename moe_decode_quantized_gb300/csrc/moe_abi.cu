@@ -140,11 +140,12 @@ size_t router_smem(int rows, int dim, int m)
     return 128 + (main > sel ? main : sel);
 }
 
+// the most ring stages (up to cap, at least 2) that fit the shared memory
 int stages_fit(size_t fixed, uint32_t stage, int cap, size_t limit)
 {
     int S = cap;
-    while (S > MOE_CONSUMER_WARPS && fixed + ring_head_bytes(S) + (size_t)S * stage + 16 > limit)
-        S -= MOE_CONSUMER_WARPS;
+    while (S > 2 && fixed + ring_head_bytes(S) + (size_t)S * stage + 16 > limit)
+        --S;
     return S;
 }
 
@@ -159,7 +160,7 @@ int geometry(const moe_cfg &c, int m, bool shared, const DevInfo &I, Geo &G)
     // gate/up: stages of max(one Q2_K task, one bf16 row)
     G.g_stage = (uint32_t)align_up(std::max<size_t>((size_t)MOE_G_TASK_SB * MOE_Q2K_BYTES, (size_t)dim * 2), 128);
     size_t g_fixed = align_up((size_t)m * act_row_bytes(dim), 128) + (shared ? align_up((size_t)m * dim * 2, 128) : 0);
-    G.g_S = stages_fit(g_fixed, G.g_stage, 2 * MOE_CONSUMER_WARPS, limit);
+    G.g_S = stages_fit(g_fixed, G.g_stage, 32, limit);
     G.g_smem = g_smem_bytes(G.g_S, m, dim, shared, G.g_stage);
     // down: stages of max(one Q3_K task, one bf16 row)
     G.d_stage = (uint32_t)align_up(std::max<size_t>((size_t)MOE_D_TASK_SB * MOE_Q3K_BYTES, (size_t)inter * 2), 128);
@@ -168,10 +169,10 @@ int geometry(const moe_cfg &c, int m, bool shared, const DevInfo &I, Geo &G)
     const long long per = (tmax + G.grid - 1) / G.grid;
     int span = (int)((per + tpr - 1) / tpr) + 1;
     G.d_pair_cap = std::min(m * k, span * m);
-    size_t d_fixed = 512 + align_up((size_t)G.d_pair_cap * act_row_bytes(inter), 128) +
+    size_t d_fixed = d_small_bytes(dim, inter) + align_up((size_t)G.d_pair_cap * act_row_bytes(inter), 128) +
                      (shared ? align_up((size_t)m * inter * 2, 128) : 0);
-    G.d_S = stages_fit(d_fixed, G.d_stage, 3 * MOE_CONSUMER_WARPS, limit);
-    G.d_smem = d_smem_bytes(G.d_S, G.d_pair_cap, m, inter, shared, G.d_stage);
+    G.d_S = stages_fit(d_fixed, G.d_stage, 48, limit);
+    G.d_smem = d_smem_bytes(G.d_S, G.d_pair_cap, m, dim, inter, shared, G.d_stage);
     if (G.r_smem > limit || G.g_smem > limit || G.d_smem > limit)
         return fail(MOE_EUNSUPPORTED, "shared memory: router %zu, gate/up %zu, down %zu > %zu bytes", G.r_smem,
                     G.g_smem, G.d_smem, limit);

@@ -21,10 +21,10 @@
 #define MOE_Q8_BYTES 36       // q8_1 block of 32
 #define MOE_WAIT_NS 2000000000ull  // 2 s bound on any single wait
 
-// one Q2_K task = 64 super-blocks of one matrix (5376 B); one Q3_K task = 32
-// super-blocks (3520 B). Both sizes are multiples of 16 so the bulk copies
+// one Q2_K task = 128 super-blocks of one matrix (10752 B); one Q3_K task =
+// 32 super-blocks (3520 B). Both sizes are multiples of 16 so the bulk copies
 // of whole tasks stay 16-byte aligned for every supported shape.
-#define MOE_G_TASK_SB 64
+#define MOE_G_TASK_SB 128
 #define MOE_D_TASK_SB 32
 // activation layout in shared memory: per 256-value segment, 256 int8 quants
 // padded to 272 bytes, and a 28-float scale record (8 block scales d8, then
@@ -32,7 +32,7 @@
 #define MOE_SEG_Q_BYTES 272
 #define MOE_SEG_REC_FLOATS 28
 
-#define MOE_CONSUMER_WARPS 8
+#define MOE_CONSUMER_WARPS 15
 #define MOE_THREADS ((MOE_CONSUMER_WARPS + 1) * 32)
 
 namespace moe {

@@ -29,13 +29,14 @@
 
 namespace moe {
 
-struct Task {
+struct __align__(16) Task {
     int kind;   // 0 end, 1 routed, 2 shared
     int mat;    // gate/up kernel: 0 gate or W1, 1 up or W3
     int p;      // plan expert
     int row;    // first row (routed) or the row (shared)
     int pair0, npair;
-    int tok[MOE_MAX_TOKENS];
+    int seq;    // the task's index in this CTA's stream (written last by the producer)
+    int pad;
 };
 
 // ------------------------------------------------------------------ q8_1 (one 32-block per warp)
@@ -144,43 +145,52 @@ __device__ __forceinline__ float q2k_dot(const uint32_t *blk, const int4 *xq, co
 
 // Q3_K super-block (110 bytes, 2-byte aligned in shared memory) against a
 // q8_1 segment: d * sum_b d8_b (sc_2b (dot_2b - 4 sum_2b) + sc_2b+1 (...)),
-// the quants taken as q + 4 in [0, 7] for dp4a and the offset removed.
+// the quants taken as q + 4 in [0, 7] for dp4a and the offset removed. The
+// block's 32-bit fields are read from the aligned words around it and shifted
+// into place (the block starts 0 or 2 bytes past a word boundary).
 __device__ __forceinline__ float q3k_dot(const uint8_t *blk, const int4 *xq, const float4 *rec)
 {
     const uintptr_t a = reinterpret_cast<uintptr_t>(blk);
     const uint32_t *W = reinterpret_cast<const uint32_t *>(a & ~(uintptr_t)3);
     const uint32_t sh = (uint32_t)(a & 3) * 8u;  // 0 or 16
-    uint32_t f[28];
+    uint32_t hm[8];
+    {
+        uint32_t w[9];
 #pragma unroll
-    for (int i = 0; i < 28; ++i)
-        f[i] = W[i];
+        for (int i = 0; i < 9; ++i)
+            w[i] = W[i];
 #pragma unroll
-    for (int i = 0; i < 27; ++i)
-        f[i] = __funnelshift_r(f[i], f[i + 1], sh);
-    const float d = f16_bits_to_f32(f[27] >> sh);
-    // sixteen 6-bit scales from bytes 96..107 (field words 24..26)
-    const uint32_t *scw = f + 24;
-    int scale[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        uint32_t low4 = i < 8 ? (byte_of(scw, i) & 15u) : (byte_of(scw, i - 8) >> 4);
-        uint32_t high2 = (byte_of(scw, 8 + (i & 3)) >> (2 * (i >> 2))) & 3u;
-        scale[i] = (int)(low4 | (high2 << 4)) - 32;
+        for (int i = 0; i < 8; ++i)
+            hm[i] = __funnelshift_r(w[i], w[i + 1], sh);
+    }
+    uint32_t scw[3];
+    float d;
+    {
+        const uint32_t w24 = W[24], w25 = W[25], w26 = W[26], w27 = W[27];
+        scw[0] = __funnelshift_r(w24, w25, sh);
+        scw[1] = __funnelshift_r(w25, w26, sh);
+        scw[2] = __funnelshift_r(w26, w27, sh);
+        d = f16_bits_to_f32(w27 >> sh);
     }
     const float4 da = rec[0], db = rec[1];
     const float d8[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
-    int sq[16];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float4 r = rec[2 + i];
-        sq[4 * i + 0] = __float_as_int(r.x);
-        sq[4 * i + 1] = __float_as_int(r.y);
-        sq[4 * i + 2] = __float_as_int(r.z);
-        sq[4 * i + 3] = __float_as_int(r.w);
-    }
     float acc = 0.0f;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
+        uint32_t q[8];
+        {
+            uint32_t w[9];
+#pragma unroll
+            for (int i = 0; i < 9; ++i)
+                w[i] = W[8 + 8 * h + i];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                q[i] = __funnelshift_r(w[i], w[i + 1], sh);
+        }
+        const float4 sqa = rec[2 + 2 * h], sqb = rec[3 + 2 * h];  // sums of sub-blocks 8h .. 8h+7
+        const int sq[8] = {__float_as_int(sqa.x), __float_as_int(sqa.y), __float_as_int(sqa.z),
+                           __float_as_int(sqa.w), __float_as_int(sqb.x), __float_as_int(sqb.y),
+                           __float_as_int(sqb.z), __float_as_int(sqb.w)};
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
             const int4 xa = xq[8 * h + 2 * g], xb = xq[8 * h + 2 * g + 1];
@@ -188,8 +198,7 @@ __device__ __forceinline__ float q3k_dot(const uint8_t *blk, const int4 *xq, con
             int v[8];
 #pragma unroll
             for (int w = 0; w < 8; ++w)
-                v[w] = (int)(((f[8 + 8 * h + w] >> qsh) & 0x03030303u) |
-                             (((f[w] >> hsh) & 0x01010101u) << 2));
+                v[w] = (int)(((q[w] >> qsh) & 0x03030303u) | (((hm[w] >> hsh) & 0x01010101u) << 2));
             int s0 = __dp4a(v[0], xa.x, 0);
             s0 = __dp4a(v[1], xa.y, s0);
             s0 = __dp4a(v[2], xa.z, s0);
@@ -198,8 +207,14 @@ __device__ __forceinline__ float q3k_dot(const uint8_t *blk, const int4 *xq, con
             s1 = __dp4a(v[5], xb.y, s1);
             s1 = __dp4a(v[6], xb.z, s1);
             s1 = __dp4a(v[7], xb.w, s1);
-            const int sub = 8 * h + 2 * g;
-            const int isum = scale[sub] * (s0 - 4 * sq[sub]) + scale[sub + 1] * (s1 - 4 * sq[sub + 1]);
+            const int i0 = 8 * h + 2 * g, i1 = i0 + 1;
+            // 6-bit scales i0, i1: low 4 bits from byte i (i < 8) or the high
+            // nibble of byte i - 8; high 2 bits at 2 * (i / 4) in byte 8 + i % 4
+            const int sc0 = (int)((i0 < 8 ? (byte_of(scw, i0) & 15u) : (byte_of(scw, i0 - 8) >> 4)) |
+                                  (((byte_of(scw, 8 + (i0 & 3)) >> (2 * (i0 >> 2))) & 3u) << 4)) - 32;
+            const int sc1 = (int)((i1 < 8 ? (byte_of(scw, i1) & 15u) : (byte_of(scw, i1 - 8) >> 4)) |
+                                  (((byte_of(scw, 8 + (i1 & 3)) >> (2 * (i1 >> 2))) & 3u) << 4)) - 32;
+            const int isum = sc0 * (s0 - 4 * sq[2 * g]) + sc1 * (s1 - 4 * sq[2 * g + 1]);
             acc = fmaf(d8[4 * h + g], (float)isum, acc);
         }
     }
@@ -208,9 +223,21 @@ __device__ __forceinline__ float q3k_dot(const uint8_t *blk, const int4 *xq, con
 
 // ------------------------------------------------------------------ pipeline helpers
 
+// The plan of the call, cached in shared memory by the producer warp (one
+// round of parallel global loads instead of dependent loads per task).
+struct PlanCache {
+    int ne;
+    int next;  // consumers' dynamic task counter
+    int pad[2];
+    int pair_start[MOE_MAX_TOKENS * MOE_MAX_TOPK + 1];
+    int rows[MOE_MAX_TOKENS * MOE_MAX_TOPK];
+    unsigned long long ptr[2][MOE_MAX_TOKENS * MOE_MAX_TOPK];
+};
+
 struct Ring {
     uint64_t *full, *empty;
     Task *desc;
+    PlanCache *pc;
     uint8_t *stage;
     uint32_t stage_bytes;
     int S;
@@ -225,7 +252,9 @@ __device__ __forceinline__ bool ring_issue(const Ring &r, int i, const Task &t, 
     const uint32_t round = (uint32_t)(i / r.S);
     if (round > 0 && !mbar_wait(&r.empty[slot], (round - 1) & 1u, status))
         return false;
-    r.desc[slot] = t;
+    Task tt = t;
+    tt.seq = i;
+    r.desc[slot] = tt;
     mbar_arrive_expect_tx(&r.full[slot], bytes);
     if (bytes)
         bulk_g2s(r.at(slot), src, bytes, &r.full[slot], pol);
@@ -238,7 +267,9 @@ __device__ __forceinline__ void ring_init(const Ring &r)
         for (int s = 0; s < r.S; ++s) {
             mbar_init(&r.full[s], 1);
             mbar_init(&r.empty[s], 1);
+            r.desc[s].seq = -1;
         }
+        r.pc->next = 0;
         fence_barrier_init();
     }
 }
@@ -248,22 +279,77 @@ __device__ __forceinline__ void consumers_sync()
     asm volatile("bar.sync 1, %0;" ::"r"(MOE_CONSUMER_WARPS * 32) : "memory");
 }
 
+__host__ __device__ inline size_t ring_desc_off(int S) { return align_up(16 * (size_t)S, 64); }
+__host__ __device__ inline size_t ring_pc_off(int S) { return align_up(ring_desc_off(S) + sizeof(Task) * (size_t)S, 16); }
+
+// bytes before the stages: barriers, descriptors, plan cache
+__host__ __device__ inline size_t ring_head_bytes(int S)
+{
+    return align_up(ring_pc_off(S) + sizeof(PlanCache), 128);
+}
+
 __device__ __forceinline__ Ring ring_carve(uint8_t *smem, int S, uint32_t stage_bytes, size_t stage_off)
 {
     Ring r;
     r.S = S;
     r.full = reinterpret_cast<uint64_t *>(smem);
     r.empty = r.full + S;
-    r.desc = reinterpret_cast<Task *>(smem + align_up(16 * (size_t)S, 64));
+    r.desc = reinterpret_cast<Task *>(smem + ring_desc_off(S));
+    r.pc = reinterpret_cast<PlanCache *>(smem + ring_pc_off(S));
     r.stage = smem + stage_off;
     r.stage_bytes = stage_bytes;
     return r;
 }
 
-// bytes before the stages: barriers, descriptors
-__host__ __device__ inline size_t ring_head_bytes(int S)
+// consumer side: the next task index (dynamic, any warp takes the next task)
+__device__ __forceinline__ int ring_grab(const Ring &r)
 {
-    return align_up(align_up(16 * (size_t)S, 64) + sizeof(Task) * (size_t)S, 128);
+    int j = 0;
+    if ((threadIdx.x & 31) == 0)
+        j = atomicAdd(&r.pc->next, 1);
+    return __shfl_sync(0xffffffffu, j, 0);
+}
+
+// Consumer side: waits until slot j % S holds task j. The producer stamps a
+// descriptor only after the slot's previous task was consumed, so once the
+// stamp reads j the barrier's current phase is task j's and the parity wait
+// is unambiguous (a parity wait cannot tell a phase two ahead from the one
+// just completed). Bounded like every wait; false after MOE_WAIT_NS.
+__device__ __forceinline__ bool ring_acquire(const Ring &r, int j, uint32_t *status)
+{
+    const int slot = j % r.S;
+    volatile const int *seq = &r.desc[slot].seq;
+    if (*seq != j) {
+        const uint64_t t0 = globaltimer();
+        while (*seq != j) {
+            __nanosleep(64);
+            if (globaltimer() - t0 > MOE_WAIT_NS) {
+                atomicOr(status, (uint32_t)MOE_WS_TIMEOUT);
+                return false;
+            }
+        }
+    }
+    return mbar_wait(&r.full[slot], (uint32_t)(j / r.S) & 1u, status);
+}
+
+// the producer warp caches the plan (all 32 lanes load in parallel); `which`
+// selects the pointer rows to keep (gate/up: 0 and 1, down: 2)
+__device__ __forceinline__ void cache_plan(const Ring &r, const int32_t *hdr, int plan_off, const int32_t *plan_rows,
+                                           const unsigned long long *ptrs, int cap, int which0, int nwhich)
+{
+    const int lane = threadIdx.x & 31;
+    PlanCache &pc = *r.pc;
+    const int ne = min(max(__ldcg(hdr + plan_off), 0), cap);
+    for (int i = lane; i <= ne; i += 32)
+        pc.pair_start[i] = min(max(__ldcg(hdr + plan_off + 1 + i), 0), cap);
+    for (int i = lane; i < cap; i += 32)
+        pc.rows[i] = min(max(__ldcg(plan_rows + i), 0), MOE_MAX_TOKENS - 1);
+    for (int i = lane; i < ne; i += 32)
+        for (int w = 0; w < nwhich; ++w)
+            pc.ptr[w][i] = __ldcg(ptrs + (size_t)(which0 + w) * cap + i);
+    if (lane == 0)
+        pc.ne = ne;
+    __syncwarp();
 }
 
 // ------------------------------------------------------------------ gate / up kernel
@@ -306,58 +392,59 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
     __syncthreads();
 
     if (warp == MOE_CONSUMER_WARPS) {
-        // ---------------- producer
-        if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
-            int i = 0;
-            bool ok = true;
-            if (shared) {
-                const int nsh = 2 * inter;
-                const int lo = (int)((long long)blockIdx.x * nsh / gridDim.x);
-                const int hi = (int)((long long)(blockIdx.x + 1) * nsh / gridDim.x);
-                for (int s = lo; s < hi && ok; ++s) {
-                    Task t{};
-                    t.kind = 2;
-                    t.mat = s / inter;
-                    t.row = s % inter;
-                    const uint16_t *src = (t.mat ? a.w3 : a.w1) + (size_t)t.row * dim;
-                    ok = ring_issue(ring, i++, t, src, (uint32_t)dim * 2u, pol, a.status);
-                }
+        // ---------------- producer warp
+        const uint64_t pol = policy_evict_first();
+        int i = 0;
+        bool ok = true;
+        if (shared && lane == 0) {
+            // the shared expert's rows depend only on x: issued before the wait
+            const int nsh = 2 * inter;
+            const int lo = (int)((long long)blockIdx.x * nsh / gridDim.x);
+            const int hi = (int)((long long)(blockIdx.x + 1) * nsh / gridDim.x);
+            for (int s = lo; s < hi && ok; ++s) {
+                Task t{};
+                t.kind = 2;
+                t.mat = s / inter;
+                t.row = s % inter;
+                const uint16_t *src = (t.mat ? a.w3 : a.w1) + (size_t)t.row * dim;
+                ok = ring_issue(ring, i++, t, src, (uint32_t)dim * 2u, pol, a.status);
             }
-            pdl_wait();  // the selection has written the plan and the pointer table
-            pdl_launch_dependents();
-            const int ne = min(max(__ldcg(a.hdr + a.plan_off), 0), a.cap);
+        }
+        __syncwarp();
+        pdl_wait();  // the selection has written the plan and the pointer table
+        pdl_launch_dependents();
+        cache_plan(ring, a.hdr, a.plan_off, a.plan_rows, a.ptrs, a.cap, 0, 2);
+        if (lane == 0) {
+            const PlanCache &pc = *ring.pc;
             const int rt = gate_rows_per_task(dim);
             const int tpm = inter / rt;  // tasks per matrix
-            const long long total = (long long)ne * 2 * tpm;
+            const long long total = (long long)pc.ne * 2 * tpm;
             const int lo = (int)(blockIdx.x * total / gridDim.x);
             const int hi = (int)((blockIdx.x + 1) * total / gridDim.x);
-            const size_t rowb = (size_t)nb * MOE_Q2K_BYTES;
+            const uint32_t bytes = (uint32_t)(rt * nb * MOE_Q2K_BYTES);
+            // walk (expert, matrix, row run) from lo without per-task divisions
+            int p = lo / (2 * tpm), mat = (lo / tpm) & 1, r = lo % tpm;
             for (int tix = lo; tix < hi && ok; ++tix) {
                 Task t{};
                 t.kind = 1;
-                t.p = tix / (2 * tpm);
-                const int rem = tix % (2 * tpm);
-                t.mat = rem / tpm;
-                t.row = (rem % tpm) * rt;
-                t.pair0 = __ldcg(a.hdr + a.plan_off + 1 + t.p);
-                t.npair = __ldcg(a.hdr + a.plan_off + 2 + t.p) - t.pair0;
-                if (t.npair < 1 || t.npair > a.m || t.pair0 < 0 || t.pair0 + t.npair > a.cap) {
+                t.p = p;
+                t.mat = mat;
+                t.row = r * rt;
+                t.pair0 = pc.pair_start[p];
+                t.npair = pc.pair_start[p + 1] - t.pair0;
+                if (t.npair >= 1 && t.npair <= a.m) {
+                    const char *src = reinterpret_cast<const char *>(pc.ptr[mat][p]) + (size_t)r * bytes;
+                    ok = ring_issue(ring, i++, t, src, bytes, pol, a.status);
+                } else {
                     atomicOr(a.status, (uint32_t)MOE_WS_PLAN);
-                    continue;
                 }
-                bool toks_ok = true;
-                for (int j = 0; j < t.npair; ++j) {
-                    t.tok[j] = __ldcg(a.plan_rows + t.pair0 + j);
-                    toks_ok &= t.tok[j] >= 0 && t.tok[j] < a.m;
+                if (++r == tpm) {
+                    r = 0;
+                    if (++mat == 2) {
+                        mat = 0;
+                        ++p;
+                    }
                 }
-                if (!toks_ok) {
-                    atomicOr(a.status, (uint32_t)MOE_WS_PLAN);
-                    continue;
-                }
-                const char *src = reinterpret_cast<const char *>(__ldcg(a.ptrs + (size_t)t.mat * a.cap + t.p)) +
-                                  (size_t)t.row * rowb;
-                ok = ring_issue(ring, i++, t, src, (uint32_t)(rt * rowb), pol, a.status);
             }
             for (int w = 0; w < MOE_CONSUMER_WARPS && ok; ++w) {
                 Task t{};
@@ -387,13 +474,18 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
     // every thread triggers the dependent launch only after the selection is
     // complete (the first routed task is issued after the producer's wait)
     bool triggered = false;
-    for (int j = warp;; j += MOE_CONSUMER_WARPS) {
+    for (;;) {
+        const int j = ring_grab(ring);
         const int slot = j % ring.S;
-        if (!mbar_wait(&ring.full[slot], (uint32_t)(j / ring.S) & 1u, a.status))
+        if (!ring_acquire(ring, j, a.status))
             break;
         const Task t = ring.desc[slot];
-        if (t.kind == 0)
+        if (t.kind == 0) {
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&ring.empty[slot]);  // END slots are reused when S < warps
             break;
+        }
         const uint8_t *st = ring.at(slot);
         if (t.kind == 1 && !triggered) {
             pdl_wait();
@@ -401,29 +493,33 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
             triggered = true;
         }
         if (t.kind == 1) {
-            // 64 super-blocks: lane covers super-blocks lane and lane + 32;
+            // MOE_G_TASK_SB super-blocks: lane covers super-blocks lane + 32 i;
             // one token at a time (tokens of this plan expert), rows reduced
             // over the nb lanes that share them
-            const uint32_t *bp0 = reinterpret_cast<const uint32_t *>(st + (size_t)lane * MOE_Q2K_BYTES);
-            const uint32_t *bp1 = reinterpret_cast<const uint32_t *>(st + (size_t)(lane + 32) * MOE_Q2K_BYTES);
-            const int blk0 = lane % nb, blk1 = (lane + 32) % nb;
+            constexpr int PER = MOE_G_TASK_SB / 32;
+            const int blk = lane % nb;  // the same for all PER super-blocks of the lane
             float *out = t.mat ? a.u : a.g;
 #pragma unroll 1
             for (int tt = 0; tt < t.npair; ++tt) {
-                const uint8_t *xr = act + ring.desc[slot].tok[tt] * arow;
-                const float4 *rec = reinterpret_cast<const float4 *>(xr + nb * MOE_SEG_Q_BYTES);
-                float v0 = q2k_dot(bp0, reinterpret_cast<const int4 *>(xr + blk0 * MOE_SEG_Q_BYTES),
-                                   rec + blk0 * (MOE_SEG_REC_FLOATS / 4));
-                float v1 = q2k_dot(bp1, reinterpret_cast<const int4 *>(xr + blk1 * MOE_SEG_Q_BYTES),
-                                   rec + blk1 * (MOE_SEG_REC_FLOATS / 4));
+                const uint8_t *xr = act + min(ring.pc->rows[t.pair0 + tt], a.m - 1) * arow;
+                const int4 *xq = reinterpret_cast<const int4 *>(xr + blk * MOE_SEG_Q_BYTES);
+                const float4 *rec = reinterpret_cast<const float4 *>(xr + nb * MOE_SEG_Q_BYTES) +
+                                    blk * (MOE_SEG_REC_FLOATS / 4);
+                float v[PER];
+#pragma unroll
+                for (int q = 0; q < PER; ++q)
+                    v[q] = q2k_dot(reinterpret_cast<const uint32_t *>(st + (size_t)(lane + 32 * q) * MOE_Q2K_BYTES),
+                                   xq, rec);
                 for (int o = nb >> 1; o > 0; o >>= 1) {
-                    v0 += __shfl_xor_sync(0xffffffffu, v0, o);
-                    v1 += __shfl_xor_sync(0xffffffffu, v1, o);
+#pragma unroll
+                    for (int q = 0; q < PER; ++q)
+                        v[q] += __shfl_xor_sync(0xffffffffu, v[q], o);
                 }
-                if (blk0 == 0) {
+                if (blk == 0) {
                     float *orow = out + (size_t)(t.pair0 + tt) * inter + t.row;
-                    orow[lane / nb] = v0;
-                    orow[(lane + 32) / nb] = v1;
+#pragma unroll
+                    for (int q = 0; q < PER; ++q)
+                        orow[(lane + 32 * q) / nb] = v[q];
                 }
             }
             __syncwarp();
@@ -499,20 +595,31 @@ struct DArgs {
     uint32_t stage_bytes;
 };
 
+// small area of the down kernel (ints): plan rows [64], plan weights [64],
+// each token's pairs in plan order [8][8], the finished-group count, and the
+// list of row groups this CTA finishes [dim / rows-per-group]
+#define D_SW 64
+#define D_TP 128
+#define D_NFIN 192
+#define D_FIN 196
+__host__ __device__ inline size_t d_small_bytes(int dim, int inter)
+{
+    return align_up(4 * ((size_t)D_FIN + dim / down_rows_per_task(inter)), 128);
+}
 __host__ __device__ inline size_t d_small_off(int S) { return ring_head_bytes(S); }
-__host__ __device__ inline size_t d_act_off(int S) { return d_small_off(S) + 512; }
-__host__ __device__ inline size_t d_hs_off(int S, int pair_cap, int inter)
+__host__ __device__ inline size_t d_act_off(int S, int dim, int inter) { return d_small_off(S) + d_small_bytes(dim, inter); }
+__host__ __device__ inline size_t d_hs_off(int S, int pair_cap, int dim, int inter)
 {
-    return d_act_off(S) + align_up((size_t)pair_cap * act_row_bytes(inter), 128);
+    return d_act_off(S, dim, inter) + align_up((size_t)pair_cap * act_row_bytes(inter), 128);
 }
-__host__ __device__ inline size_t d_stage_off(int S, int pair_cap, int m, int inter, bool shared)
+__host__ __device__ inline size_t d_stage_off(int S, int pair_cap, int m, int dim, int inter, bool shared)
 {
-    return d_hs_off(S, pair_cap, inter) + (shared ? align_up((size_t)m * inter * 2, 128) : 0);
+    return d_hs_off(S, pair_cap, dim, inter) + (shared ? align_up((size_t)m * inter * 2, 128) : 0);
 }
-__host__ __device__ inline size_t d_smem_bytes(int S, int pair_cap, int m, int inter, bool shared,
+__host__ __device__ inline size_t d_smem_bytes(int S, int pair_cap, int m, int dim, int inter, bool shared,
                                               uint32_t stage_bytes)
 {
-    return d_stage_off(S, pair_cap, m, inter, shared) + (size_t)S * stage_bytes + 16;
+    return d_stage_off(S, pair_cap, m, dim, inter, shared) + (size_t)S * stage_bytes + 16;
 }
 
 // the range of tasks of this CTA and the plan pairs its routed tasks touch
@@ -538,17 +645,23 @@ __device__ __forceinline__ DRange d_range(const DArgs &a, bool shared)
     return r;
 }
 
-// acc, residual and x_next of row group rg, by one warp
-__device__ void finish_row_group(const DArgs &a, int rg, int rd, bool shared, const int *s_rows,
+// acc, residual and x_next of row group rg, by one warp: per token its
+// pairs in plan order (ascending expert id), then the shared row
+__device__ void finish_row_group(const DArgs &a, int rg, int rd, bool shared, const int *s_tp,
                                  const float *s_w)
 {
-    const int lane = threadIdx.x & 31, npairs = a.m * a.k;
+    const int lane = threadIdx.x & 31, k = a.k;
     for (int it = lane; it < a.m * rd; it += 32) {
         const int t = it / rd, r = rg * rd + it % rd;
+        float d[MOE_MAX_TOPK];
+#pragma unroll
+        for (int i = 0; i < MOE_MAX_TOPK; ++i)
+            d[i] = i < k ? __ldcg(a.down + (size_t)s_tp[t * MOE_MAX_TOPK + i] * a.dim + r) : 0.0f;
         float acc = 0.0f;
-        for (int q = 0; q < npairs; ++q)
-            if (s_rows[q] == t)
-                acc = __fadd_rn(acc, __fmul_rn(s_w[q], __ldcg(a.down + (size_t)q * a.dim + r)));
+#pragma unroll
+        for (int i = 0; i < MOE_MAX_TOPK; ++i)
+            if (i < k)
+                acc = __fadd_rn(acc, __fmul_rn(s_w[s_tp[t * MOE_MAX_TOPK + i]], d[i]));
         if (shared)
             acc = __fadd_rn(acc, __ldcg(a.sd + (size_t)t * a.dim + r));
         a.acc[(size_t)t * a.dim + r] = acc;
@@ -565,11 +678,12 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     const bool shared = a.w2 != nullptr;
-    const Ring ring = ring_carve(smem, a.S, a.stage_bytes, d_stage_off(a.S, a.pair_cap, a.m, a.inter, shared));
+    const Ring ring = ring_carve(smem, a.S, a.stage_bytes, d_stage_off(a.S, a.pair_cap, a.m, a.dim, a.inter, shared));
     int *s_rows = reinterpret_cast<int *>(smem + d_small_off(a.S));
-    float *s_w = reinterpret_cast<float *>(s_rows + 64);
-    uint8_t *act = smem + d_act_off(a.S);
-    uint16_t *hs = reinterpret_cast<uint16_t *>(smem + d_hs_off(a.S, a.pair_cap, a.inter));
+    float *s_w = reinterpret_cast<float *>(s_rows + D_SW);
+    int *s_tp = s_rows + D_TP;
+    uint8_t *act = smem + d_act_off(a.S, a.dim, a.inter);
+    uint16_t *hs = reinterpret_cast<uint16_t *>(smem + d_hs_off(a.S, a.pair_cap, a.dim, a.inter));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int dim = a.dim, inter = a.inter, nb = inter / MOE_QK;
     const int rd = down_rows_per_task(inter);
@@ -579,33 +693,41 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
     const DRange R = d_range(a, shared);
 
     if (warp == MOE_CONSUMER_WARPS) {
-        // ---------------- producer: everything it loads depends only on the
-        // pointer table, so the whole range is issued before the wait
+        // ---------------- producer warp: everything it loads depends only on
+        // the pointer table, so the whole range is issued before the wait
+        pdl_launch_dependents();
+        cache_plan(ring, a.hdr, a.plan_off, a.plan_rows, a.ptrs, a.cap, 2, 1);
         if (lane == 0) {
-            pdl_launch_dependents();
+            const PlanCache &pc = *ring.pc;
             const uint64_t pol = policy_evict_first();
             int i = 0;
             bool ok = true;
             const bool fits = R.pair_hi - R.pair_lo <= a.pair_cap;
             if (!fits)
                 atomicOr(a.status, (uint32_t)MOE_WS_PLAN);
-            const size_t rowb = (size_t)nb * MOE_Q3K_BYTES;
-            for (int tix = R.lo; tix < (fits ? R.hi : R.lo) && ok; ++tix) {
+            const uint32_t rbytes = (uint32_t)(rd * nb * MOE_Q3K_BYTES);
+            const int end = fits ? R.hi : R.lo;
+            int p = R.lo / R.tpr, r = R.lo % R.tpr;
+            for (int tix = R.lo; tix < end && ok; ++tix) {
                 Task t{};
                 const void *src;
                 uint32_t bytes;
                 if (tix < R.Tr) {
                     t.kind = 1;
-                    t.p = tix / R.tpr;
-                    t.row = (tix % R.tpr) * rd;
-                    t.pair0 = __ldcg(a.hdr + a.plan_off + 1 + t.p);
-                    t.npair = __ldcg(a.hdr + a.plan_off + 2 + t.p) - t.pair0;
+                    t.p = p;
+                    t.row = r * rd;
+                    t.pair0 = pc.pair_start[p];
+                    t.npair = pc.pair_start[p + 1] - t.pair0;
                     if (t.npair < 1 || t.npair > a.m || t.pair0 < R.pair_lo || t.pair0 + t.npair > R.pair_hi) {
                         atomicOr(a.status, (uint32_t)MOE_WS_PLAN);
                         t.npair = 0;  // issued (the row group's ticket still counts it), computes nothing
                     }
-                    src = reinterpret_cast<const char *>(__ldcg(a.ptrs + 2 * (size_t)a.cap + t.p)) + (size_t)t.row * rowb;
-                    bytes = (uint32_t)(rd * rowb);
+                    src = reinterpret_cast<const char *>(pc.ptr[0][p]) + (size_t)r * rbytes;
+                    bytes = rbytes;
+                    if (++r == R.tpr) {
+                        r = 0;
+                        ++p;
+                    }
                 } else {
                     t.kind = 2;
                     t.row = tix - R.Tr;
@@ -645,17 +767,31 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
             hs[i] = f32_to_bf16(swiglu_f32(__ldcg(a.gs + i), __ldcg(a.us + i), a.limit));
     }
     consumers_sync();
+    // each token's pairs in plan order (pairs are grouped by ascending expert)
+    if (threadIdx.x < a.m) {
+        int c = 0;
+        for (int q = 0; q < npairs && c < MOE_MAX_TOPK; ++q)
+            if (s_rows[q] == (int)threadIdx.x)
+                s_tp[threadIdx.x * MOE_MAX_TOPK + c++] = q;
+        for (; c < MOE_MAX_TOPK; ++c)
+            s_tp[threadIdx.x * MOE_MAX_TOPK + c] = 0;
+    }
+    consumers_sync();
 
     const unsigned expected = (unsigned)R.ne + (shared ? (unsigned)rd : 0u);
-    for (int j = warp;; j += MOE_CONSUMER_WARPS) {
+    for (;;) {
+        const int j = ring_grab(ring);
         const int slot = j % ring.S;
-        if (!mbar_wait(&ring.full[slot], (uint32_t)(j / ring.S) & 1u, a.status))
+        if (!ring_acquire(ring, j, a.status))
             break;
         const Task t = ring.desc[slot];
-        if (t.kind == 0)
+        if (t.kind == 0) {
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&ring.empty[slot]);  // END slots are reused when S < warps
             break;
+        }
         const uint8_t *st = ring.at(slot);
-        int rg;
         if (t.kind == 1) {
             // 32 super-blocks: lane = (row lane / nb, block lane % nb); one
             // token (plan pair) at a time
@@ -675,7 +811,6 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&ring.empty[slot]);
-            rg = t.row / rd;
         } else {
             float acc[MOE_MAX_TOKENS];
 #pragma unroll
@@ -715,21 +850,45 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
                         a.sd[(size_t)tt * dim + t.row] = v;
                 }
             }
-            rg = t.row / rd;
         }
-        // row-group ticket: the warp that brings the count to `expected` finishes it
+    }
+
+    // Row-group tickets, once per CTA: after all of this CTA's tasks, one
+    // fence, then for every row group it touched one atomic adding its count
+    // of tasks there; the CTA whose addition completes a group finishes it.
+    consumers_sync();
+    __threadfence();
+    consumers_sync();
+    int *s_fin = s_rows + D_FIN;
+    int *s_nfin = s_rows + D_NFIN;
+    if (threadIdx.x == 0)
+        *s_nfin = 0;
+    consumers_sync();
+    const int ngroups = dim / rd;
+    const int hiR = min(R.hi, R.Tr), s_lo = max(R.lo, R.Tr) - R.Tr, s_hi = max(R.hi, R.Tr) - R.Tr;
+    for (int g = threadIdx.x; g < ngroups; g += MOE_CONSUMER_WARPS * 32) {
+        int cnt = 0;
+        if (R.lo < hiR) {
+            // experts p with lo <= p * tpr + g < hiR
+            const int a0 = R.lo - g, a1 = hiR - g;
+            const int c0 = a0 <= 0 ? 0 : (a0 + R.tpr - 1) / R.tpr;
+            const int c1 = a1 <= 0 ? 0 : (a1 + R.tpr - 1) / R.tpr;
+            cnt += max(0, c1 - c0);
+        }
+        if (shared && s_lo < s_hi)
+            cnt += max(0, min(s_hi, (g + 1) * rd) - max(s_lo, g * rd));
+        if (cnt > 0 && atomicAdd(a.rgcnt + g, (unsigned)cnt) + (unsigned)cnt == expected) {
+            s_fin[atomicAdd(s_nfin, 1)] = g;  // at most ngroups entries
+        }
+    }
+    consumers_sync();
+    const int nfin = min(*s_nfin, ngroups);
+    if (nfin > 0)
         __threadfence();
-        __syncwarp();
-        unsigned last = 0;
+    for (int f = warp; f < nfin; f += MOE_CONSUMER_WARPS) {
+        finish_row_group(a, s_fin[f], rd, shared, s_tp, s_w);
         if (lane == 0)
-            last = atomicAdd(a.rgcnt + rg, 1u) == expected - 1u;
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-            __threadfence();
-            finish_row_group(a, rg, rd, shared, s_rows, s_w);
-            if (lane == 0)
-                atomicExch(a.rgcnt + rg, 0u);
-        }
+            atomicExch(a.rgcnt + s_fin[f], 0u);
     }
 }
 

@@ -77,8 +77,15 @@ def test_decode_graph_equals_eager_and_replays_advance():
 
 
 def test_forty_layer_chain_against_oracle():
-    """40 stacked decode layers (the 40-layer step's shape), one token, eager launches
-    checked against the oracle chain; then the graph replay equals the eager chain."""
+    """40 stacked decode layers (the 40-layer step's shape), one token.
+
+    Layer by layer on the oracle's own chain: layer l of the device gets the
+    oracle's x_l and residual_l (inputs may come from the oracle, never the
+    reverse) and must match the oracle's layer l output. Two free-running chains
+    are not compared element by element: each side rounds x = bf16(residual)
+    from residuals that differ by rounding, an occasional one-ulp flip changes
+    the next layer's input, and these unnormalised synthetic layers amplify it.
+    Then the captured 40-layer graph equals the eager 40-layer chain bit for bit."""
     cfg = decode_cfg(1)
     n_layers = 40
     free, _ = torch.cuda.mem_get_info()
@@ -86,39 +93,41 @@ def test_forty_layer_chain_against_oracle():
     if free < need + (8 << 30):
         pytest.skip(f"needs {need / 2**30:.0f} GiB free, {free / 2**30:.0f} GiB available")
     wl = Workload(cfg, n_layers=n_layers, seed=9, shared=True)
-    x_bits = synth.x_bf16(9, 0, 1, cfg.dim)
-    x = bf16_tensor(x_bits, "cuda")
-    res = torch.zeros((1, cfg.dim), device="cuda")
     hw = moe.header_words(cfg, 1)
-    hdr = new_header(cfg, 1, n_layers)
+    x_bits = synth.x_bf16(9, 0, 1, cfg.dim)
     ox, ores = x_bits, np.zeros((1, cfg.dim), np.float32)
-    checked = 0
-    errs = []
-    diverged = False
+    errs, skipped = [], 0
     for l in range(n_layers):
+        ref = oracle_layer(wl, cfg, l, ox, ores)
+        x = bf16_tensor(ox, "cuda")
+        res = torch.from_numpy(ores.copy()).cuda()
         xn = torch.empty_like(x)
-        moe.layer_step(cfg, wl.layer(l), wl.arena, x, res, xn, hdr[l * hw:(l + 1) * hw], 1, wl.ws)
+        hdr = new_header(cfg, 1)
+        moe.layer_step(cfg, wl.layer(l), wl.arena, x, res, xn, hdr, 1, wl.ws)
         torch.cuda.synchronize()
-        if not diverged:
-            ref = oracle_layer(wl, cfg, l, ox, ores)
-            if near_tie(cfg, ref["logits"], wl.host_bias(l), 0):
-                diverged = True     # from here on the two chains may route differently
-            else:
-                picks = parse_all(cfg, hdr[l * hw:(l + 1) * hw].cpu().numpy(), 1)[0][1]
-                assert list(picks) == list(ref["picks"][0]), (l, picks, ref["picks"][0])
-                err = rel_inf(res.cpu().numpy(), ref["residual"])
-                errs.append(err)
-                # each layer adds its own rounding (<= the one-layer bound) and
-                # propagates the input's: x = bf16(residual) flips a bf16 ulp
-                # where the two residuals straddle a rounding boundary
-                assert err <= OUT_RTOL * (l + 1), (l, err, errs)
-                checked += 1
-            ox, ores = ref["x_next"], ref["residual"]
-        x = xn
-    assert checked >= 8, checked
-    print(f"40-layer chain: {checked} layers matched the oracle before any near-tie; "
-          f"residual rel errors {['%.1e' % e for e in errs]}")
-    xg, rg, hg = _graph_chain(wl, cfg, bf16_tensor(x_bits, "cuda"), torch.zeros((1, cfg.dim), device="cuda"),
-                              1, n_layers, replays=1)
-    assert torch.equal(xg, x) and torch.equal(rg, res) and torch.equal(hg, hdr)
+        if near_tie(cfg, ref["logits"], wl.host_bias(l), 0):
+            skipped += 1
+        else:
+            picks = parse_all(cfg, hdr.cpu().numpy(), 1)[0][1]
+            assert list(picks) == list(ref["picks"][0]), (l, picks, ref["picks"][0])
+            acc = moe_acc(wl, cfg)
+            err = rel_inf(acc, ref["acc"])
+            errs.append(err)
+            assert err <= OUT_RTOL, (l, err)
+            assert rel_inf(res.cpu().numpy(), ref["residual"]) <= OUT_RTOL, l
+        ox, ores = ref["x_next"], ref["residual"]
+    assert skipped <= 4, skipped
+    print(f"40-layer chain, layer by layer: max acc rel error {max(errs):.2e} over {len(errs)} layers, "
+          f"{skipped} near-tie layers skipped")
+    x0 = bf16_tensor(x_bits, "cuda")
+    r0 = torch.zeros((1, cfg.dim), device="cuda")
+    xe, re, he = _eager_chain(wl, cfg, x0, r0, 1, n_layers)
+    xg, rg, hg = _graph_chain(wl, cfg, x0, r0, 1, n_layers)
+    assert torch.equal(xg, xe) and torch.equal(rg, re) and torch.equal(hg, he)
     assert moe.read_status(wl.ws) == 0
+
+
+def moe_acc(wl, cfg):
+    v = moe.workspace_view(cfg, wl.ws)
+    off = v["acc"] - wl.ws.data_ptr()
+    return wl.ws[off:off + 4 * cfg.dim].view(torch.float32).cpu().numpy()[None]
