@@ -94,6 +94,7 @@ int dev_info(DevInfo **out)
         CUDA_OK(cudaDeviceGetAttribute(&I.sms, cudaDevAttrMultiProcessorCount, d));
         CUDA_OK(cudaDeviceGetAttribute(&I.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d));
         CUDA_OK(cudaFuncSetAttribute(moe_router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
+        CUDA_OK(cudaFuncSetAttribute(moe_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
         CUDA_OK(cudaFuncSetAttribute(moe_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
         CUDA_OK(cudaFuncSetAttribute(moe_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
         I.attrs = true;
@@ -153,13 +154,16 @@ int geometry(const moe_cfg &c, int m, bool shared, const DevInfo &I, Geo &G)
 {
     const int n = c.n_routed, dim = c.dim, inter = c.inter, k = c.topk;
     const size_t limit = (size_t)I.smem_optin;
-    G.r_rows = (n + I.sms - 1) / I.sms;
+    // about a third of the SMs compute the router rows, so most of the GPU is
+    // free for the gate/up kernel's shared-expert rows while routing runs
+    const int r_ctas = std::max(16, I.sms / 3);
+    G.r_rows = (n + r_ctas - 1) / r_ctas;
     G.r_grid = (n + G.r_rows - 1) / G.r_rows;
     G.r_smem = router_smem(G.r_rows, dim, m);
     G.grid = I.sms;
     // gate/up: stages of max(one Q2_K task, one bf16 row)
     G.g_stage = (uint32_t)align_up(std::max<size_t>((size_t)MOE_G_TASK_SB * MOE_Q2K_BYTES, (size_t)dim * 2), 128);
-    size_t g_fixed = align_up((size_t)m * act_row_bytes(dim), 128) + (shared ? align_up((size_t)m * dim * 2, 128) : 0);
+    size_t g_fixed = align_up((size_t)m * act_row_bytes(dim), 128) + align_up((size_t)m * dim * 2, 128);
     G.g_S = stages_fit(g_fixed, G.g_stage, 32, limit);
     G.g_smem = g_smem_bytes(G.g_S, m, dim, shared, G.g_stage);
     // down: stages of max(one Q3_K task, one bf16 row)
@@ -183,7 +187,7 @@ int geometry(const moe_cfg &c, int m, bool shared, const DevInfo &I, Geo &G)
 
 struct Bufs {
     const uint16_t *x;
-    float *logits;
+    float *logits, *scores, *keys;
     int32_t *hdr;
     float *plan_w;
     int32_t *plan_rows;
@@ -200,6 +204,8 @@ Bufs ws_bufs(const moe_cfg &c, void *ws)
     B.ctrl = reinterpret_cast<uint32_t *>(b + L.ctrl);
     B.rgcnt = reinterpret_cast<uint32_t *>(b + L.rgcnt);
     B.logits = reinterpret_cast<float *>(b + L.logits);
+    B.scores = reinterpret_cast<float *>(b + L.scores);
+    B.keys = reinterpret_cast<float *>(b + L.keys);
     B.plan_w = reinterpret_cast<float *>(b + L.plan_w);
     B.plan_rows = reinterpret_cast<int32_t *>(b + L.plan_rows);
     B.ptrs = reinterpret_cast<unsigned long long *>(b + L.ptrs);
@@ -267,6 +273,7 @@ int launch_experts(const moe_cfg &c, int m, const Geo &G, const Bufs &B, const u
     ga.gs = B.gs;
     ga.us = B.us;
     ga.status = B.ctrl + MOE_CTRL_STATUS;
+    ga.gctr = B.ctrl + MOE_CTRL_GATEUP;
     ga.dim = c.dim;
     ga.inter = c.inter;
     ga.m = m;
@@ -330,6 +337,8 @@ int layer_step(const moe_cfg &c, const moe_layer &ly, const moe_arena &ar, const
     ra.x = static_cast<const uint16_t *>(x);
     ra.w = static_cast<const uint16_t *>(ly.router_w);
     ra.logits = B.logits;
+    ra.scores = B.scores;
+    ra.keys = B.keys;
     ra.rows_per_cta = G.r_rows;
     ra.do_select = 1;
     ra.bias = ly.bias;
@@ -524,7 +533,11 @@ int moe_route_select(const moe_cfg *cfg, const float *logits, const float *bias,
     a.plan_w = plan_w;
     a.plan_rows = plan_rows;
     a.ptrs = reinterpret_cast<unsigned long long *>(ptrs);
-    return launch(moe_select_kernel, dim3(1), dim3(256), 0, (cudaStream_t)stream, false, a);
+    DevInfo *I;
+    if ((rc = dev_info(&I)))
+        return rc;
+    const size_t smem = align_up(sizeof(SelectSmem), 128) + sizeof(float) * 2 * (size_t)m * cfg->n_routed;
+    return launch(moe_select_kernel, dim3(1), dim3(256), smem, (cudaStream_t)stream, false, a);
 }
 
 int moe_expert_step(const moe_cfg *cfg, const void *x, const uint64_t *ptrs, const float *plan_w,

@@ -22,10 +22,12 @@
 #define MOE_WAIT_NS 2000000000ull  // 2 s bound on any single wait
 
 // one Q2_K task = 128 super-blocks of one matrix (10752 B); one Q3_K task =
-// 32 super-blocks (3520 B). Both sizes are multiples of 16 so the bulk copies
+// 64 super-blocks (7040 B). Both sizes are multiples of 16 so the bulk copies
 // of whole tasks stay 16-byte aligned for every supported shape.
 #define MOE_G_TASK_SB 128
-#define MOE_D_TASK_SB 32
+#define MOE_D_TASK_SB 64
+#define MOE_PRODUCER_LANES 8
+#define MOE_G_CHUNK 4  // gate/up tasks taken per grab from the grid-wide counters
 // activation layout in shared memory: per 256-value segment, 256 int8 quants
 // padded to 272 bytes, and a 28-float scale record (8 block scales d8, then
 // 16 per-sub-block values), so lanes on different segments hit different banks
@@ -40,7 +42,7 @@ namespace moe {
 // ------------------------------------------------------------------ layout
 
 struct WsLayout {
-    size_t ctrl, rgcnt, logits, plan_w, plan_rows, ptrs, g, u, gs, us, down, sd, acc, total;
+    size_t ctrl, rgcnt, logits, scores, keys, plan_w, plan_rows, ptrs, g, u, gs, us, down, sd, acc, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -57,6 +59,8 @@ inline WsLayout ws_layout(const moe_cfg &c)
     L.ctrl = take(256);
     L.rgcnt = take(sizeof(uint32_t) * (size_t)(c.dim / down_rows_per_task(c.inter)));
     L.logits = take(sizeof(float) * M * c.n_routed);
+    L.scores = take(sizeof(float) * M * c.n_routed);
+    L.keys = take(sizeof(float) * M * c.n_routed);
     L.plan_w = take(sizeof(float) * cap);
     L.plan_rows = take(sizeof(int32_t) * cap);
     L.ptrs = take(sizeof(uint64_t) * 3 * cap);
@@ -74,6 +78,7 @@ inline WsLayout ws_layout(const moe_cfg &c)
 // control words at ws + ctrl
 #define MOE_CTRL_TICKET 0
 #define MOE_CTRL_STATUS 1
+#define MOE_CTRL_GATEUP 2  // 3 words: gate/up task counters and exit ticket
 
 inline int header_words(int m, int k) { return m * (1 + 3 * k) + 2 + 2 * m * k; }
 

@@ -98,6 +98,10 @@ __device__ __forceinline__ uint32_t byte_of(const uint32_t *w, int i) { return (
 // Q2_K super-block (84 bytes, 4-byte aligned in shared memory) against a
 // q8_1 segment: d * sum_b d8_b (sc_2b dot_2b + sc_2b+1 dot_2b+1)
 //               - dmin * sum_s min_s * d8 * sum(q8 of s)
+// The 2-bit fields g < 3 of a byte are masked in place (value 4^g q <= 48,
+// still a non-negative signed byte) and the 4^g is shifted out of the
+// integer sum afterwards (exact: the sum is a multiple of 4^g), which saves a
+// shift per weight word; field 3 is shifted down first.
 __device__ __forceinline__ float q2k_dot(const uint32_t *blk, const int4 *xq, const float4 *rec)
 {
     uint32_t sc[4];
@@ -126,99 +130,104 @@ __device__ __forceinline__ float q2k_dot(const uint32_t *blk, const int4 *xq, co
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
             const int4 xa = xq[8 * h + 2 * g], xb = xq[8 * h + 2 * g + 1];
-            const int sh = 2 * g;
-            int s0 = __dp4a((int)((q[0] >> sh) & 0x03030303u), xa.x, 0);
-            s0 = __dp4a((int)((q[1] >> sh) & 0x03030303u), xa.y, s0);
-            s0 = __dp4a((int)((q[2] >> sh) & 0x03030303u), xa.z, s0);
-            s0 = __dp4a((int)((q[3] >> sh) & 0x03030303u), xa.w, s0);
-            int s1 = __dp4a((int)((q[4] >> sh) & 0x03030303u), xb.x, 0);
-            s1 = __dp4a((int)((q[5] >> sh) & 0x03030303u), xb.y, s1);
-            s1 = __dp4a((int)((q[6] >> sh) & 0x03030303u), xb.z, s1);
-            s1 = __dp4a((int)((q[7] >> sh) & 0x03030303u), xb.w, s1);
+            const int pre = g == 3 ? 6 : 0, post = g == 3 ? 0 : 2 * g;
+            const uint32_t msk = 0x03030303u << (2 * g - pre);
+            int s0 = __dp4a((int)((q[0] >> pre) & msk), xa.x, 0);
+            s0 = __dp4a((int)((q[1] >> pre) & msk), xa.y, s0);
+            s0 = __dp4a((int)((q[2] >> pre) & msk), xa.z, s0);
+            s0 = __dp4a((int)((q[3] >> pre) & msk), xa.w, s0);
+            int s1 = __dp4a((int)((q[4] >> pre) & msk), xb.x, 0);
+            s1 = __dp4a((int)((q[5] >> pre) & msk), xb.y, s1);
+            s1 = __dp4a((int)((q[6] >> pre) & msk), xb.z, s1);
+            s1 = __dp4a((int)((q[7] >> pre) & msk), xb.w, s1);
             const int sub = 8 * h + 2 * g;
-            const int isum = (int)(byte_of(sc, sub) & 15u) * s0 + (int)(byte_of(sc, sub + 1) & 15u) * s1;
+            const int isum = ((int)(byte_of(sc, sub) & 15u) * s0 + (int)(byte_of(sc, sub + 1) & 15u) * s1) >> post;
             main = fmaf(d8[4 * h + g], (float)isum, main);
         }
     }
     return f16_bits_to_f32(dd) * main - f16_bits_to_f32(dd >> 16) * mn;
 }
 
-// Q3_K super-block (110 bytes, 2-byte aligned in shared memory) against a
-// q8_1 segment: d * sum_b d8_b (sc_2b (dot_2b - 4 sum_2b) + sc_2b+1 (...)),
-// the quants taken as q + 4 in [0, 7] for dp4a and the offset removed. The
-// block's 32-bit fields are read from the aligned words around it and shifted
-// into place (the block starts 0 or 2 bytes past a word boundary).
-__device__ __forceinline__ float q3k_dot(const uint8_t *blk, const int4 *xq, const float4 *rec)
+// PER Q3_K super-blocks of one lane sharing the same activation columns
+// (as q3k_dot, the activation's quants and scale records loaded once)
+template <int PER>
+__device__ __forceinline__ void q3k_dot_multi(const uint8_t *st, int lane, const int4 *xq, const float4 *rec,
+                                              float (&out)[PER])
 {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(blk);
-    const uint32_t *W = reinterpret_cast<const uint32_t *>(a & ~(uintptr_t)3);
-    const uint32_t sh = (uint32_t)(a & 3) * 8u;  // 0 or 16
-    uint32_t hm[8];
-    {
+    const uint32_t *W[PER];
+    uint32_t sh[PER], hm[PER][8], scw[PER][3];
+    float d[PER], acc[PER];
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(st + (size_t)(lane + 32 * q) * MOE_Q3K_BYTES);
+        W[q] = reinterpret_cast<const uint32_t *>(a & ~(uintptr_t)3);
+        sh[q] = (uint32_t)(a & 3) * 8u;
         uint32_t w[9];
 #pragma unroll
         for (int i = 0; i < 9; ++i)
-            w[i] = W[i];
+            w[i] = W[q][i];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            hm[i] = __funnelshift_r(w[i], w[i + 1], sh);
-    }
-    uint32_t scw[3];
-    float d;
-    {
-        const uint32_t w24 = W[24], w25 = W[25], w26 = W[26], w27 = W[27];
-        scw[0] = __funnelshift_r(w24, w25, sh);
-        scw[1] = __funnelshift_r(w25, w26, sh);
-        scw[2] = __funnelshift_r(w26, w27, sh);
-        d = f16_bits_to_f32(w27 >> sh);
+            hm[q][i] = __funnelshift_r(w[i], w[i + 1], sh[q]);
+        const uint32_t w24 = W[q][24], w25 = W[q][25], w26 = W[q][26], w27 = W[q][27];
+        scw[q][0] = __funnelshift_r(w24, w25, sh[q]);
+        scw[q][1] = __funnelshift_r(w25, w26, sh[q]);
+        scw[q][2] = __funnelshift_r(w26, w27, sh[q]);
+        d[q] = f16_bits_to_f32(w27 >> sh[q]);
+        acc[q] = 0.0f;
     }
     const float4 da = rec[0], db = rec[1];
     const float d8[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
-    float acc = 0.0f;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        uint32_t q[8];
-        {
-            uint32_t w[9];
-#pragma unroll
-            for (int i = 0; i < 9; ++i)
-                w[i] = W[8 + 8 * h + i];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                q[i] = __funnelshift_r(w[i], w[i + 1], sh);
-        }
         const float4 sqa = rec[2 + 2 * h], sqb = rec[3 + 2 * h];  // sums of sub-blocks 8h .. 8h+7
         const int sq[8] = {__float_as_int(sqa.x), __float_as_int(sqa.y), __float_as_int(sqa.z),
                            __float_as_int(sqa.w), __float_as_int(sqb.x), __float_as_int(sqb.y),
                            __float_as_int(sqb.z), __float_as_int(sqb.w)};
+        uint32_t qv[PER][8];
+#pragma unroll
+        for (int q = 0; q < PER; ++q) {
+            uint32_t w[9];
+#pragma unroll
+            for (int i = 0; i < 9; ++i)
+                w[i] = W[q][8 + 8 * h + i];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                qv[q][i] = __funnelshift_r(w[i], w[i + 1], sh[q]);
+        }
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
             const int4 xa = xq[8 * h + 2 * g], xb = xq[8 * h + 2 * g + 1];
             const int qsh = 2 * g, hsh = 4 * h + g;
-            int v[8];
-#pragma unroll
-            for (int w = 0; w < 8; ++w)
-                v[w] = (int)(((q[w] >> qsh) & 0x03030303u) | (((hm[w] >> hsh) & 0x01010101u) << 2));
-            int s0 = __dp4a(v[0], xa.x, 0);
-            s0 = __dp4a(v[1], xa.y, s0);
-            s0 = __dp4a(v[2], xa.z, s0);
-            s0 = __dp4a(v[3], xa.w, s0);
-            int s1 = __dp4a(v[4], xb.x, 0);
-            s1 = __dp4a(v[5], xb.y, s1);
-            s1 = __dp4a(v[6], xb.z, s1);
-            s1 = __dp4a(v[7], xb.w, s1);
             const int i0 = 8 * h + 2 * g, i1 = i0 + 1;
-            // 6-bit scales i0, i1: low 4 bits from byte i (i < 8) or the high
-            // nibble of byte i - 8; high 2 bits at 2 * (i / 4) in byte 8 + i % 4
-            const int sc0 = (int)((i0 < 8 ? (byte_of(scw, i0) & 15u) : (byte_of(scw, i0 - 8) >> 4)) |
-                                  (((byte_of(scw, 8 + (i0 & 3)) >> (2 * (i0 >> 2))) & 3u) << 4)) - 32;
-            const int sc1 = (int)((i1 < 8 ? (byte_of(scw, i1) & 15u) : (byte_of(scw, i1 - 8) >> 4)) |
-                                  (((byte_of(scw, 8 + (i1 & 3)) >> (2 * (i1 >> 2))) & 3u) << 4)) - 32;
-            const int isum = sc0 * (s0 - 4 * sq[2 * g]) + sc1 * (s1 - 4 * sq[2 * g + 1]);
-            acc = fmaf(d8[4 * h + g], (float)isum, acc);
+#pragma unroll
+            for (int q = 0; q < PER; ++q) {
+                int v[8];
+#pragma unroll
+                for (int w = 0; w < 8; ++w)
+                    v[w] = (int)(((qv[q][w] >> qsh) & 0x03030303u) | (((hm[q][w] >> hsh) & 0x01010101u) << 2));
+                int s0 = __dp4a(v[0], xa.x, 0);
+                s0 = __dp4a(v[1], xa.y, s0);
+                s0 = __dp4a(v[2], xa.z, s0);
+                s0 = __dp4a(v[3], xa.w, s0);
+                int s1 = __dp4a(v[4], xb.x, 0);
+                s1 = __dp4a(v[5], xb.y, s1);
+                s1 = __dp4a(v[6], xb.z, s1);
+                s1 = __dp4a(v[7], xb.w, s1);
+                // 6-bit scales i0, i1: low 4 bits from byte i (i < 8) or the high
+                // nibble of byte i - 8; high 2 bits at 2 * (i / 4) in byte 8 + i % 4
+                const int sc0 = (int)((i0 < 8 ? (byte_of(scw[q], i0) & 15u) : (byte_of(scw[q], i0 - 8) >> 4)) |
+                                      (((byte_of(scw[q], 8 + (i0 & 3)) >> (2 * (i0 >> 2))) & 3u) << 4)) - 32;
+                const int sc1 = (int)((i1 < 8 ? (byte_of(scw[q], i1) & 15u) : (byte_of(scw[q], i1 - 8) >> 4)) |
+                                      (((byte_of(scw[q], 8 + (i1 & 3)) >> (2 * (i1 >> 2))) & 3u) << 4)) - 32;
+                const int isum = sc0 * (s0 - 4 * sq[2 * g]) + sc1 * (s1 - 4 * sq[2 * g + 1]);
+                acc[q] = fmaf(d8[4 * h + g], (float)isum, acc[q]);
+            }
         }
     }
-    return d * acc;
+#pragma unroll
+    for (int q = 0; q < PER; ++q)
+        out[q] = d[q] * acc[q];
 }
 
 // ------------------------------------------------------------------ pipeline helpers
@@ -332,21 +341,47 @@ __device__ __forceinline__ bool ring_acquire(const Ring &r, int j, uint32_t *sta
     return mbar_wait(&r.full[slot], (uint32_t)(j / r.S) & 1u, status);
 }
 
-// the producer warp caches the plan (all 32 lanes load in parallel); `which`
-// selects the pointer rows to keep (gate/up: 0 and 1, down: 2)
+// the producer warp caches the plan (all 32 lanes load in parallel, one
+// round of independent loads); `which` selects the pointer rows to keep
+// (gate/up: 0 and 1, down: 2)
 __device__ __forceinline__ void cache_plan(const Ring &r, const int32_t *hdr, int plan_off, const int32_t *plan_rows,
                                            const unsigned long long *ptrs, int cap, int which0, int nwhich)
 {
     const int lane = threadIdx.x & 31;
     PlanCache &pc = *r.pc;
+    int ps[3], rw[2];
+    unsigned long long pt[2][2];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        const int i = lane + 32 * j;
+        ps[j] = i <= cap ? __ldcg(hdr + plan_off + 1 + i) : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int i = lane + 32 * j;
+        rw[j] = i < cap ? __ldcg(plan_rows + i) : 0;
+#pragma unroll
+        for (int w = 0; w < 2; ++w)
+            pt[j][w] = (i < cap && w < nwhich) ? __ldcg(ptrs + (size_t)(which0 + w) * cap + i) : 0ull;
+    }
     const int ne = min(max(__ldcg(hdr + plan_off), 0), cap);
-    for (int i = lane; i <= ne; i += 32)
-        pc.pair_start[i] = min(max(__ldcg(hdr + plan_off + 1 + i), 0), cap);
-    for (int i = lane; i < cap; i += 32)
-        pc.rows[i] = min(max(__ldcg(plan_rows + i), 0), MOE_MAX_TOKENS - 1);
-    for (int i = lane; i < ne; i += 32)
-        for (int w = 0; w < nwhich; ++w)
-            pc.ptr[w][i] = __ldcg(ptrs + (size_t)(which0 + w) * cap + i);
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        const int i = lane + 32 * j;
+        if (i <= cap)
+            pc.pair_start[i] = min(max(ps[j], 0), cap);
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int i = lane + 32 * j;
+        if (i < cap) {
+            pc.rows[i] = min(max(rw[j], 0), MOE_MAX_TOKENS - 1);
+#pragma unroll
+            for (int w = 0; w < 2; ++w)
+                if (w < nwhich)
+                    pc.ptr[w][i] = pt[j][w];
+        }
+    }
     if (lane == 0)
         pc.ne = ne;
     __syncwarp();
@@ -363,6 +398,7 @@ struct GArgs {
     float *g, *u;                      // [cap, inter]
     float *gs, *us;                    // [m, inter]
     uint32_t *status;
+    uint32_t *gctr;                    // [0] shared-task counter, [1] routed-task counter, [2] exit ticket
     int dim, inter, m, k, cap, plan_off, S;
     uint32_t stage_bytes;
 };
@@ -371,7 +407,8 @@ __host__ __device__ inline size_t g_act_off(int S) { return ring_head_bytes(S); 
 __host__ __device__ inline size_t g_xs_off(int S, int m, int dim) { return g_act_off(S) + align_up((size_t)m * act_row_bytes(dim), 128); }
 __host__ __device__ inline size_t g_stage_off(int S, int m, int dim, bool shared)
 {
-    return g_xs_off(S, m, dim) + (shared ? align_up((size_t)m * dim * 2, 128) : 0);
+    (void)shared;  // x is staged in shared memory whether or not a shared expert runs
+    return g_xs_off(S, m, dim) + align_up((size_t)m * dim * 2, 128);
 }
 __host__ __device__ inline size_t g_smem_bytes(int S, int m, int dim, bool shared, uint32_t stage_bytes)
 {
@@ -392,82 +429,120 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
     __syncthreads();
 
     if (warp == MOE_CONSUMER_WARPS) {
-        // ---------------- producer warp
+        // ---------------- producer warp. Tasks are taken in chunks of
+        // MOE_G_CHUNK from grid-wide counters (a CTA that starts late -- its
+        // SM still busy with the previous kernel -- simply takes fewer);
+        // MOE_PRODUCER_LANES lanes issue a chunk's tasks in parallel.
         const uint64_t pol = policy_evict_first();
-        int i = 0;
+        const int P = min(MOE_PRODUCER_LANES, ring.S);
+        const bool issuer = lane < P;
+        int base = 0;  // index of the next task in this CTA's ring
         bool ok = true;
-        if (shared && lane == 0) {
+        if (shared) {
             // the shared expert's rows depend only on x: issued before the wait
             const int nsh = 2 * inter;
-            const int lo = (int)((long long)blockIdx.x * nsh / gridDim.x);
-            const int hi = (int)((long long)(blockIdx.x + 1) * nsh / gridDim.x);
-            for (int s = lo; s < hi && ok; ++s) {
-                Task t{};
-                t.kind = 2;
-                t.mat = s / inter;
-                t.row = s % inter;
-                const uint16_t *src = (t.mat ? a.w3 : a.w1) + (size_t)t.row * dim;
-                ok = ring_issue(ring, i++, t, src, (uint32_t)dim * 2u, pol, a.status);
+            unsigned nxt = 0;
+            if (lane == 0)
+                nxt = atomicAdd(a.gctr + 0, (unsigned)MOE_G_CHUNK);
+            for (;;) {
+                const int c0 = (int)__shfl_sync(0xffffffffu, nxt, 0);
+                if (c0 >= nsh || !ok)
+                    break;
+                if (lane == 0)
+                    nxt = atomicAdd(a.gctr + 0, (unsigned)MOE_G_CHUNK);  // the next chunk, in flight meanwhile
+                const int c1 = min(c0 + MOE_G_CHUNK, nsh);
+                for (int b = c0; b < c1 && ok; b += P) {
+                    const int sidx = b + lane;
+                    bool mine = true;
+                    if (issuer && sidx < c1) {
+                        Task t{};
+                        t.kind = 2;
+                        t.mat = sidx / inter;
+                        t.row = sidx % inter;
+                        const uint16_t *src = (t.mat ? a.w3 : a.w1) + (size_t)t.row * dim;
+                        mine = ring_issue(ring, base + (sidx - c0), t, src, (uint32_t)dim * 2u, pol, a.status);
+                    }
+                    ok = __all_sync(0xffffffffu, mine);
+                }
+                base += c1 - c0;
             }
         }
-        __syncwarp();
         pdl_wait();  // the selection has written the plan and the pointer table
         pdl_launch_dependents();
         cache_plan(ring, a.hdr, a.plan_off, a.plan_rows, a.ptrs, a.cap, 0, 2);
-        if (lane == 0) {
-            const PlanCache &pc = *ring.pc;
-            const int rt = gate_rows_per_task(dim);
-            const int tpm = inter / rt;  // tasks per matrix
-            const long long total = (long long)pc.ne * 2 * tpm;
-            const int lo = (int)(blockIdx.x * total / gridDim.x);
-            const int hi = (int)((blockIdx.x + 1) * total / gridDim.x);
-            const uint32_t bytes = (uint32_t)(rt * nb * MOE_Q2K_BYTES);
-            // walk (expert, matrix, row run) from lo without per-task divisions
-            int p = lo / (2 * tpm), mat = (lo / tpm) & 1, r = lo % tpm;
-            for (int tix = lo; tix < hi && ok; ++tix) {
-                Task t{};
-                t.kind = 1;
-                t.p = p;
-                t.mat = mat;
-                t.row = r * rt;
-                t.pair0 = pc.pair_start[p];
-                t.npair = pc.pair_start[p + 1] - t.pair0;
-                if (t.npair >= 1 && t.npair <= a.m) {
-                    const char *src = reinterpret_cast<const char *>(pc.ptr[mat][p]) + (size_t)r * bytes;
-                    ok = ring_issue(ring, i++, t, src, bytes, pol, a.status);
-                } else {
-                    atomicOr(a.status, (uint32_t)MOE_WS_PLAN);
-                }
-                if (++r == tpm) {
-                    r = 0;
-                    if (++mat == 2) {
-                        mat = 0;
-                        ++p;
+        const PlanCache &pc = *ring.pc;
+        const int rt = gate_rows_per_task(dim);
+        const int tpm = inter / rt;  // tasks per matrix
+        const int total = pc.ne * 2 * tpm;
+        const uint32_t bytes = (uint32_t)(rt * nb * MOE_Q2K_BYTES);
+        unsigned nxt = 0;
+        if (lane == 0)
+            nxt = atomicAdd(a.gctr + 1, (unsigned)MOE_G_CHUNK);
+        for (;;) {
+            const int c0 = (int)__shfl_sync(0xffffffffu, nxt, 0);
+            if (c0 >= total || !ok)
+                break;
+            if (lane == 0)
+                nxt = atomicAdd(a.gctr + 1, (unsigned)MOE_G_CHUNK);
+            const int c1 = min(c0 + MOE_G_CHUNK, total);
+            for (int b = c0; b < c1 && ok; b += P) {
+                const int tix = b + lane;
+                bool mine = true;
+                if (issuer && tix < c1) {
+                    Task t{};
+                    t.kind = 1;
+                    t.p = tix / (2 * tpm);
+                    t.mat = (tix / tpm) & 1;
+                    const int r = tix % tpm;
+                    t.row = r * rt;
+                    t.pair0 = pc.pair_start[t.p];
+                    t.npair = pc.pair_start[t.p + 1] - t.pair0;
+                    uint32_t nbytes = bytes;
+                    if (t.npair < 1 || t.npair > a.m) {
+                        atomicOr(a.status, (uint32_t)MOE_WS_PLAN);
+                        t.npair = 0;  // a no-op task keeps the indices contiguous
+                        nbytes = 0;
                     }
+                    const char *src = reinterpret_cast<const char *>(pc.ptr[t.mat][t.p]) + (size_t)r * bytes;
+                    mine = ring_issue(ring, base + (tix - c0), t, src, nbytes, pol, a.status);
                 }
+                ok = __all_sync(0xffffffffu, mine);
             }
-            for (int w = 0; w < MOE_CONSUMER_WARPS && ok; ++w) {
+            base += c1 - c0;
+        }
+        for (int b = 0; b < MOE_CONSUMER_WARPS && ok; b += P) {
+            bool mine = true;
+            if (issuer && b + lane < MOE_CONSUMER_WARPS) {
                 Task t{};
                 t.kind = 0;
-                ok = ring_issue(ring, i++, t, nullptr, 0, pol, a.status);
+                mine = ring_issue(ring, base + b + lane, t, nullptr, 0, pol, a.status);
             }
+            ok = __all_sync(0xffffffffu, mine);
+        }
+        // the last producer to finish taking tasks resets the counters
+        if (lane == 0 && atomicAdd(a.gctr + 2, 1u) == gridDim.x - 1) {
+            atomicExch(a.gctr + 0, 0u);
+            atomicExch(a.gctr + 1, 0u);
+            atomicExch(a.gctr + 2, 0u);
         }
         return;
     }
 
     // ---------------- consumers: the activation first (x is ready: the
-    // previous kernel in the stream let this one start only after its own wait)
-    const int nblk = a.m * dim / 32;
-    for (int b = warp; b < nblk; b += MOE_CONSUMER_WARPS) {
-        const int t = b / (dim / 32), bi = b % (dim / 32);
-        const float v = bf16_to_f32(__ldcg(a.x + (size_t)t * dim + bi * 32 + lane));
-        q8_store_smem(act + t * arow, nb, bi, q8_quant_warp(v), true);
-    }
-    if (shared) {
+    // previous kernel in the stream let this one start only after its own
+    // wait). x is staged with all loads in flight, then quantised from smem.
+    {
         const uint4 *gx = reinterpret_cast<const uint4 *>(a.x);
         uint4 *s4 = reinterpret_cast<uint4 *>(xs);
         for (int i = threadIdx.x; i < a.m * dim / 8; i += MOE_CONSUMER_WARPS * 32)
             s4[i] = __ldcg(gx + i);
+    }
+    consumers_sync();
+    const int nblk = a.m * dim / 32;
+    for (int b = warp; b < nblk; b += MOE_CONSUMER_WARPS) {
+        const int t = b / (dim / 32), bi = b % (dim / 32);
+        const float v = bf16_to_f32(xs[(size_t)t * dim + bi * 32 + lane]);
+        q8_store_smem(act + t * arow, nb, bi, q8_quant_warp(v), true);
     }
     consumers_sync();
 
@@ -694,39 +769,41 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
 
     if (warp == MOE_CONSUMER_WARPS) {
         // ---------------- producer warp: everything it loads depends only on
-        // the pointer table, so the whole range is issued before the wait
+        // the pointer table, so the whole range is issued before the wait;
+        // MOE_PRODUCER_LANES lanes issue consecutive tasks in parallel
         pdl_launch_dependents();
         cache_plan(ring, a.hdr, a.plan_off, a.plan_rows, a.ptrs, a.cap, 2, 1);
-        if (lane == 0) {
-            const PlanCache &pc = *ring.pc;
-            const uint64_t pol = policy_evict_first();
-            int i = 0;
-            bool ok = true;
-            const bool fits = R.pair_hi - R.pair_lo <= a.pair_cap;
-            if (!fits)
-                atomicOr(a.status, (uint32_t)MOE_WS_PLAN);
-            const uint32_t rbytes = (uint32_t)(rd * nb * MOE_Q3K_BYTES);
-            const int end = fits ? R.hi : R.lo;
-            int p = R.lo / R.tpr, r = R.lo % R.tpr;
-            for (int tix = R.lo; tix < end && ok; ++tix) {
+        const PlanCache &pc = *ring.pc;
+        const uint64_t pol = policy_evict_first();
+        const int P = min(MOE_PRODUCER_LANES, ring.S);
+        const bool issuer = lane < P;
+        bool ok = true;
+        const bool fits = R.pair_hi - R.pair_lo <= a.pair_cap;
+        if (!fits && lane == 0)
+            atomicOr(a.status, (uint32_t)MOE_WS_PLAN);
+        const uint32_t rbytes = (uint32_t)(rd * nb * MOE_Q3K_BYTES);
+        for (int b = R.lo; b < R.hi && ok; b += P) {
+            const int tix = b + lane;
+            bool mine = true;
+            if (issuer && tix < R.hi) {
                 Task t{};
-                const void *src;
+                const void *src = nullptr;
                 uint32_t bytes;
                 if (tix < R.Tr) {
                     t.kind = 1;
-                    t.p = p;
+                    t.p = tix / R.tpr;
+                    const int r = tix % R.tpr;
                     t.row = r * rd;
-                    t.pair0 = pc.pair_start[p];
-                    t.npair = pc.pair_start[p + 1] - t.pair0;
-                    if (t.npair < 1 || t.npair > a.m || t.pair0 < R.pair_lo || t.pair0 + t.npair > R.pair_hi) {
-                        atomicOr(a.status, (uint32_t)MOE_WS_PLAN);
-                        t.npair = 0;  // issued (the row group's ticket still counts it), computes nothing
-                    }
-                    src = reinterpret_cast<const char *>(pc.ptr[0][p]) + (size_t)r * rbytes;
+                    t.pair0 = pc.pair_start[t.p];
+                    t.npair = pc.pair_start[t.p + 1] - t.pair0;
                     bytes = rbytes;
-                    if (++r == R.tpr) {
-                        r = 0;
-                        ++p;
+                    src = reinterpret_cast<const char *>(pc.ptr[0][t.p]) + (size_t)r * rbytes;
+                    if (!fits || t.npair < 1 || t.npair > a.m || t.pair0 < R.pair_lo ||
+                        t.pair0 + t.npair > R.pair_hi) {
+                        if (fits)
+                            atomicOr(a.status, (uint32_t)MOE_WS_PLAN);
+                        t.npair = 0;  // a no-op task: still counted by its row group
+                        bytes = 0;
                     }
                 } else {
                     t.kind = 2;
@@ -734,13 +811,19 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
                     src = a.w2 + (size_t)t.row * inter;
                     bytes = (uint32_t)inter * 2u;
                 }
-                ok = ring_issue(ring, i++, t, src, bytes, pol, a.status);
+                mine = ring_issue(ring, tix - R.lo, t, src, bytes, pol, a.status);
             }
-            for (int w = 0; w < MOE_CONSUMER_WARPS && ok; ++w) {
+            ok = __all_sync(0xffffffffu, mine);
+        }
+        const int base = R.hi - R.lo;
+        for (int b = 0; b < MOE_CONSUMER_WARPS && ok; b += P) {
+            bool mine = true;
+            if (issuer && b + lane < MOE_CONSUMER_WARPS) {
                 Task t{};
                 t.kind = 0;
-                ok = ring_issue(ring, i++, t, nullptr, 0, pol, a.status);
+                mine = ring_issue(ring, base + b + lane, t, nullptr, 0, pol, a.status);
             }
+            ok = __all_sync(0xffffffffu, mine);
         }
         return;
     }
@@ -793,20 +876,30 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
         }
         const uint8_t *st = ring.at(slot);
         if (t.kind == 1) {
-            // 32 super-blocks: lane = (row lane / nb, block lane % nb); one
-            // token (plan pair) at a time
+            // MOE_D_TASK_SB super-blocks: lane covers super-blocks lane + 32 q
+            // (row (lane + 32 q) / nb, block lane % nb); one token (plan pair)
+            // at a time
+            constexpr int PER = MOE_D_TASK_SB / 32;
             const int blk = lane % nb;
-            const uint8_t *bp = st + (size_t)lane * MOE_Q3K_BYTES;
 #pragma unroll 1
             for (int tt = 0; tt < t.npair; ++tt) {
                 const uint8_t *xr = act + (t.pair0 + tt - R.pair_lo) * arow;
-                float v = q3k_dot(bp, reinterpret_cast<const int4 *>(xr + blk * MOE_SEG_Q_BYTES),
-                                  reinterpret_cast<const float4 *>(xr + nb * MOE_SEG_Q_BYTES) +
-                                      blk * (MOE_SEG_REC_FLOATS / 4));
-                for (int o = nb >> 1; o > 0; o >>= 1)
-                    v += __shfl_xor_sync(0xffffffffu, v, o);
-                if (blk == 0)
-                    a.down[(size_t)(t.pair0 + tt) * dim + t.row + lane / nb] = v;
+                const int4 *xq = reinterpret_cast<const int4 *>(xr + blk * MOE_SEG_Q_BYTES);
+                const float4 *rec = reinterpret_cast<const float4 *>(xr + nb * MOE_SEG_Q_BYTES) +
+                                    blk * (MOE_SEG_REC_FLOATS / 4);
+                float v[PER];
+                q3k_dot_multi<PER>(st, lane, xq, rec, v);
+                for (int o = nb >> 1; o > 0; o >>= 1) {
+#pragma unroll
+                    for (int q = 0; q < PER; ++q)
+                        v[q] += __shfl_xor_sync(0xffffffffu, v[q], o);
+                }
+                if (blk == 0) {
+                    float *orow = a.down + (size_t)(t.pair0 + tt) * dim + t.row;
+#pragma unroll
+                    for (int q = 0; q < PER; ++q)
+                        orow[(lane + 32 * q) / nb] = v[q];
+                }
             }
             __syncwarp();
             if (lane == 0)

@@ -27,6 +27,8 @@ struct RouteArgs {
     const uint16_t *x;  // bf16 [m, dim]
     const uint16_t *w;  // bf16 [n, dim]
     float *logits;      // f32 [m, n]
+    float *scores;      // f32 [m, n]: exact scores (written by the router when selecting)
+    float *keys;        // f32 [m, n]: score + bias
     int dim, n, m, rows_per_cta;
     // selection
     int do_select;
@@ -45,173 +47,51 @@ struct RouteArgs {
 
 // ------------------------------------------------------------------ scores
 
-__device__ __forceinline__ float score_approx(float t)
+// The score as defined: the f32 rounding of sqrt(softplus(t)), t = f32(l / temp),
+// softplus(x) = x for x > 20. Evaluated in f64 (CUDA's exp, log1p, sqrt) and
+// rounded once: the f64 chain's error is far below half an f32 ulp, so the
+// rounding equals the exact one except within ~2^-50 of an f32 midpoint.
+__device__ __forceinline__ float score_exact(float l, float temp)
 {
-    float sp = t > 20.0f ? t : log1pf(expf(t));
-    return sqrtf(sp);
-}
-
-__device__ __forceinline__ float score_exact(float t)
-{
-    double sp = t > 20.0f ? (double)t : log1p(exp((double)t));
+    const float t = __fdiv_rn(l, temp);
+    const double sp = t > 20.0f ? (double)t : log1p(exp((double)t));
     return __double2float_rn(sqrt(sp));
 }
 
-// |score_approx - score_exact| plus the key rounding, with a wide margin
-// (the single-precision chain is within ~3 ulp; this allows 32 ulp relative
-// on the score, 4 ulp on the key, and an absolute floor for subnormal exp).
-__device__ __forceinline__ float key_bound(float s, float key)
+// ------------------------------------------------------------------ sortable keys
+
+// One 64-bit value per expert that orders exactly as "ranks before": the key
+// mapped to an unsigned integer that grows with it (-0 equal to +0, NaN below
+// every number), then the complement of the id so equal keys put the lower id
+// first. 0 (a NaN key with id 2^32 - 1) pads empty slots and ranks last.
+__device__ __forceinline__ unsigned long long rank_value(float key, int id)
 {
-    return s * 0x1p-18f + fabsf(key) * 0x1p-21f + 0x1p-60f;
+    uint32_t u;
+    if (isnan(key)) {
+        u = 0u;
+    } else {
+        uint32_t b = key == 0.0f ? 0u : __float_as_uint(key);
+        u = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    }
+    return ((unsigned long long)u << 32) | (0xFFFFFFFFu - (uint32_t)id);
 }
 
-// a ranks before b: larger key first; NaN keys after all numbers; equal keys
-// (and two NaNs) by ascending id
-__device__ __forceinline__ bool ranks_before(float ka, int ia, float kb, int ib)
-{
-    bool na = isnan(ka), nb = isnan(kb);
-    if (na || nb)
-        return (na && nb) ? ia < ib : nb;
-    return ka > kb || (ka == kb && ia < ib);
-}
-
-// ------------------------------------------------------------------ warp-level top-k merges
-
-// Per-lane best-first lists of (key, id, score), MOE_MAX_TOPK long; the
-// sentinel (NaN key, largest id) ranks after everything.
-struct CandList {
-    float k[MOE_MAX_TOPK], s[MOE_MAX_TOPK];
-    int i[MOE_MAX_TOPK];
-    __device__ __forceinline__ void clear()
-    {
-#pragma unroll
-        for (int j = 0; j < MOE_MAX_TOPK; ++j) {
-            k[j] = __int_as_float(0x7fffffff);
-            i[j] = 0x7fffffff;
-            s[j] = 0.0f;
-        }
-    }
-    __device__ __forceinline__ void insert(float key, int id, float sc)
-    {
-        if (!ranks_before(key, id, k[MOE_MAX_TOPK - 1], i[MOE_MAX_TOPK - 1]))
-            return;
-        k[MOE_MAX_TOPK - 1] = key;
-        i[MOE_MAX_TOPK - 1] = id;
-        s[MOE_MAX_TOPK - 1] = sc;
-#pragma unroll
-        for (int j = MOE_MAX_TOPK - 1; j > 0; --j) {
-            if (ranks_before(k[j], i[j], k[j - 1], i[j - 1])) {
-                float tk = k[j], ts = s[j];
-                int ti = i[j];
-                k[j] = k[j - 1];
-                i[j] = i[j - 1];
-                s[j] = s[j - 1];
-                k[j - 1] = tk;
-                i[j - 1] = ti;
-                s[j - 1] = ts;
-            }
-        }
-    }
-    __device__ __forceinline__ void pop()
-    {
-#pragma unroll
-        for (int j = 0; j < MOE_MAX_TOPK - 1; ++j) {
-            k[j] = k[j + 1];
-            i[j] = i[j + 1];
-            s[j] = s[j + 1];
-        }
-        k[MOE_MAX_TOPK - 1] = __int_as_float(0x7fffffff);
-        i[MOE_MAX_TOPK - 1] = 0x7fffffff;
-        s[MOE_MAX_TOPK - 1] = 0.0f;
-    }
-};
-
-// k rounds of a warp-wide best-of-heads: writes the warp's best k (key, id,
-// score) to out (lane 0) in rank order. All lanes must call.
-__device__ __forceinline__ void warp_merge(CandList &L, int kk, float *ok, int *oi, float *os)
-{
-    const unsigned full = 0xffffffffu;
-    const int lane = threadIdx.x & 31;
-    for (int r = 0; r < kk; ++r) {
-        float bk = L.k[0], bs = L.s[0];
-        int bi = L.i[0];
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            const float xk = __shfl_xor_sync(full, bk, o), xs = __shfl_xor_sync(full, bs, o);
-            const int xi = __shfl_xor_sync(full, bi, o);
-            if (ranks_before(xk, xi, bk, bi)) {
-                bk = xk;
-                bi = xi;
-                bs = xs;
-            }
-        }
-        if (L.i[0] == bi && bi != 0x7fffffff)
-            L.pop();  // the lane that held the winner (ids are unique)
-        if (lane == 0) {
-            ok[r] = bk;
-            oi[r] = bi;
-            os[r] = bs;
-        }
-    }
-}
-
-// per-lane lists of lower bounds (values only): the warp's k largest
-__device__ __forceinline__ void warp_topk_values(float (&lo)[MOE_MAX_TOPK], int kk, float *out)
-{
-    const unsigned full = 0xffffffffu;
-    const int lane = threadIdx.x & 31;
-    for (int r = 0; r < kk; ++r) {
-        float v = lo[0], mx = v;
-#pragma unroll
-        for (int o = 16; o; o >>= 1)
-            mx = fmaxf(mx, __shfl_xor_sync(full, mx, o));
-        const unsigned who = __ballot_sync(full, v == mx);
-        if (lane == __ffs(who) - 1) {
-#pragma unroll
-            for (int j = 0; j < MOE_MAX_TOPK - 1; ++j)
-                lo[j] = lo[j + 1];
-            lo[MOE_MAX_TOPK - 1] = -INFINITY;
-        }
-        if (lane == 0)
-            out[r] = mx;
-    }
-}
-
-__device__ __forceinline__ void lo_insert(float (&lo)[MOE_MAX_TOPK], float v)
-{
-    if (!(v > lo[MOE_MAX_TOPK - 1]))
-        return;
-    lo[MOE_MAX_TOPK - 1] = v;
-#pragma unroll
-    for (int j = MOE_MAX_TOPK - 1; j > 0; --j) {
-        if (lo[j] > lo[j - 1]) {
-            float t = lo[j];
-            lo[j] = lo[j - 1];
-            lo[j - 1] = t;
-        }
-    }
-}
-
-struct TokenPick {
-    int id[MOE_MAX_TOPK];
-    float s[MOE_MAX_TOPK];
-    int flags;
-};
+__device__ __forceinline__ int rank_id(unsigned long long v) { return (int)(0xFFFFFFFFu - (uint32_t)v); }
 
 // ------------------------------------------------------------------ selection + plan (whole CTA, 256 threads)
 
+#define SEL_PER_WARP MOE_MAX_ROUTED  // values per warp in the first ranking stage
+
 struct SelectSmem {
-    TokenPick tok[MOE_MAX_TOKENS];
+    int pick[MOE_MAX_TOKENS][MOE_MAX_TOPK];
+    float sc[MOE_MAX_TOKENS][MOE_MAX_TOPK];
     float w[MOE_MAX_TOKENS][MOE_MAX_TOPK];
-    float wlo[8][MOE_MAX_TOPK];                       // per warp: its k largest lower bounds
-    float wk[8][MOE_MAX_TOPK], ws[8][MOE_MAX_TOPK];   // per warp: its k best exact candidates
-    int wi[8][MOE_MAX_TOPK];
+    int flags[MOE_MAX_TOKENS];
     int wflag[8];
-    int warp_sum[2][8];
-    int ne;
-    int cnt[MOE_MAX_ROUTED];   // tokens that picked expert e
-    int pidx[MOE_MAX_ROUTED];  // plan index of e (exclusive prefix of cnt > 0)
-    int poff[MOE_MAX_ROUTED];  // first pair of e (exclusive prefix of cnt)
+    unsigned long long v[8][SEL_PER_WARP];               // per warp: its experts' values
+    unsigned long long cand[8][MOE_MAX_TOPK];            // per warp: its k best
+    int first[MOE_MAX_TOKENS * MOE_MAX_TOPK], rank[MOE_MAX_TOKENS * MOE_MAX_TOPK],
+        ent[MOE_MAX_TOKENS * MOE_MAX_TOPK];
 };
 
 __device__ __forceinline__ void group_sync(int group, int gsz)
@@ -222,93 +102,90 @@ __device__ __forceinline__ void group_sync(int group, int gsz)
         asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(gsz * 32) : "memory");
 }
 
-// The picks of one token by a group of gsz warps (experts split across them).
-// Pass 1: single-precision keys with error bounds give T, the k-th largest
-// lower bound; pass 2: exact keys (f64 scores) for the experts whose upper
-// bound reaches T, merged best-first. Writes sm.tok[t] and sm.w[t].
-__device__ void select_token_group(const RouteArgs &a, const float *logits, int t, int group, int gsz,
-                                   SelectSmem &sm)
+// The picks of token t by a group of gsz warps from exact scores and keys.
+// Ranking by counting (no long shuffle chains): every value's rank is the
+// number of values ranking before it; stage 1 inside each warp over its
+// experts, stage 2 over the group's k best of each warp.
+__device__ void select_token_group(const RouteArgs &a, const float *logits, const float *scores,
+                                   const float *keys, int t, int group, int gsz, SelectSmem &sm)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, wig = warp - group * gsz;
     const int n = a.n, k = a.k, stride = gsz * 32;
-    const float *lg = logits + (size_t)t * n;
-    float lo[MOE_MAX_TOPK];
-#pragma unroll
-    for (int j = 0; j < MOE_MAX_TOPK; ++j)
-        lo[j] = -INFINITY;
+    const size_t row = (size_t)t * n;
+    const int per_lane = (n + stride - 1) / stride;  // <= SEL_PER_WARP / 32
     bool nonfinite = false;
-    for (int e = wig * 32 + lane; e < n; e += stride) {
-        const float l = __ldcg(lg + e);
-        const float tt = __fdiv_rn(l, a.temp);
-        const float sa = score_approx(tt);
-        const float ka = __fadd_rn(sa, __ldg(a.bias + e));
-        nonfinite |= !isfinite(l) || !isfinite(ka);
-        lo_insert(lo, isnan(ka) ? -INFINITY : (isinf(ka) ? ka : ka - key_bound(sa, ka)));
+    for (int i = 0; i < per_lane; ++i) {
+        const int e = wig * 32 + lane + i * stride;
+        unsigned long long v = 0ull;
+        if (e < n) {
+            const float key = keys[row + e];
+            nonfinite |= !isfinite(logits[row + e]) || !isfinite(key);
+            v = rank_value(key, e);
+        }
+        sm.v[warp][lane + 32 * i] = v;
     }
-    warp_topk_values(lo, k, sm.wlo[warp]);
+    if (lane < MOE_MAX_TOPK)
+        sm.cand[warp][lane] = 0ull;
     const unsigned nf = __ballot_sync(0xffffffffu, nonfinite);
     if (lane == 0)
         sm.wflag[warp] = nf ? MOE_HDR_NONFINITE : 0;
-    group_sync(group, gsz);
-    // T: the k-th largest of the group's gsz * k values (every warp of the group)
-#pragma unroll
-    for (int j = 0; j < MOE_MAX_TOPK; ++j)
-        lo[j] = -INFINITY;
-    for (int j = lane; j < gsz * k; j += 32)
-        lo_insert(lo, sm.wlo[group * gsz + j / k][j % k]);
-    float tops[MOE_MAX_TOPK];
-    warp_topk_values(lo, k, tops);
-    const float T = __shfl_sync(0xffffffffu, tops[k - 1], 0);
-    // pass 2
-    CandList L;
-    L.clear();
-    for (int e = wig * 32 + lane; e < n; e += stride) {
-        const float l = __ldcg(lg + e);
-        const float tt = __fdiv_rn(l, a.temp);
-        const float sa = score_approx(tt);
-        const float b = __ldg(a.bias + e);
-        const float ka = __fadd_rn(sa, b);
-        const float hi = isnan(ka) ? -INFINITY : (isinf(ka) ? ka : ka + key_bound(sa, ka));
-        if (hi >= T) {
-            const float sx = score_exact(tt);
-            L.insert(__fadd_rn(sx, b), e, sx);
+    __syncwarp();
+    const int nv = 32 * per_lane;
+    for (int i = 0; i < per_lane; ++i) {
+        const unsigned long long mv = sm.v[warp][lane + 32 * i];
+        if (mv != 0ull) {
+            int r = 0;
+            for (int j = 0; j < nv; ++j)
+                r += sm.v[warp][j] > mv;
+            if (r < k)
+                sm.cand[warp][r] = mv;
         }
     }
-    warp_merge(L, k, sm.wk[warp], sm.wi[warp], sm.ws[warp]);
     group_sync(group, gsz);
     if (wig == 0) {
-        L.clear();
-        for (int j = lane; j < gsz * k; j += 32) {
-            const int w = group * gsz + j / k, r = j % k;
-            L.insert(sm.wk[w][r], sm.wi[w][r], sm.ws[w][r]);
+        // stage 2: the group's gsz * k candidates (<= 64), two per lane
+        const int nc = gsz * k;
+        for (int c = lane; c < nc; c += 32) {
+            const unsigned long long v = sm.cand[group * gsz + c / k][c % k];
+            if (v == 0ull)
+                continue;
+            int r = 0;
+            for (int j = 0; j < nc; ++j)
+                r += sm.cand[group * gsz + j / k][j % k] > v;
+            if (r < k) {
+                const int id = rank_id(v);
+                sm.pick[t][r] = id;
+                sm.sc[t][r] = scores[row + id];
+            }
         }
-        TokenPick &p = sm.tok[t];
-        float kk_[MOE_MAX_TOPK];
-        warp_merge(L, k, kk_, p.id, p.s);
+        __syncwarp();
         if (lane == 0) {
             int fl = 0;
             for (int w = 0; w < gsz; ++w)
                 fl |= sm.wflag[group * gsz + w];
-            p.flags = fl;
+            sm.flags[t] = fl;
             // weights in pick order, each step one f32 rounding
             if (a.norm && k > 1) {
                 float sum = 0.0f;
                 for (int i = 0; i < k; ++i)
-                    sum = __fadd_rn(sum, p.s[i]);
+                    sum = __fadd_rn(sum, sm.sc[t][i]);
                 sum = __fadd_rn(sum, 1e-20f);
                 for (int i = 0; i < k; ++i)
-                    sm.w[t][i] = __fmul_rn(__fdiv_rn(p.s[i], sum), a.route_scale);
+                    sm.w[t][i] = __fmul_rn(__fdiv_rn(sm.sc[t][i], sum), a.route_scale);
             } else {
                 for (int i = 0; i < k; ++i)
-                    sm.w[t][i] = __fmul_rn(p.s[i], a.route_scale);
+                    sm.w[t][i] = __fmul_rn(sm.sc[t][i], a.route_scale);
             }
         }
     }
 }
 
-__device__ void select_and_plan(const RouteArgs &a, const float *logits, SelectSmem &sm)
+// Selection for all m tokens, then the plan: the distinct picked experts in
+// ascending id with their (expert, token) pairs, pair-major, and the header.
+__device__ void select_and_plan(const RouteArgs &a, const float *logits, const float *scores, const float *keys,
+                                SelectSmem &sm)
 {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int n = a.n, k = a.k, m = a.m, cap = m * k;
     // warps in groups: all 8 on one token for m = 1, down to one warp per token
     int gsz = 8;
@@ -316,102 +193,67 @@ __device__ void select_and_plan(const RouteArgs &a, const float *logits, SelectS
         gsz >>= 1;
     const int group = warp / gsz;
     if (group < m)
-        select_token_group(a, logits, group, group, gsz, sm);
-    for (int e = tid; e < n; e += blockDim.x)
-        sm.cnt[e] = 0;
+        select_token_group(a, logits, scores, keys, group, group, gsz, sm);
     __syncthreads();
-    // defensive: a pick outside [0, n) would index the tables below
+    // pairs: entry q = (token q / k, its pick q % k); rank by (expert, token)
     if (tid < cap) {
-        int &id = sm.tok[tid / k].id[tid % k];
-        if (id < 0 || id >= n) {
+        int e = sm.pick[tid / k][tid % k];
+        if (e < 0 || e >= n) {  // defensive: a pick outside [0, n) would index the tables
             if (a.ctrl)
                 atomicOr(a.ctrl + MOE_CTRL_STATUS, (uint32_t)MOE_WS_PLAN);
-            id = 0;
+            e = 0;
+            sm.pick[tid / k][tid % k] = 0;
         }
+        sm.ent[tid] = e;
     }
     __syncthreads();
-    if (tid < cap)
-        atomicAdd(&sm.cnt[sm.tok[tid / k].id[tid % k]], 1);
-    __syncthreads();
-    // exclusive prefix sums of (cnt > 0) and cnt over e; 4 experts per thread
-    int e0 = tid * 4, f[4], c[4], fs = 0, cs = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        int e = e0 + i;
-        c[i] = e < n ? sm.cnt[e] : 0;
-        f[i] = c[i] > 0;
-        fs += f[i];
-        cs += c[i];
-    }
-    int fi = fs, ci = cs;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        int fv = __shfl_up_sync(0xffffffffu, fi, o), cv = __shfl_up_sync(0xffffffffu, ci, o);
-        if (lane >= o) {
-            fi += fv;
-            ci += cv;
-        }
-    }
-    if (lane == 31) {
-        sm.warp_sum[0][warp] = fi;
-        sm.warp_sum[1][warp] = ci;
-    }
-    __syncthreads();
-    int fb = 0, cb = 0;
-    for (int w = 0; w < warp; ++w) {
-        fb += sm.warp_sum[0][w];
-        cb += sm.warp_sum[1][w];
-    }
-    if (tid == blockDim.x - 1)
-        sm.ne = fb + fi;
-    fi = fb + fi - fs;  // exclusive
-    ci = cb + ci - cs;
-    const int po = m * (1 + 3 * k);  // plan tail of the header
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        int e = e0 + i;
-        if (e < n) {
-            sm.pidx[e] = fi;
-            sm.poff[e] = ci;
-            if (f[i]) {
-                int slot = __ldg(a.slot_row + e);
-                unsigned long long s = slot < 0 ? 0ull : (unsigned long long)slot;
-                unsigned long long base = (unsigned long long)a.arena_base + s * a.slot_bytes;
-                a.ptrs[fi] = base + a.gate_off;
-                a.ptrs[cap + fi] = base + a.up_off;
-                a.ptrs[2 * cap + fi] = base + a.down_off;
-                a.hdr[po + 1 + fi] = ci;
-                a.hdr[po + 2 + cap + fi] = e;
-            }
-        }
-        fi += f[i];
-        ci += c[i];
-    }
-    __syncthreads();
-    if (tid == 0) {
-        a.hdr[po] = sm.ne;
-        a.hdr[po + 1 + sm.ne] = cap;
-    }
-    // pairs: token t's pick e goes to poff[e] + (number of earlier tokens that picked e)
     if (tid < cap) {
-        int t = tid / k, i = tid % k, e = sm.tok[t].id[i], rank = 0;
-        for (int t2 = 0; t2 < t; ++t2)
-            for (int i2 = 0; i2 < k; ++i2)
-                rank += sm.tok[t2].id[i2] == e;
-        int pair = sm.poff[e] + rank;
-        a.plan_rows[pair] = t;
-        a.plan_w[pair] = sm.w[t][i];
+        const int e = sm.ent[tid], t = tid / k;
+        int rank = 0, earlier = 0;
+        for (int q = 0; q < cap; ++q) {
+            const int e2 = sm.ent[q], t2 = q / k;
+            rank += e2 < e || (e2 == e && t2 < t);
+            earlier += e2 == e && t2 < t;
+        }
+        sm.rank[tid] = rank;
+        sm.first[tid] = earlier == 0;
+        a.plan_rows[rank] = t;
+        a.plan_w[rank] = sm.w[t][tid % k];
+    }
+    __syncthreads();
+    const int po = m * (1 + 3 * k);  // plan tail of the header
+    if (tid < cap && sm.first[tid]) {
+        const int e = sm.ent[tid];
+        int p = 0;
+        for (int q = 0; q < cap; ++q)
+            p += sm.first[q] && sm.ent[q] < e;
+        const int slot = __ldg(a.slot_row + e);
+        const unsigned long long base =
+            (unsigned long long)a.arena_base + (unsigned long long)(slot < 0 ? 0 : slot) * a.slot_bytes;
+        a.ptrs[p] = base + a.gate_off;
+        a.ptrs[cap + p] = base + a.up_off;
+        a.ptrs[2 * cap + p] = base + a.down_off;
+        a.hdr[po + 1 + p] = sm.rank[tid];
+        a.hdr[po + 2 + cap + p] = e;
+    }
+    if (tid == 0) {
+        int ne = 0;
+        for (int q = 0; q < cap; ++q)
+            ne += sm.first[q];
+        a.hdr[po] = ne;
+        a.hdr[po + 1 + ne] = cap;
     }
     // header rows: status, picks, weight bits, slots of the picks in ascending id
-    if (tid < m) {
-        const TokenPick &p = sm.tok[tid];
-        int32_t *h = a.hdr + (size_t)tid * (1 + 3 * k);
+    if (tid >= 32 && tid < 32 + m) {
+        const int t = tid - 32;
+        int32_t *h = a.hdr + (size_t)t * (1 + 3 * k);
         int sorted[MOE_MAX_TOPK];
-        int status = p.flags;
+        int status = sm.flags[t];
         for (int i = 0; i < k; ++i) {
-            h[1 + i] = p.id[i];
-            h[1 + k + i] = __float_as_int(sm.w[tid][i]);
-            int v = p.id[i], j = i;
+            h[1 + i] = sm.pick[t][i];
+            h[1 + k + i] = __float_as_int(sm.w[t][i]);
+            const int v = sm.pick[t][i];
+            int j = i;
             while (j > 0 && sorted[j - 1] > v) {
                 sorted[j] = sorted[j - 1];
                 --j;
@@ -419,7 +261,7 @@ __device__ void select_and_plan(const RouteArgs &a, const float *logits, SelectS
             sorted[j] = v;
         }
         for (int i = 0; i < k; ++i) {
-            int slot = __ldg(a.slot_row + sorted[i]);
+            const int slot = __ldg(a.slot_row + sorted[i]);
             if (slot < 0)
                 status |= MOE_HDR_MISS;
             h[1 + 2 * k + i] = slot < 0 ? 0 : slot;
@@ -430,6 +272,8 @@ __device__ void select_and_plan(const RouteArgs &a, const float *logits, SelectS
 
 // ------------------------------------------------------------------ kernels
 
+// smem: [0,128) barrier + flag; then the CTA's router rows, x, warp partials;
+// the last CTA reuses the rows area for the selection
 __global__ void __launch_bounds__(256) moe_router_kernel(RouteArgs a)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -451,7 +295,7 @@ __global__ void __launch_bounds__(256) moe_router_kernel(RouteArgs a)
     __syncthreads();
     if (tid == 0 && nrows > 0) {
         // this CTA's router rows: constant weights, fetched before the wait
-        uint64_t pol = policy_evict_first();
+        const uint64_t pol = policy_evict_first();
         mbar_arrive_expect_tx(bar, wbytes);
         const char *src = reinterpret_cast<const char *>(a.w + (size_t)row0 * dim);
         char *dst = reinterpret_cast<char *>(sw);
@@ -467,7 +311,7 @@ __global__ void __launch_bounds__(256) moe_router_kernel(RouteArgs a)
             s4[i] = __ldcg(gx + i);
     }
     __syncthreads();
-    bool ok = nrows <= 0 || mbar_wait(bar, 0, a.ctrl + MOE_CTRL_STATUS);
+    const bool ok = nrows <= 0 || mbar_wait(bar, 0, a.ctrl + MOE_CTRL_STATUS);
     if (__syncthreads_and(ok) == 0)
         return;
     // logits: thread-strided 16-byte chunks, warp butterfly, then the 8 warp
@@ -479,7 +323,7 @@ __global__ void __launch_bounds__(256) moe_router_kernel(RouteArgs a)
             const uint4 *xr = reinterpret_cast<const uint4 *>(sx + (size_t)t * dim);
             float acc = 0.0f;
             for (int c = tid; c < nch; c += blockDim.x) {
-                uint4 wv = wr[c], xv = xr[c];
+                const uint4 wv = wr[c], xv = xr[c];
                 acc = fmaf(bf16_lo(wv.x), bf16_lo(xv.x), acc);
                 acc = fmaf(bf16_hi(wv.x), bf16_hi(xv.x), acc);
                 acc = fmaf(bf16_lo(wv.y), bf16_lo(xv.y), acc);
@@ -499,36 +343,57 @@ __global__ void __launch_bounds__(256) moe_router_kernel(RouteArgs a)
     __syncthreads();
     const int nw = blockDim.x >> 5;
     for (int i = tid; i < nrows * m; i += blockDim.x) {
-        int r = i / m, t = i % m;
-        float s = 0.0f;
+        const int r = i / m, t = i % m;
+        float l = 0.0f;
         for (int w = 0; w < nw; ++w)
-            s += red[((size_t)w * a.rows_per_cta + r) * m + t];
-        a.logits[(size_t)t * a.n + row0 + r] = s;
+            l += red[((size_t)w * a.rows_per_cta + r) * m + t];
+        const size_t o = (size_t)t * a.n + row0 + r;
+        a.logits[o] = l;
+        if (a.do_select) {
+            // the exact score of this row, here: the f64 chain runs on a few
+            // threads of every CTA in parallel instead of in the selecting CTA
+            const float sc = score_exact(l, a.temp);
+            a.scores[o] = sc;
+            a.keys[o] = __fadd_rn(sc, __ldg(a.bias + row0 + r));
+        }
     }
     if (!a.do_select)
         return;
-    // the last CTA to finish its logits runs the selection
-    __threadfence();
+    // the last CTA to finish its rows runs the selection (no CTA waits)
     __syncthreads();
-    if (tid == 0)
-        *s_last = atomicAdd(a.ctrl + MOE_CTRL_TICKET, 1u) == gridDim.x - 1;
+    if (tid == 0) {
+        // acq_rel: releases this CTA's logits/scores/keys (ordered before by
+        // the barrier), and the last CTA acquires everyone else's
+        unsigned old;
+        asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.ctrl + MOE_CTRL_TICKET) : "memory");
+        *s_last = old == gridDim.x - 1;
+    }
     __syncthreads();
     if (!*s_last)
         return;
-    __threadfence();
     SelectSmem *sel = reinterpret_cast<SelectSmem *>(sw);  // the weights are no longer needed
-    select_and_plan(a, a.logits, *sel);
+    select_and_plan(a, a.logits, a.scores, a.keys, *sel);
     if (tid == 0)
         atomicExch(a.ctrl + MOE_CTRL_TICKET, 0u);
 }
 
 // the selection alone, on caller-provided logits: one CTA of 256 threads
+// computes every score and key into shared memory, then selects
 __global__ void __launch_bounds__(256) moe_select_kernel(RouteArgs a)
 {
-    __shared__ SelectSmem sel;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    SelectSmem &sel = *reinterpret_cast<SelectSmem *>(smem);
+    float *sc = reinterpret_cast<float *>(smem + align_up(sizeof(SelectSmem), 128));
+    float *ky = sc + (size_t)a.m * a.n;
     pdl_wait();
     pdl_launch_dependents();
-    select_and_plan(a, a.logits, sel);
+    for (int i = threadIdx.x; i < a.m * a.n; i += blockDim.x) {
+        const float s = score_exact(a.logits[i], a.temp);
+        sc[i] = s;
+        ky[i] = __fadd_rn(s, __ldg(a.bias + i % a.n));
+    }
+    __syncthreads();
+    select_and_plan(a, a.logits, sc, ky, sel);
 }
 
 }  // namespace moe
