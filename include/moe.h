@@ -177,6 +177,29 @@ int moe_layer_step(const moe_cfg *cfg, const moe_layer *layer, const moe_arena *
                    const void *x_dev, float *residual_dev, void *x_next_dev,
                    int32_t *header_dev, int m, void *ws_dev, moe_stream_t stream);
 
+/* moe_layer_step without a caller workspace and without any device
+ * allocation. The pages have no counterpart of this call: it exists for
+ * callers that cannot allocate device memory (a plain C host program linking
+ * only this library, with no device allocator of its own; a serving loop that
+ * must not allocate once it runs, since cudaMalloc and cudaFree can
+ * synchronise the device and can fail under memory pressure).
+ * The workspace is a 4 MiB array in the library's device memory, one per
+ * device. The first call on a device (with that device current) looks it up
+ * with cudaGetSymbolAddress and zeroes it; make that first call before any
+ * stream capture. Every call clears the array's control words and counters
+ * on `stream` first, then runs the same kernels as moe_layer_step.
+ * Arguments as moe_layer_step; status_host: NULL, or a host word that
+ * receives the workspace status (MOE_WS_*) of this call once `stream`
+ * reaches the end of the call (pinned memory keeps the copy asynchronous).
+ * The array is shared by every call on the device: calls that overlap in
+ * time (other streams, other host threads) race on it and must be
+ * serialised by the caller. Errors: MOE_EUNSUPPORTED when the configuration
+ * needs more than 4 MiB of workspace (moe_workspace_bytes); MOE_EINVAL for
+ * bad arguments; MOE_ECUDA when the look-up or a launch fails. */
+int moe_layer_step_static(const moe_cfg *cfg, const moe_layer *layer, const moe_arena *arena,
+                          const void *x_dev, float *residual_dev, void *x_next_dev,
+                          int32_t *header_dev, int m, uint32_t *status_host, moe_stream_t stream);
+
 /* Same step with HOST buffers: copies x (bf16 [m, dim], host) and residual
  * (f32 [m, dim], host) in, runs moe_layer_step, copies residual, x_next and
  * the header back to host buffers, all on `stream` (pinned host memory makes

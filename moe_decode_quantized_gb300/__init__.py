@@ -26,7 +26,7 @@ SLOT_TABLE_LAYERS = 64
 __all__ = ["Config", "Arena", "Layer", "MoeError", "header_words", "workspace_bytes",
            "workspace_init", "router_logits", "quantize_q8_1", "route_select", "expert_step",
            "swiglu_q8", "layer_step", "host_io_bytes", "layer_step_host", "workspace_view",
-           "read_status", "layer_step_profiled", "slot_table_set", "dedupe_triples", "parse_header", "Graph"]
+           "read_status", "layer_step_profiled", "layer_step_static", "slot_table_set", "dedupe_triples", "parse_header", "Graph"]
 
 
 class MoeError(RuntimeError):
@@ -153,6 +153,16 @@ def swiglu_q8(cfg: Config, g, u, rows: int, h, hq8, stream=None):
 def layer_step(cfg: Config, layer: Layer, arena: Arena, x, residual, x_next, header, m: int, ws, stream=None):
     _check(_lib.moe().moe_layer_step(C.byref(cfg.c()), C.byref(layer.c()), C.byref(arena.c()), _ptr(x),
                                      _ptr(residual), _ptr(x_next), _ptr(header), m, _ptr(ws), _stream(stream)))
+
+
+def layer_step_static(cfg: Config, layer: Layer, arena: Arena, x, residual, x_next, header, m: int,
+                      status=None, stream=None):
+    """layer_step on the library's own static device workspace (no allocation).
+    status: None, or a host uint32 array of one element that receives the
+    workspace status once the stream reaches the end of the call."""
+    _check(_lib.moe().moe_layer_step_static(C.byref(cfg.c()), C.byref(layer.c()), C.byref(arena.c()), _ptr(x),
+                                            _ptr(residual), _ptr(x_next), _ptr(header), m, _ptr(status),
+                                            _stream(stream)))
 
 
 def host_io_bytes(cfg: Config, m: int) -> int:

@@ -53,6 +53,8 @@ MOE_SYMBOLS = {
     "moe_swiglu_q8": (C.c_int, [C.POINTER(MoeCfg), P, P, C.c_int, P, P, P]),
     "moe_layer_step": (C.c_int, [C.POINTER(MoeCfg), C.POINTER(MoeLayer), C.POINTER(MoeArena), P, P,
                                  P, P, C.c_int, P, P]),
+    "moe_layer_step_static": (C.c_int, [C.POINTER(MoeCfg), C.POINTER(MoeLayer), C.POINTER(MoeArena),
+                                        P, P, P, P, C.c_int, P, P]),
     "moe_host_io_bytes": (C.c_int, [C.POINTER(MoeCfg), C.c_int, C.POINTER(SZ)]),
     "moe_layer_step_host": (C.c_int, [C.POINTER(MoeCfg), C.POINTER(MoeLayer), C.POINTER(MoeArena),
                                       P, P, P, P, C.c_int, P, P, P]),

@@ -375,6 +375,42 @@ int check_layer(const moe_cfg &c, const moe_layer *ly)
     return MOE_OK;
 }
 
+// ------------------------------------------------------------------ static workspace
+//
+// Workspace of moe_layer_step_static: a file-scope device array, so that the
+// call needs no device allocation at all. It serves callers that cannot
+// allocate device memory: a plain C host program that links only this
+// library and has no device allocator of its own, and a serving loop that
+// must not allocate once it runs, because cudaMalloc and cudaFree can
+// synchronise the whole device and can fail under memory pressure.
+// MOE_STATIC_WS_BYTES bounds moe_workspace_bytes of the configurations it
+// accepts (4 MiB: dim 4096, inter 2048, 384 routed experts, top-8, 8 tokens
+// need 2.5 MB).
+#define MOE_STATIC_WS_BYTES (4u << 20)
+static __device__ __align__(256) unsigned char g_static_ws[MOE_STATIC_WS_BYTES];
+
+void *g_static_ptr[64];  // per device ordinal, under g_mu
+
+// Address of this device's copy of g_static_ws. The first call on a device
+// (with that device current) looks the symbol up and zeroes the whole array
+// on `s`, as moe_workspace_init does for a caller's workspace.
+int static_ws(cudaStream_t s, void **out)
+{
+    int d = 0;
+    CUDA_OK(cudaGetDevice(&d));
+    if (d < 0 || d >= 64)
+        return fail(MOE_EUNSUPPORTED, "device ordinal %d", d);
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_static_ptr[d]) {
+        void *p = nullptr;
+        CUDA_OK(cudaGetSymbolAddress(&p, g_static_ws));
+        CUDA_OK(cudaMemsetAsync(p, 0, MOE_STATIC_WS_BYTES, s));
+        g_static_ptr[d] = p;
+    }
+    *out = g_static_ptr[d];
+    return MOE_OK;
+}
+
 struct GraphObj {
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
@@ -574,6 +610,37 @@ int moe_layer_step(const moe_cfg *cfg, const moe_layer *layer, const moe_arena *
     if (!x || !residual || !x_next || !header || !ws || !aligned16(x))
         return fail(MOE_EINVAL, "moe_layer_step: a buffer is NULL or x is not 16-byte aligned");
     return layer_step(*cfg, *layer, *arena, x, residual, x_next, header, m, ws, (cudaStream_t)stream);
+}
+
+int moe_layer_step_static(const moe_cfg *cfg, const moe_layer *layer, const moe_arena *arena,
+                          const void *x, float *residual, void *x_next, int32_t *header, int m,
+                          uint32_t *status_host, moe_stream_t stream)
+{
+    int rc = check_cfg(cfg);
+    if (rc || (rc = check_m(cfg, m)) || (rc = check_arena(arena)) || (rc = check_layer(*cfg, layer)))
+        return rc;
+    const WsLayout L = ws_layout(*cfg);
+    if (L.total > MOE_STATIC_WS_BYTES)
+        return fail(MOE_EUNSUPPORTED,
+                    "moe_layer_step_static: this configuration needs %zu bytes of workspace, the static "
+                    "workspace holds %u; use moe_layer_step with a workspace of its own",
+                    L.total, (unsigned)MOE_STATIC_WS_BYTES);
+    if (m > 0 && (!x || !residual || !x_next || !header || !aligned16(x)))
+        return fail(MOE_EINVAL, "moe_layer_step_static: a buffer is NULL or x is not 16-byte aligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    void *ws = nullptr;
+    if ((rc = static_ws(s, &ws)))
+        return rc;
+    // the array keeps the last call's contents: the control words and the
+    // row-group counters (everything before the logits) must start at zero,
+    // also after a call whose wait ran out and left them set
+    CUDA_OK(cudaMemsetAsync(ws, 0, L.logits, s));
+    if (m > 0 && (rc = layer_step(*cfg, *layer, *arena, x, residual, x_next, header, m, ws, s)))
+        return rc;
+    if (status_host)
+        CUDA_OK(cudaMemcpyAsync(status_host, static_cast<char *>(ws) + L.ctrl + 4 * MOE_CTRL_STATUS,
+                                sizeof(uint32_t), cudaMemcpyDeviceToHost, s));
+    return MOE_OK;
 }
 
 int moe_host_io_bytes(const moe_cfg *cfg, int m, size_t *bytes)
