@@ -134,11 +134,11 @@ struct Geo {
     int grid;  // persistent grid of the expert kernels
 };
 
-size_t router_smem(int rows, int dim, int m)
+size_t router_smem(int rows, int dim, int m, int n)
 {
-    size_t main = (size_t)rows * dim * 2 + (size_t)m * dim * 2 + sizeof(float) * 8 * rows * m;
-    size_t sel = sizeof(SelectSmem);
-    return 128 + (main > sel ? main : sel);
+    size_t main = (size_t)rows * dim * 2 + (size_t)m * dim * 2 + sizeof(float) * rows * m;
+    size_t sel = sel_bytes(m, n);
+    return 128 + router_pre_bytes(n, rows) + (main > sel ? main : sel);
 }
 
 // the most ring stages (up to cap, at least 2) that fit the shared memory
@@ -159,7 +159,7 @@ int geometry(const moe_cfg &c, int m, bool shared, const DevInfo &I, Geo &G)
     const int r_ctas = std::max(16, I.sms / 3);
     G.r_rows = (n + r_ctas - 1) / r_ctas;
     G.r_grid = (n + G.r_rows - 1) / G.r_rows;
-    G.r_smem = router_smem(G.r_rows, dim, m);
+    G.r_smem = router_smem(G.r_rows, dim, m, c.n_routed);
     G.grid = I.sms;
     // gate/up: stages of max(one Q2_K task, one bf16 row)
     G.g_stage = (uint32_t)align_up(std::max<size_t>((size_t)MOE_G_TASK_SB * MOE_Q2K_BYTES, (size_t)dim * 2), 128);
@@ -572,7 +572,10 @@ int moe_route_select(const moe_cfg *cfg, const float *logits, const float *bias,
     DevInfo *I;
     if ((rc = dev_info(&I)))
         return rc;
-    const size_t smem = align_up(sizeof(SelectSmem), 128) + sizeof(float) * 2 * (size_t)m * cfg->n_routed;
+    const size_t smem = align_up(sel_bytes(m, cfg->n_routed), 128) + sizeof(float) * 2 * (size_t)m * cfg->n_routed +
+                        sizeof(int) * (size_t)cfg->n_routed;
+    if (smem > (size_t)I->smem_optin)
+        return fail(MOE_EUNSUPPORTED, "moe_route_select: %zu bytes of shared memory needed", smem);
     return launch(moe_select_kernel, dim3(1), dim3(256), smem, (cudaStream_t)stream, false, a);
 }
 

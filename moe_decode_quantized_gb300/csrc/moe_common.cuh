@@ -200,6 +200,45 @@ __device__ __forceinline__ float f16_bits_to_f32(uint32_t h)
     return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
 }
 
+// ------------------------------------------------------------------ token count
+
+// Calls f with the token count as a compile-time constant (IntC<m>), so that
+// loops over tokens issue exactly m tokens' work: a loop to MOE_MAX_TOKENS
+// with "if (t < m)" is predicated, not branched, and costs all 8.
+template <int N>
+struct IntC {
+    static constexpr int value = N;
+};
+
+template <typename F>
+__device__ __forceinline__ void with_m(int m, F &&f)
+{
+    switch (m) {
+    case 1: f(IntC<1>{}); break;
+    case 2: f(IntC<2>{}); break;
+    case 3: f(IntC<3>{}); break;
+    case 4: f(IntC<4>{}); break;
+    case 5: f(IntC<5>{}); break;
+    case 6: f(IntC<6>{}); break;
+    case 7: f(IntC<7>{}); break;
+    default: f(IntC<8>{}); break;
+    }
+}
+
+// s += w . x over one 16-byte chunk of 8 bf16 each, in element order
+__device__ __forceinline__ float fma_bf16x8(const uint4 &w, const uint4 &x, float s)
+{
+    s = fmaf(bf16_lo(w.x), bf16_lo(x.x), s);
+    s = fmaf(bf16_hi(w.x), bf16_hi(x.x), s);
+    s = fmaf(bf16_lo(w.y), bf16_lo(x.y), s);
+    s = fmaf(bf16_hi(w.y), bf16_hi(x.y), s);
+    s = fmaf(bf16_lo(w.z), bf16_lo(x.z), s);
+    s = fmaf(bf16_hi(w.z), bf16_hi(x.z), s);
+    s = fmaf(bf16_lo(w.w), bf16_lo(x.w), s);
+    s = fmaf(bf16_hi(w.w), bf16_hi(x.w), s);
+    return s;
+}
+
 // clamped SwiGLU in f32: silu(min(g, L)) * clamp(u, -L, L); L <= 0: no clamp
 __device__ __forceinline__ float swiglu_f32(float g, float u, float limit)
 {

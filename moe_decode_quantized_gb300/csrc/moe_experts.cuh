@@ -467,6 +467,11 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
                 base += c1 - c0;
             }
         }
+        // the first routed chunk's ticket does not depend on the plan: taken
+        // before the wait, its round trip overlaps the selection
+        unsigned nxt = 0;
+        if (lane == 0)
+            nxt = atomicAdd(a.gctr + 1, (unsigned)MOE_G_CHUNK);
         pdl_wait();  // the selection has written the plan and the pointer table
         pdl_launch_dependents();
         cache_plan(ring, a.hdr, a.plan_off, a.plan_rows, a.ptrs, a.cap, 0, 2);
@@ -475,9 +480,6 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
         const int tpm = inter / rt;  // tasks per matrix
         const int total = pc.ne * 2 * tpm;
         const uint32_t bytes = (uint32_t)(rt * nb * MOE_Q2K_BYTES);
-        unsigned nxt = 0;
-        if (lane == 0)
-            nxt = atomicAdd(a.gctr + 1, (unsigned)MOE_G_CHUNK);
         for (;;) {
             const int c0 = (int)__shfl_sync(0xffffffffu, nxt, 0);
             if (c0 >= total || !ok)
@@ -602,37 +604,26 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
                 mbar_arrive(&ring.empty[slot]);
         } else {
             // one bf16 row of W1 or W3 against every token's bf16 x
-            float acc[MOE_MAX_TOKENS];
-#pragma unroll
-            for (int tt = 0; tt < MOE_MAX_TOKENS; ++tt)
-                acc[tt] = 0.0f;
             const uint4 *wr = reinterpret_cast<const uint4 *>(st);
-            for (int c = lane; c < dim / 8; c += 32) {
-                const uint4 wv = wr[c];
-#pragma unroll
-                for (int tt = 0; tt < MOE_MAX_TOKENS; ++tt) {
-                    if (tt < a.m) {
-                        const uint4 xv = reinterpret_cast<const uint4 *>(xs + (size_t)tt * dim)[c];
-                        float s = acc[tt];
-                        s = fmaf(bf16_lo(wv.x), bf16_lo(xv.x), s);
-                        s = fmaf(bf16_hi(wv.x), bf16_hi(xv.x), s);
-                        s = fmaf(bf16_lo(wv.y), bf16_lo(xv.y), s);
-                        s = fmaf(bf16_hi(wv.y), bf16_hi(xv.y), s);
-                        s = fmaf(bf16_lo(wv.z), bf16_lo(xv.z), s);
-                        s = fmaf(bf16_hi(wv.z), bf16_hi(xv.z), s);
-                        s = fmaf(bf16_lo(wv.w), bf16_lo(xv.w), s);
-                        s = fmaf(bf16_hi(wv.w), bf16_hi(xv.w), s);
-                        acc[tt] = s;
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&ring.empty[slot]);
+            const uint4 *x4 = reinterpret_cast<const uint4 *>(xs);
             float *out = t.mat ? a.us : a.gs;
+            with_m(a.m, [&](auto MC) {
+                constexpr int M = decltype(MC)::value;
+                float acc[M];
 #pragma unroll
-            for (int tt = 0; tt < MOE_MAX_TOKENS; ++tt) {
-                if (tt < a.m) {
+                for (int tt = 0; tt < M; ++tt)
+                    acc[tt] = 0.0f;
+                for (int c = lane; c < dim / 8; c += 32) {
+                    const uint4 wv = wr[c];
+#pragma unroll
+                    for (int tt = 0; tt < M; ++tt)
+                        acc[tt] = fma_bf16x8(wv, x4[(size_t)tt * (dim / 8) + c], acc[tt]);
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&ring.empty[slot]);
+#pragma unroll
+                for (int tt = 0; tt < M; ++tt) {
                     float v = acc[tt];
 #pragma unroll
                     for (int o = 16; o; o >>= 1)
@@ -640,7 +631,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
                     if (lane == 0)
                         out[(size_t)tt * inter + t.row] = v;
                 }
-            }
+            });
         }
     }
     if (!triggered) {
@@ -697,6 +688,11 @@ __host__ __device__ inline size_t d_smem_bytes(int S, int pair_cap, int m, int d
     return d_stage_off(S, pair_cap, m, dim, inter, shared) + (size_t)S * stage_bytes + 16;
 }
 
+// relative costs of the down kernel's tasks (bytes and instructions of a
+// 64-super-block Q3_K task against one bf16 row of the shared expert)
+#define D_W_ROUTED 2
+#define D_W_SHARED 1
+
 // the range of tasks of this CTA and the plan pairs its routed tasks touch
 struct DRange {
     int ne, tpr, Tr, lo, hi, pair_lo, pair_hi;
@@ -708,9 +704,16 @@ __device__ __forceinline__ DRange d_range(const DArgs &a, bool shared)
     r.ne = min(max(__ldcg(a.hdr + a.plan_off), 0), a.cap);
     r.tpr = a.dim / down_rows_per_task(a.inter);
     r.Tr = r.ne * r.tpr;
-    const long long T = (long long)r.Tr + (shared ? a.dim : 0);
-    r.lo = (int)(blockIdx.x * T / gridDim.x);
-    r.hi = (int)((blockIdx.x + 1) * T / gridDim.x);
+    // contiguous ranges of equal cost: a Q3_K task (MOE_D_TASK_SB super-blocks)
+    // weighs D_W_ROUTED, a bf16 shared row D_W_SHARED
+    const long long cr = (long long)r.Tr * D_W_ROUTED;
+    const long long C = cr + (shared ? (long long)a.dim * D_W_SHARED : 0);
+    auto first_at = [&](long long c) -> int {
+        return c <= cr ? (int)((c + D_W_ROUTED - 1) / D_W_ROUTED)
+                       : r.Tr + (int)((c - cr + D_W_SHARED - 1) / D_W_SHARED);
+    };
+    r.lo = first_at(blockIdx.x * C / gridDim.x);
+    r.hi = first_at((blockIdx.x + 1) * C / gridDim.x);
     r.pair_lo = r.pair_hi = 0;
     if (r.lo < r.Tr && r.lo < r.hi) {
         const int p_lo = r.lo / r.tpr, p_hi = (min(r.hi, r.Tr) - 1) / r.tpr;
@@ -836,18 +839,49 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
         s_rows[q] = __ldcg(a.plan_rows + q);
         s_w[q] = __ldcg(a.plan_w + q);
     }
+    // q8_1(SwiGLU(g, u)) of the plan pairs this CTA's routed tasks touch, and
+    // bf16(SwiGLU(gs, us)) when it has shared rows; loads in batches, the first
+    // batch of both in flight together
     const int np = min(R.pair_hi - R.pair_lo, a.pair_cap);
     const int nblk = np * inter / 32;
-    for (int b = warp; b < nblk; b += MOE_CONSUMER_WARPS) {
-        const int pr = b / (inter / 32), bi = b % (inter / 32);
-        const size_t o = (size_t)(R.pair_lo + pr) * inter + bi * 32 + lane;
-        const float h = swiglu_f32(__ldcg(a.g + o), __ldcg(a.u + o), a.limit);
-        q8_store_smem(act + pr * arow, nb, bi, q8_quant_warp(h), false);
-    }
     const bool my_shared = shared && R.hi > R.Tr;
-    if (my_shared) {
-        for (int i = threadIdx.x; i < a.m * inter; i += MOE_CONSUMER_WARPS * 32)
-            hs[i] = f32_to_bf16(swiglu_f32(__ldcg(a.gs + i), __ldcg(a.us + i), a.limit));
+    const int nsh = my_shared ? a.m * inter : 0;
+    constexpr int HB = 8;  // q8 blocks a warp loads at once
+    constexpr int HS = 8;  // shared-expert values a thread loads at once
+    constexpr int CT = MOE_CONSUMER_WARPS * 32;
+    for (int r0 = 0;; ++r0) {
+        const int b0 = warp + r0 * MOE_CONSUMER_WARPS * HB, i0 = threadIdx.x + r0 * CT * HS;
+        if (b0 >= nblk && i0 >= nsh)
+            break;
+        float gv[HB], uv[HB], sg[HS], su[HS];
+#pragma unroll
+        for (int j = 0; j < HB; ++j) {
+            const int b = b0 + j * MOE_CONSUMER_WARPS;
+            const int pr = b / (inter / 32), bi = b % (inter / 32);
+            const size_t o = (size_t)(R.pair_lo + pr) * inter + bi * 32 + lane;
+            gv[j] = b < nblk ? __ldcg(a.g + o) : 0.0f;
+            uv[j] = b < nblk ? __ldcg(a.u + o) : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < HS; ++j) {
+            const int i = i0 + j * CT;
+            sg[j] = i < nsh ? __ldcg(a.gs + i) : 0.0f;
+            su[j] = i < nsh ? __ldcg(a.us + i) : 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < HB; ++j) {
+            const int b = b0 + j * MOE_CONSUMER_WARPS;
+            if (b < nblk) {
+                const int pr = b / (inter / 32), bi = b % (inter / 32);
+                q8_store_smem(act + pr * arow, nb, bi, q8_quant_warp(swiglu_f32(gv[j], uv[j], a.limit)), false);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < HS; ++j) {
+            const int i = i0 + j * CT;
+            if (i < nsh)
+                hs[i] = f32_to_bf16(swiglu_f32(sg[j], su[j], a.limit));
+        }
     }
     consumers_sync();
     // each token's pairs in plan order (pairs are grouped by ascending expert)
@@ -905,36 +939,26 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
             if (lane == 0)
                 mbar_arrive(&ring.empty[slot]);
         } else {
-            float acc[MOE_MAX_TOKENS];
-#pragma unroll
-            for (int tt = 0; tt < MOE_MAX_TOKENS; ++tt)
-                acc[tt] = 0.0f;
+            // one bf16 row of W2 against every token's bf16 SwiGLU output
             const uint4 *wr = reinterpret_cast<const uint4 *>(st);
-            for (int c = lane; c < inter / 8; c += 32) {
-                const uint4 wv = wr[c];
+            const uint4 *h4 = reinterpret_cast<const uint4 *>(hs);
+            with_m(a.m, [&](auto MC) {
+                constexpr int M = decltype(MC)::value;
+                float acc[M];
 #pragma unroll
-                for (int tt = 0; tt < MOE_MAX_TOKENS; ++tt) {
-                    if (tt < a.m) {
-                        const uint4 xv = reinterpret_cast<const uint4 *>(hs + (size_t)tt * inter)[c];
-                        float s = acc[tt];
-                        s = fmaf(bf16_lo(wv.x), bf16_lo(xv.x), s);
-                        s = fmaf(bf16_hi(wv.x), bf16_hi(xv.x), s);
-                        s = fmaf(bf16_lo(wv.y), bf16_lo(xv.y), s);
-                        s = fmaf(bf16_hi(wv.y), bf16_hi(xv.y), s);
-                        s = fmaf(bf16_lo(wv.z), bf16_lo(xv.z), s);
-                        s = fmaf(bf16_hi(wv.z), bf16_hi(xv.z), s);
-                        s = fmaf(bf16_lo(wv.w), bf16_lo(xv.w), s);
-                        s = fmaf(bf16_hi(wv.w), bf16_hi(xv.w), s);
-                        acc[tt] = s;
-                    }
+                for (int tt = 0; tt < M; ++tt)
+                    acc[tt] = 0.0f;
+                for (int c = lane; c < inter / 8; c += 32) {
+                    const uint4 wv = wr[c];
+#pragma unroll
+                    for (int tt = 0; tt < M; ++tt)
+                        acc[tt] = fma_bf16x8(wv, h4[(size_t)tt * (inter / 8) + c], acc[tt]);
                 }
-            }
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&ring.empty[slot]);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&ring.empty[slot]);
 #pragma unroll
-            for (int tt = 0; tt < MOE_MAX_TOKENS; ++tt) {
-                if (tt < a.m) {
+                for (int tt = 0; tt < M; ++tt) {
                     float v = acc[tt];
 #pragma unroll
                     for (int o = 16; o; o >>= 1)
@@ -942,7 +966,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
                     if (lane == 0)
                         a.sd[(size_t)tt * dim + t.row] = v;
                 }
-            }
+            });
         }
     }
 

@@ -11,13 +11,12 @@
 // Selection (page spark_model/layers/moe_v41.rs, fn softplus and
 // fn route_from_logits): score = f32(sqrt(softplus(l / temp))), key = score +
 // bias, stable descending order, top k, weights renormalised in f32. The
-// score is defined as the correctly rounded f32 of the exact value. FP64 is a
-// slow pipe on GB300, so each lane first ranks all its experts with a
-// single-precision score (CUDA's expf / log1pf / sqrtf, error a few ulp) and a
-// generous error bound, finds the k-th largest lower bound T, and evaluates
-// the double-precision score only for the candidates whose upper bound
-// reaches T. Every expert outside that set is provably below k candidates,
-// so the picks equal the ranking by exact keys.
+// score is the correctly rounded f32 of the exact value, evaluated in double
+// precision in the router epilogue, where every CTA takes a few of the rows
+// (FP64 is a slow pipe on GB300; spread over the CTAs its latency is paid
+// once). The selecting CTA is latency-bound: it reads everything it needs in
+// one round of loads, ranks each token with one warp (k rounds of a warp-wide
+// maximum over 64-bit sortable values), and only stores afterwards.
 #pragma once
 #include "moe_common.cuh"
 
@@ -80,120 +79,122 @@ __device__ __forceinline__ int rank_id(unsigned long long v) { return (int)(0xFF
 
 // ------------------------------------------------------------------ selection + plan (whole CTA, 256 threads)
 
-#define SEL_PER_WARP MOE_MAX_ROUTED  // values per warp in the first ranking stage
-
+// Shared memory of the selection: a fixed part, then per token its n sortable
+// values (u64) and n exact scores (f32).
 struct SelectSmem {
     int pick[MOE_MAX_TOKENS][MOE_MAX_TOPK];
-    float sc[MOE_MAX_TOKENS][MOE_MAX_TOPK];
     float w[MOE_MAX_TOKENS][MOE_MAX_TOPK];
     int flags[MOE_MAX_TOKENS];
-    int wflag[8];
-    unsigned long long v[8][SEL_PER_WARP];               // per warp: its experts' values
-    unsigned long long cand[8][MOE_MAX_TOPK];            // per warp: its k best
     int first[MOE_MAX_TOKENS * MOE_MAX_TOPK], rank[MOE_MAX_TOKENS * MOE_MAX_TOPK],
         ent[MOE_MAX_TOKENS * MOE_MAX_TOPK];
 };
 
-__device__ __forceinline__ void group_sync(int group, int gsz)
+__host__ __device__ inline size_t sel_v_off() { return align_up(sizeof(SelectSmem), 16); }
+__host__ __device__ inline size_t sel_bytes(int m, int n) { return sel_v_off() + (size_t)m * n * (8 + 4); }
+
+template <bool kGlobal>
+__device__ __forceinline__ float sel_ld(const float *p)
 {
-    if (gsz == 1)
-        __syncwarp();
+    if constexpr (kGlobal)
+        return __ldcg(p);  // written by other CTAs of this kernel: read at L2
     else
-        asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(gsz * 32) : "memory");
+        return *p;
 }
 
-// The picks of token t by a group of gsz warps from exact scores and keys.
-// Ranking by counting (no long shuffle chains): every value's rank is the
-// number of values ranking before it; stage 1 inside each warp over its
-// experts, stage 2 over the group's k best of each warp.
-__device__ void select_token_group(const RouteArgs &a, const float *logits, const float *scores,
-                                   const float *keys, int t, int group, int gsz, SelectSmem &sm)
+#define SEL_UNROLL 8
+
+// Selection for all m tokens (256 threads), then the plan: the distinct
+// picked experts in ascending id with their (expert, token) pairs, and the
+// header. logits, scores, keys: [m, n] in global memory (kGlobal) or shared;
+// slot: the slot-table row of every expert, already in shared memory.
+template <bool kGlobal>
+__device__ void select_and_plan(const RouteArgs &a, const float *logits, const float *scores, const float *keys,
+                                const int *slot, uint8_t *smem)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, wig = warp - group * gsz;
-    const int n = a.n, k = a.k, stride = gsz * 32;
-    const size_t row = (size_t)t * n;
-    const int per_lane = (n + stride - 1) / stride;  // <= SEL_PER_WARP / 32
-    bool nonfinite = false;
-    for (int i = 0; i < per_lane; ++i) {
-        const int e = wig * 32 + lane + i * stride;
-        unsigned long long v = 0ull;
-        if (e < n) {
-            const float key = keys[row + e];
-            nonfinite |= !isfinite(logits[row + e]) || !isfinite(key);
-            v = rank_value(key, e);
+    SelectSmem &sm = *reinterpret_cast<SelectSmem *>(smem);
+    unsigned long long *val = reinterpret_cast<unsigned long long *>(smem + sel_v_off());
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n = a.n, k = a.k, m = a.m, cap = m * k, mn = m * n;
+    float *sco = reinterpret_cast<float *>(val + (size_t)mn);
+    if (tid < MOE_MAX_TOKENS)
+        sm.flags[tid] = 0;
+    __syncthreads();
+
+    // one round of loads (SEL_UNROLL entries a thread in flight at once)
+    for (int b = 0; b < mn; b += 256 * SEL_UNROLL) {
+        float kk[SEL_UNROLL], ll[SEL_UNROLL], ss[SEL_UNROLL];
+#pragma unroll
+        for (int u = 0; u < SEL_UNROLL; ++u) {
+            const int i = b + tid + 256 * u;
+            kk[u] = i < mn ? sel_ld<kGlobal>(keys + i) : 0.0f;
+            ll[u] = i < mn ? sel_ld<kGlobal>(logits + i) : 0.0f;
+            ss[u] = i < mn ? sel_ld<kGlobal>(scores + i) : 0.0f;
         }
-        sm.v[warp][lane + 32 * i] = v;
-    }
-    if (lane < MOE_MAX_TOPK)
-        sm.cand[warp][lane] = 0ull;
-    const unsigned nf = __ballot_sync(0xffffffffu, nonfinite);
-    if (lane == 0)
-        sm.wflag[warp] = nf ? MOE_HDR_NONFINITE : 0;
-    __syncwarp();
-    const int nv = 32 * per_lane;
-    for (int i = 0; i < per_lane; ++i) {
-        const unsigned long long mv = sm.v[warp][lane + 32 * i];
-        if (mv != 0ull) {
-            int r = 0;
-            for (int j = 0; j < nv; ++j)
-                r += sm.v[warp][j] > mv;
-            if (r < k)
-                sm.cand[warp][r] = mv;
+#pragma unroll
+        for (int u = 0; u < SEL_UNROLL; ++u) {
+            const int i = b + tid + 256 * u;
+            if (i < mn) {
+                const int t = i / n, e = i - t * n;
+                val[i] = rank_value(kk[u], e);
+                sco[i] = ss[u];
+                if (!isfinite(ll[u]) || !isfinite(kk[u]))
+                    atomicOr(&sm.flags[t], MOE_HDR_NONFINITE);
+            }
         }
     }
-    group_sync(group, gsz);
-    if (wig == 0) {
-        // stage 2: the group's gsz * k candidates (<= 64), two per lane
-        const int nc = gsz * k;
-        for (int c = lane; c < nc; c += 32) {
-            const unsigned long long v = sm.cand[group * gsz + c / k][c % k];
-            if (v == 0ull)
-                continue;
-            int r = 0;
-            for (int j = 0; j < nc; ++j)
-                r += sm.cand[group * gsz + j / k][j % k] > v;
-            if (r < k) {
-                const int id = rank_id(v);
+    __syncthreads();
+
+    // token t = warp: k rounds of the warp-wide maximum (values are distinct:
+    // the id is in the low word); the owning lane (id % 32) removes the winner
+    // and rescans its own values, held in registers
+    if (warp < m) {
+        const int t = warp;
+        const unsigned long long *vt = val + (size_t)t * n;
+        const int per_lane = (n + 31) >> 5;
+        unsigned long long v[MOE_MAX_ROUTED / 32];  // lane's values e = lane + 32 i
+        unsigned long long best = 0ull;
+#pragma unroll
+        for (int i = 0; i < MOE_MAX_ROUTED / 32; ++i) {
+            const int e = lane + 32 * i;
+            v[i] = (i < per_lane && e < n) ? vt[e] : 0ull;
+            best = max(best, v[i]);
+        }
+        for (int r = 0; r < k; ++r) {
+            const unsigned hi = __reduce_max_sync(0xffffffffu, (unsigned)(best >> 32));
+            const unsigned lo = __reduce_max_sync(0xffffffffu, (unsigned)(best >> 32) == hi ? (unsigned)best : 0u);
+            const int id = rank_id(((unsigned long long)hi << 32) | lo);
+            if (lane == 0)
                 sm.pick[t][r] = id;
-                sm.sc[t][r] = scores[row + id];
+            if ((id & 31) == lane) {
+                best = 0ull;
+#pragma unroll
+                for (int i = 0; i < MOE_MAX_ROUTED / 32; ++i) {
+                    v[i] = i == (id >> 5) ? 0ull : v[i];
+                    best = max(best, v[i]);
+                }
             }
         }
         __syncwarp();
-        if (lane == 0) {
-            int fl = 0;
-            for (int w = 0; w < gsz; ++w)
-                fl |= sm.wflag[group * gsz + w];
-            sm.flags[t] = fl;
-            // weights in pick order, each step one f32 rounding
-            if (a.norm && k > 1) {
-                float sum = 0.0f;
-                for (int i = 0; i < k; ++i)
-                    sum = __fadd_rn(sum, sm.sc[t][i]);
-                sum = __fadd_rn(sum, 1e-20f);
-                for (int i = 0; i < k; ++i)
-                    sm.w[t][i] = __fmul_rn(__fdiv_rn(sm.sc[t][i], sum), a.route_scale);
-            } else {
-                for (int i = 0; i < k; ++i)
-                    sm.w[t][i] = __fmul_rn(sm.sc[t][i], a.route_scale);
-            }
+        // weights in pick order, each step one f32 rounding
+        float sv[MOE_MAX_TOPK];
+#pragma unroll
+        for (int i = 0; i < MOE_MAX_TOPK; ++i)
+            sv[i] = i < k ? sco[(size_t)t * n + sm.pick[t][i]] : 0.0f;
+        float sum = 0.0f;
+#pragma unroll
+        for (int i = 0; i < MOE_MAX_TOPK; ++i)
+            if (i < k)
+                sum = __fadd_rn(sum, sv[i]);
+        sum = __fadd_rn(sum, 1e-20f);
+        if (lane < k) {
+            float s = 0.0f;
+#pragma unroll
+            for (int i = 0; i < MOE_MAX_TOPK; ++i)
+                s = lane == i ? sv[i] : s;
+            sm.w[t][lane] = (a.norm && k > 1) ? __fmul_rn(__fdiv_rn(s, sum), a.route_scale)
+                                              : __fmul_rn(s, a.route_scale);
         }
     }
-}
-
-// Selection for all m tokens, then the plan: the distinct picked experts in
-// ascending id with their (expert, token) pairs, pair-major, and the header.
-__device__ void select_and_plan(const RouteArgs &a, const float *logits, const float *scores, const float *keys,
-                                SelectSmem &sm)
-{
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int n = a.n, k = a.k, m = a.m, cap = m * k;
-    // warps in groups: all 8 on one token for m = 1, down to one warp per token
-    int gsz = 8;
-    while (gsz > 1 && gsz * m > 8)
-        gsz >>= 1;
-    const int group = warp / gsz;
-    if (group < m)
-        select_token_group(a, logits, scores, keys, group, group, gsz, sm);
     __syncthreads();
     // pairs: entry q = (token q / k, its pick q % k); rank by (expert, token)
     if (tid < cap) {
@@ -227,9 +228,9 @@ __device__ void select_and_plan(const RouteArgs &a, const float *logits, const f
         int p = 0;
         for (int q = 0; q < cap; ++q)
             p += sm.first[q] && sm.ent[q] < e;
-        const int slot = __ldg(a.slot_row + e);
+        const int sl = slot[e];
         const unsigned long long base =
-            (unsigned long long)a.arena_base + (unsigned long long)(slot < 0 ? 0 : slot) * a.slot_bytes;
+            (unsigned long long)a.arena_base + (unsigned long long)(sl < 0 ? 0 : sl) * a.slot_bytes;
         a.ptrs[p] = base + a.gate_off;
         a.ptrs[cap + p] = base + a.up_off;
         a.ptrs[2 * cap + p] = base + a.down_off;
@@ -247,24 +248,18 @@ __device__ void select_and_plan(const RouteArgs &a, const float *logits, const f
     if (tid >= 32 && tid < 32 + m) {
         const int t = tid - 32;
         int32_t *h = a.hdr + (size_t)t * (1 + 3 * k);
-        int sorted[MOE_MAX_TOPK];
         int status = sm.flags[t];
         for (int i = 0; i < k; ++i) {
-            h[1 + i] = sm.pick[t][i];
-            h[1 + k + i] = __float_as_int(sm.w[t][i]);
             const int v = sm.pick[t][i];
-            int j = i;
-            while (j > 0 && sorted[j - 1] > v) {
-                sorted[j] = sorted[j - 1];
-                --j;
-            }
-            sorted[j] = v;
-        }
-        for (int i = 0; i < k; ++i) {
-            const int slot = __ldg(a.slot_row + sorted[i]);
-            if (slot < 0)
+            h[1 + i] = v;
+            h[1 + k + i] = __float_as_int(sm.w[t][i]);
+            int pos = 0;  // the picks of a token are distinct: position in ascending id
+            for (int j = 0; j < k; ++j)
+                pos += sm.pick[t][j] < v;
+            const int sl = slot[v];
+            if (sl < 0)
                 status |= MOE_HDR_MISS;
-            h[1 + 2 * k + i] = slot < 0 ? 0 : slot;
+            h[1 + 2 * k + pos] = sl < 0 ? 0 : sl;
         }
         h[0] = status;
     }
@@ -272,20 +267,26 @@ __device__ void select_and_plan(const RouteArgs &a, const float *logits, const f
 
 // ------------------------------------------------------------------ kernels
 
-// smem: [0,128) barrier + flag; then the CTA's router rows, x, warp partials;
-// the last CTA reuses the rows area for the selection
+// the router's constants staged before the wait: the slot table (for the
+// selection) and the bias of the CTA's rows
+__host__ __device__ inline size_t router_pre_bytes(int n, int rows) { return align_up(4 * ((size_t)n + rows), 128); }
+
+// smem: [0,128) barrier + flag; the staged constants; then the CTA's router
+// rows, x, logits; the last CTA reuses the rows area for the selection
 __global__ void __launch_bounds__(256) moe_router_kernel(RouteArgs a)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
     int *s_last = reinterpret_cast<int *>(smem + 8);
-    uint16_t *sw = reinterpret_cast<uint16_t *>(smem + 128);
+    int *s_slot = reinterpret_cast<int *>(smem + 128);
+    float *s_bias = reinterpret_cast<float *>(s_slot + a.n);
+    uint16_t *sw = reinterpret_cast<uint16_t *>(smem + 128 + router_pre_bytes(a.n, a.rows_per_cta));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int dim = a.dim, m = a.m;
     const int row0 = blockIdx.x * a.rows_per_cta;
     const int nrows = min(a.rows_per_cta, a.n - row0);
     uint16_t *sx = sw + (size_t)a.rows_per_cta * dim;
-    float *red = reinterpret_cast<float *>(sx + (size_t)m * dim);  // [8 warps][rows][m]
+    float *red = reinterpret_cast<float *>(sx + (size_t)m * dim);  // logits [rows][m]
     const uint32_t wbytes = (uint32_t)nrows * dim * 2;
 
     if (tid == 0) {
@@ -302,6 +303,14 @@ __global__ void __launch_bounds__(256) moe_router_kernel(RouteArgs a)
         for (uint32_t off = 0; off < wbytes; off += 32768u)
             bulk_g2s(dst + off, src + off, min(32768u, wbytes - off), bar, pol);
     }
+    // the bias and the slot table are layer constants too (kernels that write
+    // them, such as the slot-table update, complete before a dependent starts)
+    if (a.do_select) {
+        for (int e = tid; e < a.n; e += blockDim.x)
+            s_slot[e] = __ldg(a.slot_row + e);
+        if (tid < nrows)
+            s_bias[tid] = __ldg(a.bias + row0 + tid);
+    }
     pdl_wait();  // x is produced by the previous kernel
     pdl_launch_dependents();
     {
@@ -314,39 +323,48 @@ __global__ void __launch_bounds__(256) moe_router_kernel(RouteArgs a)
     const bool ok = nrows <= 0 || mbar_wait(bar, 0, a.ctrl + MOE_CTRL_STATUS);
     if (__syncthreads_and(ok) == 0)
         return;
-    // logits: thread-strided 16-byte chunks, warp butterfly, then the 8 warp
-    // partials in order -- a fixed order per (token, row), whatever m is
+    // logits: one warp per row, all tokens at once; lane j takes the 16-byte
+    // chunks j + 32 i into four partial sums (i mod 4), added pairwise, then a
+    // warp butterfly -- a fixed order per (token, row), whatever m is
     const int nch = dim / 8;
-    for (int r = 0; r < nrows; ++r) {
-        const uint4 *wr = reinterpret_cast<const uint4 *>(sw + (size_t)r * dim);
-        for (int t = 0; t < m; ++t) {
-            const uint4 *xr = reinterpret_cast<const uint4 *>(sx + (size_t)t * dim);
-            float acc = 0.0f;
-            for (int c = tid; c < nch; c += blockDim.x) {
-                const uint4 wv = wr[c], xv = xr[c];
-                acc = fmaf(bf16_lo(wv.x), bf16_lo(xv.x), acc);
-                acc = fmaf(bf16_hi(wv.x), bf16_hi(xv.x), acc);
-                acc = fmaf(bf16_lo(wv.y), bf16_lo(xv.y), acc);
-                acc = fmaf(bf16_hi(wv.y), bf16_hi(xv.y), acc);
-                acc = fmaf(bf16_lo(wv.z), bf16_lo(xv.z), acc);
-                acc = fmaf(bf16_hi(wv.z), bf16_hi(xv.z), acc);
-                acc = fmaf(bf16_lo(wv.w), bf16_lo(xv.w), acc);
-                acc = fmaf(bf16_hi(wv.w), bf16_hi(xv.w), acc);
+    with_m(m, [&](auto MC) {
+        constexpr int M = decltype(MC)::value;
+        const uint4 *x4 = reinterpret_cast<const uint4 *>(sx);
+        for (int r = warp; r < nrows; r += blockDim.x >> 5) {
+            const uint4 *wr = reinterpret_cast<const uint4 *>(sw + (size_t)r * dim);
+            float acc[M][4];
+#pragma unroll
+            for (int t = 0; t < M; ++t)
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    acc[t][q] = 0.0f;
+            for (int c0 = lane; c0 < nch; c0 += 128) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int c = c0 + 32 * q;
+                    if (c < nch) {
+                        const uint4 wv = wr[c];
+#pragma unroll
+                        for (int t = 0; t < M; ++t)
+                            acc[t][q] = fma_bf16x8(wv, x4[(size_t)t * nch + c], acc[t][q]);
+                    }
+                }
             }
 #pragma unroll
-            for (int o = 16; o; o >>= 1)
-                acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            if (lane == 0)
-                red[((size_t)warp * a.rows_per_cta + r) * m + t] = acc;
+            for (int t = 0; t < M; ++t) {
+                float v = (acc[t][0] + acc[t][1]) + (acc[t][2] + acc[t][3]);
+#pragma unroll
+                for (int o = 16; o; o >>= 1)
+                    v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (lane == 0)
+                    red[(size_t)r * m + t] = v;
+            }
         }
-    }
+    });
     __syncthreads();
-    const int nw = blockDim.x >> 5;
     for (int i = tid; i < nrows * m; i += blockDim.x) {
         const int r = i / m, t = i % m;
-        float l = 0.0f;
-        for (int w = 0; w < nw; ++w)
-            l += red[((size_t)w * a.rows_per_cta + r) * m + t];
+        const float l = red[i];
         const size_t o = (size_t)t * a.n + row0 + r;
         a.logits[o] = l;
         if (a.do_select) {
@@ -354,7 +372,7 @@ __global__ void __launch_bounds__(256) moe_router_kernel(RouteArgs a)
             // threads of every CTA in parallel instead of in the selecting CTA
             const float sc = score_exact(l, a.temp);
             a.scores[o] = sc;
-            a.keys[o] = __fadd_rn(sc, __ldg(a.bias + row0 + r));
+            a.keys[o] = __fadd_rn(sc, s_bias[r]);
         }
     }
     if (!a.do_select)
@@ -371,8 +389,8 @@ __global__ void __launch_bounds__(256) moe_router_kernel(RouteArgs a)
     __syncthreads();
     if (!*s_last)
         return;
-    SelectSmem *sel = reinterpret_cast<SelectSmem *>(sw);  // the weights are no longer needed
-    select_and_plan(a, a.logits, a.scores, a.keys, *sel);
+    // the rows area is no longer needed: it holds the selection
+    select_and_plan<true>(a, a.logits, a.scores, a.keys, s_slot, reinterpret_cast<uint8_t *>(sw));
     if (tid == 0)
         atomicExch(a.ctrl + MOE_CTRL_TICKET, 0u);
 }
@@ -382,18 +400,21 @@ __global__ void __launch_bounds__(256) moe_router_kernel(RouteArgs a)
 __global__ void __launch_bounds__(256) moe_select_kernel(RouteArgs a)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
-    SelectSmem &sel = *reinterpret_cast<SelectSmem *>(smem);
-    float *sc = reinterpret_cast<float *>(smem + align_up(sizeof(SelectSmem), 128));
-    float *ky = sc + (size_t)a.m * a.n;
+    const size_t mn = (size_t)a.m * a.n;
+    float *sc = reinterpret_cast<float *>(smem + align_up(sel_bytes(a.m, a.n), 128));
+    float *ky = sc + mn;
+    int *slot = reinterpret_cast<int *>(ky + mn);
     pdl_wait();
     pdl_launch_dependents();
-    for (int i = threadIdx.x; i < a.m * a.n; i += blockDim.x) {
+    for (int e = threadIdx.x; e < a.n; e += blockDim.x)
+        slot[e] = __ldg(a.slot_row + e);
+    for (int i = threadIdx.x; i < (int)mn; i += blockDim.x) {
         const float s = score_exact(a.logits[i], a.temp);
         sc[i] = s;
         ky[i] = __fadd_rn(s, __ldg(a.bias + i % a.n));
     }
     __syncthreads();
-    select_and_plan(a, a.logits, sc, ky, sel);
+    select_and_plan<false>(a, a.logits, sc, ky, slot, smem);
 }
 
 }  // namespace moe

@@ -90,6 +90,20 @@ def assert_logits_close(got, ref):
         assert np.all(np.abs(got[t] - ref[t]) <= bound), (t, np.abs(got[t] - ref[t]).max())
 
 
+def assert_weights_close(cfg, w, ref_w, dl):
+    """Routing weights against the oracle's when the logits differ by at most dl.
+
+    d ln(sqrt(softplus(x))) / dx = sigmoid(x) / (2 softplus(x)) <= 1/2, since
+    ln(1 + y) >= y / (1 + y); above the x > 20 cut the score is sqrt(x), slope
+    1/(2x). So each score moves by at most dl / (2 temp) relatively, and a
+    renormalised weight (a score over the sum of k scores) by at most twice
+    that; the f32 roundings of the sum, quotient and product add k + 4 ulp."""
+    w = np.asarray(w, np.float64)
+    ref_w = np.asarray(ref_w, np.float64)
+    rel = dl / cfg.gate_temp + (cfg.topk + 4) * 2.0 ** -24
+    assert np.all(np.abs(w - ref_w) <= rel * np.abs(ref_w)), (w, ref_w, dl)
+
+
 def keys_of(cfg, logits, bias):
     """Exact-rounded keys as the oracle defines them (for near-tie detection)."""
     _, _, scores, _ = oracle.route(ocfg(cfg), logits, bias)

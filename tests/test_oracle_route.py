@@ -158,3 +158,30 @@ def test_temperature_divides_in_f32():
     s1, _ = oracle.score(3.0, 2.0)
     s2, _ = oracle.score(1.5, 1.0)
     assert s1 == s2
+
+
+@pytest.mark.parametrize("temp", [1.0, 0.7])
+def test_weight_tolerance_covers_logit_perturbations(temp):
+    """The bound the GPU tests use for weights against the oracle (helpers'
+    assert_weights_close): perturbing the oracle's logits by at most dl moves
+    each renormalised weight by at most dl / temp relatively (plus roundings),
+    whenever the picks stay the same."""
+    from helpers import assert_weights_close
+    import moe_decode_quantized_gb300 as moe
+    cfg = moe.Config(dim=4096, inter=2048, n_routed=384, topk=6, gate_temp=temp)
+    c = oracle.cfg(4096, 2048, 384, 6, True, temp, 2.5, 7.0)
+    rng = np.random.default_rng(5)
+    checked = 0
+    for trial in range(40):
+        logits = rng.normal(0, 1.5, (1, 384)).astype(np.float32)
+        bias = rng.uniform(-0.1, 0.1, 384).astype(np.float32)
+        dl = float(10.0 ** rng.uniform(-7, -4))
+        moved = (logits + rng.uniform(-dl, dl, logits.shape)).astype(np.float32)
+        dl_real = float(np.abs(moved.astype(np.float64) - logits).max())
+        p0, w0, _, _ = oracle.route(c, logits, bias)
+        p1, w1, _, _ = oracle.route(c, moved, bias)
+        if list(p0[0]) != list(p1[0]):
+            continue
+        assert_weights_close(cfg, w1[0], w0[0], dl_real)
+        checked += 1
+    assert checked >= 30
