@@ -172,6 +172,16 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// Atomic add at GPU scope with acquire-release semantics: releases what the
+// calling thread (and, after a CTA barrier, its CTA) wrote before, acquires
+// what the earlier adders released. Returns the old value.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(uint32_t *p, unsigned v)
+{
+    unsigned old;
+    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 // Programmatic dependent launch. wait: block until the preceding kernel in
 // the stream has completed and its memory is visible (a no-op without a
 // programmatic predecessor). launch_dependents: let the next kernel start.

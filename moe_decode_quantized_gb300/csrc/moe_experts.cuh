@@ -723,32 +723,31 @@ __device__ __forceinline__ DRange d_range(const DArgs &a, bool shared)
     return r;
 }
 
-// acc, residual and x_next of row group rg, by one warp: per token its
-// pairs in plan order (ascending expert id), then the shared row
-__device__ void finish_row_group(const DArgs &a, int rg, int rd, bool shared, const int *s_tp,
-                                 const float *s_w)
+// acc, residual and x_next of row r for token t: the token's pairs in plan
+// order (ascending expert id), then the shared row
+__device__ __forceinline__ void finish_row(const DArgs &a, int t, int r, bool shared, const int *s_tp,
+                                           const float *s_w)
 {
-    const int lane = threadIdx.x & 31, k = a.k;
-    for (int it = lane; it < a.m * rd; it += 32) {
-        const int t = it / rd, r = rg * rd + it % rd;
-        float d[MOE_MAX_TOPK];
+    const int k = a.k;
+    float d[MOE_MAX_TOPK];
 #pragma unroll
-        for (int i = 0; i < MOE_MAX_TOPK; ++i)
-            d[i] = i < k ? __ldcg(a.down + (size_t)s_tp[t * MOE_MAX_TOPK + i] * a.dim + r) : 0.0f;
-        float acc = 0.0f;
+    for (int i = 0; i < MOE_MAX_TOPK; ++i)
+        d[i] = i < k ? __ldcg(a.down + (size_t)s_tp[t * MOE_MAX_TOPK + i] * a.dim + r) : 0.0f;
+    const float sdv = shared ? __ldcg(a.sd + (size_t)t * a.dim + r) : 0.0f;
+    const float res0 = a.residual ? a.residual[(size_t)t * a.dim + r] : 0.0f;
+    float acc = 0.0f;
 #pragma unroll
-        for (int i = 0; i < MOE_MAX_TOPK; ++i)
-            if (i < k)
-                acc = __fadd_rn(acc, __fmul_rn(s_w[s_tp[t * MOE_MAX_TOPK + i]], d[i]));
-        if (shared)
-            acc = __fadd_rn(acc, __ldcg(a.sd + (size_t)t * a.dim + r));
-        a.acc[(size_t)t * a.dim + r] = acc;
-        if (a.residual) {
-            const float res = __fadd_rn(a.residual[(size_t)t * a.dim + r], acc);
-            a.residual[(size_t)t * a.dim + r] = res;
-            if (a.x_next)
-                a.x_next[(size_t)t * a.dim + r] = f32_to_bf16(res);
-        }
+    for (int i = 0; i < MOE_MAX_TOPK; ++i)
+        if (i < k)
+            acc = __fadd_rn(acc, __fmul_rn(s_w[s_tp[t * MOE_MAX_TOPK + i]], d[i]));
+    if (shared)
+        acc = __fadd_rn(acc, sdv);
+    a.acc[(size_t)t * a.dim + r] = acc;
+    if (a.residual) {
+        const float res = __fadd_rn(res0, acc);
+        a.residual[(size_t)t * a.dim + r] = res;
+        if (a.x_next)
+            a.x_next[(size_t)t * a.dim + r] = f32_to_bf16(res);
     }
 }
 
@@ -970,12 +969,12 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
         }
     }
 
-    // Row-group tickets, once per CTA: after all of this CTA's tasks, one
-    // fence, then for every row group it touched one atomic adding its count
-    // of tasks there; the CTA whose addition completes a group finishes it.
-    consumers_sync();
-    __threadfence();
-    consumers_sync();
+    // Row-group tickets, once per CTA: after all of this CTA's tasks, for
+    // every row group it touched one acq_rel atomic adding its count of tasks
+    // there (release: the CTA's down rows, ordered before it by the barrier;
+    // acquire: the other CTAs' rows of a group it completes). The CTA whose
+    // addition completes a group finishes it.
+    constexpr int CTH = MOE_CONSUMER_WARPS * 32;
     int *s_fin = s_rows + D_FIN;
     int *s_nfin = s_rows + D_NFIN;
     if (threadIdx.x == 0)
@@ -983,7 +982,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
     consumers_sync();
     const int ngroups = dim / rd;
     const int hiR = min(R.hi, R.Tr), s_lo = max(R.lo, R.Tr) - R.Tr, s_hi = max(R.hi, R.Tr) - R.Tr;
-    for (int g = threadIdx.x; g < ngroups; g += MOE_CONSUMER_WARPS * 32) {
+    auto count_in = [&](int g) {
         int cnt = 0;
         if (R.lo < hiR) {
             // experts p with lo <= p * tpr + g < hiR
@@ -994,19 +993,32 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
         }
         if (shared && s_lo < s_hi)
             cnt += max(0, min(s_hi, (g + 1) * rd) - max(s_lo, g * rd));
-        if (cnt > 0 && atomicAdd(a.rgcnt + g, (unsigned)cnt) + (unsigned)cnt == expected) {
-            s_fin[atomicAdd(s_nfin, 1)] = g;  // at most ngroups entries
+        return cnt;
+    };
+    for (int g0 = threadIdx.x; g0 < ngroups; g0 += 2 * CTH) {
+        int cnt[2];
+        unsigned old[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {  // both atomics in flight together
+            const int g = g0 + j * CTH;
+            cnt[j] = g < ngroups ? count_in(g) : 0;
+            old[j] = cnt[j] > 0 ? atom_add_acq_rel_gpu(a.rgcnt + g, (unsigned)cnt[j]) : 0u;
         }
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            if (cnt[j] > 0 && old[j] + (unsigned)cnt[j] == expected)
+                s_fin[atomicAdd(s_nfin, 1)] = g0 + j * CTH;  // at most ngroups entries
     }
     consumers_sync();
-    const int nfin = min(*s_nfin, ngroups);
-    if (nfin > 0)
-        __threadfence();
-    for (int f = warp; f < nfin; f += MOE_CONSUMER_WARPS) {
-        finish_row_group(a, s_fin[f], rd, shared, s_tp, s_w);
-        if (lane == 0)
-            atomicExch(a.rgcnt + s_fin[f], 0u);
+    // the rows of every group this CTA completed, spread over all consumer
+    // threads so that their loads are in flight together
+    const int nfin = min(*s_nfin, ngroups), per = a.m * rd;
+    for (int it = threadIdx.x; it < nfin * per; it += CTH) {
+        const int f = it / per, rem = it - f * per;
+        finish_row(a, rem / rd, s_fin[f] * rd + rem % rd, shared, s_tp, s_w);
     }
+    for (int f = threadIdx.x; f < nfin; f += CTH)
+        atomicExch(a.rgcnt + s_fin[f], 0u);
 }
 
 // ------------------------------------------------------------------ standalone q8_1 / swiglu

@@ -82,12 +82,59 @@ __device__ __forceinline__ int rank_id(unsigned long long v) { return (int)(0xFF
 // Shared memory of the selection: a fixed part, then per token its n sortable
 // values (u64) and n exact scores (f32).
 struct SelectSmem {
+    unsigned long long cand[8][MOE_MAX_TOPK];               // per warp: the k best of its share
+    unsigned long long fin[MOE_MAX_TOKENS][MOE_MAX_TOPK];   // per token: its k best
     int pick[MOE_MAX_TOKENS][MOE_MAX_TOPK];
     float w[MOE_MAX_TOKENS][MOE_MAX_TOPK];
     int flags[MOE_MAX_TOKENS];
-    int first[MOE_MAX_TOKENS * MOE_MAX_TOPK], rank[MOE_MAX_TOKENS * MOE_MAX_TOPK],
-        ent[MOE_MAX_TOKENS * MOE_MAX_TOPK];
+    int first[MOE_MAX_TOKENS * MOE_MAX_TOPK], ent[MOE_MAX_TOKENS * MOE_MAX_TOPK];
 };
+
+// k rounds of the warp-wide maximum over PL values per lane (distinct; 0
+// marks an empty place and ranks last): out[r] = the r-th largest, written
+// by lane 0. The lane holding the winner removes it and rescans its values.
+template <int PL>
+__device__ __forceinline__ void warp_topk(unsigned long long (&v)[PL], int k, unsigned long long *out)
+{
+    const int lane = threadIdx.x & 31;
+    unsigned long long best = 0ull;
+#pragma unroll
+    for (int i = 0; i < PL; ++i)
+        best = max(best, v[i]);
+    for (int r = 0; r < k; ++r) {
+        const unsigned hi = __reduce_max_sync(0xffffffffu, (unsigned)(best >> 32));
+        const unsigned lo = __reduce_max_sync(0xffffffffu, (unsigned)(best >> 32) == hi ? (unsigned)best : 0u);
+        const unsigned long long win = ((unsigned long long)hi << 32) | lo;
+        if (lane == 0)
+            out[r] = win;
+        if (win != 0ull && best == win) {
+            best = 0ull;
+#pragma unroll
+            for (int i = 0; i < PL; ++i) {
+                v[i] = v[i] == win ? 0ull : v[i];
+                best = max(best, v[i]);
+            }
+        }
+    }
+}
+
+// Calls f with IntC<PL>, PL = per_lane rounded up to a power of two (<= 32)
+template <typename F>
+__device__ __forceinline__ void with_per_lane(int per_lane, F &&f)
+{
+    if (per_lane <= 1)
+        f(IntC<1>{});
+    else if (per_lane <= 2)
+        f(IntC<2>{});
+    else if (per_lane <= 4)
+        f(IntC<4>{});
+    else if (per_lane <= 8)
+        f(IntC<8>{});
+    else if (per_lane <= 16)
+        f(IntC<16>{});
+    else
+        f(IntC<32>{});
+}
 
 __host__ __device__ inline size_t sel_v_off() { return align_up(sizeof(SelectSmem), 16); }
 __host__ __device__ inline size_t sel_bytes(int m, int n) { return sel_v_off() + (size_t)m * n * (8 + 4); }
@@ -144,109 +191,140 @@ __device__ void select_and_plan(const RouteArgs &a, const float *logits, const f
     }
     __syncthreads();
 
-    // token t = warp: k rounds of the warp-wide maximum (values are distinct:
-    // the id is in the low word); the owning lane (id % 32) removes the winner
-    // and rescans its own values, held in registers
-    if (warp < m) {
-        const int t = warp;
+    // Ranking. Each token has a group of gsz warps (8 for one token, down to
+    // one warp per token); each warp takes the k best of its share (the
+    // experts lane + 32 (wig + gsz i)), then the group's first warp takes the
+    // k best of those gsz * k candidates.
+    int gsz = 8;
+    while (gsz > 1 && gsz * m > 8)
+        gsz >>= 1;
+    const int group = warp / gsz, wig = warp - group * gsz;
+    if (group < m) {
+        const int t = group;
         const unsigned long long *vt = val + (size_t)t * n;
-        const int per_lane = (n + 31) >> 5;
-        unsigned long long v[MOE_MAX_ROUTED / 32];  // lane's values e = lane + 32 i
-        unsigned long long best = 0ull;
+        const int stride = 32 * gsz;
+        unsigned long long *fin = sm.fin[t];
+        unsigned long long *out1 = gsz == 1 ? fin : sm.cand[warp];
+        with_per_lane((n + stride - 1) / stride, [&](auto PC) {
+            constexpr int PL = decltype(PC)::value;
+            unsigned long long v[PL];
 #pragma unroll
-        for (int i = 0; i < MOE_MAX_ROUTED / 32; ++i) {
-            const int e = lane + 32 * i;
-            v[i] = (i < per_lane && e < n) ? vt[e] : 0ull;
-            best = max(best, v[i]);
-        }
-        for (int r = 0; r < k; ++r) {
-            const unsigned hi = __reduce_max_sync(0xffffffffu, (unsigned)(best >> 32));
-            const unsigned lo = __reduce_max_sync(0xffffffffu, (unsigned)(best >> 32) == hi ? (unsigned)best : 0u);
-            const int id = rank_id(((unsigned long long)hi << 32) | lo);
-            if (lane == 0)
-                sm.pick[t][r] = id;
-            if ((id & 31) == lane) {
-                best = 0ull;
+            for (int i = 0; i < PL; ++i) {
+                const int e = wig * 32 + lane + i * stride;
+                v[i] = e < n ? vt[e] : 0ull;
+            }
+            warp_topk<PL>(v, k, out1);
+        });
+        if (gsz > 1) {
+            asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(gsz * 32) : "memory");
+            if (wig == 0) {
+                const int nc = gsz * k;  // <= 64
+                unsigned long long v[2];
 #pragma unroll
-                for (int i = 0; i < MOE_MAX_ROUTED / 32; ++i) {
-                    v[i] = i == (id >> 5) ? 0ull : v[i];
-                    best = max(best, v[i]);
+                for (int j = 0; j < 2; ++j) {
+                    const int c = lane + 32 * j;
+                    v[j] = c < nc ? sm.cand[group * gsz + c / k][c % k] : 0ull;
                 }
+                warp_topk<2>(v, k, fin);
             }
         }
-        __syncwarp();
-        // weights in pick order, each step one f32 rounding
-        float sv[MOE_MAX_TOPK];
-#pragma unroll
-        for (int i = 0; i < MOE_MAX_TOPK; ++i)
-            sv[i] = i < k ? sco[(size_t)t * n + sm.pick[t][i]] : 0.0f;
-        float sum = 0.0f;
-#pragma unroll
-        for (int i = 0; i < MOE_MAX_TOPK; ++i)
-            if (i < k)
-                sum = __fadd_rn(sum, sv[i]);
-        sum = __fadd_rn(sum, 1e-20f);
-        if (lane < k) {
-            float s = 0.0f;
+        if (wig == 0) {
+            // lane 0 holds the picks; a pick outside [0, n) (fewer than k
+            // values, impossible for k <= n) would index the tables
+            if (lane == 0) {
+                for (int r = 0; r < k; ++r) {
+                    int id = rank_id(fin[r]);
+                    if (id < 0 || id >= n) {
+                        if (a.ctrl)
+                            atomicOr(a.ctrl + MOE_CTRL_STATUS, (uint32_t)MOE_WS_PLAN);
+                        id = 0;
+                    }
+                    sm.pick[t][r] = id;
+                }
+            }
+            __syncwarp();
+            // weights in pick order, each step one f32 rounding
+            float sv[MOE_MAX_TOPK];
 #pragma unroll
             for (int i = 0; i < MOE_MAX_TOPK; ++i)
-                s = lane == i ? sv[i] : s;
-            sm.w[t][lane] = (a.norm && k > 1) ? __fmul_rn(__fdiv_rn(s, sum), a.route_scale)
-                                              : __fmul_rn(s, a.route_scale);
+                sv[i] = i < k ? sco[(size_t)t * n + sm.pick[t][i]] : 0.0f;
+            float sum = 0.0f;
+#pragma unroll
+            for (int i = 0; i < MOE_MAX_TOPK; ++i)
+                if (i < k)
+                    sum = __fadd_rn(sum, sv[i]);
+            sum = __fadd_rn(sum, 1e-20f);
+            if (lane < k) {
+                float sc = 0.0f;
+#pragma unroll
+                for (int i = 0; i < MOE_MAX_TOPK; ++i)
+                    sc = lane == i ? sv[i] : sc;
+                sm.w[t][lane] = (a.norm && k > 1) ? __fmul_rn(__fdiv_rn(sc, sum), a.route_scale)
+                                                  : __fmul_rn(sc, a.route_scale);
+            }
         }
-    }
-    __syncthreads();
-    // pairs: entry q = (token q / k, its pick q % k); rank by (expert, token)
-    if (tid < cap) {
-        int e = sm.pick[tid / k][tid % k];
-        if (e < 0 || e >= n) {  // defensive: a pick outside [0, n) would index the tables
-            if (a.ctrl)
-                atomicOr(a.ctrl + MOE_CTRL_STATUS, (uint32_t)MOE_WS_PLAN);
-            e = 0;
-            sm.pick[tid / k][tid % k] = 0;
-        }
-        sm.ent[tid] = e;
-    }
-    __syncthreads();
-    if (tid < cap) {
-        const int e = sm.ent[tid], t = tid / k;
-        int rank = 0, earlier = 0;
-        for (int q = 0; q < cap; ++q) {
-            const int e2 = sm.ent[q], t2 = q / k;
-            rank += e2 < e || (e2 == e && t2 < t);
-            earlier += e2 == e && t2 < t;
-        }
-        sm.rank[tid] = rank;
-        sm.first[tid] = earlier == 0;
-        a.plan_rows[rank] = t;
-        a.plan_w[rank] = sm.w[t][tid % k];
     }
     __syncthreads();
     const int po = m * (1 + 3 * k);  // plan tail of the header
-    if (tid < cap && sm.first[tid]) {
-        const int e = sm.ent[tid];
-        int p = 0;
-        for (int q = 0; q < cap; ++q)
-            p += sm.first[q] && sm.ent[q] < e;
-        const int sl = slot[e];
-        const unsigned long long base =
-            (unsigned long long)a.arena_base + (unsigned long long)(sl < 0 ? 0 : sl) * a.slot_bytes;
-        a.ptrs[p] = base + a.gate_off;
-        a.ptrs[cap + p] = base + a.up_off;
-        a.ptrs[2 * cap + p] = base + a.down_off;
-        a.hdr[po + 1 + p] = sm.rank[tid];
-        a.hdr[po + 2 + cap + p] = e;
-    }
-    if (tid == 0) {
+    if (warp == 0) {
+        // the plan, by one warp: pair q = (token q / k, its pick q % k), two per
+        // lane; ranked by (expert, token); the distinct experts in ascending id
+        int eq[2], tq[2], rq[2];
+        bool fq[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int q = lane + 32 * j;
+            eq[j] = q < cap ? sm.pick[q / k][q % k] : 0;
+            tq[j] = q / k;
+            if (q < cap)
+                sm.ent[q] = eq[j];
+        }
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int q = lane + 32 * j;
+            rq[j] = 0;
+            fq[j] = false;
+            if (q < cap) {
+                int earlier = 0;
+                for (int q2 = 0; q2 < cap; ++q2) {
+                    const int e2 = sm.ent[q2], t2 = q2 / k;
+                    rq[j] += e2 < eq[j] || (e2 == eq[j] && t2 < tq[j]);
+                    earlier += e2 == eq[j] && t2 < tq[j];
+                }
+                fq[j] = earlier == 0;
+                sm.first[q] = fq[j];
+                a.plan_rows[rq[j]] = tq[j];
+                a.plan_w[rq[j]] = sm.w[tq[j]][q % k];
+            }
+        }
+        __syncwarp();
         int ne = 0;
-        for (int q = 0; q < cap; ++q)
-            ne += sm.first[q];
-        a.hdr[po] = ne;
-        a.hdr[po + 1 + ne] = cap;
-    }
-    // header rows: status, picks, weight bits, slots of the picks in ascending id
-    if (tid >= 32 && tid < 32 + m) {
-        const int t = tid - 32;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int q = lane + 32 * j;
+            ne += __popc(__ballot_sync(0xffffffffu, q < cap && fq[j]));
+            if (q < cap && fq[j]) {
+                int p = 0;  // distinct experts below this one
+                for (int q2 = 0; q2 < cap; ++q2)
+                    p += sm.first[q2] && sm.ent[q2] < eq[j];
+                const int sl = slot[eq[j]];
+                const unsigned long long base =
+                    (unsigned long long)a.arena_base + (unsigned long long)(sl < 0 ? 0 : sl) * a.slot_bytes;
+                a.ptrs[p] = base + a.gate_off;
+                a.ptrs[cap + p] = base + a.up_off;
+                a.ptrs[2 * cap + p] = base + a.down_off;
+                a.hdr[po + 1 + p] = rq[j];  // the expert's first pair: its pairs start here
+                a.hdr[po + 2 + cap + p] = eq[j];
+            }
+        }
+        if (lane == 0) {
+            a.hdr[po] = ne;
+            a.hdr[po + 1 + ne] = cap;
+        }
+    } else if (warp == 1 && lane < m) {
+        // header rows: status, picks, weight bits, slots of the picks in ascending id
+        const int t = lane;
         int32_t *h = a.hdr + (size_t)t * (1 + 3 * k);
         int status = sm.flags[t];
         for (int i = 0; i < k; ++i) {
