@@ -125,7 +125,7 @@ int launch(void (*kernel)(Args), dim3 grid, dim3 block, size_t smem, cudaStream_
 struct Geo {
     int r_rows, r_grid;
     size_t r_smem;
-    int g_S;
+    int g_S, w2r;
     uint32_t g_stage;
     size_t g_smem;
     int d_S, d_pair_cap;
@@ -161,22 +161,29 @@ int geometry(const moe_cfg &c, int m, bool shared, const DevInfo &I, Geo &G)
     G.r_grid = (n + G.r_rows - 1) / G.r_rows;
     G.r_smem = router_smem(G.r_rows, dim, m, c.n_routed);
     G.grid = I.sms;
-    // gate/up: stages of max(one Q2_K task, one bf16 row)
-    G.g_stage = (uint32_t)align_up(std::max<size_t>((size_t)MOE_G_TASK_SB * MOE_Q2K_BYTES, (size_t)dim * 2), 128);
-    size_t g_fixed = align_up((size_t)m * act_row_bytes(dim), 128) + align_up((size_t)m * dim * 2, 128);
+    // gate/up: stages of max(one Q2_K task, a shared row pair W1 + W3, one W2 row);
+    // w2r W2 rows a task, as many as a stage holds (<= 4, dividing dim)
+    size_t gst = (size_t)MOE_G_TASK_SB * MOE_Q2K_BYTES;
+    if (shared)
+        gst = std::max(gst, std::max((size_t)dim * 2 * 2, (size_t)inter * 2));
+    G.g_stage = (uint32_t)align_up(gst, 128);
+    G.w2r = 1;
+    while (shared && G.w2r < 4 && (size_t)G.w2r * 2 * inter * 2 <= G.g_stage && dim % (G.w2r * 2) == 0)
+        G.w2r *= 2;
+    size_t g_fixed = align_up((size_t)m * act_row_bytes(dim), 128) + align_up((size_t)m * dim * 2, 128) +
+                     (shared ? align_up((size_t)m * inter * 2, 128) : 0);
     G.g_S = stages_fit(g_fixed, G.g_stage, 32, limit);
-    G.g_smem = g_smem_bytes(G.g_S, m, dim, shared, G.g_stage);
-    // down: stages of max(one Q3_K task, one bf16 row)
-    G.d_stage = (uint32_t)align_up(std::max<size_t>((size_t)MOE_D_TASK_SB * MOE_Q3K_BYTES, (size_t)inter * 2), 128);
+    G.g_smem = g_smem_bytes(G.g_S, m, dim, inter, shared, G.g_stage);
+    // down: stages of one Q3_K task (the shared expert is done by the gate/up kernel)
+    G.d_stage = (uint32_t)align_up((size_t)MOE_D_TASK_SB * MOE_Q3K_BYTES, 128);
     const int tpr = dim / down_rows_per_task(inter);
-    const long long tmax = (long long)m * k * tpr + (shared ? dim : 0);
+    const long long tmax = (long long)m * k * tpr;
     const long long per = (tmax + G.grid - 1) / G.grid;
     int span = (int)((per + tpr - 1) / tpr) + 1;
     G.d_pair_cap = std::min(m * k, span * m);
-    size_t d_fixed = d_small_bytes(dim, inter) + align_up((size_t)G.d_pair_cap * act_row_bytes(inter), 128) +
-                     (shared ? align_up((size_t)m * inter * 2, 128) : 0);
+    size_t d_fixed = d_small_bytes(dim, inter) + align_up((size_t)G.d_pair_cap * act_row_bytes(inter), 128);
     G.d_S = stages_fit(d_fixed, G.d_stage, 48, limit);
-    G.d_smem = d_smem_bytes(G.d_S, G.d_pair_cap, m, dim, inter, shared, G.d_stage);
+    G.d_smem = d_smem_bytes(G.d_S, G.d_pair_cap, dim, inter, G.d_stage);
     if (G.r_smem > limit || G.g_smem > limit || G.d_smem > limit)
         return fail(MOE_EUNSUPPORTED, "shared memory: router %zu, gate/up %zu, down %zu > %zu bytes", G.r_smem,
                     G.g_smem, G.d_smem, limit);
@@ -193,6 +200,7 @@ struct Bufs {
     int32_t *plan_rows;
     unsigned long long *ptrs;
     float *g, *u, *gs, *us, *down, *sd, *acc;
+    uint16_t *hs;
     uint32_t *ctrl, *rgcnt;
 };
 
@@ -213,6 +221,7 @@ Bufs ws_bufs(const moe_cfg &c, void *ws)
     B.u = reinterpret_cast<float *>(b + L.u);
     B.gs = reinterpret_cast<float *>(b + L.gs);
     B.us = reinterpret_cast<float *>(b + L.us);
+    B.hs = reinterpret_cast<uint16_t *>(b + L.hs);
     B.down = reinterpret_cast<float *>(b + L.down);
     B.sd = reinterpret_cast<float *>(b + L.sd);
     B.acc = reinterpret_cast<float *>(b + L.acc);
@@ -265,6 +274,11 @@ int launch_experts(const moe_cfg &c, int m, const Geo &G, const Bufs &B, const u
     ga.x = x;
     ga.w1 = w1;
     ga.w3 = w3;
+    ga.w2 = w2;
+    ga.hs = B.hs;
+    ga.sd = B.sd;
+    ga.limit = c.swiglu_limit;
+    ga.w2r = G.w2r;
     ga.hdr = hdr;
     ga.ptrs = ptrs;
     ga.plan_rows = plan_rows;
@@ -294,9 +308,7 @@ int launch_experts(const moe_cfg &c, int m, const Geo &G, const Bufs &B, const u
     da.plan_w = plan_w;
     da.g = B.g;
     da.u = B.u;
-    da.gs = B.gs;
-    da.us = B.us;
-    da.w2 = w2;
+    da.has_shared = w2 != nullptr;
     da.down = B.down;
     da.sd = B.sd;
     da.acc = acc;

@@ -42,7 +42,7 @@ namespace moe {
 // ------------------------------------------------------------------ layout
 
 struct WsLayout {
-    size_t ctrl, rgcnt, logits, scores, keys, plan_w, plan_rows, ptrs, g, u, gs, us, down, sd, acc, total;
+    size_t ctrl, rgcnt, logits, scores, keys, plan_w, plan_rows, ptrs, g, u, gs, us, hs, down, sd, acc, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -68,6 +68,7 @@ inline WsLayout ws_layout(const moe_cfg &c)
     L.u = take(sizeof(float) * cap * c.inter);
     L.gs = take(sizeof(float) * M * c.inter);
     L.us = take(sizeof(float) * M * c.inter);
+    L.hs = take(sizeof(uint16_t) * M * c.inter);  // bf16 SwiGLU of the shared expert
     L.down = take(sizeof(float) * cap * c.dim);
     L.sd = take(sizeof(float) * M * c.dim);
     L.acc = take(sizeof(float) * M * c.dim);
@@ -78,7 +79,7 @@ inline WsLayout ws_layout(const moe_cfg &c)
 // control words at ws + ctrl
 #define MOE_CTRL_TICKET 0
 #define MOE_CTRL_STATUS 1
-#define MOE_CTRL_GATEUP 2  // 3 words: gate/up task counters and exit ticket
+#define MOE_CTRL_GATEUP 2  // 5 words: gate/up task counters, exit ticket, shared rows done
 
 inline int header_words(int m, int k) { return m * (1 + 3 * k) + 2 + 2 * m * k; }
 
@@ -180,6 +181,20 @@ __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(uint32_t *p, unsigned v
     unsigned old;
     asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
+}
+
+// Fire-and-forget add at GPU scope with release semantics: what the calling
+// thread wrote before is visible to whoever acquires the new value.
+__device__ __forceinline__ void red_add_release_gpu(uint32_t *p, unsigned v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const uint32_t *p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 // Programmatic dependent launch. wait: block until the preceding kernel in

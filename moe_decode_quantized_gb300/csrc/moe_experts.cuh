@@ -236,8 +236,9 @@ __device__ __forceinline__ void q3k_dot_multi(const uint8_t *st, int lane, const
 // round of parallel global loads instead of dependent loads per task).
 struct PlanCache {
     int ne;
-    int next;  // consumers' dynamic task counter
-    int pad[2];
+    int next;      // consumers' dynamic task counter
+    int hs_ready;  // gate/up: the shared expert's SwiGLU output is in shared memory
+    int pad;
     int pair_start[MOE_MAX_TOKENS * MOE_MAX_TOPK + 1];
     int rows[MOE_MAX_TOKENS * MOE_MAX_TOPK];
     unsigned long long ptr[2][MOE_MAX_TOKENS * MOE_MAX_TOPK];
@@ -253,9 +254,11 @@ struct Ring {
     __device__ uint8_t *at(int slot) const { return stage + (size_t)slot * stage_bytes; }
 };
 
-// producer side: publishes task i into its slot once the slot is free
+// producer side: publishes task i into its slot once the slot is free; the
+// stage receives src (bytes) and, after it, src2 (bytes2)
 __device__ __forceinline__ bool ring_issue(const Ring &r, int i, const Task &t, const void *src,
-                                           uint32_t bytes, uint64_t pol, uint32_t *status)
+                                           uint32_t bytes, uint64_t pol, uint32_t *status,
+                                           const void *src2 = nullptr, uint32_t bytes2 = 0)
 {
     const int slot = i % r.S;
     const uint32_t round = (uint32_t)(i / r.S);
@@ -264,9 +267,11 @@ __device__ __forceinline__ bool ring_issue(const Ring &r, int i, const Task &t, 
     Task tt = t;
     tt.seq = i;
     r.desc[slot] = tt;
-    mbar_arrive_expect_tx(&r.full[slot], bytes);
+    mbar_arrive_expect_tx(&r.full[slot], bytes + bytes2);
     if (bytes)
         bulk_g2s(r.at(slot), src, bytes, &r.full[slot], pol);
+    if (bytes2)
+        bulk_g2s(r.at(slot) + bytes, src2, bytes2, &r.full[slot], pol);
     return true;
 }
 
@@ -279,6 +284,7 @@ __device__ __forceinline__ void ring_init(const Ring &r)
             r.desc[s].seq = -1;
         }
         r.pc->next = 0;
+        r.pc->hs_ready = 0;
         fence_barrier_init();
     }
 }
@@ -392,36 +398,85 @@ __device__ __forceinline__ void cache_plan(const Ring &r, const int32_t *hdr, in
 struct GArgs {
     const uint16_t *x;                 // bf16 [m, dim]
     const uint16_t *w1, *w3;           // shared expert bf16 [inter, dim] (NULL: none)
+    const uint16_t *w2;                // shared expert bf16 [dim, inter]
     const int32_t *hdr;                // route header (plan tail at plan_off)
     const unsigned long long *ptrs;    // [3][cap]
     const int32_t *plan_rows;          // [cap]
     float *g, *u;                      // [cap, inter]
     float *gs, *us;                    // [m, inter]
+    uint16_t *hs;                      // [m, inter] bf16(SwiGLU(gs, us))
+    float *sd;                         // [m, dim] W2 hs
     uint32_t *status;
-    uint32_t *gctr;                    // [0] shared-task counter, [1] routed-task counter, [2] exit ticket
-    int dim, inter, m, k, cap, plan_off, S;
+    // [0] shared row-pair counter, [1] routed-task counter, [2] exit ticket,
+    // [3] W2 task counter, [4] shared row pairs done
+    uint32_t *gctr;
+    float limit;
+    int dim, inter, m, k, cap, plan_off, S, w2r;
     uint32_t stage_bytes;
 };
 
 __host__ __device__ inline size_t g_act_off(int S) { return ring_head_bytes(S); }
 __host__ __device__ inline size_t g_xs_off(int S, int m, int dim) { return g_act_off(S) + align_up((size_t)m * act_row_bytes(dim), 128); }
-__host__ __device__ inline size_t g_stage_off(int S, int m, int dim, bool shared)
+__host__ __device__ inline size_t g_hs_off(int S, int m, int dim) { return g_xs_off(S, m, dim) + align_up((size_t)m * dim * 2, 128); }
+__host__ __device__ inline size_t g_stage_off(int S, int m, int dim, int inter, bool shared)
 {
-    (void)shared;  // x is staged in shared memory whether or not a shared expert runs
-    return g_xs_off(S, m, dim) + align_up((size_t)m * dim * 2, 128);
+    // x is staged in shared memory whether or not a shared expert runs
+    return g_hs_off(S, m, dim) + (shared ? align_up((size_t)m * inter * 2, 128) : 0);
 }
-__host__ __device__ inline size_t g_smem_bytes(int S, int m, int dim, bool shared, uint32_t stage_bytes)
+__host__ __device__ inline size_t g_smem_bytes(int S, int m, int dim, int inter, bool shared, uint32_t stage_bytes)
 {
-    return g_stage_off(S, m, dim, shared) + (size_t)S * stage_bytes + 16;
+    return g_stage_off(S, m, dim, inter, shared) + (size_t)S * stage_bytes + 16;
+}
+
+// The producer warp: waits (bounded) until every row pair of the shared
+// expert is done grid-wide, copies hs into shared memory and raises the CTA's
+// flag (2 instead of 1 after a timeout, so that no consumer waits forever).
+__device__ bool g_load_hs(const GArgs &a, const Ring &ring, uint16_t *hs_s, int lane)
+{
+    const uint32_t target = (uint32_t)a.inter;
+    bool ok = true;
+    if (ld_acquire_gpu(a.gctr + 4) < target) {
+        const uint64_t t0 = globaltimer();
+        while (ld_acquire_gpu(a.gctr + 4) < target) {
+            __nanosleep(128);
+            if (globaltimer() - t0 > MOE_WAIT_NS) {
+                atomicOr(a.status, (uint32_t)MOE_WS_TIMEOUT);
+                ok = false;
+                break;
+            }
+        }
+    }
+    // every lane polled itself: its loads below come after its own acquire
+    const int n16 = a.m * a.inter / 8;
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.hs);
+    uint4 *dst = reinterpret_cast<uint4 *>(hs_s);
+    for (int i0 = lane; i0 < n16; i0 += 32 * 8) {
+        uint4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            v[j] = i0 + 32 * j < n16 ? __ldcg(src + i0 + 32 * j) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (i0 + 32 * j < n16)
+                dst[i0 + 32 * j] = v[j];
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    __syncwarp();
+    if (lane == 0) {
+        __threadfence_block();
+        *reinterpret_cast<volatile int *>(&ring.pc->hs_ready) = ok ? 1 : 2;
+    }
+    return ok;
 }
 
 __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     const bool shared = a.w1 != nullptr;
-    const Ring ring = ring_carve(smem, a.S, a.stage_bytes, g_stage_off(a.S, a.m, a.dim, shared));
+    const Ring ring = ring_carve(smem, a.S, a.stage_bytes, g_stage_off(a.S, a.m, a.dim, a.inter, shared));
     uint8_t *act = smem + g_act_off(a.S);
     uint16_t *xs = reinterpret_cast<uint16_t *>(smem + g_xs_off(a.S, a.m, a.dim));
+    uint16_t *hs_s = reinterpret_cast<uint16_t *>(smem + g_hs_off(a.S, a.m, a.dim));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int dim = a.dim, inter = a.inter, nb = dim / MOE_QK;
     const size_t arow = act_row_bytes(dim);
@@ -439,33 +494,71 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
         int base = 0;  // index of the next task in this CTA's ring
         bool ok = true;
         if (shared) {
-            // the shared expert's rows depend only on x: issued before the wait
-            const int nsh = 2 * inter;
+            // The shared expert depends only on x: all of it runs before the
+            // wait. (1) Row pairs: W1 row i and W3 row i in one stage; the
+            // consumer that takes pair i also writes hs[i] = bf16(SwiGLU).
             unsigned nxt = 0;
             if (lane == 0)
                 nxt = atomicAdd(a.gctr + 0, (unsigned)MOE_G_CHUNK);
             for (;;) {
                 const int c0 = (int)__shfl_sync(0xffffffffu, nxt, 0);
-                if (c0 >= nsh || !ok)
+                if (c0 >= inter || !ok)
                     break;
                 if (lane == 0)
                     nxt = atomicAdd(a.gctr + 0, (unsigned)MOE_G_CHUNK);  // the next chunk, in flight meanwhile
-                const int c1 = min(c0 + MOE_G_CHUNK, nsh);
+                const int c1 = min(c0 + MOE_G_CHUNK, inter);
                 for (int b = c0; b < c1 && ok; b += P) {
-                    const int sidx = b + lane;
+                    const int i = b + lane;
                     bool mine = true;
-                    if (issuer && sidx < c1) {
+                    if (issuer && i < c1) {
                         Task t{};
                         t.kind = 2;
-                        t.mat = sidx / inter;
-                        t.row = sidx % inter;
-                        const uint16_t *src = (t.mat ? a.w3 : a.w1) + (size_t)t.row * dim;
-                        mine = ring_issue(ring, base + (sidx - c0), t, src, (uint32_t)dim * 2u, pol, a.status);
+                        t.row = i;
+                        mine = ring_issue(ring, base + (i - c0), t, a.w1 + (size_t)i * dim, (uint32_t)dim * 2u, pol,
+                                          a.status, a.w3 + (size_t)i * dim, (uint32_t)dim * 2u);
                     }
                     ok = __all_sync(0xffffffffu, mine);
                 }
                 base += c1 - c0;
             }
+            // (2) W2, w2r rows a task. The first ones (at most S: their slots
+            // were freed by row pairs, which never wait) go out before hs is
+            // complete; then this warp waits until every row pair is done
+            // grid-wide, loads hs into shared memory, and issues the rest.
+            const int nw2 = dim / a.w2r;
+            const uint32_t w2bytes = (uint32_t)a.w2r * inter * 2u;
+            int issued2 = 0;
+            bool have_hs = false;
+            if (lane == 0)
+                nxt = atomicAdd(a.gctr + 3, (unsigned)MOE_G_CHUNK);
+            while (ok) {
+                const int c0 = (int)__shfl_sync(0xffffffffu, nxt, 0);
+                const int c1 = min(c0 + MOE_G_CHUNK, nw2);
+                if (!have_hs && (c0 >= nw2 || issued2 + (c1 - c0) > ring.S)) {
+                    g_load_hs(a, ring, hs_s, lane);
+                    have_hs = true;
+                }
+                if (c0 >= nw2)
+                    break;
+                if (lane == 0)
+                    nxt = atomicAdd(a.gctr + 3, (unsigned)MOE_G_CHUNK);
+                for (int b = c0; b < c1 && ok; b += P) {
+                    const int j = b + lane;
+                    bool mine = true;
+                    if (issuer && j < c1) {
+                        Task t{};
+                        t.kind = 3;
+                        t.row = j * a.w2r;
+                        mine = ring_issue(ring, base + (j - c0), t, a.w2 + (size_t)t.row * inter, w2bytes, pol,
+                                          a.status);
+                    }
+                    ok = __all_sync(0xffffffffu, mine);
+                }
+                base += c1 - c0;
+                issued2 += c1 - c0;
+            }
+            if (!have_hs)  // only after a failed wait: still raise the flag
+                g_load_hs(a, ring, hs_s, lane);
         }
         // the first routed chunk's ticket does not depend on the plan: taken
         // before the wait, its round trip overlaps the selection
@@ -521,12 +614,6 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
             }
             ok = __all_sync(0xffffffffu, mine);
         }
-        // the last producer to finish taking tasks resets the counters
-        if (lane == 0 && atomicAdd(a.gctr + 2, 1u) == gridDim.x - 1) {
-            atomicExch(a.gctr + 0, 0u);
-            atomicExch(a.gctr + 1, 0u);
-            atomicExch(a.gctr + 2, 0u);
-        }
         return;
     }
 
@@ -551,6 +638,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
     // every thread triggers the dependent launch only after the selection is
     // complete (the first routed task is issued after the producer's wait)
     bool triggered = false;
+    bool hs_seen = false;
     for (;;) {
         const int j = ring_grab(ring);
         const int slot = j % ring.S;
@@ -602,41 +690,113 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&ring.empty[slot]);
-        } else {
-            // one bf16 row of W1 or W3 against every token's bf16 x
-            const uint4 *wr = reinterpret_cast<const uint4 *>(st);
+        } else if (t.kind == 2) {
+            // W1 row i and W3 row i against every token's bf16 x, then hs[i]
+            const int i = t.row;
+            const uint4 *w1r = reinterpret_cast<const uint4 *>(st);
+            const uint4 *w3r = w1r + dim / 8;
             const uint4 *x4 = reinterpret_cast<const uint4 *>(xs);
-            float *out = t.mat ? a.us : a.gs;
             with_m(a.m, [&](auto MC) {
                 constexpr int M = decltype(MC)::value;
-                float acc[M];
+                float ag[M], au[M];
 #pragma unroll
                 for (int tt = 0; tt < M; ++tt)
-                    acc[tt] = 0.0f;
+                    ag[tt] = au[tt] = 0.0f;
                 for (int c = lane; c < dim / 8; c += 32) {
-                    const uint4 wv = wr[c];
+                    const uint4 v1 = w1r[c], v3 = w3r[c];
 #pragma unroll
-                    for (int tt = 0; tt < M; ++tt)
-                        acc[tt] = fma_bf16x8(wv, x4[(size_t)tt * (dim / 8) + c], acc[tt]);
+                    for (int tt = 0; tt < M; ++tt) {
+                        const uint4 xv = x4[(size_t)tt * (dim / 8) + c];
+                        ag[tt] = fma_bf16x8(v1, xv, ag[tt]);
+                        au[tt] = fma_bf16x8(v3, xv, au[tt]);
+                    }
                 }
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&ring.empty[slot]);
 #pragma unroll
                 for (int tt = 0; tt < M; ++tt) {
-                    float v = acc[tt];
 #pragma unroll
-                    for (int o = 16; o; o >>= 1)
-                        v += __shfl_xor_sync(0xffffffffu, v, o);
-                    if (lane == 0)
-                        out[(size_t)tt * inter + t.row] = v;
+                    for (int o = 16; o; o >>= 1) {
+                        ag[tt] += __shfl_xor_sync(0xffffffffu, ag[tt], o);
+                        au[tt] += __shfl_xor_sync(0xffffffffu, au[tt], o);
+                    }
                 }
+                if (lane == 0) {
+#pragma unroll
+                    for (int tt = 0; tt < M; ++tt) {
+                        a.gs[(size_t)tt * inter + i] = ag[tt];
+                        a.us[(size_t)tt * inter + i] = au[tt];
+                        a.hs[(size_t)tt * inter + i] = f32_to_bf16(swiglu_f32(ag[tt], au[tt], a.limit));
+                    }
+                    red_add_release_gpu(a.gctr + 4, 1u);  // after this lane's own stores
+                }
+            });
+        } else {
+            // w2r rows of W2 against every token's hs (in shared memory once
+            // the producer has loaded it)
+            if (!hs_seen) {
+                if (lane == 0) {
+                    volatile int *f = &ring.pc->hs_ready;
+                    if (*f == 0) {
+                        const uint64_t t0 = globaltimer();
+                        while (*f == 0) {
+                            __nanosleep(64);
+                            if (globaltimer() - t0 > MOE_WAIT_NS) {
+                                atomicOr(a.status, (uint32_t)MOE_WS_TIMEOUT);
+                                break;
+                            }
+                        }
+                    }
+                    __threadfence_block();
+                }
+                __syncwarp();
+                hs_seen = true;
+            }
+            const uint4 *h4 = reinterpret_cast<const uint4 *>(hs_s);
+            with_m(a.m, [&](auto MC) {
+                constexpr int M = decltype(MC)::value;
+                for (int rr = 0; rr < a.w2r; ++rr) {
+                    const uint4 *wr = reinterpret_cast<const uint4 *>(st) + (size_t)rr * (inter / 8);
+                    float acc[M];
+#pragma unroll
+                    for (int tt = 0; tt < M; ++tt)
+                        acc[tt] = 0.0f;
+                    for (int c = lane; c < inter / 8; c += 32) {
+                        const uint4 wv = wr[c];
+#pragma unroll
+                        for (int tt = 0; tt < M; ++tt)
+                            acc[tt] = fma_bf16x8(wv, h4[(size_t)tt * (inter / 8) + c], acc[tt]);
+                    }
+#pragma unroll
+                    for (int tt = 0; tt < M; ++tt) {
+                        float v = acc[tt];
+#pragma unroll
+                        for (int o = 16; o; o >>= 1)
+                            v += __shfl_xor_sync(0xffffffffu, v, o);
+                        if (lane == 0)
+                            a.sd[(size_t)tt * dim + t.row + rr] = v;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&ring.empty[slot]);
             });
         }
     }
     if (!triggered) {
         pdl_wait();
         pdl_launch_dependents();
+    }
+    // the last CTA out resets the grid-wide counters: by then every producer
+    // has stopped taking tasks and every consumer has counted its row pairs
+    consumers_sync();
+    if (threadIdx.x == 0 && atomicAdd(a.gctr + 2, 1u) == gridDim.x - 1) {
+        atomicExch(a.gctr + 0, 0u);
+        atomicExch(a.gctr + 1, 0u);
+        atomicExch(a.gctr + 3, 0u);
+        atomicExch(a.gctr + 4, 0u);
+        atomicExch(a.gctr + 2, 0u);
     }
 }
 
@@ -648,15 +808,14 @@ struct DArgs {
     const int32_t *plan_rows;
     const float *plan_w;
     const float *g, *u;           // [cap, inter]
-    const float *gs, *us;         // [m, inter]
-    const uint16_t *w2;           // shared bf16 [dim, inter] (NULL: none)
     float *down;                  // [cap, dim]
-    float *sd;                    // [m, dim]
+    const float *sd;              // [m, dim] the shared expert's output (the gate/up kernel's)
     float *acc;                   // [m, dim]
     float *residual;              // [m, dim] or NULL
     uint16_t *x_next;             // [m, dim] or NULL
     uint32_t *rgcnt, *status;
     float limit;
+    int has_shared;  // add sd to the routed sum
     int dim, inter, m, k, cap, plan_off, S, pair_cap;
     uint32_t stage_bytes;
 };
@@ -674,49 +833,31 @@ __host__ __device__ inline size_t d_small_bytes(int dim, int inter)
 }
 __host__ __device__ inline size_t d_small_off(int S) { return ring_head_bytes(S); }
 __host__ __device__ inline size_t d_act_off(int S, int dim, int inter) { return d_small_off(S) + d_small_bytes(dim, inter); }
-__host__ __device__ inline size_t d_hs_off(int S, int pair_cap, int dim, int inter)
+__host__ __device__ inline size_t d_stage_off(int S, int pair_cap, int dim, int inter)
 {
     return d_act_off(S, dim, inter) + align_up((size_t)pair_cap * act_row_bytes(inter), 128);
 }
-__host__ __device__ inline size_t d_stage_off(int S, int pair_cap, int m, int dim, int inter, bool shared)
+__host__ __device__ inline size_t d_smem_bytes(int S, int pair_cap, int dim, int inter, uint32_t stage_bytes)
 {
-    return d_hs_off(S, pair_cap, dim, inter) + (shared ? align_up((size_t)m * inter * 2, 128) : 0);
+    return d_stage_off(S, pair_cap, dim, inter) + (size_t)S * stage_bytes + 16;
 }
-__host__ __device__ inline size_t d_smem_bytes(int S, int pair_cap, int m, int dim, int inter, bool shared,
-                                              uint32_t stage_bytes)
-{
-    return d_stage_off(S, pair_cap, m, dim, inter, shared) + (size_t)S * stage_bytes + 16;
-}
-
-// relative costs of the down kernel's tasks (bytes and instructions of a
-// 64-super-block Q3_K task against one bf16 row of the shared expert)
-#define D_W_ROUTED 2
-#define D_W_SHARED 1
 
 // the range of tasks of this CTA and the plan pairs its routed tasks touch
 struct DRange {
     int ne, tpr, Tr, lo, hi, pair_lo, pair_hi;
 };
 
-__device__ __forceinline__ DRange d_range(const DArgs &a, bool shared)
+__device__ __forceinline__ DRange d_range(const DArgs &a)
 {
     DRange r;
     r.ne = min(max(__ldcg(a.hdr + a.plan_off), 0), a.cap);
     r.tpr = a.dim / down_rows_per_task(a.inter);
     r.Tr = r.ne * r.tpr;
-    // contiguous ranges of equal cost: a Q3_K task (MOE_D_TASK_SB super-blocks)
-    // weighs D_W_ROUTED, a bf16 shared row D_W_SHARED
-    const long long cr = (long long)r.Tr * D_W_ROUTED;
-    const long long C = cr + (shared ? (long long)a.dim * D_W_SHARED : 0);
-    auto first_at = [&](long long c) -> int {
-        return c <= cr ? (int)((c + D_W_ROUTED - 1) / D_W_ROUTED)
-                       : r.Tr + (int)((c - cr + D_W_SHARED - 1) / D_W_SHARED);
-    };
-    r.lo = first_at(blockIdx.x * C / gridDim.x);
-    r.hi = first_at((blockIdx.x + 1) * C / gridDim.x);
+    r.lo = (int)((long long)blockIdx.x * r.Tr / gridDim.x);
+    r.hi = (int)((long long)(blockIdx.x + 1) * r.Tr / gridDim.x);
     r.pair_lo = r.pair_hi = 0;
-    if (r.lo < r.Tr && r.lo < r.hi) {
-        const int p_lo = r.lo / r.tpr, p_hi = (min(r.hi, r.Tr) - 1) / r.tpr;
+    if (r.lo < r.hi) {
+        const int p_lo = r.lo / r.tpr, p_hi = (r.hi - 1) / r.tpr;
         r.pair_lo = min(max(__ldcg(a.hdr + a.plan_off + 1 + p_lo), 0), a.cap);
         r.pair_hi = min(max(__ldcg(a.hdr + a.plan_off + 2 + p_hi), r.pair_lo), a.cap);
     }
@@ -754,20 +895,19 @@ __device__ __forceinline__ void finish_row(const DArgs &a, int t, int r, bool sh
 __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
-    const bool shared = a.w2 != nullptr;
-    const Ring ring = ring_carve(smem, a.S, a.stage_bytes, d_stage_off(a.S, a.pair_cap, a.m, a.dim, a.inter, shared));
+    const bool shared = a.has_shared != 0;
+    const Ring ring = ring_carve(smem, a.S, a.stage_bytes, d_stage_off(a.S, a.pair_cap, a.dim, a.inter));
     int *s_rows = reinterpret_cast<int *>(smem + d_small_off(a.S));
     float *s_w = reinterpret_cast<float *>(s_rows + D_SW);
     int *s_tp = s_rows + D_TP;
     uint8_t *act = smem + d_act_off(a.S, a.dim, a.inter);
-    uint16_t *hs = reinterpret_cast<uint16_t *>(smem + d_hs_off(a.S, a.pair_cap, a.dim, a.inter));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int dim = a.dim, inter = a.inter, nb = inter / MOE_QK;
     const int rd = down_rows_per_task(inter);
     const size_t arow = act_row_bytes(inter);
     ring_init(ring);
     __syncthreads();
-    const DRange R = d_range(a, shared);
+    const DRange R = d_range(a);
 
     if (warp == MOE_CONSUMER_WARPS) {
         // ---------------- producer warp: everything it loads depends only on
@@ -789,29 +929,19 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
             bool mine = true;
             if (issuer && tix < R.hi) {
                 Task t{};
-                const void *src = nullptr;
-                uint32_t bytes;
-                if (tix < R.Tr) {
-                    t.kind = 1;
-                    t.p = tix / R.tpr;
-                    const int r = tix % R.tpr;
-                    t.row = r * rd;
-                    t.pair0 = pc.pair_start[t.p];
-                    t.npair = pc.pair_start[t.p + 1] - t.pair0;
-                    bytes = rbytes;
-                    src = reinterpret_cast<const char *>(pc.ptr[0][t.p]) + (size_t)r * rbytes;
-                    if (!fits || t.npair < 1 || t.npair > a.m || t.pair0 < R.pair_lo ||
-                        t.pair0 + t.npair > R.pair_hi) {
-                        if (fits)
-                            atomicOr(a.status, (uint32_t)MOE_WS_PLAN);
-                        t.npair = 0;  // a no-op task: still counted by its row group
-                        bytes = 0;
-                    }
-                } else {
-                    t.kind = 2;
-                    t.row = tix - R.Tr;
-                    src = a.w2 + (size_t)t.row * inter;
-                    bytes = (uint32_t)inter * 2u;
+                t.kind = 1;
+                t.p = tix / R.tpr;
+                const int r = tix % R.tpr;
+                t.row = r * rd;
+                t.pair0 = pc.pair_start[t.p];
+                t.npair = pc.pair_start[t.p + 1] - t.pair0;
+                uint32_t bytes = rbytes;
+                const void *src = reinterpret_cast<const char *>(pc.ptr[0][t.p]) + (size_t)r * rbytes;
+                if (!fits || t.npair < 1 || t.npair > a.m || t.pair0 < R.pair_lo || t.pair0 + t.npair > R.pair_hi) {
+                    if (fits)
+                        atomicOr(a.status, (uint32_t)MOE_WS_PLAN);
+                    t.npair = 0;  // a no-op task: still counted by its row group
+                    bytes = 0;
                 }
                 mine = ring_issue(ring, tix - R.lo, t, src, bytes, pol, a.status);
             }
@@ -830,7 +960,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
         return;
     }
 
-    // ---------------- consumers: wait for g, u, gs, us; build the activations
+    // ---------------- consumers: wait for g, u; build the activations
     pdl_launch_dependents();
     pdl_wait();
     const int npairs = a.m * a.k;
@@ -838,21 +968,13 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
         s_rows[q] = __ldcg(a.plan_rows + q);
         s_w[q] = __ldcg(a.plan_w + q);
     }
-    // q8_1(SwiGLU(g, u)) of the plan pairs this CTA's routed tasks touch, and
-    // bf16(SwiGLU(gs, us)) when it has shared rows; loads in batches, the first
-    // batch of both in flight together
+    // q8_1(SwiGLU(g, u)) of the plan pairs this CTA's tasks touch; loads in
+    // batches of HB blocks a warp
     const int np = min(R.pair_hi - R.pair_lo, a.pair_cap);
     const int nblk = np * inter / 32;
-    const bool my_shared = shared && R.hi > R.Tr;
-    const int nsh = my_shared ? a.m * inter : 0;
-    constexpr int HB = 8;  // q8 blocks a warp loads at once
-    constexpr int HS = 8;  // shared-expert values a thread loads at once
-    constexpr int CT = MOE_CONSUMER_WARPS * 32;
-    for (int r0 = 0;; ++r0) {
-        const int b0 = warp + r0 * MOE_CONSUMER_WARPS * HB, i0 = threadIdx.x + r0 * CT * HS;
-        if (b0 >= nblk && i0 >= nsh)
-            break;
-        float gv[HB], uv[HB], sg[HS], su[HS];
+    constexpr int HB = 8;
+    for (int b0 = warp; b0 < nblk; b0 += MOE_CONSUMER_WARPS * HB) {
+        float gv[HB], uv[HB];
 #pragma unroll
         for (int j = 0; j < HB; ++j) {
             const int b = b0 + j * MOE_CONSUMER_WARPS;
@@ -862,24 +984,12 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
             uv[j] = b < nblk ? __ldcg(a.u + o) : 0.0f;
         }
 #pragma unroll
-        for (int j = 0; j < HS; ++j) {
-            const int i = i0 + j * CT;
-            sg[j] = i < nsh ? __ldcg(a.gs + i) : 0.0f;
-            su[j] = i < nsh ? __ldcg(a.us + i) : 0.0f;
-        }
-#pragma unroll
         for (int j = 0; j < HB; ++j) {
             const int b = b0 + j * MOE_CONSUMER_WARPS;
             if (b < nblk) {
                 const int pr = b / (inter / 32), bi = b % (inter / 32);
                 q8_store_smem(act + pr * arow, nb, bi, q8_quant_warp(swiglu_f32(gv[j], uv[j], a.limit)), false);
             }
-        }
-#pragma unroll
-        for (int j = 0; j < HS; ++j) {
-            const int i = i0 + j * CT;
-            if (i < nsh)
-                hs[i] = f32_to_bf16(swiglu_f32(sg[j], su[j], a.limit));
         }
     }
     consumers_sync();
@@ -894,7 +1004,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
     }
     consumers_sync();
 
-    const unsigned expected = (unsigned)R.ne + (shared ? (unsigned)rd : 0u);
+    const unsigned expected = (unsigned)R.ne;
     for (;;) {
         const int j = ring_grab(ring);
         const int slot = j % ring.S;
@@ -937,35 +1047,6 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&ring.empty[slot]);
-        } else {
-            // one bf16 row of W2 against every token's bf16 SwiGLU output
-            const uint4 *wr = reinterpret_cast<const uint4 *>(st);
-            const uint4 *h4 = reinterpret_cast<const uint4 *>(hs);
-            with_m(a.m, [&](auto MC) {
-                constexpr int M = decltype(MC)::value;
-                float acc[M];
-#pragma unroll
-                for (int tt = 0; tt < M; ++tt)
-                    acc[tt] = 0.0f;
-                for (int c = lane; c < inter / 8; c += 32) {
-                    const uint4 wv = wr[c];
-#pragma unroll
-                    for (int tt = 0; tt < M; ++tt)
-                        acc[tt] = fma_bf16x8(wv, h4[(size_t)tt * (inter / 8) + c], acc[tt]);
-                }
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&ring.empty[slot]);
-#pragma unroll
-                for (int tt = 0; tt < M; ++tt) {
-                    float v = acc[tt];
-#pragma unroll
-                    for (int o = 16; o; o >>= 1)
-                        v += __shfl_xor_sync(0xffffffffu, v, o);
-                    if (lane == 0)
-                        a.sd[(size_t)tt * dim + t.row] = v;
-                }
-            });
         }
     }
 
@@ -981,19 +1062,12 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
         *s_nfin = 0;
     consumers_sync();
     const int ngroups = dim / rd;
-    const int hiR = min(R.hi, R.Tr), s_lo = max(R.lo, R.Tr) - R.Tr, s_hi = max(R.hi, R.Tr) - R.Tr;
     auto count_in = [&](int g) {
-        int cnt = 0;
-        if (R.lo < hiR) {
-            // experts p with lo <= p * tpr + g < hiR
-            const int a0 = R.lo - g, a1 = hiR - g;
-            const int c0 = a0 <= 0 ? 0 : (a0 + R.tpr - 1) / R.tpr;
-            const int c1 = a1 <= 0 ? 0 : (a1 + R.tpr - 1) / R.tpr;
-            cnt += max(0, c1 - c0);
-        }
-        if (shared && s_lo < s_hi)
-            cnt += max(0, min(s_hi, (g + 1) * rd) - max(s_lo, g * rd));
-        return cnt;
+        // experts p with lo <= p * tpr + g < hi
+        const int a0 = R.lo - g, a1 = R.hi - g;
+        const int c0 = a0 <= 0 ? 0 : (a0 + R.tpr - 1) / R.tpr;
+        const int c1 = a1 <= 0 ? 0 : (a1 + R.tpr - 1) / R.tpr;
+        return max(0, c1 - c0);
     };
     for (int g0 = threadIdx.x; g0 < ngroups; g0 += 2 * CTH) {
         int cnt[2];
