@@ -79,7 +79,7 @@ inline WsLayout ws_layout(const moe_cfg &c)
 // control words at ws + ctrl
 #define MOE_CTRL_TICKET 0
 #define MOE_CTRL_STATUS 1
-#define MOE_CTRL_GATEUP 2  // 5 words: gate/up task counters, exit ticket, shared rows done
+#define MOE_CTRL_GATEUP 2  // 6 words: gate/up task counters, exit ticket, shared rows done, plan hint
 
 inline int header_words(int m, int k) { return m * (1 + 3 * k) + 2 + 2 * m * k; }
 

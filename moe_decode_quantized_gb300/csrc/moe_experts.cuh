@@ -77,6 +77,47 @@ __host__ __device__ inline size_t act_row_bytes(int cols)
     return (size_t)(cols / MOE_QK) * (MOE_SEG_Q_BYTES + 4 * MOE_SEG_REC_FLOATS);
 }
 
+// One q8_1 block by a group of 4 lanes, 8 values each (the same arithmetic
+// as q8_quant_warp: the maximum is exact, each quotient one IEEE division,
+// the sums integers), so that a warp quantises 8 blocks at once. sub: the
+// lane's place in its group (lanes 4g .. 4g + 3); v: its values
+// 8 sub .. 8 sub + 7 of the block. Stored like q8_store_smem. All 32 lanes
+// of the warp call it together (callers loop over 4 x blocks lanes, a
+// multiple of 32 since dim and inter are multiples of 256).
+__device__ __forceinline__ void q8_block_quad(const float (&v)[8], int sub, uint8_t *row, int nseg, int blk,
+                                              bool min_term)
+{
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        amax = fmaxf(amax, fabsf(v[j]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const float d = __fdiv_rn(amax, 127.0f);
+    uint32_t w[2];
+    int sum = 0;
+#pragma unroll
+    for (int j4 = 0; j4 < 2; ++j4) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int q = amax == 0.0f ? 0 : (int)roundf(__fdiv_rn(v[4 * j4 + b], d));
+            sum += q;
+            word |= (uint32_t)(q & 0xFF) << (8 * b);
+        }
+        w[j4] = word;
+    }
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);  // the half: lanes 0-1 or 2-3 of the group
+    const int sg = blk >> 3, bi = blk & 7;
+    *reinterpret_cast<uint2 *>(row + sg * MOE_SEG_Q_BYTES + bi * 32 + 8 * sub) = make_uint2(w[0], w[1]);
+    const float d8 = __half2float(__float2half_rn(d));
+    float *rec = reinterpret_cast<float *>(row + nseg * MOE_SEG_Q_BYTES) + sg * MOE_SEG_REC_FLOATS;
+    if (sub == 0)
+        rec[bi] = d8;
+    if ((sub & 1) == 0)
+        rec[8 + 2 * bi + (sub >> 1)] = min_term ? __fmul_rn(d8, (float)sum) : __int_as_float(sum);
+}
+
 __device__ __forceinline__ void q8_store_smem(uint8_t *row, int nseg, int blk, const Q8Block &b,
                                               bool min_term)
 {
@@ -408,7 +449,8 @@ struct GArgs {
     float *sd;                         // [m, dim] W2 hs
     uint32_t *status;
     // [0] shared row-pair counter, [1] routed-task counter, [2] exit ticket,
-    // [3] W2 task counter, [4] shared row pairs done
+    // [3] W2 task counter, [4] shared row pairs done, [5] the selection's
+    // plan-ready hint
     uint32_t *gctr;
     float limit;
     int dim, inter, m, k, cap, plan_off, S, w2r;
@@ -493,6 +535,23 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
         const bool issuer = lane < P;
         int base = 0;  // index of the next task in this CTA's ring
         bool ok = true;
+        int w2_pending = -1;  // W2 left for after the routed work: a chunk taken, or -2 (none taken)
+        bool have_hs = false;
+        auto issue_w2 = [&](int c0, int c1) {
+            for (int b = c0; b < c1 && ok; b += P) {
+                const int j = b + lane;
+                bool mine = true;
+                if (issuer && j < c1) {
+                    Task t{};
+                    t.kind = 3;
+                    t.row = j * a.w2r;
+                    mine = ring_issue(ring, base + (j - c0), t, a.w2 + (size_t)t.row * inter,
+                                      (uint32_t)a.w2r * inter * 2u, pol, a.status);
+                }
+                ok = __all_sync(0xffffffffu, mine);
+            }
+            base += c1 - c0;
+        };
         if (shared) {
             // The shared expert depends only on x: all of it runs before the
             // wait. (1) Row pairs: W1 row i and W3 row i in one stage; the
@@ -521,44 +580,54 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
                 }
                 base += c1 - c0;
             }
-            // (2) W2, w2r rows a task. The first ones (at most S: their slots
-            // were freed by row pairs, which never wait) go out before hs is
-            // complete; then this warp waits until every row pair is done
-            // grid-wide, loads hs into shared memory, and issues the rest.
+            // (2) W2, w2r rows a task, against hs. This warp polls (bounded)
+            // two words: every row pair done grid-wide -> it loads hs into
+            // shared memory and issues W2; the selection's plan-ready hint ->
+            // the routed work goes first and W2 (or its rest) after it. No W2
+            // task is issued before hs is in shared memory, so nothing queued
+            // ahead of a routed task ever waits.
             const int nw2 = dim / a.w2r;
-            const uint32_t w2bytes = (uint32_t)a.w2r * inter * 2u;
-            int issued2 = 0;
-            bool have_hs = false;
-            if (lane == 0)
-                nxt = atomicAdd(a.gctr + 3, (unsigned)MOE_G_CHUNK);
-            while (ok) {
-                const int c0 = (int)__shfl_sync(0xffffffffu, nxt, 0);
-                const int c1 = min(c0 + MOE_G_CHUNK, nw2);
-                if (!have_hs && (c0 >= nw2 || issued2 + (c1 - c0) > ring.S)) {
-                    g_load_hs(a, ring, hs_s, lane);
-                    have_hs = true;
+            {
+                const uint64_t t0 = globaltimer();
+                for (;;) {
+                    uint32_t done = 0, hint = 0;
+                    if (lane == 0) {
+                        done = *reinterpret_cast<volatile uint32_t *>(a.gctr + 4);
+                        hint = *reinterpret_cast<volatile uint32_t *>(a.gctr + 5);
+                    }
+                    done = __shfl_sync(0xffffffffu, done, 0);
+                    hint = __shfl_sync(0xffffffffu, hint, 0);
+                    if (hint != 0u)
+                        break;  // W2 entirely after the routed work
+                    if (done >= (uint32_t)inter || globaltimer() - t0 > MOE_WAIT_NS) {
+                        g_load_hs(a, ring, hs_s, lane);  // acquires; times out itself
+                        have_hs = true;
+                        break;
+                    }
+                    __nanosleep(256);
                 }
-                if (c0 >= nw2)
-                    break;
+            }
+            if (have_hs) {
+                uint32_t hint = lane == 0 ? *reinterpret_cast<volatile uint32_t *>(a.gctr + 5) : 0u;
                 if (lane == 0)
                     nxt = atomicAdd(a.gctr + 3, (unsigned)MOE_G_CHUNK);
-                for (int b = c0; b < c1 && ok; b += P) {
-                    const int j = b + lane;
-                    bool mine = true;
-                    if (issuer && j < c1) {
-                        Task t{};
-                        t.kind = 3;
-                        t.row = j * a.w2r;
-                        mine = ring_issue(ring, base + (j - c0), t, a.w2 + (size_t)t.row * inter, w2bytes, pol,
-                                          a.status);
+                while (ok) {
+                    const int c0 = (int)__shfl_sync(0xffffffffu, nxt, 0);
+                    if (c0 >= nw2)
+                        break;
+                    if (__shfl_sync(0xffffffffu, hint, 0) != 0u) {
+                        w2_pending = c0;  // taken: issued after the routed work
+                        break;
                     }
-                    ok = __all_sync(0xffffffffu, mine);
+                    if (lane == 0) {
+                        nxt = atomicAdd(a.gctr + 3, (unsigned)MOE_G_CHUNK);
+                        hint = *reinterpret_cast<volatile uint32_t *>(a.gctr + 5);  // read one chunk ahead
+                    }
+                    issue_w2(c0, min(c0 + MOE_G_CHUNK, nw2));
                 }
-                base += c1 - c0;
-                issued2 += c1 - c0;
+            } else {
+                w2_pending = -2;  // nothing taken yet
             }
-            if (!have_hs)  // only after a failed wait: still raise the flag
-                g_load_hs(a, ring, hs_s, lane);
         }
         // the first routed chunk's ticket does not depend on the plan: taken
         // before the wait, its round trip overlaps the selection
@@ -605,6 +674,27 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
             }
             base += c1 - c0;
         }
+        if (w2_pending != -1) {
+            // the rest of W2, hs first if it is not in shared memory yet (the
+            // routed tasks ahead of it never wait)
+            const int nw2 = dim / a.w2r;
+            if (!have_hs)
+                g_load_hs(a, ring, hs_s, lane);
+            int c0 = w2_pending;
+            if (c0 < 0) {
+                unsigned nx = 0;
+                if (lane == 0)
+                    nx = atomicAdd(a.gctr + 3, (unsigned)MOE_G_CHUNK);
+                c0 = (int)__shfl_sync(0xffffffffu, nx, 0);
+            }
+            while (ok && c0 < nw2) {
+                unsigned nx = 0;
+                if (lane == 0)
+                    nx = atomicAdd(a.gctr + 3, (unsigned)MOE_G_CHUNK);
+                issue_w2(c0, min(c0 + MOE_G_CHUNK, nw2));
+                c0 = (int)__shfl_sync(0xffffffffu, nx, 0);
+            }
+        }
         for (int b = 0; b < MOE_CONSUMER_WARPS && ok; b += P) {
             bool mine = true;
             if (issuer && b + lane < MOE_CONSUMER_WARPS) {
@@ -628,10 +718,13 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
     }
     consumers_sync();
     const int nblk = a.m * dim / 32;
-    for (int b = warp; b < nblk; b += MOE_CONSUMER_WARPS) {
+    for (int i = threadIdx.x; i < nblk * 4; i += MOE_CONSUMER_WARPS * 32) {  // four lanes a block
+        const int b = i >> 2, sub = i & 3;
         const int t = b / (dim / 32), bi = b % (dim / 32);
-        const float v = bf16_to_f32(xs[(size_t)t * dim + bi * 32 + lane]);
-        q8_store_smem(act + t * arow, nb, bi, q8_quant_warp(v), true);
+        const uint4 w = *reinterpret_cast<const uint4 *>(xs + (size_t)t * dim + bi * 32 + 8 * sub);
+        const float v[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                            bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+        q8_block_quad(v, sub, act + t * arow, nb, bi, true);
     }
     consumers_sync();
 
@@ -796,6 +889,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
         atomicExch(a.gctr + 1, 0u);
         atomicExch(a.gctr + 3, 0u);
         atomicExch(a.gctr + 4, 0u);
+        atomicExch(a.gctr + 5, 0u);
         atomicExch(a.gctr + 2, 0u);
     }
 }
@@ -968,29 +1062,23 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
         s_rows[q] = __ldcg(a.plan_rows + q);
         s_w[q] = __ldcg(a.plan_w + q);
     }
-    // q8_1(SwiGLU(g, u)) of the plan pairs this CTA's tasks touch; loads in
-    // batches of HB blocks a warp
+    // q8_1(SwiGLU(g, u)) of the plan pairs this CTA's tasks touch, four lanes
+    // a block
     const int np = min(R.pair_hi - R.pair_lo, a.pair_cap);
     const int nblk = np * inter / 32;
-    constexpr int HB = 8;
-    for (int b0 = warp; b0 < nblk; b0 += MOE_CONSUMER_WARPS * HB) {
-        float gv[HB], uv[HB];
-#pragma unroll
-        for (int j = 0; j < HB; ++j) {
-            const int b = b0 + j * MOE_CONSUMER_WARPS;
-            const int pr = b / (inter / 32), bi = b % (inter / 32);
-            const size_t o = (size_t)(R.pair_lo + pr) * inter + bi * 32 + lane;
-            gv[j] = b < nblk ? __ldcg(a.g + o) : 0.0f;
-            uv[j] = b < nblk ? __ldcg(a.u + o) : 0.0f;
-        }
-#pragma unroll
-        for (int j = 0; j < HB; ++j) {
-            const int b = b0 + j * MOE_CONSUMER_WARPS;
-            if (b < nblk) {
-                const int pr = b / (inter / 32), bi = b % (inter / 32);
-                q8_store_smem(act + pr * arow, nb, bi, q8_quant_warp(swiglu_f32(gv[j], uv[j], a.limit)), false);
-            }
-        }
+    for (int i = threadIdx.x; i < nblk * 4; i += MOE_CONSUMER_WARPS * 32) {
+        const int b = i >> 2, sub = i & 3;
+        const int pr = b / (inter / 32), bi = b % (inter / 32);
+        const size_t o = (size_t)(R.pair_lo + pr) * inter + bi * 32 + 8 * sub;
+        const float4 g0 = __ldcg(reinterpret_cast<const float4 *>(a.g + o));
+        const float4 g1 = __ldcg(reinterpret_cast<const float4 *>(a.g + o) + 1);
+        const float4 u0 = __ldcg(reinterpret_cast<const float4 *>(a.u + o));
+        const float4 u1 = __ldcg(reinterpret_cast<const float4 *>(a.u + o) + 1);
+        const float v[8] = {swiglu_f32(g0.x, u0.x, a.limit), swiglu_f32(g0.y, u0.y, a.limit),
+                            swiglu_f32(g0.z, u0.z, a.limit), swiglu_f32(g0.w, u0.w, a.limit),
+                            swiglu_f32(g1.x, u1.x, a.limit), swiglu_f32(g1.y, u1.y, a.limit),
+                            swiglu_f32(g1.z, u1.z, a.limit), swiglu_f32(g1.w, u1.w, a.limit)};
+        q8_block_quad(v, sub, act + pr * arow, nb, bi, false);
     }
     consumers_sync();
     // each token's pairs in plan order (pairs are grouped by ascending expert)

@@ -469,8 +469,13 @@ __global__ void __launch_bounds__(256) moe_router_kernel(RouteArgs a)
         return;
     // the rows area is no longer needed: it holds the selection
     select_and_plan<true>(a, a.logits, a.scores, a.keys, s_slot, reinterpret_cast<uint8_t *>(sw));
-    if (tid == 0)
+    __syncthreads();
+    if (tid == 0) {
         atomicExch(a.ctrl + MOE_CTRL_TICKET, 0u);
+        // a hint for the gate/up kernel's producer: the plan is written, so
+        // its dependency wait is about to end (its own wait still orders it)
+        *reinterpret_cast<volatile uint32_t *>(a.ctrl + MOE_CTRL_GATEUP + 5) = 1u;
+    }
 }
 
 // the selection alone, on caller-provided logits: one CTA of 256 threads
