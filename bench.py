@@ -131,12 +131,12 @@ def algorithmic_bytes(cfg, m, ne):
     q3 = dim * (inter // 256) * 110
     router = n * dim * 2 + m * dim * 2 + m * n * 4
     # gate/up: routed Q2_K gate+up, the whole bf16 shared expert (W1, W3, W2),
-    # x; writes g, u, gs, us, hs and sd
-    gateup = 2 * ne * q2 + 3 * inter * dim * 2 + m * dim * 2 + 2 * m * k * inter * 4 \
+    # x; writes g, u, h, gs, us, hs and sd
+    gateup = 2 * ne * q2 + 3 * inter * dim * 2 + m * dim * 2 + 3 * m * k * inter * 4 \
         + m * inter * (4 + 4 + 2) + m * dim * 4
-    # down: routed Q3_K down, g and u of the plan; writes down rows; reads sd
-    # and the residual, writes acc, the residual and x_next
-    down = ne * q3 + 2 * m * k * inter * 4 + m * k * dim * 4 + m * dim * (4 + 4 + 4 + 4 + 2)
+    # down: routed Q3_K down, h of the plan; writes down rows; reads sd and the
+    # residual, writes acc, the residual and x_next
+    down = ne * q3 + m * k * inter * 4 + m * k * dim * 4 + m * dim * (4 + 4 + 4 + 4 + 2)
     return router, gateup, down
 
 

@@ -199,7 +199,7 @@ struct Bufs {
     float *plan_w;
     int32_t *plan_rows;
     unsigned long long *ptrs;
-    float *g, *u, *gs, *us, *down, *sd, *acc;
+    float *g, *u, *h, *gs, *us, *down, *sd, *acc;
     uint16_t *hs;
     uint32_t *ctrl, *rgcnt;
 };
@@ -219,6 +219,7 @@ Bufs ws_bufs(const moe_cfg &c, void *ws)
     B.ptrs = reinterpret_cast<unsigned long long *>(b + L.ptrs);
     B.g = reinterpret_cast<float *>(b + L.g);
     B.u = reinterpret_cast<float *>(b + L.u);
+    B.h = reinterpret_cast<float *>(b + L.h);
     B.gs = reinterpret_cast<float *>(b + L.gs);
     B.us = reinterpret_cast<float *>(b + L.us);
     B.hs = reinterpret_cast<uint16_t *>(b + L.hs);
@@ -284,6 +285,7 @@ int launch_experts(const moe_cfg &c, int m, const Geo &G, const Bufs &B, const u
     ga.plan_rows = plan_rows;
     ga.g = B.g;
     ga.u = B.u;
+    ga.h = B.h;
     ga.gs = B.gs;
     ga.us = B.us;
     ga.status = B.ctrl + MOE_CTRL_STATUS;
@@ -306,8 +308,7 @@ int launch_experts(const moe_cfg &c, int m, const Geo &G, const Bufs &B, const u
     da.ptrs = ptrs;
     da.plan_rows = plan_rows;
     da.plan_w = plan_w;
-    da.g = B.g;
-    da.u = B.u;
+    da.h = B.h;
     da.has_shared = w2 != nullptr;
     da.down = B.down;
     da.sd = B.sd;

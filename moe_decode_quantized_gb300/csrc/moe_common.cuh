@@ -42,14 +42,16 @@ namespace moe {
 // ------------------------------------------------------------------ layout
 
 struct WsLayout {
-    size_t ctrl, rgcnt, logits, scores, keys, plan_w, plan_rows, ptrs, g, u, gs, us, hs, down, sd, acc, total;
+    size_t ctrl, rgcnt, logits, scores, keys, plan_w, plan_rows, ptrs, g, u, h, gs, us, hs, down, sd, acc, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // rows per down-projection task and row group: 32 super-blocks of Q3_K
 __host__ __device__ inline int down_rows_per_task(int inter) { return MOE_D_TASK_SB / (inter / MOE_QK); }
-__host__ __device__ inline int gate_rows_per_task(int dim) { return MOE_G_TASK_SB / (dim / MOE_QK); }
+// a routed gate/up task: this many rows of the gate matrix and the same rows
+// of the up matrix (MOE_G_TASK_SB super-blocks in all)
+__host__ __device__ inline int gate_rows_per_task(int dim) { return MOE_G_TASK_SB / 2 / (dim / MOE_QK); }
 
 inline WsLayout ws_layout(const moe_cfg &c)
 {
@@ -66,6 +68,7 @@ inline WsLayout ws_layout(const moe_cfg &c)
     L.ptrs = take(sizeof(uint64_t) * 3 * cap);
     L.g = take(sizeof(float) * cap * c.inter);
     L.u = take(sizeof(float) * cap * c.inter);
+    L.h = take(sizeof(float) * cap * c.inter);  // SwiGLU(g, u) per plan pair
     L.gs = take(sizeof(float) * M * c.inter);
     L.us = take(sizeof(float) * M * c.inter);
     L.hs = take(sizeof(uint16_t) * M * c.inter);  // bf16 SwiGLU of the shared expert

@@ -8,35 +8,38 @@
 // added after the routed experts.
 //
 // Two persistent kernels, one CTA per SM, each a warp-specialised pipeline:
-// one producer lane streams whole tasks (contiguous runs of rows) from HBM
-// into a ring of shared-memory stages with 1-D bulk copies (TMA engine,
-// L2 evict-first), eight consumer warps decode the 2/3-bit quants from shared
-// memory with dp4a integer dots and reduce rows with warp shuffles.
+// one producer warp (eight issuing lanes) streams whole tasks from HBM into a
+// ring of shared-memory stages with 1-D bulk copies (TMA engine, L2
+// evict-first), fifteen consumer warps take tasks as they land, decode the
+// 2/3-bit quants from shared memory with dp4a integer dots and reduce rows
+// with warp shuffles. Tasks are taken from grid-wide counters in chunks.
 //
-//   gate/up kernel: tasks = rows of shared W1 / W3 (issued before the
-//     programmatic-launch wait: they depend only on x, so they overlap the
-//     router and the selection), then 64-super-block row runs of every plan
-//     expert's gate and up matrices. Writes g, u (per plan pair) and gs, us.
-//   down kernel: tasks = 32-super-block row runs of every plan expert's down
-//     matrix and rows of shared W2, all prefetched before the wait (they need
-//     only the pointer table); after the wait each CTA builds the q8_1 of
-//     SwiGLU(g, u) for the pairs it needs and bf16(SwiGLU(gs, us)). A row
-//     group is finished by the warp that completes its last task (a ticket
-//     counter per group, no waiting): acc = plan-order sum of w * down, then
-//     the shared row, residual += acc, x_next = bf16(residual).
+//   gate/up kernel: first the whole shared expert, which depends only on x
+//     and so runs before the programmatic-launch wait, beside the router and
+//     the selection: row pairs (W1 row i and W3 row i in one stage; their
+//     consumer writes gs, us and hs = bf16(SwiGLU)), then W2 against hs (once
+//     every pair is done, grid-wide) into sd. Then, after the wait, the plan
+//     experts' gate and up rows, rt rows of each in one task; the consumer
+//     writes g, u and h = SwiGLU(g, u) per plan pair. Once the selection has
+//     raised its plan-ready hint the routed rows go before the rest of W2.
+//   down kernel: tasks = 64-super-block row runs of every plan expert's down
+//     matrix, all prefetched before the wait (they need only the pointer
+//     table); after the wait each CTA builds q8_1(h) for the pairs it needs.
+//     Row groups are finished by the CTA whose ticket completes them: acc =
+//     plan-order sum of w * down, then sd, residual += acc,
+//     x_next = bf16(residual).
 #pragma once
 #include "moe_common.cuh"
 
 namespace moe {
 
 struct __align__(16) Task {
-    int kind;   // 0 end, 1 routed, 2 shared
-    int mat;    // gate/up kernel: 0 gate or W1, 1 up or W3
+    int kind;   // 0 end, 1 routed, 2 shared row pair (gate/up), 3 shared W2 rows (gate/up)
     int p;      // plan expert
     int row;    // first row (routed) or the row (shared)
     int pair0, npair;
     int seq;    // the task's index in this CTA's stream (written last by the producer)
-    int pad;
+    int pad[2];
 };
 
 // ------------------------------------------------------------------ q8_1 (one 32-block per warp)
@@ -443,7 +446,7 @@ struct GArgs {
     const int32_t *hdr;                // route header (plan tail at plan_off)
     const unsigned long long *ptrs;    // [3][cap]
     const int32_t *plan_rows;          // [cap]
-    float *g, *u;                      // [cap, inter]
+    float *g, *u, *h;                  // [cap, inter]: h = SwiGLU(g, u)
     float *gs, *us;                    // [m, inter]
     uint16_t *hs;                      // [m, inter] bf16(SwiGLU(gs, us))
     float *sd;                         // [m, dim] W2 hs
@@ -639,9 +642,9 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
         cache_plan(ring, a.hdr, a.plan_off, a.plan_rows, a.ptrs, a.cap, 0, 2);
         const PlanCache &pc = *ring.pc;
         const int rt = gate_rows_per_task(dim);
-        const int tpm = inter / rt;  // tasks per matrix
-        const int total = pc.ne * 2 * tpm;
-        const uint32_t bytes = (uint32_t)(rt * nb * MOE_Q2K_BYTES);
+        const int tpe = inter / rt;  // tasks per expert: rt gate rows and the same up rows each
+        const int total = pc.ne * tpe;
+        const uint32_t bytes = (uint32_t)(rt * nb * MOE_Q2K_BYTES);  // one matrix's rows
         for (;;) {
             const int c0 = (int)__shfl_sync(0xffffffffu, nxt, 0);
             if (c0 >= total || !ok)
@@ -655,9 +658,8 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
                 if (issuer && tix < c1) {
                     Task t{};
                     t.kind = 1;
-                    t.p = tix / (2 * tpm);
-                    t.mat = (tix / tpm) & 1;
-                    const int r = tix % tpm;
+                    t.p = tix / tpe;
+                    const int r = tix % tpe;
                     t.row = r * rt;
                     t.pair0 = pc.pair_start[t.p];
                     t.npair = pc.pair_start[t.p + 1] - t.pair0;
@@ -667,8 +669,10 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
                         t.npair = 0;  // a no-op task keeps the indices contiguous
                         nbytes = 0;
                     }
-                    const char *src = reinterpret_cast<const char *>(pc.ptr[t.mat][t.p]) + (size_t)r * bytes;
-                    mine = ring_issue(ring, base + (tix - c0), t, src, nbytes, pol, a.status);
+                    const size_t off = (size_t)r * bytes;
+                    mine = ring_issue(ring, base + (tix - c0), t, reinterpret_cast<const char *>(pc.ptr[0][t.p]) + off,
+                                      nbytes, pol, a.status, reinterpret_cast<const char *>(pc.ptr[1][t.p]) + off,
+                                      nbytes);
                 }
                 ok = __all_sync(0xffffffffu, mine);
             }
@@ -751,12 +755,13 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
             triggered = true;
         }
         if (t.kind == 1) {
-            // MOE_G_TASK_SB super-blocks: lane covers super-blocks lane + 32 i;
-            // one token at a time (tokens of this plan expert), rows reduced
-            // over the nb lanes that share them
+            // rt gate rows then the same rt up rows, MOE_G_TASK_SB super-blocks:
+            // lane covers super-blocks lane + 32 q, so q and q + 2 are the gate
+            // and up parts of the same row (row (lane + 32 q) / nb, block
+            // lane % nb); one token at a time, rows reduced over the nb lanes
+            // that share them, then h = SwiGLU(g, u) of the row
             constexpr int PER = MOE_G_TASK_SB / 32;
             const int blk = lane % nb;  // the same for all PER super-blocks of the lane
-            float *out = t.mat ? a.u : a.g;
 #pragma unroll 1
             for (int tt = 0; tt < t.npair; ++tt) {
                 const uint8_t *xr = act + min(ring.pc->rows[t.pair0 + tt], a.m - 1) * arow;
@@ -774,10 +779,14 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
                         v[q] += __shfl_xor_sync(0xffffffffu, v[q], o);
                 }
                 if (blk == 0) {
-                    float *orow = out + (size_t)(t.pair0 + tt) * inter + t.row;
+                    const size_t o = (size_t)(t.pair0 + tt) * inter + t.row;
 #pragma unroll
-                    for (int q = 0; q < PER; ++q)
-                        orow[(lane + 32 * q) / nb] = v[q];
+                    for (int q = 0; q < PER / 2; ++q) {
+                        const int r = (lane + 32 * q) / nb;
+                        a.g[o + r] = v[q];
+                        a.u[o + r] = v[q + PER / 2];
+                        a.h[o + r] = swiglu_f32(v[q], v[q + PER / 2], a.limit);
+                    }
                 }
             }
             __syncwarp();
@@ -901,7 +910,7 @@ struct DArgs {
     const unsigned long long *ptrs;
     const int32_t *plan_rows;
     const float *plan_w;
-    const float *g, *u;           // [cap, inter]
+    const float *h;               // [cap, inter] SwiGLU(g, u) per plan pair
     float *down;                  // [cap, dim]
     const float *sd;              // [m, dim] the shared expert's output (the gate/up kernel's)
     float *acc;                   // [m, dim]
@@ -1054,7 +1063,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
         return;
     }
 
-    // ---------------- consumers: wait for g, u; build the activations
+    // ---------------- consumers: wait for h; build the activations
     pdl_launch_dependents();
     pdl_wait();
     const int npairs = a.m * a.k;
@@ -1062,22 +1071,15 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
         s_rows[q] = __ldcg(a.plan_rows + q);
         s_w[q] = __ldcg(a.plan_w + q);
     }
-    // q8_1(SwiGLU(g, u)) of the plan pairs this CTA's tasks touch, four lanes
-    // a block
+    // q8_1(h) of the plan pairs this CTA's tasks touch, four lanes a block
     const int np = min(R.pair_hi - R.pair_lo, a.pair_cap);
     const int nblk = np * inter / 32;
     for (int i = threadIdx.x; i < nblk * 4; i += MOE_CONSUMER_WARPS * 32) {
         const int b = i >> 2, sub = i & 3;
         const int pr = b / (inter / 32), bi = b % (inter / 32);
-        const size_t o = (size_t)(R.pair_lo + pr) * inter + bi * 32 + 8 * sub;
-        const float4 g0 = __ldcg(reinterpret_cast<const float4 *>(a.g + o));
-        const float4 g1 = __ldcg(reinterpret_cast<const float4 *>(a.g + o) + 1);
-        const float4 u0 = __ldcg(reinterpret_cast<const float4 *>(a.u + o));
-        const float4 u1 = __ldcg(reinterpret_cast<const float4 *>(a.u + o) + 1);
-        const float v[8] = {swiglu_f32(g0.x, u0.x, a.limit), swiglu_f32(g0.y, u0.y, a.limit),
-                            swiglu_f32(g0.z, u0.z, a.limit), swiglu_f32(g0.w, u0.w, a.limit),
-                            swiglu_f32(g1.x, u1.x, a.limit), swiglu_f32(g1.y, u1.y, a.limit),
-                            swiglu_f32(g1.z, u1.z, a.limit), swiglu_f32(g1.w, u1.w, a.limit)};
+        const float4 *h4 = reinterpret_cast<const float4 *>(a.h + (size_t)(R.pair_lo + pr) * inter + bi * 32 + 8 * sub);
+        const float4 h0 = __ldcg(h4), h1 = __ldcg(h4 + 1);
+        const float v[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
         q8_block_quad(v, sub, act + pr * arow, nb, bi, false);
     }
     consumers_sync();
