@@ -144,6 +144,16 @@ int moe_route_select(const moe_cfg *cfg, const float *logits_dev, const float *b
                      int32_t *header_dev, float *plan_w_dev, int32_t *plan_rows_dev,
                      uint64_t *ptrs_dev, moe_stream_t stream);
 
+/* The routing score of each logit ([moe_v41] fn softplus, fn
+ * route_from_logits): scores[i] = the f32 rounding of the exact
+ * sqrt(softplus(t)), t = f32(logits[i] / gate_temp), softplus(x) = x for
+ * x > 20, else ln(1 + e^x) -- the score the router and the selection use.
+ * Evaluated in float-float single precision, in double precision when that
+ * cannot decide the rounding. logits_dev, scores_dev f32 [count], count >= 0
+ * (0: nothing is launched). */
+int moe_route_scores(const moe_cfg *cfg, const float *logits_dev, int count, float *scores_dev,
+                     moe_stream_t stream);
+
 /* The routed experts of one call ([moe_v41] module doc: three K-quant GEMVs
  * per expert on the raw blocks, gate and up Q2_K, down Q3_K, q8_1 activation;
  * struct Kernels mmvq_q2k_experts / swiglu_q8 / mmvq_q3k_experts /

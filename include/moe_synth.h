@@ -23,8 +23,11 @@ extern "C" {
 
 typedef struct CUstream_st *moe_synth_stream_t;
 
-/* nblocks random Q2_K blocks (84 B): random bytes, the high byte of d and
- * dmin (bytes 81, 83) forced to (b & 3) | 0x18. dst: device, 8-byte aligned. */
+/* nblocks centred Q2_K blocks (84 B), from the random bytes r of the
+ * stream: scale bytes 0..15 = sc | (3 sc) << 4 with sc = ((r & 15) * 6) >> 4
+ * (min = 3 x scale), quants 16..79 = r, d = bytes 80, 81 with byte 81 =
+ * (r & 3) | 0x18, dmin = d / 2 (byte 82 = byte 80, byte 83 = (r81 & 3) | 0x14):
+ * each weight is d * sc * (q - 1.5). dst: device, 8-byte aligned. */
 int moe_synth_q2k(void *dst, uint64_t nblocks, uint64_t key, moe_synth_stream_t stream);
 
 /* nblocks random Q3_K blocks (110 B): random bytes, byte 109 (high byte of d)

@@ -26,7 +26,7 @@ SLOT_TABLE_LAYERS = 64
 __all__ = ["Config", "Arena", "Layer", "MoeError", "header_words", "workspace_bytes",
            "workspace_init", "router_logits", "quantize_q8_1", "route_select", "expert_step",
            "swiglu_q8", "layer_step", "host_io_bytes", "layer_step_host", "workspace_view",
-           "read_status", "layer_step_profiled", "layer_step_static", "slot_table_set", "dedupe_triples", "parse_header", "Graph"]
+           "read_status", "layer_step_profiled", "layer_step_static", "route_scores", "slot_table_set", "dedupe_triples", "parse_header", "Graph"]
 
 
 class MoeError(RuntimeError):
@@ -163,6 +163,11 @@ def layer_step_static(cfg: Config, layer: Layer, arena: Arena, x, residual, x_ne
     _check(_lib.moe().moe_layer_step_static(C.byref(cfg.c()), C.byref(layer.c()), C.byref(arena.c()), _ptr(x),
                                             _ptr(residual), _ptr(x_next), _ptr(header), m, _ptr(status),
                                             _stream(stream)))
+
+
+def route_scores(cfg: Config, logits, scores, count: int, stream=None):
+    """scores[i] = f32(sqrt(softplus(logits[i] / gate_temp))), correctly rounded."""
+    _check(_lib.moe().moe_route_scores(C.byref(cfg.c()), _ptr(logits), count, _ptr(scores), _stream(stream)))
 
 
 def host_io_bytes(cfg: Config, m: int) -> int:

@@ -49,6 +49,7 @@ MOE_SYMBOLS = {
     "moe_quantize_q8_1": (C.c_int, [C.POINTER(MoeCfg), P, C.c_int, P, P]),
     "moe_route_select": (C.c_int, [C.POINTER(MoeCfg), P, P, P, C.POINTER(MoeArena), C.c_int, P, P,
                                    P, P, P]),
+    "moe_route_scores": (C.c_int, [C.POINTER(MoeCfg), P, C.c_int, P, P]),
     "moe_expert_step": (C.c_int, [C.POINTER(MoeCfg), P, P, P, P, P, C.c_int, P, P, P]),
     "moe_swiglu_q8": (C.c_int, [C.POINTER(MoeCfg), P, P, C.c_int, P, P, P]),
     "moe_layer_step": (C.c_int, [C.POINTER(MoeCfg), C.POINTER(MoeLayer), C.POINTER(MoeArena), P, P,

@@ -562,6 +562,21 @@ int moe_swiglu_q8(const moe_cfg *cfg, const float *g, const float *u, int rows, 
     return MOE_OK;
 }
 
+int moe_route_scores(const moe_cfg *cfg, const float *logits, int count, float *scores, moe_stream_t stream)
+{
+    int rc = check_cfg(cfg);
+    if (rc)
+        return rc;
+    if (count < 0)
+        return fail(MOE_EINVAL, "moe_route_scores: count (%d) < 0", count);
+    if (count == 0)
+        return MOE_OK;
+    if (!logits || !scores)
+        return fail(MOE_EINVAL, "moe_route_scores: a buffer is NULL");
+    ScoreArgs a{logits, scores, cfg->gate_temp, count};
+    return launch(moe_score_kernel, dim3((count + 255) / 256), dim3(256), 0, (cudaStream_t)stream, false, a);
+}
+
 int moe_route_select(const moe_cfg *cfg, const float *logits, const float *bias, const int32_t *slot_row,
                      const moe_arena *arena, int m, int32_t *header, float *plan_w, int32_t *plan_rows,
                      uint64_t *ptrs, moe_stream_t stream)

@@ -11,10 +11,10 @@
 // Selection (page spark_model/layers/moe_v41.rs, fn softplus and
 // fn route_from_logits): score = f32(sqrt(softplus(l / temp))), key = score +
 // bias, stable descending order, top k, weights renormalised in f32. The
-// score is the correctly rounded f32 of the exact value, evaluated in double
-// precision in the router epilogue, where every CTA takes a few of the rows
-// (FP64 is a slow pipe on GB300; spread over the CTAs its latency is paid
-// once). The selecting CTA is latency-bound: it reads everything it needs in
+// score is the correctly rounded f32 of the exact value, evaluated in the
+// router epilogue, where every CTA takes a few of the rows, in float-float
+// single precision with a double-precision fallback near rounding midpoints
+// (FP64 is a slow pipe on GB300). The selecting CTA is latency-bound: it reads everything it needs in
 // one round of loads, ranks each token with one warp (k rounds of a warp-wide
 // maximum over 64-bit sortable values), and only stores afterwards.
 #pragma once
@@ -50,11 +50,270 @@ struct RouteArgs {
 // softplus(x) = x for x > 20. Evaluated in f64 (CUDA's exp, log1p, sqrt) and
 // rounded once: the f64 chain's error is far below half an f32 ulp, so the
 // rounding equals the exact one except within ~2^-50 of an f32 midpoint.
-__device__ __forceinline__ float score_exact(float l, float temp)
+__device__ __noinline__ float score_exact(float l, float temp)
 {
     const float t = __fdiv_rn(l, temp);
     const double sp = t > 20.0f ? (double)t : log1p(exp((double)t));
     return __double2float_rn(sqrt(sp));
+}
+
+// ------------------------------------------------------------------ the score without FP64
+//
+// The same correctly rounded score in single precision (FP64 is a slow pipe
+// on GB300: the double-precision chain above costs microseconds of latency).
+// A candidate s comes from CUDA's expf / log1pf / sqrtf (a few ulp off);
+// then, for each midpoint m between two neighbouring f32 values, the exact
+// score S satisfies S >= m  <=>  softplus(t) >= m^2  <=>  e^t >= expm1(m^2)
+// (both sides increasing), and e^t and expm1(m^2) are evaluated in
+// float-float (pairs of f32, unevaluated sums hi + lo: Dekker's and Knuth's
+// exact sum and product) to about 2^-39 relative. A decision closer than
+// 2^-37 relative, or t below -170, goes to the double-precision path.
+
+struct ff {
+    float hi, lo;
+};
+
+__device__ __forceinline__ ff ff_two_sum(float a, float b)
+{
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    return {s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
+}
+
+__device__ __forceinline__ ff ff_fast_two_sum(float a, float b)  // |a| >= |b|
+{
+    const float s = __fadd_rn(a, b);
+    return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+
+__device__ __forceinline__ ff ff_two_prod(float a, float b)
+{
+    const float p = __fmul_rn(a, b);
+    return {p, __fmaf_rn(a, b, -p)};
+}
+
+__device__ __forceinline__ ff ff_add(ff a, ff b)
+{
+    const ff s = ff_two_sum(a.hi, b.hi);
+    return ff_fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
+}
+
+__device__ __forceinline__ ff ff_mul(ff a, ff b)
+{
+    const ff p = ff_two_prod(a.hi, b.hi);
+    return ff_fast_two_sum(p.hi, __fmaf_rn(a.hi, b.lo, __fmaf_rn(a.lo, b.hi, p.lo)));
+}
+
+// 1/n!, n = 0 .. 14: the exact rationals rounded to f32 twice (hi, then the
+// rest). A table in constant memory (one broadcast load a step) and loops
+// that are not unrolled keep this code small: it runs once per launch, so its
+// instructions are fetched cold.
+__constant__ float2 c_inv_fact[15] = {
+    {1.0f, 0.0f},
+    {1.0f, 0.0f},
+    {0x1.0p-1f, 0.0f},
+    {0x1.555556p-3f, -0x1.555556p-28f},
+    {0x1.555556p-5f, -0x1.555556p-30f},
+    {0x1.111112p-7f, -0x1.dddddep-32f},
+    {0x1.6c16c2p-10f, -0x1.27d27ep-35f},
+    {0x1.a01a02p-13f, -0x1.7f97fap-39f},
+    {0x1.a01a02p-16f, -0x1.7f97fap-42f},
+    {0x1.71de3ap-19f, 0x1.55b1ccp-45f},
+    {0x1.27e4fcp-22f, -0x1.10ec14p-47f},
+    {0x1.ae6456p-26f, 0x1.fd5138p-52f},
+    {0x1.1eed8ep-29f, 0x1.ff1b12p-54f},
+    {0x1.612462p-33f, -0x1.8af25ep-58f},
+    {0x1.93974ap-37f, 0x1.180f94p-62f},
+};
+
+__device__ __forceinline__ ff ff_inv_fact(int n)
+{
+    const float2 c = c_inv_fact[n];
+    return {c.x, c.y};
+}
+
+// 2^(j / 32), j = 0 .. 31, as float-float pairs (hi = the f32 rounding, lo =
+// the f32 rounding of the rest; the pairs are within 2^-49 relative)
+__constant__ float2 c_exp2_32[32] = {
+    {0x1p+0f, 0x0p+0f},
+    {0x1.059b0ep+0f, -0x1.9d4f52p-25f},
+    {0x1.0b5586p+0f, 0x1.9f3122p-25f},
+    {0x1.11301ep+0f, -0x1.fdb496p-25f},
+    {0x1.172b84p+0f, -0x1.c15742p-27f},
+    {0x1.1d4874p+0f, -0x1.d2e8cap-25f},
+    {0x1.2387a6p+0f, 0x1.ceac48p-25f},
+    {0x1.29e9ep+0f, -0x1.5c0424p-25f},
+    {0x1.306fep+0f, 0x1.4636e2p-25f},
+    {0x1.371a74p+0f, -0x1.18aac6p-25f},
+    {0x1.3dea64p+0f, 0x1.824684p-25f},
+    {0x1.44e086p+0f, 0x1.8624b4p-30f},
+    {0x1.4bfdaep+0f, -0x1.593abcp-25f},
+    {0x1.5342b6p+0f, -0x1.2c561p-25f},
+    {0x1.5ab07ep+0f, -0x1.5bd5ecp-27f},
+    {0x1.6247ecp+0f, -0x1.f8b55p-25f},
+    {0x1.6a09e6p+0f, 0x1.9fcef4p-26f},
+    {0x1.71f75ep+0f, 0x1.1d8beep-25f},
+    {0x1.7a1148p+0f, -0x1.829fdp-25f},
+    {0x1.82589ap+0f, -0x1.accc7cp-26f},
+    {0x1.8ace54p+0f, 0x1.15506ep-27f},
+    {0x1.93737cp+0f, -0x1.e64744p-25f},
+    {0x1.9c4918p+0f, 0x1.51f848p-27f},
+    {0x1.a5503cp+0f, -0x1.b83b54p-25f},
+    {0x1.ae89fap+0f, -0x1.a94b14p-26f},
+    {0x1.b7f77p+0f, -0x1.a09438p-25f},
+    {0x1.c199bep+0f, -0x1.3d56b2p-27f},
+    {0x1.cb720ep+0f, -0x1.8837ccp-27f},
+    {0x1.d5818ep+0f, -0x1.822dbcp-27f},
+    {0x1.dfc974p+0f, -0x1.908c94p-25f},
+    {0x1.ea4afap+0f, 0x1.52486cp-27f},
+    {0x1.f50766p+0f, -0x1.246ebp-26f},
+};
+
+// 2^q for q in [-126, 127], exactly
+__device__ __forceinline__ float pow2i(int q) { return __int_as_float((q + 127) << 23); }
+
+// One step of the five lockstep Horner chains below
+__device__ __forceinline__ ff horner_step(ff p, ff r, bool ser, ff c0, ff c1)
+{
+    return ff_add(ff_mul(p, r), ser ? c1 : c0);
+}
+
+// Tang's table-driven reduction of x (|x| < 120): k = round(x 32 / ln2),
+// x = k ln2 / 32 + r with ln2 / 32 in three parts, the first with 12
+// significant bits so that k times it is exact; |r| < 0.011. Returns r; j =
+// k mod 32, q = floor(k / 32): e^x = 2^q 2^(j / 32) e^r.
+__device__ __forceinline__ ff tang_reduce(ff x, int &j, int &q)
+{
+    const float P1 = 0x1.62ep-6f, P2 = 0x1.0bfbe8p-20f, P3 = 0x1.cf79acp-45f;
+    const float kf = rintf(x.hi * 0x1.715476p+5f);
+    const int k = (int)kf;
+    j = k & 31;
+    q = k >> 5;  // arithmetic shift: floor
+    ff r = ff_two_sum(x.hi, -kf * P1);  // kf * P1 is exact
+    r = ff_add(r, {x.lo, 0.0f});
+    const ff k2 = ff_two_prod(kf, P2);
+    r = ff_add(r, {-k2.hi, -k2.lo});
+    return ff_add(r, {-kf * P3, 0.0f});
+}
+
+// For t in [-40, 20]: the candidate s and its neighbours s_-2 .. s_+2 (f32
+// steps), the four midpoints m_i between them, and five independent values
+// in float-float evaluated in lockstep: e^t and expm1(m_i^2). The number c of
+// midpoints below the exact score places it: the rounding is s_c (c = 1..3).
+// e^x by Tang's reduction and the Taylor series of e^r to r^5 / 5!
+// (remainder below 2^-48), times 2^(j/32) from the table and 2^q; expm1(M)
+// below 2^-6: M times the series of (e^M - 1) / M to M^5 / 6! (remainder
+// below 2^-48), else e^M - 1 (e^M - 1 >= 2^-6: at most 6 bits lost). Returns
+// -1 when a decision is closer than 2^-37 relative or the candidate is off by
+// two steps.
+__device__ __noinline__ float score_ff(float t)
+{
+    const float s = sqrtf(log1pf(expf(t)));
+    const unsigned sb = __float_as_uint(s);  // positive and normal: +-1 on the bits steps one f32
+    float sv[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i)
+        sv[i] = __uint_as_float(sb + i - 2);
+    ff x[5], r[5], p[5];
+    bool ser[5];
+    int j[5], q[5];
+    x[0] = {t, 0.0f};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const ff m = {sv[i + 1], __fmul_rn(__fsub_rn(sv[i], sv[i + 1]), 0.5f)};  // exact midpoint
+        x[i + 1] = ff_mul(m, m);
+    }
+#pragma unroll
+    for (int v = 0; v < 5; ++v) {
+        ser[v] = v > 0 && x[v].hi < 0x1.0p-6f;
+        j[v] = 0;
+        q[v] = 0;
+        r[v] = ser[v] ? x[v] : tang_reduce(x[v], j[v], q[v]);
+        p[v] = ff_inv_fact(ser[v] ? 6 : 5);
+    }
+#pragma unroll 1
+    for (int n = 4; n >= 0; --n) {
+        const ff c0 = ff_inv_fact(n), c1 = ff_inv_fact(n + 1);
+#pragma unroll
+        for (int v = 0; v < 5; ++v)
+            p[v] = horner_step(p[v], r[v], ser[v], c0, c1);
+    }
+    ff val[5];
+#pragma unroll
+    for (int v = 0; v < 5; ++v) {
+        if (ser[v]) {
+            val[v] = ff_mul(p[v], x[v]);
+        } else {
+            const float2 tj = c_exp2_32[j[v]];
+            const ff e = ff_mul({tj.x, tj.y}, p[v]);
+            const float sc = pow2i(q[v]);
+            val[v] = {__fmul_rn(e.hi, sc), __fmul_rn(e.lo, sc)};
+            if (v > 0)
+                val[v] = ff_add(val[v], {-1.0f, 0.0f});
+        }
+    }
+    const float tol = 0x1.0p-37f * val[0].hi;
+    int c = 0;
+    bool sure = true;
+#pragma unroll
+    for (int i = 1; i < 5; ++i) {
+        const ff D = ff_add(val[0], {-val[i].hi, -val[i].lo});
+        sure = sure && fabsf(D.hi) > tol;
+        c += D.hi > 0.0f;
+    }
+    if (!sure || c == 0 || c == 4)
+        return -1.0f;
+    return c == 1 ? sv[1] : (c == 2 ? sv[2] : sv[3]);
+}
+
+// For t in [-170, -40]: softplus(t) = e^t (1 - e^t / 2 + ...) with e^t below
+// 4.2e-18, so S = e^(t/2) (1 + d), |d| < 2^-59, far inside the 2^-37 margin:
+// S rounds as e^(t/2) does. e^(t/2) = 2^q 2^(j/32) e^r (as in score_ff),
+// compared with the midpoints scaled by 2^-q (exact), so that nothing
+// underflows. Returns -1 when a decision is too close or the candidate is
+// off by two steps.
+__device__ __noinline__ float score_ff_tiny(float t)
+{
+    const float h = __fmul_rn(t, 0.5f);  // exact
+    const float s = expf(h);
+    const unsigned sb = __float_as_uint(s);
+    float sv[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i)
+        sv[i] = __uint_as_float(sb + i - 2);
+    int j, q;
+    const ff r = tang_reduce({h, 0.0f}, j, q);
+    ff p = ff_inv_fact(5);
+#pragma unroll 1
+    for (int n = 4; n >= 0; --n)
+        p = ff_add(ff_mul(p, r), ff_inv_fact(n));
+    const float2 tj = c_exp2_32[j];
+    p = ff_mul({tj.x, tj.y}, p);
+    const float sc = pow2i(-q);
+    const float tol = 0x1.0p-37f * p.hi;
+    int c = 0;
+    bool sure = true;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float mh = __fmul_rn(__fsub_rn(sv[i], sv[i + 1]), 0.5f);  // the midpoint is sv[i + 1] + mh
+        const ff D = ff_add(p, {-__fmul_rn(sv[i + 1], sc), -__fmul_rn(mh, sc)});
+        sure = sure && fabsf(D.hi) > tol;
+        c += D.hi > 0.0f;
+    }
+    if (!sure || c == 0 || c == 4)
+        return -1.0f;
+    return c == 1 ? sv[1] : (c == 2 ? sv[2] : sv[3]);
+}
+
+__device__ __forceinline__ float score_fast(float l, float temp)
+{
+    const float t = __fdiv_rn(l, temp);
+    if (t > 20.0f)
+        return __fsqrt_rn(t);  // sqrt(t) correctly rounded
+    if (!(t >= -170.0f))
+        return score_exact(l, temp);  // also NaN
+    const float s = t >= -40.0f ? score_ff(t) : score_ff_tiny(t);
+    return s > 0.0f ? s : score_exact(l, temp);
 }
 
 // ------------------------------------------------------------------ sortable keys
@@ -440,15 +699,19 @@ __global__ void __launch_bounds__(256) moe_router_kernel(RouteArgs a)
         }
     });
     __syncthreads();
-    for (int i = tid; i < nrows * m; i += blockDim.x) {
+    // one score a warp first (lane-major over the warps): the scores take
+    // different paths by range, and paths in one warp would run one after
+    // another
+    const int nw = blockDim.x >> 5;
+    for (int i = warp + nw * lane; i < nrows * m; i += blockDim.x) {
         const int r = i / m, t = i % m;
         const float l = red[i];
         const size_t o = (size_t)t * a.n + row0 + r;
         a.logits[o] = l;
         if (a.do_select) {
-            // the exact score of this row, here: the f64 chain runs on a few
-            // threads of every CTA in parallel instead of in the selecting CTA
-            const float sc = score_exact(l, a.temp);
+            // the exact score of this row, here: a few threads of every CTA
+            // in parallel instead of the selecting CTA
+            const float sc = score_fast(l, a.temp);
             a.scores[o] = sc;
             a.keys[o] = __fadd_rn(sc, s_bias[r]);
         }
@@ -492,12 +755,28 @@ __global__ void __launch_bounds__(256) moe_select_kernel(RouteArgs a)
     for (int e = threadIdx.x; e < a.n; e += blockDim.x)
         slot[e] = __ldg(a.slot_row + e);
     for (int i = threadIdx.x; i < (int)mn; i += blockDim.x) {
-        const float s = score_exact(a.logits[i], a.temp);
+        const float s = score_fast(a.logits[i], a.temp);
         sc[i] = s;
         ky[i] = __fadd_rn(s, __ldg(a.bias + i % a.n));
     }
     __syncthreads();
     select_and_plan<false>(a, a.logits, sc, ky, slot, smem);
+}
+
+struct ScoreArgs {
+    const float *logits;
+    float *scores;
+    float temp;
+    int count;
+};
+
+// the routing score of each of count logits (one thread each)
+__global__ void moe_score_kernel(ScoreArgs a)
+{
+    pdl_wait();
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < a.count)
+        a.scores[i] = score_fast(a.logits[i], a.temp);
 }
 
 }  // namespace moe

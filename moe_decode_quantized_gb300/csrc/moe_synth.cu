@@ -49,6 +49,49 @@ __global__ void kblocks_kernel(uint8_t *dst, uint64_t nbytes, uint64_t key, uint
     }
 }
 
+__device__ __forceinline__ uint32_t rbyte(uint64_t key, uint64_t pos)
+{
+    return (uint32_t)(word(key, pos >> 3) >> (8 * (pos & 7))) & 0xFFu;
+}
+
+// centred Q2_K blocks (see moe_synth_q2k): one thread per 8 bytes
+__global__ void q2k_kernel(uint8_t *dst, uint64_t nbytes, uint64_t key)
+{
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t w = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; w * 8 < nbytes; w += stride) {
+        const uint64_t p0 = w * 8;
+        uint8_t b[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint64_t p = p0 + j;
+            const uint32_t off = (uint32_t)(p % 84);
+            const uint32_t r = rbyte(key, p);
+            uint32_t v = r;
+            if (off < 16) {
+                const uint32_t sc = ((r & 0x0Fu) * 6u) >> 4;
+                v = sc | ((3u * sc) << 4);
+            } else if (off == 81) {
+                v = (r & 3u) | 0x18u;
+            } else if (off == 82) {
+                v = rbyte(key, p - 2);
+            } else if (off == 83) {
+                v = (rbyte(key, p - 2) & 3u) | 0x14u;
+            }
+            b[j] = (uint8_t)v;
+        }
+        if (p0 + 8 <= nbytes) {
+            uint64_t o = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                o |= (uint64_t)b[j] << (8 * j);
+            *reinterpret_cast<uint64_t *>(dst + p0) = o;
+        } else {
+            for (int j = 0; p0 + j < nbytes; ++j)
+                dst[p0 + j] = b[j];
+        }
+    }
+}
+
 __global__ void normal_bf16_kernel(uint16_t *dst, uint64_t n, uint64_t key, float scale)
 {
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
@@ -83,8 +126,7 @@ extern "C" {
 int moe_synth_q2k(void *dst, uint64_t nblocks, uint64_t key, moe_synth_stream_t stream)
 {
     const uint64_t nb = nblocks * 84;
-    kblocks_kernel<<<grid_for((nb + 7) / 8), 256, 0, (cudaStream_t)stream>>>(static_cast<uint8_t *>(dst), nb, key,
-                                                                            84, 81, 83, 0x18);
+    q2k_kernel<<<grid_for((nb + 7) / 8), 256, 0, (cudaStream_t)stream>>>(static_cast<uint8_t *>(dst), nb, key);
     return (int)cudaGetLastError();
 }
 

@@ -23,8 +23,11 @@ expert blocks):
 * bf16: the approx-normal f32 rounded to nearest-even bf16.
 * uniform f32 in [lo, hi): the top 24 bits of a word as u * 2^-24, then
   lo + (hi - lo) * u with two f32 roundings.
-* random Q2_K blocks (84 B): uniform random bytes, except that the high byte
-  of the f16 `d` and `dmin` fields is forced into [2^-9, 2^-8).
+* Q2_K blocks (84 B), centred like quantised weights: random quants, each
+  sub-block's scale sc in 0..5 with min 3 sc, f16 `d` in [2^-9, 2^-8) and
+  `dmin` = d / 2, so every weight is d * sc * (q - 1.5) (uniform random bytes
+  everywhere would make biased weights whose dot products grow with the
+  length instead of its square root).
 * random Q3_K blocks (110 B): uniform random bytes, except that the high byte
   of the f16 `d` field is forced into [2^-12, 2^-11).
 """
@@ -122,10 +125,17 @@ def random_bytes(key: int, nbytes: int) -> np.ndarray:
 
 
 def q2k_blocks(key: int, nblocks: int) -> np.ndarray:
-    """`nblocks` random Q2_K super-blocks as raw bytes, shape (nblocks, 84)."""
-    b = random_bytes(key, nblocks * Q2K_BYTES).reshape(nblocks, Q2K_BYTES)
-    b[:, 81] = (b[:, 81] & 0x03) | 0x18   # d    in [2^-9, 2^-8)
-    b[:, 83] = (b[:, 83] & 0x03) | 0x18   # dmin in [2^-9, 2^-8)
+    """`nblocks` random Q2_K super-blocks as raw bytes, shape (nblocks, 84),
+    centred like quantised weights: every sub-block's min is 3x its scale
+    (scale sc in 0..5, min 3 sc) and dmin = d / 2, so that each weight is
+    d * sc * (q - 1.5); random quants, d in [2^-9, 2^-8)."""
+    r = random_bytes(key, nblocks * Q2K_BYTES).reshape(nblocks, Q2K_BYTES)
+    b = r.copy()
+    sc = ((r[:, :16] & 0x0F).astype(np.uint32) * 6) >> 4                  # 0..5
+    b[:, :16] = (sc | ((3 * sc) << 4)).astype(np.uint8)                  # scale | min << 4
+    b[:, 81] = (r[:, 81] & 0x03) | 0x18                                    # d in [2^-9, 2^-8)
+    b[:, 82] = r[:, 80]                                                    # dmin = d / 2:
+    b[:, 83] = (r[:, 81] & 0x03) | 0x14                                    # exponent one lower
     return b
 
 

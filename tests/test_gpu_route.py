@@ -175,6 +175,53 @@ def _arena(size=1 << 20):
     return t, a, (t.data_ptr(), 4096, 0, 1024, 2048)
 
 
+# ------------------------------------------------------------------ the score
+
+def _oracle_scores(logits, temp):
+    """The oracle's exact scores (long double, correctly rounded) and the
+    mask of values within 2^-46 relative of an f32 rounding midpoint."""
+    n = 1024
+    lg = np.asarray(logits, np.float32)
+    pad = (-len(lg)) % n
+    rows = np.concatenate([lg, np.zeros(pad, np.float32)]).reshape(-1, n)
+    c = oracle.cfg(256, 256, n, 1, True, temp, 1.0, 0.0)
+    _, _, scores, flags = oracle.route(c, rows, np.zeros(n, np.float32))
+    near = np.zeros(rows.shape, bool)
+    for r in np.nonzero(flags & 4)[0]:  # rows holding a near-midpoint score
+        for j in range(n):
+            near[r, j] = oracle.score(float(rows[r, j]), temp)[1]
+    return scores.ravel()[:len(lg)], near.ravel()[:len(lg)]
+
+
+@pytest.mark.parametrize("temp", [1.0, 0.7])
+def test_route_scores_are_correctly_rounded(temp):
+    """Page moe_v41.rs fn softplus / fn route_from_logits: the score is the
+    f32 rounding of the exact sqrt(softplus(l / temp)); the device's
+    float-float evaluation (double precision near midpoints) equals the
+    oracle's long-double rounding bit for bit."""
+    rng = np.random.default_rng(11)
+    parts = [rng.normal(0.0, 3.0, 1 << 19),
+             rng.uniform(-60.0, 30.0, 1 << 18),
+             rng.uniform(19.9, 20.1, 1 << 14) * temp,       # around the x > 20 cut
+             rng.uniform(-40.5, -39.5, 1 << 14) * temp,     # where softplus becomes e^t to f32 precision
+             rng.uniform(-175.0, -40.0, 1 << 16) * temp,    # the e^(t/2) path and below it
+             rng.uniform(-171.0, -169.0, 1 << 12) * temp,
+             rng.normal(0.0, 1e-3, 1 << 14),
+             np.array([0.0, -0.0, 20.0 * temp, -40.0 * temp, 1e-30, -1e-30, 88.0, -88.0, 300.0, -300.0])]
+    lg = np.concatenate(parts).astype(np.float32)
+    d_in = torch.from_numpy(lg).cuda()
+    d_out = torch.full_like(d_in, float("nan"))
+    cfg = tiny_cfg(1, gate_temp=temp)
+    moe.route_scores(cfg, d_in, d_out, len(lg))
+    torch.cuda.synchronize()
+    got = d_out.cpu().numpy()
+    ref, near = _oracle_scores(lg, temp)
+    ok = (got.view(np.uint32) == ref.view(np.uint32)) | near
+    bad = np.nonzero(~ok)[0]
+    assert len(bad) == 0, [(float(lg[i]), float(got[i]), float(ref[i])) for i in bad[:5]]
+    assert near.sum() < 50
+
+
 @pytest.mark.parametrize("case", ["tiny", "decode_m1", "decode_m8", "tie_m8", "no_norm", "top1",
                                   "temp", "wide_bias"])
 def test_route_select_bit_exact(case):
