@@ -280,6 +280,7 @@ int launch_experts(const moe_cfg &c, int m, const Geo &G, const Bufs &B, const u
     ga.sd = B.sd;
     ga.limit = c.swiglu_limit;
     ga.w2r = G.w2r;
+    ga.plan_hint = pdl_gateup ? 1 : 0;  // only a layer step's router raises the hint
     ga.hdr = hdr;
     ga.ptrs = ptrs;
     ga.plan_rows = plan_rows;

@@ -456,6 +456,7 @@ struct GArgs {
     // plan-ready hint
     uint32_t *gctr;
     float limit;
+    int plan_hint;  // the plan comes from the selection in this stream (its hint at gctr[5])
     int dim, inter, m, k, cap, plan_off, S, w2r;
     uint32_t stage_bytes;
 };
@@ -637,8 +638,26 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
         unsigned nxt = 0;
         if (lane == 0)
             nxt = atomicAdd(a.gctr + 1, (unsigned)MOE_G_CHUNK);
-        pdl_wait();  // the selection has written the plan and the pointer table
-        pdl_launch_dependents();
+        if (a.plan_hint) {
+            // the selecting CTA publishes the plan with a release store of the
+            // hint: acquiring it, the plan can be read before the router grid
+            // has finished (bounded poll; the wait below still comes before
+            // this CTA lets the next kernel start)
+            if (ld_acquire_gpu(a.gctr + 5) == 0u) {
+                const uint64_t t0 = globaltimer();
+                while (ld_acquire_gpu(a.gctr + 5) == 0u) {
+                    __nanosleep(64);
+                    if (globaltimer() - t0 > MOE_WAIT_NS) {
+                        if (lane == 0)
+                            atomicOr(a.status, (uint32_t)MOE_WS_TIMEOUT);
+                        break;
+                    }
+                }
+            }
+            __syncwarp();
+        } else {
+            pdl_wait();  // the plan and the pointer table come from the caller
+        }
         cache_plan(ring, a.hdr, a.plan_off, a.plan_rows, a.ptrs, a.cap, 0, 2);
         const PlanCache &pc = *ring.pc;
         const int rt = gate_rows_per_task(dim);
@@ -678,6 +697,10 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
             }
             base += c1 - c0;
         }
+        // the next kernel may start once the router grid has completed (it
+        // reads the plan before its own wait)
+        pdl_wait();
+        pdl_launch_dependents();
         if (w2_pending != -1) {
             // the rest of W2, hs first if it is not in shared memory yet (the
             // routed tasks ahead of it never wait)
@@ -732,9 +755,8 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
     }
     consumers_sync();
 
-    // every thread triggers the dependent launch only after the selection is
-    // complete (the first routed task is issued after the producer's wait)
-    bool triggered = false;
+    // (the producer triggers the dependent launch, after its wait on the
+    // router grid; consumers read the plan from shared memory only)
     bool hs_seen = false;
     for (;;) {
         const int j = ring_grab(ring);
@@ -749,11 +771,6 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
             break;
         }
         const uint8_t *st = ring.at(slot);
-        if (t.kind == 1 && !triggered) {
-            pdl_wait();
-            pdl_launch_dependents();
-            triggered = true;
-        }
         if (t.kind == 1) {
             // rt gate rows then the same rt up rows, MOE_G_TASK_SB super-blocks:
             // lane covers super-blocks lane + 32 q, so q and q + 2 are the gate
@@ -885,10 +902,6 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
                     mbar_arrive(&ring.empty[slot]);
             });
         }
-    }
-    if (!triggered) {
-        pdl_wait();
-        pdl_launch_dependents();
     }
     // the last CTA out resets the grid-wide counters: by then every producer
     // has stopped taking tasks and every consumer has counted its row pairs

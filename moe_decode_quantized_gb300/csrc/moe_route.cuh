@@ -735,9 +735,10 @@ __global__ void __launch_bounds__(256) moe_router_kernel(RouteArgs a)
     __syncthreads();
     if (tid == 0) {
         atomicExch(a.ctrl + MOE_CTRL_TICKET, 0u);
-        // a hint for the gate/up kernel's producer: the plan is written, so
-        // its dependency wait is about to end (its own wait still orders it)
-        *reinterpret_cast<volatile uint32_t *>(a.ctrl + MOE_CTRL_GATEUP + 5) = 1u;
+        // the plan is written: released to the gate/up kernel's producers,
+        // which read it without waiting for this grid to finish (release:
+        // this CTA's stores, ordered before by the barrier)
+        asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a.ctrl + MOE_CTRL_GATEUP + 5), "r"(1u) : "memory");
     }
 }
 
