@@ -161,11 +161,11 @@ int geometry(const moe_cfg &c, int m, bool shared, const DevInfo &I, Geo &G)
     G.r_grid = (n + G.r_rows - 1) / G.r_rows;
     G.r_smem = router_smem(G.r_rows, dim, m, c.n_routed);
     G.grid = I.sms;
-    // gate/up: stages of max(one Q2_K task, a shared row pair W1 + W3, one W2 row);
+    // gate/up: stages of max(one Q2_K task, one shared W1 or W3 row, one W2 row);
     // w2r W2 rows a task, as many as a stage holds (<= 4, dividing dim)
     size_t gst = (size_t)MOE_G_TASK_SB * MOE_Q2K_BYTES;
     if (shared)
-        gst = std::max(gst, std::max((size_t)dim * 2 * 2, (size_t)inter * 2));
+        gst = std::max(gst, std::max((size_t)dim * 2, (size_t)inter * 2));
     G.g_stage = (uint32_t)align_up(gst, 128);
     G.w2r = 1;
     while (shared && G.w2r < 4 && (size_t)G.w2r * 2 * inter * 2 <= G.g_stage && dim % (G.w2r * 2) == 0)
@@ -201,7 +201,7 @@ struct Bufs {
     unsigned long long *ptrs;
     float *g, *u, *h, *gs, *us, *down, *sd, *acc;
     uint16_t *hs;
-    uint32_t *ctrl, *rgcnt;
+    uint32_t *ctrl, *rgcnt, *pcnt;
 };
 
 Bufs ws_bufs(const moe_cfg &c, void *ws)
@@ -211,6 +211,7 @@ Bufs ws_bufs(const moe_cfg &c, void *ws)
     Bufs B{};
     B.ctrl = reinterpret_cast<uint32_t *>(b + L.ctrl);
     B.rgcnt = reinterpret_cast<uint32_t *>(b + L.rgcnt);
+    B.pcnt = reinterpret_cast<uint32_t *>(b + L.pcnt);
     B.logits = reinterpret_cast<float *>(b + L.logits);
     B.scores = reinterpret_cast<float *>(b + L.scores);
     B.keys = reinterpret_cast<float *>(b + L.keys);
@@ -289,6 +290,7 @@ int launch_experts(const moe_cfg &c, int m, const Geo &G, const Bufs &B, const u
     ga.h = B.h;
     ga.gs = B.gs;
     ga.us = B.us;
+    ga.pcnt = B.pcnt;
     ga.status = B.ctrl + MOE_CTRL_STATUS;
     ga.gctr = B.ctrl + MOE_CTRL_GATEUP;
     ga.dim = c.dim;

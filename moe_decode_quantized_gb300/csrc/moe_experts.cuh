@@ -16,9 +16,10 @@
 //
 //   gate/up kernel: first the whole shared expert, which depends only on x
 //     and so runs before the programmatic-launch wait, beside the router and
-//     the selection: row pairs (W1 row i and W3 row i in one stage; their
-//     consumer writes gs, us and hs = bf16(SwiGLU)), then W2 against hs (once
-//     every pair is done, grid-wide) into sd. Then, after the wait, the plan
+//     the selection: W1 row i and W3 row i as two tasks (one row a stage;
+//     the consumers write gs and us, the second of the two also
+//     hs = bf16(SwiGLU)), then W2 against hs (once every row is done,
+//     grid-wide) into sd. Then, after the wait, the plan
 //     experts' gate and up rows, rt rows of each in one task; the consumer
 //     writes g, u and h = SwiGLU(g, u) per plan pair. Once the selection has
 //     raised its plan-ready hint the routed rows go before the rest of W2.
@@ -34,8 +35,8 @@
 namespace moe {
 
 struct __align__(16) Task {
-    int kind;   // 0 end, 1 routed, 2 shared row pair (gate/up), 3 shared W2 rows (gate/up)
-    int p;      // plan expert
+    int kind;   // 0 end, 1 routed, 2 shared W1 or W3 row (gate/up), 3 shared W2 rows (gate/up)
+    int p;      // plan expert (routed); 0 W1, 1 W3 (shared row)
     int row;    // first row (routed) or the row (shared)
     int pair0, npair;
     int seq;    // the task's index in this CTA's stream (written last by the producer)
@@ -450,10 +451,11 @@ struct GArgs {
     float *gs, *us;                    // [m, inter]
     uint16_t *hs;                      // [m, inter] bf16(SwiGLU(gs, us))
     float *sd;                         // [m, dim] W2 hs
+    uint32_t *pcnt;                    // [inter] halves (W1 row, W3 row) done; zero between launches
     uint32_t *status;
-    // [0] shared row-pair counter, [1] routed-task counter, [2] exit ticket,
-    // [3] W2 task counter, [4] shared row pairs done, [5] the selection's
-    // plan-ready hint
+    // [0] shared row-task counter, [1] routed-task counter, [2] exit ticket,
+    // [3] W2 task counter, [4] shared rows done (hs[i] written), [5] the
+    // selection's plan-ready hint
     uint32_t *gctr;
     float limit;
     int plan_hint;  // the plan comes from the selection in this stream (its hint at gctr[5])
@@ -474,7 +476,7 @@ __host__ __device__ inline size_t g_smem_bytes(int S, int m, int dim, int inter,
     return g_stage_off(S, m, dim, inter, shared) + (size_t)S * stage_bytes + 16;
 }
 
-// The producer warp: waits (bounded) until every row pair of the shared
+// The producer warp: waits (bounded) until every hs row of the shared
 // expert is done grid-wide, copies hs into shared memory and raises the CTA's
 // flag (2 instead of 1 after a timeout, so that no consumer waits forever).
 __device__ bool g_load_hs(const GArgs &a, const Ring &ring, uint16_t *hs_s, int lane)
@@ -558,34 +560,38 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
         };
         if (shared) {
             // The shared expert depends only on x: all of it runs before the
-            // wait. (1) Row pairs: W1 row i and W3 row i in one stage; the
-            // consumer that takes pair i also writes hs[i] = bf16(SwiGLU).
+            // wait. (1) Rows: task 2i is W1 row i, task 2i + 1 is W3 row i (one
+            // row a stage, so the stages fit the routed tasks); of the two
+            // consumers of row i the one that finishes second writes
+            // hs[i] = bf16(SwiGLU).
+            const int nsh = 2 * inter;
             unsigned nxt = 0;
             if (lane == 0)
                 nxt = atomicAdd(a.gctr + 0, (unsigned)MOE_G_CHUNK);
             for (;;) {
                 const int c0 = (int)__shfl_sync(0xffffffffu, nxt, 0);
-                if (c0 >= inter || !ok)
+                if (c0 >= nsh || !ok)
                     break;
                 if (lane == 0)
                     nxt = atomicAdd(a.gctr + 0, (unsigned)MOE_G_CHUNK);  // the next chunk, in flight meanwhile
-                const int c1 = min(c0 + MOE_G_CHUNK, inter);
+                const int c1 = min(c0 + MOE_G_CHUNK, nsh);
                 for (int b = c0; b < c1 && ok; b += P) {
-                    const int i = b + lane;
+                    const int j = b + lane;
                     bool mine = true;
-                    if (issuer && i < c1) {
+                    if (issuer && j < c1) {
                         Task t{};
                         t.kind = 2;
-                        t.row = i;
-                        mine = ring_issue(ring, base + (i - c0), t, a.w1 + (size_t)i * dim, (uint32_t)dim * 2u, pol,
-                                          a.status, a.w3 + (size_t)i * dim, (uint32_t)dim * 2u);
+                        t.row = j >> 1;
+                        t.p = j & 1;  // 0: W1 (gate), 1: W3 (up)
+                        mine = ring_issue(ring, base + (j - c0), t, (t.p ? a.w3 : a.w1) + (size_t)t.row * dim,
+                                          (uint32_t)dim * 2u, pol, a.status);
                     }
                     ok = __all_sync(0xffffffffu, mine);
                 }
                 base += c1 - c0;
             }
             // (2) W2, w2r rows a task, against hs. This warp polls (bounded)
-            // two words: every row pair done grid-wide -> it loads hs into
+            // two words: every hs row done grid-wide -> it loads hs into
             // shared memory and issues W2; the selection's plan-ready hint ->
             // the routed work goes first and W2 (or its rest) after it. No W2
             // task is issued before hs is in shared memory, so nothing queued
@@ -810,25 +816,23 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
             if (lane == 0)
                 mbar_arrive(&ring.empty[slot]);
         } else if (t.kind == 2) {
-            // W1 row i and W3 row i against every token's bf16 x, then hs[i]
+            // W1 row i (t.p = 0) or W3 row i (t.p = 1) against every token's
+            // bf16 x into gs or us; the second of the two finishes hs[i]
             const int i = t.row;
-            const uint4 *w1r = reinterpret_cast<const uint4 *>(st);
-            const uint4 *w3r = w1r + dim / 8;
+            const bool up = t.p != 0;
+            const uint4 *wr = reinterpret_cast<const uint4 *>(st);
             const uint4 *x4 = reinterpret_cast<const uint4 *>(xs);
             with_m(a.m, [&](auto MC) {
                 constexpr int M = decltype(MC)::value;
-                float ag[M], au[M];
+                float ac[M];
 #pragma unroll
                 for (int tt = 0; tt < M; ++tt)
-                    ag[tt] = au[tt] = 0.0f;
+                    ac[tt] = 0.0f;
                 for (int c = lane; c < dim / 8; c += 32) {
-                    const uint4 v1 = w1r[c], v3 = w3r[c];
+                    const uint4 v = wr[c];
 #pragma unroll
-                    for (int tt = 0; tt < M; ++tt) {
-                        const uint4 xv = x4[(size_t)tt * (dim / 8) + c];
-                        ag[tt] = fma_bf16x8(v1, xv, ag[tt]);
-                        au[tt] = fma_bf16x8(v3, xv, au[tt]);
-                    }
+                    for (int tt = 0; tt < M; ++tt)
+                        ac[tt] = fma_bf16x8(v, x4[(size_t)tt * (dim / 8) + c], ac[tt]);
                 }
                 __syncwarp();
                 if (lane == 0)
@@ -836,19 +840,26 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
 #pragma unroll
                 for (int tt = 0; tt < M; ++tt) {
 #pragma unroll
-                    for (int o = 16; o; o >>= 1) {
-                        ag[tt] += __shfl_xor_sync(0xffffffffu, ag[tt], o);
-                        au[tt] += __shfl_xor_sync(0xffffffffu, au[tt], o);
-                    }
+                    for (int o = 16; o; o >>= 1)
+                        ac[tt] += __shfl_xor_sync(0xffffffffu, ac[tt], o);
                 }
                 if (lane == 0) {
+                    float *mine = up ? a.us : a.gs;
+                    const float *other = up ? a.gs : a.us;
 #pragma unroll
-                    for (int tt = 0; tt < M; ++tt) {
-                        a.gs[(size_t)tt * inter + i] = ag[tt];
-                        a.us[(size_t)tt * inter + i] = au[tt];
-                        a.hs[(size_t)tt * inter + i] = f32_to_bf16(swiglu_f32(ag[tt], au[tt], a.limit));
+                    for (int tt = 0; tt < M; ++tt)
+                        mine[(size_t)tt * inter + i] = ac[tt];
+                    // release: the stores above; acquire: the other half's
+                    if (atom_add_acq_rel_gpu(a.pcnt + i, 1u) == 1u) {
+#pragma unroll
+                        for (int tt = 0; tt < M; ++tt) {
+                            const float o = __ldcg(other + (size_t)tt * inter + i);
+                            const float gv = up ? o : ac[tt], uv = up ? ac[tt] : o;
+                            a.hs[(size_t)tt * inter + i] = f32_to_bf16(swiglu_f32(gv, uv, a.limit));
+                        }
+                        a.pcnt[i] = 0u;  // both halves are in: nothing else touches it this launch
+                        red_add_release_gpu(a.gctr + 4, 1u);  // after this lane's own stores
                     }
-                    red_add_release_gpu(a.gctr + 4, 1u);  // after this lane's own stores
                 }
             });
         } else {
@@ -904,7 +915,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
         }
     }
     // the last CTA out resets the grid-wide counters: by then every producer
-    // has stopped taking tasks and every consumer has counted its row pairs
+    // has stopped taking tasks and every consumer has counted its hs rows
     consumers_sync();
     if (threadIdx.x == 0 && atomicAdd(a.gctr + 2, 1u) == gridDim.x - 1) {
         atomicExch(a.gctr + 0, 0u);
