@@ -128,7 +128,7 @@ struct Geo {
     int g_S, w2r;
     uint32_t g_stage;
     size_t g_smem;
-    int d_S, d_pair_cap;
+    int d_S, d_pair_cap, d_own_rows;
     uint32_t d_stage;
     size_t d_smem;
     int grid;  // persistent grid of the expert kernels
@@ -181,9 +181,23 @@ int geometry(const moe_cfg &c, int m, bool shared, const DevInfo &I, Geo &G)
     const long long per = (tmax + G.grid - 1) / G.grid;
     int span = (int)((per + tpr - 1) / tpr) + 1;
     G.d_pair_cap = std::min(m * k, span * m);
+    G.d_own_rows = 0;
     size_t d_fixed = d_small_bytes(dim, inter) + align_up((size_t)G.d_pair_cap * act_row_bytes(inter), 128);
     G.d_S = stages_fit(d_fixed, G.d_stage, 48, limit);
-    G.d_smem = d_smem_bytes(G.d_S, G.d_pair_cap, dim, inter, G.d_stage);
+    // row ownership for a few plan pairs: every CTA quantises all of them but
+    // finishes its own rows without tickets, if the ring keeps 16 stages
+    if (m * k <= 16) {
+        const int own = (tpr + G.grid - 1) / G.grid * down_rows_per_task(inter);
+        const size_t fo = d_small_bytes(dim, inter) + align_up((size_t)m * k * act_row_bytes(inter), 128) +
+                          align_up(4 * (size_t)m * k * own, 128);
+        const int So = stages_fit(fo, G.d_stage, 48, limit);
+        if (So >= 16) {
+            G.d_own_rows = own;
+            G.d_pair_cap = m * k;
+            G.d_S = So;
+        }
+    }
+    G.d_smem = d_smem_bytes(G.d_S, G.d_pair_cap, dim, inter, G.d_own_rows, G.d_stage);
     if (G.r_smem > limit || G.g_smem > limit || G.d_smem > limit)
         return fail(MOE_EUNSUPPORTED, "shared memory: router %zu, gate/up %zu, down %zu > %zu bytes", G.r_smem,
                     G.g_smem, G.d_smem, limit);
@@ -329,6 +343,7 @@ int launch_experts(const moe_cfg &c, int m, const Geo &G, const Bufs &B, const u
     da.plan_off = m * (1 + 3 * k);
     da.S = G.d_S;
     da.pair_cap = G.d_pair_cap;
+    da.own_rows = G.d_own_rows;
     da.stage_bytes = G.d_stage;
     if ((rc = launch(moe_down_kernel, dim3(G.grid), dim3(MOE_THREADS), G.d_smem, s, ev == nullptr, da)))
         return rc;

@@ -943,6 +943,12 @@ struct DArgs {
     uint32_t *rgcnt, *status;
     float limit;
     int has_shared;  // add sd to the routed sum
+    // own_rows > 0: each CTA owns a range of row groups of the output (at
+    // most own_rows rows), takes every plan expert's down rows of them,
+    // quantises h of every plan pair (pair_cap = m * k) and finishes its own
+    // rows from shared memory, with no row-group tickets. 0: expert-major task
+    // ranges, tickets, and the CTA that completes a group finishes it.
+    int own_rows;
     int dim, inter, m, k, cap, plan_off, S, pair_cap;
     uint32_t stage_bytes;
 };
@@ -960,19 +966,41 @@ __host__ __device__ inline size_t d_small_bytes(int dim, int inter)
 }
 __host__ __device__ inline size_t d_small_off(int S) { return ring_head_bytes(S); }
 __host__ __device__ inline size_t d_act_off(int S, int dim, int inter) { return d_small_off(S) + d_small_bytes(dim, inter); }
-__host__ __device__ inline size_t d_stage_off(int S, int pair_cap, int dim, int inter)
+// row ownership: the CTA's down rows of every plan pair, f32 [pair_cap][own_rows]
+__host__ __device__ inline size_t d_own_off(int S, int pair_cap, int dim, int inter)
 {
     return d_act_off(S, dim, inter) + align_up((size_t)pair_cap * act_row_bytes(inter), 128);
 }
-__host__ __device__ inline size_t d_smem_bytes(int S, int pair_cap, int dim, int inter, uint32_t stage_bytes)
+__host__ __device__ inline size_t d_stage_off(int S, int pair_cap, int dim, int inter, int own_rows)
 {
-    return d_stage_off(S, pair_cap, dim, inter) + (size_t)S * stage_bytes + 16;
+    return d_own_off(S, pair_cap, dim, inter) + align_up(4 * (size_t)pair_cap * own_rows, 128);
+}
+__host__ __device__ inline size_t d_smem_bytes(int S, int pair_cap, int dim, int inter, int own_rows,
+                                               uint32_t stage_bytes)
+{
+    return d_stage_off(S, pair_cap, dim, inter, own_rows) + (size_t)S * stage_bytes + 16;
 }
 
-// the range of tasks of this CTA and the plan pairs its routed tasks touch
+// the range of tasks of this CTA and the plan pairs its routed tasks touch;
+// with row ownership the tasks are (plan expert, owned row group) expert by
+// expert, local indices [0, ne * ng)
 struct DRange {
     int ne, tpr, Tr, lo, hi, pair_lo, pair_hi;
+    bool own;
+    int g_lo, ng;
 };
+
+// plan expert and row group of the CTA's task tix
+__device__ __forceinline__ void d_task(const DRange &R, int tix, int &p, int &grp)
+{
+    if (R.own) {
+        p = tix / R.ng;
+        grp = R.g_lo + tix % R.ng;
+    } else {
+        p = tix / R.tpr;
+        grp = tix % R.tpr;
+    }
+}
 
 __device__ __forceinline__ DRange d_range(const DArgs &a)
 {
@@ -980,6 +1008,17 @@ __device__ __forceinline__ DRange d_range(const DArgs &a)
     r.ne = min(max(__ldcg(a.hdr + a.plan_off), 0), a.cap);
     r.tpr = a.dim / down_rows_per_task(a.inter);
     r.Tr = r.ne * r.tpr;
+    r.own = a.own_rows > 0;
+    r.g_lo = r.ng = 0;
+    if (r.own) {
+        r.g_lo = (int)((long long)blockIdx.x * r.tpr / gridDim.x);
+        r.ng = (int)((long long)(blockIdx.x + 1) * r.tpr / gridDim.x) - r.g_lo;
+        r.lo = 0;
+        r.hi = r.ne * r.ng;
+        r.pair_lo = 0;
+        r.pair_hi = r.hi > 0 ? min(max(__ldcg(a.hdr + a.plan_off + 1 + r.ne), 0), a.cap) : 0;
+        return r;
+    }
     r.lo = (int)((long long)blockIdx.x * r.Tr / gridDim.x);
     r.hi = (int)((long long)(blockIdx.x + 1) * r.Tr / gridDim.x);
     r.pair_lo = r.pair_hi = 0;
@@ -992,17 +1031,24 @@ __device__ __forceinline__ DRange d_range(const DArgs &a)
 }
 
 // acc, residual and x_next of row r for token t: the token's pairs in plan
-// order (ascending expert id), then the shared row
+// order (ascending expert id), then the shared row. The down values of pair
+// q are dsrc[q * dstride + dcol]: the global down rows (kGlobal, written by
+// other CTAs) or the CTA's own rows in shared memory.
+template <bool kGlobal>
 __device__ __forceinline__ void finish_row(const DArgs &a, int t, int r, bool shared, const int *s_tp,
-                                           const float *s_w)
+                                           const float *s_w, const float *dsrc, size_t dstride, int dcol,
+                                           bool pre = false, float sd_pre = 0.0f, float res_pre = 0.0f)
 {
     const int k = a.k;
     float d[MOE_MAX_TOPK];
 #pragma unroll
-    for (int i = 0; i < MOE_MAX_TOPK; ++i)
-        d[i] = i < k ? __ldcg(a.down + (size_t)s_tp[t * MOE_MAX_TOPK + i] * a.dim + r) : 0.0f;
-    const float sdv = shared ? __ldcg(a.sd + (size_t)t * a.dim + r) : 0.0f;
-    const float res0 = a.residual ? a.residual[(size_t)t * a.dim + r] : 0.0f;
+    for (int i = 0; i < MOE_MAX_TOPK; ++i) {
+        const float *src = dsrc + (size_t)s_tp[t * MOE_MAX_TOPK + i] * dstride + dcol;
+        d[i] = i < k ? (kGlobal ? __ldcg(src) : *src) : 0.0f;
+    }
+    // sd and residual: loaded here, or earlier by the caller (pre)
+    const float sdv = pre ? sd_pre : shared ? __ldcg(a.sd + (size_t)t * a.dim + r) : 0.0f;
+    const float res0 = pre ? res_pre : a.residual ? a.residual[(size_t)t * a.dim + r] : 0.0f;
     float acc = 0.0f;
 #pragma unroll
     for (int i = 0; i < MOE_MAX_TOPK; ++i)
@@ -1023,7 +1069,8 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     const bool shared = a.has_shared != 0;
-    const Ring ring = ring_carve(smem, a.S, a.stage_bytes, d_stage_off(a.S, a.pair_cap, a.dim, a.inter));
+    const Ring ring = ring_carve(smem, a.S, a.stage_bytes, d_stage_off(a.S, a.pair_cap, a.dim, a.inter, a.own_rows));
+    float *s_own = reinterpret_cast<float *>(smem + d_own_off(a.S, a.pair_cap, a.dim, a.inter));
     int *s_rows = reinterpret_cast<int *>(smem + d_small_off(a.S));
     float *s_w = reinterpret_cast<float *>(s_rows + D_SW);
     int *s_tp = s_rows + D_TP;
@@ -1057,8 +1104,8 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
             if (issuer && tix < R.hi) {
                 Task t{};
                 t.kind = 1;
-                t.p = tix / R.tpr;
-                const int r = tix % R.tpr;
+                int r;
+                d_task(R, tix, t.p, r);
                 t.row = r * rd;
                 t.pair0 = pc.pair_start[t.p];
                 t.npair = pc.pair_start[t.p + 1] - t.pair0;
@@ -1095,16 +1142,34 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
         s_rows[q] = __ldcg(a.plan_rows + q);
         s_w[q] = __ldcg(a.plan_w + q);
     }
-    // q8_1(h) of the plan pairs this CTA's tasks touch, four lanes a block
+    // q8_1(h) of the plan pairs this CTA's tasks touch, four lanes a block:
+    // nq lane items, a multiple of 32, so each warp is wholly in or out of a
+    // round; up to DQ rounds a thread with all their loads in flight
+    constexpr int DQ = 4, CTH = MOE_CONSUMER_WARPS * 32;
     const int np = min(R.pair_hi - R.pair_lo, a.pair_cap);
-    const int nblk = np * inter / 32;
-    for (int i = threadIdx.x; i < nblk * 4; i += MOE_CONSUMER_WARPS * 32) {
-        const int b = i >> 2, sub = i & 3;
-        const int pr = b / (inter / 32), bi = b % (inter / 32);
-        const float4 *h4 = reinterpret_cast<const float4 *>(a.h + (size_t)(R.pair_lo + pr) * inter + bi * 32 + 8 * sub);
-        const float4 h0 = __ldcg(h4), h1 = __ldcg(h4 + 1);
-        const float v[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-        q8_block_quad(v, sub, act + pr * arow, nb, bi, false);
+    const int nq = np * inter / 32 * 4;
+    for (int i0 = 0; i0 < nq; i0 += CTH * DQ) {
+        float4 hv[DQ][2];
+#pragma unroll
+        for (int u = 0; u < DQ; ++u) {
+            const int i = i0 + (int)threadIdx.x + CTH * u, b = i >> 2, sub = i & 3;
+            const int pr = b / (inter / 32), bi = b % (inter / 32);
+            const float4 *h4 =
+                reinterpret_cast<const float4 *>(a.h + (size_t)(R.pair_lo + pr) * inter + bi * 32 + 8 * sub);
+            const bool in = i < nq;
+            hv[u][0] = in ? __ldcg(h4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            hv[u][1] = in ? __ldcg(h4 + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < DQ; ++u) {
+            const int i = i0 + (int)threadIdx.x + CTH * u, b = i >> 2, sub = i & 3;
+            const int pr = b / (inter / 32), bi = b % (inter / 32);
+            if (i >= nq)
+                continue;
+            const float v[8] = {hv[u][0].x, hv[u][0].y, hv[u][0].z, hv[u][0].w,
+                                hv[u][1].x, hv[u][1].y, hv[u][1].z, hv[u][1].w};
+            q8_block_quad(v, sub, act + pr * arow, nb, bi, false);
+        }
     }
     consumers_sync();
     // each token's pairs in plan order (pairs are grouped by ascending expert)
@@ -1118,6 +1183,15 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
     }
     consumers_sync();
 
+    // row ownership: the first round of finished rows (row it = thread) has
+    // its sd and residual loaded now, in flight while the tasks compute
+    float sd_pre = 0.0f, res_pre = 0.0f;
+    const int own_nr = R.ng * rd;
+    if (R.own && (int)threadIdx.x < a.m * own_nr) {
+        const int tk = (int)threadIdx.x / own_nr, r = R.g_lo * rd + (int)threadIdx.x % own_nr;
+        sd_pre = shared ? __ldcg(a.sd + (size_t)tk * dim + r) : 0.0f;
+        res_pre = a.residual ? a.residual[(size_t)tk * dim + r] : 0.0f;
+    }
     const unsigned expected = (unsigned)R.ne;
     for (;;) {
         const int j = ring_grab(ring);
@@ -1156,6 +1230,12 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
 #pragma unroll
                     for (int q = 0; q < PER; ++q)
                         orow[(lane + 32 * q) / nb] = v[q];
+                    if (R.own) {
+                        float *srow = s_own + (size_t)(t.pair0 + tt) * a.own_rows + (t.row - R.g_lo * rd);
+#pragma unroll
+                        for (int q = 0; q < PER; ++q)
+                            srow[(lane + 32 * q) / nb] = v[q];
+                    }
                 }
             }
             __syncwarp();
@@ -1164,12 +1244,23 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
         }
     }
 
+    if (R.own) {
+        // the CTA's own rows of every token, from its down rows in shared memory
+        consumers_sync();
+        const int nr = own_nr, r0 = R.g_lo * rd;
+        for (int it = threadIdx.x; it < a.m * nr; it += CTH) {
+            const int tk = it / nr, rl = it - tk * nr;
+            finish_row<false>(a, tk, r0 + rl, shared, s_tp, s_w, s_own, (size_t)a.own_rows, rl,
+                              it == (int)threadIdx.x, sd_pre, res_pre);
+        }
+        return;
+    }
+
     // Row-group tickets, once per CTA: after all of this CTA's tasks, for
     // every row group it touched one acq_rel atomic adding its count of tasks
     // there (release: the CTA's down rows, ordered before it by the barrier;
     // acquire: the other CTAs' rows of a group it completes). The CTA whose
     // addition completes a group finishes it.
-    constexpr int CTH = MOE_CONSUMER_WARPS * 32;
     int *s_fin = s_rows + D_FIN;
     int *s_nfin = s_rows + D_NFIN;
     if (threadIdx.x == 0)
@@ -1203,7 +1294,8 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
     const int nfin = min(*s_nfin, ngroups), per = a.m * rd;
     for (int it = threadIdx.x; it < nfin * per; it += CTH) {
         const int f = it / per, rem = it - f * per;
-        finish_row(a, rem / rd, s_fin[f] * rd + rem % rd, shared, s_tp, s_w);
+        const int r = s_fin[f] * rd + rem % rd;
+        finish_row<true>(a, rem / rd, r, shared, s_tp, s_w, a.down, (size_t)a.dim, r);
     }
     for (int f = threadIdx.x; f < nfin; f += CTH)
         atomicExch(a.rgcnt + s_fin[f], 0u);
