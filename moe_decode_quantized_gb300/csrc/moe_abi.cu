@@ -592,7 +592,8 @@ int moe_route_scores(const moe_cfg *cfg, const float *logits, int count, float *
     if (!logits || !scores)
         return fail(MOE_EINVAL, "moe_route_scores: a buffer is NULL");
     ScoreArgs a{logits, scores, cfg->gate_temp, count};
-    return launch(moe_score_kernel, dim3((count + 255) / 256), dim3(256), 0, (cudaStream_t)stream, false, a);
+    return launch(moe_score_kernel, dim3((count + MOE_SCORES_PER_CTA - 1) / MOE_SCORES_PER_CTA), dim3(256), 0,
+                  (cudaStream_t)stream, false, a);
 }
 
 int moe_route_select(const moe_cfg *cfg, const float *logits, const float *bias, const int32_t *slot_row,

@@ -172,7 +172,7 @@ __constant__ float2 c_exp2_32[32] = {
 // 2^q for q in [-126, 127], exactly
 __device__ __forceinline__ float pow2i(int q) { return __int_as_float((q + 127) << 23); }
 
-// One step of the five lockstep Horner chains below
+// One step of the Horner chains below
 __device__ __forceinline__ ff horner_step(ff p, ff r, bool ser, ff c0, ff c1)
 {
     return ff_add(ff_mul(p, r), ser ? c1 : c0);
@@ -198,7 +198,7 @@ __device__ __forceinline__ ff tang_reduce(ff x, int &j, int &q)
 
 // For t in [-40, 20]: the candidate s and its neighbours s_-2 .. s_+2 (f32
 // steps), the four midpoints m_i between them, and five independent values
-// in float-float evaluated in lockstep: e^t and expm1(m_i^2). The number c of
+// in float-float: e^t and expm1(m_i^2). The number c of
 // midpoints below the exact score places it: the rounding is s_c (c = 1..3).
 // e^x by Tang's reduction and the Taylor series of e^r to r^5 / 5!
 // (remainder below 2^-48), times 2^(j/32) from the table and 2^q; expm1(M)
@@ -206,64 +206,57 @@ __device__ __forceinline__ ff tang_reduce(ff x, int &j, int &q)
 // below 2^-48), else e^M - 1 (e^M - 1 >= 2^-6: at most 6 bits lost). Returns
 // -1 when a decision is closer than 2^-37 relative or the candidate is off by
 // two steps.
-__device__ __noinline__ float score_ff(float t)
+// The five values are independent until the decision, so they run one a
+// lane: lane v (0..4) of a converged group of five lanes that share t (mask
+// gmask, first lane src0) evaluates value v -- e^t for v = 0, expm1 of the
+// squared midpoint between candidates v - 1 and v for v > 0 -- then every
+// lane of the group gathers the five and takes the same decision.
+__device__ __noinline__ float score_ff(float t, int v, unsigned gmask, int src0)
 {
     const float s = sqrtf(log1pf(expf(t)));
     const unsigned sb = __float_as_uint(s);  // positive and normal: +-1 on the bits steps one f32
-    float sv[5];
-#pragma unroll
-    for (int i = 0; i < 5; ++i)
-        sv[i] = __uint_as_float(sb + i - 2);
-    ff x[5], r[5], p[5];
-    bool ser[5];
-    int j[5], q[5];
-    x[0] = {t, 0.0f};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const ff m = {sv[i + 1], __fmul_rn(__fsub_rn(sv[i], sv[i + 1]), 0.5f)};  // exact midpoint
-        x[i + 1] = ff_mul(m, m);
+    ff x = {t, 0.0f};
+    if (v > 0) {
+        const float lo = __uint_as_float(sb + v - 3), hi = __uint_as_float(sb + v - 2);
+        const ff m = {hi, __fmul_rn(__fsub_rn(lo, hi), 0.5f)};  // exact midpoint
+        x = ff_mul(m, m);
     }
-#pragma unroll
-    for (int v = 0; v < 5; ++v) {
-        ser[v] = v > 0 && x[v].hi < 0x1.0p-6f;
-        j[v] = 0;
-        q[v] = 0;
-        r[v] = ser[v] ? x[v] : tang_reduce(x[v], j[v], q[v]);
-        p[v] = ff_inv_fact(ser[v] ? 6 : 5);
-    }
+    const bool ser = v > 0 && x.hi < 0x1.0p-6f;
+    int j = 0, q = 0;
+    const ff r = ser ? x : tang_reduce(x, j, q);
+    ff p = ff_inv_fact(ser ? 6 : 5);
 #pragma unroll 1
-    for (int n = 4; n >= 0; --n) {
-        const ff c0 = ff_inv_fact(n), c1 = ff_inv_fact(n + 1);
-#pragma unroll
-        for (int v = 0; v < 5; ++v)
-            p[v] = horner_step(p[v], r[v], ser[v], c0, c1);
+    for (int n = 4; n >= 0; --n)
+        p = horner_step(p, r, ser, ff_inv_fact(n), ff_inv_fact(n + 1));
+    ff val;
+    if (ser) {
+        val = ff_mul(p, x);
+    } else {
+        const float2 tj = c_exp2_32[j];
+        const ff e = ff_mul({tj.x, tj.y}, p);
+        const float sc = pow2i(q);
+        val = {__fmul_rn(e.hi, sc), __fmul_rn(e.lo, sc)};
+        if (v > 0)
+            val = ff_add(val, {-1.0f, 0.0f});
     }
-    ff val[5];
+    float vh[5], vl[5];
 #pragma unroll
-    for (int v = 0; v < 5; ++v) {
-        if (ser[v]) {
-            val[v] = ff_mul(p[v], x[v]);
-        } else {
-            const float2 tj = c_exp2_32[j[v]];
-            const ff e = ff_mul({tj.x, tj.y}, p[v]);
-            const float sc = pow2i(q[v]);
-            val[v] = {__fmul_rn(e.hi, sc), __fmul_rn(e.lo, sc)};
-            if (v > 0)
-                val[v] = ff_add(val[v], {-1.0f, 0.0f});
-        }
+    for (int i = 0; i < 5; ++i) {
+        vh[i] = __shfl_sync(gmask, val.hi, src0 + i);
+        vl[i] = __shfl_sync(gmask, val.lo, src0 + i);
     }
-    const float tol = 0x1.0p-37f * val[0].hi;
+    const float tol = 0x1.0p-37f * vh[0];
     int c = 0;
     bool sure = true;
 #pragma unroll
     for (int i = 1; i < 5; ++i) {
-        const ff D = ff_add(val[0], {-val[i].hi, -val[i].lo});
+        const ff D = ff_add({vh[0], vl[0]}, {-vh[i], -vl[i]});
         sure = sure && fabsf(D.hi) > tol;
         c += D.hi > 0.0f;
     }
     if (!sure || c == 0 || c == 4)
         return -1.0f;
-    return c == 1 ? sv[1] : (c == 2 ? sv[2] : sv[3]);
+    return __uint_as_float(sb + (c == 1 ? -1 : (c == 2 ? 0 : 1)));
 }
 
 // For t in [-170, -40]: softplus(t) = e^t (1 - e^t / 2 + ...) with e^t below
@@ -305,14 +298,18 @@ __device__ __noinline__ float score_ff_tiny(float t)
     return c == 1 ? sv[1] : (c == 2 ? sv[2] : sv[3]);
 }
 
-__device__ __forceinline__ float score_fast(float l, float temp)
+// The routing score of l on a group of five converged lanes that share l
+// (v = 0..4, mask gmask, first lane src0): sqrt for t > 20, f64 below -170
+// (and NaN), else the float-float paths (score_ff: one value a lane) with
+// the f64 fallback; every lane of the group returns the score.
+__device__ __forceinline__ float score_fast(float l, float temp, int v, unsigned gmask, int src0)
 {
     const float t = __fdiv_rn(l, temp);
     if (t > 20.0f)
-        return __fsqrt_rn(t);  // sqrt(t) correctly rounded
+        return __fsqrt_rn(t);
     if (!(t >= -170.0f))
-        return score_exact(l, temp);  // also NaN
-    const float s = t >= -40.0f ? score_ff(t) : score_ff_tiny(t);
+        return score_exact(l, temp);
+    const float s = t >= -40.0f ? score_ff(t, v, gmask, src0) : score_ff_tiny(t);
     return s > 0.0f ? s : score_exact(l, temp);
 }
 
@@ -699,21 +696,28 @@ __global__ void __launch_bounds__(256) moe_router_kernel(RouteArgs a)
         }
     });
     __syncthreads();
-    // one score a warp first (lane-major over the warps): the scores take
-    // different paths by range, and paths in one warp would run one after
-    // another
-    const int nw = blockDim.x >> 5;
-    for (int i = warp + nw * lane; i < nrows * m; i += blockDim.x) {
-        const int r = i / m, t = i % m;
-        const float l = red[i];
-        const size_t o = (size_t)t * a.n + row0 + r;
-        a.logits[o] = l;
-        if (a.do_select) {
-            // the exact score of this row, here: a few threads of every CTA
-            // in parallel instead of the selecting CTA
-            const float sc = score_fast(l, a.temp);
-            a.scores[o] = sc;
-            a.keys[o] = __fadd_rn(sc, s_bias[r]);
+    // one score a warp first (lane groups of five, lane-major over the
+    // warps): the scores take different paths by range, and paths in one
+    // warp would run one after another; a group computes one score, the five
+    // chains of its float-float range one a lane
+    const int nw = blockDim.x >> 5, grp = lane / 5, gv = lane - 5 * grp;
+    if (grp < 6) {
+        const unsigned gmask = 0x1Fu << (5 * grp);
+        for (int i = warp + nw * grp; i < nrows * m; i += nw * 6) {
+            const int r = i / m, t = i % m;
+            const float l = red[i];
+            const size_t o = (size_t)t * a.n + row0 + r;
+            if (gv == 0)
+                a.logits[o] = l;
+            if (a.do_select) {
+                // the exact score of this row, here: a few lanes of every CTA
+                // in parallel instead of the selecting CTA
+                const float sc = score_fast(l, a.temp, gv, gmask, 5 * grp);
+                if (gv == 0) {
+                    a.scores[o] = sc;
+                    a.keys[o] = __fadd_rn(sc, s_bias[r]);
+                }
+            }
         }
     }
     if (!a.do_select)
@@ -755,14 +759,26 @@ __global__ void __launch_bounds__(256) moe_select_kernel(RouteArgs a)
     pdl_launch_dependents();
     for (int e = threadIdx.x; e < a.n; e += blockDim.x)
         slot[e] = __ldg(a.slot_row + e);
-    for (int i = threadIdx.x; i < (int)mn; i += blockDim.x) {
-        const float s = score_fast(a.logits[i], a.temp);
-        sc[i] = s;
-        ky[i] = __fadd_rn(s, __ldg(a.bias + i % a.n));
+    {
+        // a group of five lanes a score (six groups a warp)
+        const int lane = threadIdx.x & 31, grp = lane / 5, gv = lane - 5 * grp;
+        const int ng = (int)(blockDim.x >> 5) * 6;
+        if (grp < 6) {
+            const unsigned gmask = 0x1Fu << (5 * grp);
+            for (int i = (int)(threadIdx.x >> 5) * 6 + grp; i < (int)mn; i += ng) {
+                const float s = score_fast(a.logits[i], a.temp, gv, gmask, 5 * grp);
+                if (gv == 0) {
+                    sc[i] = s;
+                    ky[i] = __fadd_rn(s, __ldg(a.bias + i % a.n));
+                }
+            }
+        }
     }
     __syncthreads();
     select_and_plan<false>(a, a.logits, sc, ky, slot, smem);
 }
+
+#define MOE_SCORES_PER_CTA 48  // eight warps of six five-lane groups
 
 struct ScoreArgs {
     const float *logits;
@@ -771,13 +787,18 @@ struct ScoreArgs {
     int count;
 };
 
-// the routing score of each of count logits (one thread each)
+// the routing score of each of count logits: a group of five lanes each
+// (six groups a warp, MOE_SCORES_PER_CTA a CTA of 256 threads)
 __global__ void moe_score_kernel(ScoreArgs a)
 {
     pdl_wait();
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < a.count)
-        a.scores[i] = score_fast(a.logits[i], a.temp);
+    const int lane = threadIdx.x & 31, grp = lane / 5, gv = lane - 5 * grp;
+    const int i = blockIdx.x * MOE_SCORES_PER_CTA + (int)(threadIdx.x >> 5) * 6 + grp;
+    if (grp < 6 && i < a.count) {
+        const float s = score_fast(a.logits[i], a.temp, gv, 0x1Fu << (5 * grp), 5 * grp);
+        if (gv == 0)
+            a.scores[i] = s;
+    }
 }
 
 }  // namespace moe
