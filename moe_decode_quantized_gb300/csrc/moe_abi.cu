@@ -171,7 +171,7 @@ int geometry(const moe_cfg &c, int m, bool shared, const DevInfo &I, Geo &G)
     while (shared && G.w2r < 4 && (size_t)G.w2r * 2 * inter * 2 <= G.g_stage && dim % (G.w2r * 2) == 0)
         G.w2r *= 2;
     size_t g_fixed = align_up((size_t)m * act_row_bytes(dim), 128) + align_up((size_t)m * dim * 2, 128) +
-                     (shared ? align_up((size_t)m * inter * 2, 128) : 0);
+                     (shared ? align_up((size_t)m * inter * 2, 128) : 0) + g_pair_bytes(shared);
     G.g_S = stages_fit(g_fixed, G.g_stage, 32, limit);
     G.g_smem = g_smem_bytes(G.g_S, m, dim, inter, shared, G.g_stage);
     // down: stages of one Q3_K task (the shared expert is done by the gate/up kernel)
@@ -215,7 +215,7 @@ struct Bufs {
     unsigned long long *ptrs;
     float *g, *u, *h, *gs, *us, *down, *sd, *acc;
     uint16_t *hs;
-    uint32_t *ctrl, *rgcnt, *pcnt;
+    uint32_t *ctrl, *rgcnt;
 };
 
 Bufs ws_bufs(const moe_cfg &c, void *ws)
@@ -225,7 +225,6 @@ Bufs ws_bufs(const moe_cfg &c, void *ws)
     Bufs B{};
     B.ctrl = reinterpret_cast<uint32_t *>(b + L.ctrl);
     B.rgcnt = reinterpret_cast<uint32_t *>(b + L.rgcnt);
-    B.pcnt = reinterpret_cast<uint32_t *>(b + L.pcnt);
     B.logits = reinterpret_cast<float *>(b + L.logits);
     B.scores = reinterpret_cast<float *>(b + L.scores);
     B.keys = reinterpret_cast<float *>(b + L.keys);
@@ -304,7 +303,6 @@ int launch_experts(const moe_cfg &c, int m, const Geo &G, const Bufs &B, const u
     ga.h = B.h;
     ga.gs = B.gs;
     ga.us = B.us;
-    ga.pcnt = B.pcnt;
     ga.status = B.ctrl + MOE_CTRL_STATUS;
     ga.gctr = B.ctrl + MOE_CTRL_GATEUP;
     ga.dim = c.dim;

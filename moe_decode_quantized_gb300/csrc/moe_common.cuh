@@ -42,7 +42,7 @@ namespace moe {
 // ------------------------------------------------------------------ layout
 
 struct WsLayout {
-    size_t ctrl, rgcnt, pcnt, logits, scores, keys, plan_w, plan_rows, ptrs, g, u, h, gs, us, hs, down, sd, acc, total;
+    size_t ctrl, rgcnt, logits, scores, keys, plan_w, plan_rows, ptrs, g, u, h, gs, us, hs, down, sd, acc, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -60,7 +60,6 @@ inline WsLayout ws_layout(const moe_cfg &c)
     auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
     L.ctrl = take(256);
     L.rgcnt = take(sizeof(uint32_t) * (size_t)(c.dim / down_rows_per_task(c.inter)));
-    L.pcnt = take(sizeof(uint32_t) * (size_t)c.inter);  // shared rows: W1/W3 halves in
     L.logits = take(sizeof(float) * M * c.n_routed);
     L.scores = take(sizeof(float) * M * c.n_routed);
     L.keys = take(sizeof(float) * M * c.n_routed);

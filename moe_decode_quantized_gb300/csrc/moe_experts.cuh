@@ -451,7 +451,6 @@ struct GArgs {
     float *gs, *us;                    // [m, inter]
     uint16_t *hs;                      // [m, inter] bf16(SwiGLU(gs, us))
     float *sd;                         // [m, dim] W2 hs
-    uint32_t *pcnt;                    // [inter] halves (W1 row, W3 row) done; zero between launches
     uint32_t *status;
     // [0] shared row-task counter, [1] routed-task counter, [2] exit ticket,
     // [3] W2 task counter, [4] shared rows done (hs[i] written), [5] the
@@ -466,10 +465,28 @@ struct GArgs {
 __host__ __device__ inline size_t g_act_off(int S) { return ring_head_bytes(S); }
 __host__ __device__ inline size_t g_xs_off(int S, int m, int dim) { return g_act_off(S) + align_up((size_t)m * act_row_bytes(dim), 128); }
 __host__ __device__ inline size_t g_hs_off(int S, int m, int dim) { return g_xs_off(S, m, dim) + align_up((size_t)m * dim * 2, 128); }
-__host__ __device__ inline size_t g_stage_off(int S, int m, int dim, int inter, bool shared)
+// Shared rows: the W1 and W3 tasks of a row go to one CTA (chunks of
+// MOE_G_CHUNK tasks start at multiples of it) and meet in one of these cells,
+// picked by the CTA's pair sequence number: an arrival count (odd after the
+// first) and both halves' values
+struct PairCell {
+    int cnt;
+    float v[2][MOE_MAX_TOKENS];
+};
+#define MOE_PAIR_CELLS 32  // more than the pairs one ring holds
+static_assert(MOE_G_CHUNK % 2 == 0, "a chunk holds whole shared-row pairs");
+__host__ __device__ inline size_t g_pair_bytes(bool shared)
+{
+    return shared ? align_up(sizeof(PairCell) * MOE_PAIR_CELLS, 128) : 0;
+}
+__host__ __device__ inline size_t g_pair_off(int S, int m, int dim, int inter, bool shared)
 {
     // x is staged in shared memory whether or not a shared expert runs
     return g_hs_off(S, m, dim) + (shared ? align_up((size_t)m * inter * 2, 128) : 0);
+}
+__host__ __device__ inline size_t g_stage_off(int S, int m, int dim, int inter, bool shared)
+{
+    return g_pair_off(S, m, dim, inter, shared) + g_pair_bytes(shared);
 }
 __host__ __device__ inline size_t g_smem_bytes(int S, int m, int dim, int inter, bool shared, uint32_t stage_bytes)
 {
@@ -525,9 +542,12 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
     uint8_t *act = smem + g_act_off(a.S);
     uint16_t *xs = reinterpret_cast<uint16_t *>(smem + g_xs_off(a.S, a.m, a.dim));
     uint16_t *hs_s = reinterpret_cast<uint16_t *>(smem + g_hs_off(a.S, a.m, a.dim));
+    PairCell *cells = reinterpret_cast<PairCell *>(smem + g_pair_off(a.S, a.m, a.dim, a.inter, shared));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int dim = a.dim, inter = a.inter, nb = dim / MOE_QK;
     const size_t arow = act_row_bytes(dim);
+    if (shared && threadIdx.x < MOE_PAIR_CELLS)
+        cells[threadIdx.x].cnt = 0;
     ring_init(ring);
     __syncthreads();
 
@@ -563,8 +583,10 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
             // wait. (1) Rows: task 2i is W1 row i, task 2i + 1 is W3 row i (one
             // row a stage, so the stages fit the routed tasks); of the two
             // consumers of row i the one that finishes second writes
-            // hs[i] = bf16(SwiGLU).
+            // hs[i] = bf16(SwiGLU). pair0 carries the CTA's pair sequence
+            // number (its meeting cell).
             const int nsh = 2 * inter;
+            int pseq = 0;
             unsigned nxt = 0;
             if (lane == 0)
                 nxt = atomicAdd(a.gctr + 0, (unsigned)MOE_G_CHUNK);
@@ -583,12 +605,14 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
                         t.kind = 2;
                         t.row = j >> 1;
                         t.p = j & 1;  // 0: W1 (gate), 1: W3 (up)
+                        t.pair0 = pseq + ((j - c0) >> 1);
                         mine = ring_issue(ring, base + (j - c0), t, (t.p ? a.w3 : a.w1) + (size_t)t.row * dim,
                                           (uint32_t)dim * 2u, pol, a.status);
                     }
                     ok = __all_sync(0xffffffffu, mine);
                 }
                 base += c1 - c0;
+                pseq += (c1 - c0) >> 1;
             }
             // (2) W2, w2r rows a task, against hs. This warp polls (bounded)
             // two words: every hs row done grid-wide -> it loads hs into
@@ -845,20 +869,23 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
                 }
                 if (lane == 0) {
                     float *mine = up ? a.us : a.gs;
-                    const float *other = up ? a.gs : a.us;
+                    PairCell &pc2 = cells[t.pair0 % MOE_PAIR_CELLS];
 #pragma unroll
-                    for (int tt = 0; tt < M; ++tt)
+                    for (int tt = 0; tt < M; ++tt) {
                         mine[(size_t)tt * inter + i] = ac[tt];
-                    // release: the stores above; acquire: the other half's
-                    if (atom_add_acq_rel_gpu(a.pcnt + i, 1u) == 1u) {
+                        pc2.v[up][tt] = ac[tt];
+                    }
+                    __threadfence_block();  // this half's value before the count
+                    if (atomicAdd(&pc2.cnt, 1) & 1) {
+                        __threadfence_block();  // the other half's value after the count
+                        const volatile float *ov = pc2.v[!up];
 #pragma unroll
                         for (int tt = 0; tt < M; ++tt) {
-                            const float o = __ldcg(other + (size_t)tt * inter + i);
+                            const float o = ov[tt];
                             const float gv = up ? o : ac[tt], uv = up ? ac[tt] : o;
                             a.hs[(size_t)tt * inter + i] = f32_to_bf16(swiglu_f32(gv, uv, a.limit));
                         }
-                        a.pcnt[i] = 0u;  // both halves are in: nothing else touches it this launch
-                        red_add_release_gpu(a.gctr + 4, 1u);  // after this lane's own stores
+                        red_add_release_gpu(a.gctr + 4, 1u);  // after this lane's hs stores
                     }
                 }
             });
