@@ -106,7 +106,8 @@ int moe_header_words(const moe_cfg *cfg, int m);
 int moe_workspace_bytes(const moe_cfg *cfg, size_t *bytes);
 
 /* Zeroes a workspace (its counters must start at zero). Call once after
- * allocating it, on the stream that will use it. */
+ * allocating it, on the stream that will use it, and again after a call whose
+ * status has MOE_WS_TIMEOUT (a wait that gave up can leave counters mid-count). */
 int moe_workspace_init(void *ws_dev, size_t bytes, moe_stream_t stream);
 
 /* Router logits ([moe_v41] module doc: an f32-accumulated product of the bf16
