@@ -147,6 +147,14 @@ __device__ __forceinline__ uint32_t byte_of(const uint32_t *w, int i) { return (
 // still a non-negative signed byte) and the 4^g is shifted out of the
 // integer sum afterwards (exact: the sum is a multiple of 4^g), which saves a
 // shift per weight word; field 3 is shifted down first.
+// sum of the four products of unsigned bytes of a and signed bytes of b, plus c
+__device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c)
+{
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 __device__ __forceinline__ float q2k_dot(const uint32_t *blk, const int4 *xq, const float4 *rec)
 {
     uint32_t sc[4];
@@ -175,18 +183,22 @@ __device__ __forceinline__ float q2k_dot(const uint32_t *blk, const int4 *xq, co
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
             const int4 xa = xq[8 * h + 2 * g], xb = xq[8 * h + 2 * g + 1];
-            const int pre = g == 3 ? 6 : 0, post = g == 3 ? 0 : 2 * g;
-            const uint32_t msk = 0x03030303u << (2 * g - pre);
-            int s0 = __dp4a((int)((q[0] >> pre) & msk), xa.x, 0);
-            s0 = __dp4a((int)((q[1] >> pre) & msk), xa.y, s0);
-            s0 = __dp4a((int)((q[2] >> pre) & msk), xa.z, s0);
-            s0 = __dp4a((int)((q[3] >> pre) & msk), xa.w, s0);
-            int s1 = __dp4a((int)((q[4] >> pre) & msk), xb.x, 0);
-            s1 = __dp4a((int)((q[5] >> pre) & msk), xb.y, s1);
-            s1 = __dp4a((int)((q[6] >> pre) & msk), xb.z, s1);
-            s1 = __dp4a((int)((q[7] >> pre) & msk), xb.w, s1);
+            // field g masked in place (4^g times the quant); the top field's
+            // bytes reach 0xC0, so its products take the bytes as unsigned
+            const uint32_t msk = 0x03030303u << (2 * g);
+            auto dot = [&](uint32_t a, int b, int c) {
+                return g == 3 ? dp4a_us(a, b, c) : __dp4a((int)a, b, c);
+            };
+            int s0 = dot(q[0] & msk, xa.x, 0);
+            s0 = dot(q[1] & msk, xa.y, s0);
+            s0 = dot(q[2] & msk, xa.z, s0);
+            s0 = dot(q[3] & msk, xa.w, s0);
+            int s1 = dot(q[4] & msk, xb.x, 0);
+            s1 = dot(q[5] & msk, xb.y, s1);
+            s1 = dot(q[6] & msk, xb.z, s1);
+            s1 = dot(q[7] & msk, xb.w, s1);
             const int sub = 8 * h + 2 * g;
-            const int isum = ((int)(byte_of(sc, sub) & 15u) * s0 + (int)(byte_of(sc, sub + 1) & 15u) * s1) >> post;
+            const int isum = ((int)(byte_of(sc, sub) & 15u) * s0 + (int)(byte_of(sc, sub + 1) & 15u) * s1) >> (2 * g);
             main = fmaf(d8[4 * h + g], (float)isum, main);
         }
     }
