@@ -52,6 +52,22 @@ struct Q8Block {
     int s16;    // sum of the quants of this lane's 16-value half
 };
 
+// round-half-away(fl(v / d)), the q8_1 quant of v, for |v| <= amax and
+// d = fl(amax / 127) > 0, given r = fl(1 / d). z = fl(v r) is within
+// |v / d| (3 2^-24 + 2^-48) < 381 2^-24 < 2^-15 of fl(v / d) (three relative
+// roundings of at most 2^-24 each; |v / d| < 127.0001), so when z is at least
+// 2^-15 from every half-integer the two round to the same integer. Nearer
+// one (and when r or z is not finite), the quotient itself decides.
+__device__ __forceinline__ int q8_code(float v, float d, float r)
+{
+    const float z = __fmul_rn(v, r);
+    const float a = fabsf(z);
+    const float f = __fsub_rn(a, floorf(a));  // exact for a < 2^23
+    if (!(fabsf(__fsub_rn(f, 0.5f)) >= 0x1.0p-15f))
+        return (int)roundf(__fdiv_rn(v, d));
+    return (int)roundf(z);
+}
+
 // per 32 values: d = amax / 127, q = round-half-away(v / d), q = 0 when amax = 0
 __device__ __forceinline__ Q8Block q8_quant_warp(float v)
 {
@@ -62,7 +78,7 @@ __device__ __forceinline__ Q8Block q8_quant_warp(float v)
         amax = fmaxf(amax, __shfl_xor_sync(full, amax, o));
     Q8Block b;
     b.d = __fdiv_rn(amax, 127.0f);
-    b.q = amax == 0.0f ? 0 : (int)roundf(__fdiv_rn(v, b.d));
+    b.q = amax == 0.0f ? 0 : q8_code(v, b.d, __frcp_rn(b.d));
     b.d8 = __half2float(__float2half_rn(b.d));
     int s = b.q;
 #pragma unroll
@@ -82,8 +98,9 @@ __host__ __device__ inline size_t act_row_bytes(int cols)
 }
 
 // One q8_1 block by a group of 4 lanes, 8 values each (the same arithmetic
-// as q8_quant_warp: the maximum is exact, each quotient one IEEE division,
-// the sums integers), so that a warp quantises 8 blocks at once. sub: the
+// as q8_quant_warp: the maximum is exact, each quant the rounding of one IEEE
+// quotient (q8_code), the sums integers), so that a warp quantises 8 blocks
+// at once. sub: the
 // lane's place in its group (lanes 4g .. 4g + 3); v: its values
 // 8 sub .. 8 sub + 7 of the block. Stored like q8_store_smem. All 32 lanes
 // of the warp call it together (callers loop over 4 x blocks lanes, a
@@ -98,6 +115,7 @@ __device__ __forceinline__ void q8_block_quad(const float (&v)[8], int sub, uint
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     const float d = __fdiv_rn(amax, 127.0f);
+    const float r = __frcp_rn(d);
     uint32_t w[2];
     int sum = 0;
 #pragma unroll
@@ -105,7 +123,7 @@ __device__ __forceinline__ void q8_block_quad(const float (&v)[8], int sub, uint
         uint32_t word = 0;
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-            const int q = amax == 0.0f ? 0 : (int)roundf(__fdiv_rn(v[4 * j4 + b], d));
+            const int q = amax == 0.0f ? 0 : q8_code(v[4 * j4 + b], d, r);
             sum += q;
             word |= (uint32_t)(q & 0xFF) << (8 * b);
         }
