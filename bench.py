@@ -365,7 +365,8 @@ def run_ours(args):
             },
             "roofline": {"bound": "hbm", "kernel": f"moe_{names[dom]}_kernel", "achieved": achieved, "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                         "traffic": measured_traffic(names[dom]), "algorithmic_bytes": b_dom,
+                         # the committed DRAM counts are per launch of the one-token step
+                         "traffic": measured_traffic(names[dom]) if m == 1 else None, "algorithmic_bytes": b_dom,
                          "avg_launch_us": k_ms[dom] * 1e3,
                          "timing": "per-kernel CUDA events on the launching stream, kernels launched one at a "
                                    "time over the workload's layers after the timed region"},
