@@ -16,19 +16,22 @@
 //
 //   gate/up kernel: first the whole shared expert, which depends only on x
 //     and so runs before the programmatic-launch wait, beside the router and
-//     the selection: W1 row i and W3 row i as two tasks (one row a stage;
-//     the consumers write gs and us, the second of the two also
-//     hs = bf16(SwiGLU)), then W2 against hs (once every row is done,
-//     grid-wide) into sd. Then, after the wait, the plan
-//     experts' gate and up rows, rt rows of each in one task; the consumer
-//     writes g, u and h = SwiGLU(g, u) per plan pair. Once the selection has
-//     raised its plan-ready hint the routed rows go before the rest of W2.
-//   down kernel: tasks = 64-super-block row runs of every plan expert's down
-//     matrix, all prefetched before the wait (they need only the pointer
+//     the selection: W1 row i and W3 row i as two tasks of one CTA (one row
+//     a stage; the consumers write gs and us and meet in a shared-memory
+//     cell, the second also writes hs = bf16(SwiGLU)), then W2 against hs
+//     (once every row is done, grid-wide) into sd. Then, after the wait, the
+//     plan experts' gate and up rows, rt rows of each in one task; the
+//     consumer writes g, u and h = SwiGLU(g, u) per plan pair. Once the
+//     selection has raised its plan-ready hint the routed rows go before the
+//     rest of W2.
+//   down kernel: tasks = 64-super-block row runs of plan experts' down
+//     matrices, all prefetched before the wait (they need only the pointer
 //     table); after the wait each CTA builds q8_1(h) for the pairs it needs.
-//     Row groups are finished by the CTA whose ticket completes them: acc =
-//     plan-order sum of w * down, then sd, residual += acc,
-//     x_next = bf16(residual).
+//     With few plan pairs a CTA owns whole row groups of the output (every
+//     plan expert's rows of them) and finishes them itself; otherwise its
+//     tasks are an expert-major range and a row group is finished by the
+//     CTA whose ticket completes it. Finishing: acc = plan-order sum of
+//     w * down, then sd, residual += acc, x_next = bf16(residual).
 #pragma once
 #include "moe_common.cuh"
 
