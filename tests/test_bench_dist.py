@@ -66,3 +66,23 @@ def test_algorithmic_bytes_of_the_decode_layer():
     assert g >= 2 * 6 * 2_752_512 + 3 * 2048 * 4096 * 2
     assert d >= 6 * 3_604_480 and d < 6 * 3_604_480 + 1_000_000
     assert (r + g + d) / 1e6 == pytest.approx(108.3, abs=0.4)
+
+
+def test_kernel_hash_ignores_comments_only(tmp_path, monkeypatch):
+    """The committed ncu counts stay attached across comment-only edits of
+    the kernel sources and drop off (traffic null) after a code edit."""
+    sys.path.insert(0, ROOT)
+    import shutil
+
+    import bench
+    src = os.path.join(ROOT, "moe_decode_quantized_gb300", "csrc")
+    fake = tmp_path / "moe_decode_quantized_gb300" / "csrc"
+    shutil.copytree(src, fake, ignore=shutil.ignore_patterns("*.o", "*.so"))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_hash()
+    f = fake / "moe_common.cuh"
+    text = f.read_text()
+    f.write_text("// a new line comment\n" + text.replace("namespace moe {", "namespace moe {  /* block */\n", 1))
+    assert bench.kernel_hash() == h0
+    f.write_text(text.replace("namespace moe {", "namespace moe {\nconstexpr int kNewCode = 1;", 1))
+    assert bench.kernel_hash() != h0
