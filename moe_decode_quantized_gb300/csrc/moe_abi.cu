@@ -128,6 +128,7 @@ struct Geo {
     int g_S, w2r;
     uint32_t g_stage;
     size_t g_smem;
+    bool stage_x;
     int d_S, d_pair_cap, d_own_rows;
     uint32_t d_stage;
     size_t d_smem;
@@ -170,10 +171,14 @@ int geometry(const moe_cfg &c, int m, bool shared, const DevInfo &I, Geo &G)
     G.w2r = 1;
     while (shared && G.w2r < 4 && (size_t)G.w2r * 2 * inter * 2 <= G.g_stage && dim % (G.w2r * 2) == 0)
         G.w2r *= 2;
-    size_t g_fixed = align_up((size_t)m * act_row_bytes(dim), 128) + align_up((size_t)m * dim * 2, 128) +
-                     (shared ? align_up((size_t)m * inter * 2, 128) : 0) + g_pair_bytes(shared);
+    // bf16 x and hs in shared memory for up to two tokens; beyond, the ring
+    // keeps the room and the consumers read them from L2
+    G.stage_x = g_stage_x(m);
+    size_t g_fixed = align_up((size_t)m * act_row_bytes(dim), 128) +
+                     (G.stage_x ? align_up((size_t)m * dim * 2, 128) : 0) +
+                     (shared && G.stage_x ? align_up((size_t)m * inter * 2, 128) : 0) + g_pair_bytes(shared);
     G.g_S = stages_fit(g_fixed, G.g_stage, 32, limit);
-    G.g_smem = g_smem_bytes(G.g_S, m, dim, inter, shared, G.g_stage);
+    G.g_smem = g_smem_bytes(G.g_S, m, dim, inter, shared, G.stage_x, G.g_stage);
     // down: stages of one Q3_K task (the shared expert is done by the gate/up kernel)
     G.d_stage = (uint32_t)align_up((size_t)MOE_D_TASK_SB * MOE_Q3K_BYTES, 128);
     const int tpr = dim / down_rows_per_task(inter);
@@ -295,6 +300,7 @@ int launch_experts(const moe_cfg &c, int m, const Geo &G, const Bufs &B, const u
     ga.limit = c.swiglu_limit;
     ga.w2r = G.w2r;
     ga.plan_hint = pdl_gateup ? 1 : 0;  // only a layer step's router raises the hint
+    ga.stage_x = G.stage_x ? 1 : 0;
     ga.hdr = hdr;
     ga.ptrs = ptrs;
     ga.plan_rows = plan_rows;

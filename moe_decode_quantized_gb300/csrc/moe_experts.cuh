@@ -491,13 +491,20 @@ struct GArgs {
     uint32_t *gctr;
     float limit;
     int plan_hint;  // the plan comes from the selection in this stream (its hint at gctr[5])
+    int stage_x;    // bf16 x and hs staged in shared memory (few tokens); else read from L2
     int dim, inter, m, k, cap, plan_off, S, w2r;
     uint32_t stage_bytes;
 };
 
 __host__ __device__ inline size_t g_act_off(int S) { return ring_head_bytes(S); }
 __host__ __device__ inline size_t g_xs_off(int S, int m, int dim) { return g_act_off(S) + align_up((size_t)m * act_row_bytes(dim), 128); }
-__host__ __device__ inline size_t g_hs_off(int S, int m, int dim) { return g_xs_off(S, m, dim) + align_up((size_t)m * dim * 2, 128); }
+// stage: bf16 x and hs are staged in shared memory (few tokens); else the
+// consumers read them from L2 and the ring keeps the room
+__host__ __device__ constexpr bool g_stage_x(int m) { return m <= 2; }
+__host__ __device__ inline size_t g_hs_off(int S, int m, int dim, bool stage)
+{
+    return g_xs_off(S, m, dim) + (stage ? align_up((size_t)m * dim * 2, 128) : 0);
+}
 // Shared rows: the W1 and W3 tasks of a row go to one CTA (chunks of
 // MOE_G_CHUNK tasks start at multiples of it) and meet in one of these cells,
 // picked by the CTA's pair sequence number: an arrival count (odd after the
@@ -512,18 +519,18 @@ __host__ __device__ inline size_t g_pair_bytes(bool shared)
 {
     return shared ? align_up(sizeof(PairCell) * MOE_PAIR_CELLS, 128) : 0;
 }
-__host__ __device__ inline size_t g_pair_off(int S, int m, int dim, int inter, bool shared)
+__host__ __device__ inline size_t g_pair_off(int S, int m, int dim, int inter, bool shared, bool stage)
 {
-    // x is staged in shared memory whether or not a shared expert runs
-    return g_hs_off(S, m, dim) + (shared ? align_up((size_t)m * inter * 2, 128) : 0);
+    return g_hs_off(S, m, dim, stage) + (shared && stage ? align_up((size_t)m * inter * 2, 128) : 0);
 }
-__host__ __device__ inline size_t g_stage_off(int S, int m, int dim, int inter, bool shared)
+__host__ __device__ inline size_t g_stage_off(int S, int m, int dim, int inter, bool shared, bool stage)
 {
-    return g_pair_off(S, m, dim, inter, shared) + g_pair_bytes(shared);
+    return g_pair_off(S, m, dim, inter, shared, stage) + g_pair_bytes(shared);
 }
-__host__ __device__ inline size_t g_smem_bytes(int S, int m, int dim, int inter, bool shared, uint32_t stage_bytes)
+__host__ __device__ inline size_t g_smem_bytes(int S, int m, int dim, int inter, bool shared, bool stage,
+                                               uint32_t stage_bytes)
 {
-    return g_stage_off(S, m, dim, inter, shared) + (size_t)S * stage_bytes + 16;
+    return g_stage_off(S, m, dim, inter, shared, stage) + (size_t)S * stage_bytes + 16;
 }
 
 // The producer warp: waits (bounded) until every hs row of the shared
@@ -545,7 +552,8 @@ __device__ bool g_load_hs(const GArgs &a, const Ring &ring, uint16_t *hs_s, int 
         }
     }
     // every lane polled itself: its loads below come after its own acquire
-    const int n16 = a.m * a.inter / 8;
+    // (unstaged, the consumers read hs from L2 once the flag is up)
+    const int n16 = a.stage_x ? a.m * a.inter / 8 : 0;
     const uint4 *src = reinterpret_cast<const uint4 *>(a.hs);
     uint4 *dst = reinterpret_cast<uint4 *>(hs_s);
     for (int i0 = lane; i0 < n16; i0 += 32 * 8) {
@@ -571,11 +579,17 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     const bool shared = a.w1 != nullptr;
-    const Ring ring = ring_carve(smem, a.S, a.stage_bytes, g_stage_off(a.S, a.m, a.dim, a.inter, shared));
+    const bool stage = a.stage_x != 0;
+    const Ring ring = ring_carve(smem, a.S, a.stage_bytes, g_stage_off(a.S, a.m, a.dim, a.inter, shared, stage));
     uint8_t *act = smem + g_act_off(a.S);
-    uint16_t *xs = reinterpret_cast<uint16_t *>(smem + g_xs_off(a.S, a.m, a.dim));
-    uint16_t *hs_s = reinterpret_cast<uint16_t *>(smem + g_hs_off(a.S, a.m, a.dim));
-    PairCell *cells = reinterpret_cast<PairCell *>(smem + g_pair_off(a.S, a.m, a.dim, a.inter, shared));
+    uint16_t *xs = reinterpret_cast<uint16_t *>(smem + g_xs_off(a.S, a.m, a.dim));  // staged only
+    uint16_t *hs_s = reinterpret_cast<uint16_t *>(smem + g_hs_off(a.S, a.m, a.dim, stage));  // staged only
+    PairCell *cells = reinterpret_cast<PairCell *>(smem + g_pair_off(a.S, a.m, a.dim, a.inter, shared, stage));
+    // 16-byte chunk i of bf16 x / of hs: shared memory when staged, else L2
+    // (kStage: the staging of the token count g_stage_x, known where M is)
+    const uint4 *x4s = reinterpret_cast<const uint4 *>(xs), *x4g = reinterpret_cast<const uint4 *>(a.x);
+    const uint4 *h4s = reinterpret_cast<const uint4 *>(hs_s), *h4g = reinterpret_cast<const uint4 *>(a.hs);
+    auto ldx = [&](size_t i) { return stage ? x4s[i] : __ldcg(x4g + i); };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int dim = a.dim, inter = a.inter, nb = dim / MOE_QK;
     const size_t arow = act_row_bytes(dim);
@@ -800,7 +814,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
     // ---------------- consumers: the activation first (x is ready: the
     // previous kernel in the stream let this one start only after its own
     // wait). x is staged with all loads in flight, then quantised from smem.
-    {
+    if (stage) {
         const uint4 *gx = reinterpret_cast<const uint4 *>(a.x);
         uint4 *s4 = reinterpret_cast<uint4 *>(xs);
         for (int i = threadIdx.x; i < a.m * dim / 8; i += MOE_CONSUMER_WARPS * 32)
@@ -811,7 +825,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
     for (int i = threadIdx.x; i < nblk * 4; i += MOE_CONSUMER_WARPS * 32) {  // four lanes a block
         const int b = i >> 2, sub = i & 3;
         const int t = b / (dim / 32), bi = b % (dim / 32);
-        const uint4 w = *reinterpret_cast<const uint4 *>(xs + (size_t)t * dim + bi * 32 + 8 * sub);
+        const uint4 w = ldx(((size_t)t * dim + bi * 32 + 8 * sub) / 8);
         const float v[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
                             bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
         q8_block_quad(v, sub, act + t * arow, nb, bi, true);
@@ -878,7 +892,6 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
             const int i = t.row;
             const bool up = t.p != 0;
             const uint4 *wr = reinterpret_cast<const uint4 *>(st);
-            const uint4 *x4 = reinterpret_cast<const uint4 *>(xs);
             with_m(a.m, [&](auto MC) {
                 constexpr int M = decltype(MC)::value;
                 float ac[M];
@@ -889,7 +902,9 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
                     const uint4 v = wr[c];
 #pragma unroll
                     for (int tt = 0; tt < M; ++tt)
-                        ac[tt] = fma_bf16x8(v, x4[(size_t)tt * (dim / 8) + c], ac[tt]);
+                        ac[tt] = fma_bf16x8(
+                            v, g_stage_x(M) ? x4s[(size_t)tt * (dim / 8) + c] : __ldcg(x4g + (size_t)tt * (dim / 8) + c),
+                            ac[tt]);
                 }
                 __syncwarp();
                 if (lane == 0)
@@ -943,7 +958,6 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
                 __syncwarp();
                 hs_seen = true;
             }
-            const uint4 *h4 = reinterpret_cast<const uint4 *>(hs_s);
             with_m(a.m, [&](auto MC) {
                 constexpr int M = decltype(MC)::value;
                 for (int rr = 0; rr < a.w2r; ++rr) {
@@ -956,7 +970,10 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
                         const uint4 wv = wr[c];
 #pragma unroll
                         for (int tt = 0; tt < M; ++tt)
-                            acc[tt] = fma_bf16x8(wv, h4[(size_t)tt * (inter / 8) + c], acc[tt]);
+                            acc[tt] = fma_bf16x8(wv,
+                                                 g_stage_x(M) ? h4s[(size_t)tt * (inter / 8) + c]
+                                                              : __ldcg(h4g + (size_t)tt * (inter / 8) + c),
+                                                 acc[tt]);
                     }
 #pragma unroll
                     for (int tt = 0; tt < M; ++tt) {
