@@ -78,6 +78,9 @@ def lib():
             L.orc_score.argtypes = [C.c_float, C.c_float, C.POINTER(C.c_int)]
             L.orc_route.restype = C.c_int
             L.orc_route.argtypes = [C.POINTER(Cfg), P, P, C.c_int, P, P, P, P]
+            L.orc_plan.restype = C.c_int
+            L.orc_plan.argtypes = [C.c_int, C.c_int, C.c_int, P, P, P, P, C.c_uint64, C.c_uint64,
+                                   C.c_uint64, C.c_uint64, C.c_uint64, P, P, P, P]
             L.orc_swiglu.restype = C.c_double
             L.orc_swiglu.argtypes = [C.c_double, C.c_double, C.c_double]
             L.orc_expert_token.restype = None
@@ -235,6 +238,32 @@ def route(c: Cfg, logits: np.ndarray, bias: np.ndarray):
     rc = lib().orc_route(C.byref(c), _p(lg), _p(b), m, _p(picks), _p(weights), _p(scores), _p(flags))
     assert rc == 0
     return picks, weights, scores, flags
+
+
+def header_words(m: int, k: int) -> int:
+    """Words of the route header of m tokens: m rows of 1 + 3k, then the plan
+    tail (ne, m k + 1 pair starts, m k plan experts)."""
+    return m * (1 + 3 * k) + 2 + 2 * m * k
+
+
+def plan(picks, weights, flags, slot_row, arena, n_routed: int, fill: int = -7):
+    """The header, plan weights / rows and pointer table of m tokens (see
+    orc_plan). arena = (base, slot_bytes, gate_off, up_off, down_off). Header
+    words the layout leaves unused keep `fill`. -> (hdr, plan_w, plan_rows,
+    ptrs, ne)."""
+    pk = np.ascontiguousarray(picks, dtype=np.int32)
+    m, k = pk.shape
+    w = _f32(weights).reshape(m, k)
+    fl = np.ascontiguousarray(flags if flags is not None else np.zeros(m), dtype=np.int32)
+    sr = np.ascontiguousarray(slot_row, dtype=np.int32)
+    hdr = np.full(header_words(m, k), fill, np.int32)
+    pw = np.zeros(m * k, np.float32)
+    pr = np.zeros(m * k, np.int32)
+    ptrs = np.zeros(3 * m * k, np.uint64)
+    base, sb, go, uo, do = (int(v) for v in arena)
+    ne = lib().orc_plan(m, k, int(n_routed), _p(pk), _p(w), _p(fl), _p(sr), base, sb, go, uo, do,
+                        _p(hdr), _p(pw), _p(pr), _p(ptrs))
+    return hdr, pw, pr, ptrs, ne
 
 
 def swiglu(g: float, u: float, limit: float) -> float:

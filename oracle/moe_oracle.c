@@ -10,7 +10,7 @@
  * against library conversions; hand-packed Q2_K / Q3_K blocks against closed
  * forms; the integer-dot form against the dequantise-then-dot form by brute
  * force; q8_1 round-trip bounds; router sums against exact rational sums;
- * scores against 60-digit arithmetic; the selection against brute force over
+ * each step of the score against 60-digit arithmetic; the selection against brute force over
  * all k-subsets and its invariants; SwiGLU against its closed form; the
  * layer against special cases with closed-form outputs.
  */
@@ -277,29 +277,53 @@ void orc_router_logits(const uint16_t *x, const uint16_t *w, int dim, int n, int
 
 /* ---------------------------------------------------------------- selection */
 
+/* 1 when the long-double value v lies within 2^-56 (relative) of the
+ * midpoint between r = (float)v and its neighbour on v's side: there the
+ * long-double evaluation (error far below 2^-60 relative) cannot certify on
+ * which side of the midpoint the exact value lies. */
 static int near_midpoint(long double v, float r)
 {
     if (!isfinite(r) || (long double)r == v)
         return 0;
     float nb = v > (long double)r ? nextafterf(r, INFINITY) : nextafterf(r, -INFINITY);
     long double mid = ((long double)r + (long double)nb) / 2.0L;
-    return fabsl(v - mid) <= ldexpl(fabsl(v), -46);
+    return fabsl(v - mid) <= ldexpl(fabsl(v), -56);
 }
 
-/* score = sqrt(softplus(logit / temp)) with softplus(x) = x for x > 20, else
- * ln(1 + e^x) (moe_v41.rs, fn softplus and fn route_from_logits). The
- * division is the page's f32 division; the rest is evaluated in long double
- * and rounded once to f32. *near_mid is set when that rounding is not certain
- * at f64 precision (the value lies within 2^-46 of an f32 midpoint). */
+/* The f32 rounding (to nearest, ties to even) of an exact value known as the
+ * long double v; *near_mid is set when that rounding is not certain. */
+static float rn_f32(long double v, int *near_mid)
+{
+    float r = (float)v;
+    if (near_midpoint(v, r))
+        *near_mid = 1;
+    return r;
+}
+
+/* score = sqrt(softplus(logit / temp)) as the page writes it in f32
+ * (moe_v41.rs, fn softplus: x for x > 20, else x.exp().ln_1p(); fn
+ * route_from_logits: the .sqrt() of that), each f32 operation taken as
+ * correctly rounded:
+ *   t  = f32(logit / temp)
+ *   e  = f32(e^t)                (t <= 20)
+ *   sp = f32(ln(1 + e))          (t <= 20), else sp = t
+ *   s  = f32(sqrt(sp))
+ * e and sp are evaluated in long double and rounded to f32; *near_mid is set
+ * when either rounding lies within 2^-56 of a midpoint (then not certain). */
 float orc_score(float logit, float temp, int *near_mid)
 {
+    int nm = 0;
     float t = logit / temp;
-    long double sp = t > 20.0f ? (long double)t : log1pl(expl((long double)t));
-    long double s = sqrtl(sp);
-    float r = (float)s;
+    float sp;
+    if (t > 20.0f) {
+        sp = t;
+    } else {
+        float e = rn_f32(expl((long double)t), &nm);
+        sp = rn_f32(log1pl((long double)e), &nm);
+    }
     if (near_mid)
-        *near_mid = near_midpoint(s, r);
-    return r;
+        *near_mid = nm;
+    return sqrtf(sp);
 }
 
 /* a ranks before b: larger key first, NaN keys after all others, equal keys
@@ -383,6 +407,79 @@ int orc_route(const orc_cfg *c, const float *logits, const float *bias, int m,
     free(key);
     free(order);
     return 0;
+}
+
+/* The route header, the plan and the pointer table of m tokens from their
+ * picks and weights (pick order), as moe_v41/device_route.rs describes them:
+ * module doc and fn header_words (per token: status, picks, weight bits, the
+ * slots of the plan), fn route_select_launch (pointer = base + slot *
+ * slot_bytes + offset; a slot of -1 is read as slot 0 and sets the miss
+ * flag), fn device_route_check (the plan in ascending expert id). The pages
+ * give the layout for one token; for m tokens the reading is one header row
+ * per token, then the plan tail:
+ *   row t, 1 + 3k words: [0] status (flags & ORC_FLAG_NONFINITE, | 1 for a
+ *     miss); [1..k] picks; [k+1..2k] weight bits; [2k+1..3k] the slots of
+ *     the token's picks in ascending id (-1 written as 0);
+ *   tail at po = m (1 + 3k): [po] ne = distinct picked experts;
+ *     [po + 1 + p] = first pair of plan expert p (p < ne), [po + 1 + ne] =
+ *     m k; [po + 2 + m k + p] = plan expert p (ascending id).
+ * Pairs (expert, token) run expert by expert in ascending id, tokens ascending
+ * within one; plan_w / plan_rows hold each pair's weight and token; ptrs holds
+ * gate at [p], up at [m k + p], down at [2 m k + p] for plan expert p. Words
+ * of hdr beyond these are left as they are. Returns ne. */
+int orc_plan(int m, int k, int n, const int32_t *picks, const float *weights,
+             const int32_t *flags, const int32_t *slot_row, uint64_t base,
+             uint64_t slot_bytes, uint64_t gate_off, uint64_t up_off, uint64_t down_off,
+             int32_t *hdr, float *plan_w, int32_t *plan_rows, uint64_t *ptrs)
+{
+    int cap = m * k, po = m * (1 + 3 * k);
+    for (int t = 0; t < m; t++) {
+        int32_t *row = hdr + (size_t)t * (1 + 3 * k);
+        int status = flags ? (flags[t] & ORC_FLAG_NONFINITE) : 0;
+        int asc[64];
+        for (int i = 0; i < k; i++) {
+            row[1 + i] = picks[t * k + i];
+            memcpy(&row[1 + k + i], &weights[t * k + i], 4);
+            asc[i] = picks[t * k + i];
+        }
+        for (int i = 1; i < k; i++)
+            for (int j = i; j > 0 && asc[j] < asc[j - 1]; j--) {
+                int v = asc[j];
+                asc[j] = asc[j - 1];
+                asc[j - 1] = v;
+            }
+        for (int i = 0; i < k; i++) {
+            int sl = slot_row[asc[i]];
+            if (sl < 0)
+                status |= 1;
+            row[1 + 2 * k + i] = sl < 0 ? 0 : sl;
+        }
+        row[0] = status;
+    }
+    int ne = 0, q = 0;
+    for (int e = 0; e < n; e++) {
+        int first = q;
+        for (int t = 0; t < m; t++)
+            for (int i = 0; i < k; i++)
+                if (picks[t * k + i] == e) {
+                    plan_rows[q] = t;
+                    plan_w[q] = weights[t * k + i];
+                    q++;
+                }
+        if (q == first)
+            continue;
+        int sl = slot_row[e] < 0 ? 0 : slot_row[e];
+        uint64_t b = base + (uint64_t)sl * slot_bytes;
+        ptrs[ne] = b + gate_off;
+        ptrs[cap + ne] = b + up_off;
+        ptrs[2 * cap + ne] = b + down_off;
+        hdr[po + 1 + ne] = first;
+        hdr[po + 2 + cap + ne] = e;
+        ne++;
+    }
+    hdr[po] = ne;
+    hdr[po + 1 + ne] = q;
+    return ne;
 }
 
 /* Clamped SwiGLU: silu(min(g, L)) * clamp(u, -L, L), silu(z) = z / (1 + e^-z);

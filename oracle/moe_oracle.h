@@ -6,8 +6,8 @@
  * header, table or helper with the CUDA library.
  *
  * Every routine is a plain restatement of what the layer computes, in f64
- * unless the page fixes the precision (the selection's f32 key arithmetic and
- * the q8_1 quantisation decisions, which are f32). Sources, by page:
+ * unless the page fixes the precision (the score's f32 chain, the selection's
+ * f32 key arithmetic and the q8_1 quantisation decisions). Sources, by page:
  *   moe_v41.rs          -- module doc (three K-quant GEMVs on raw Q2_K / Q3_K
  *                          blocks, q8_1 activation, bf16 shared expert,
  *                          routing rule), MoeV41Cfg, MoeV41LayerWeights,
@@ -19,7 +19,7 @@
  *                          device_route_check (plan in ascending id).
  * Points the pages leave open take the readings listed in the design notes
  * (Q2_K / Q3_K byte layout = the public GGUF layout; q8_1 = 32 values with an
- * f16 scale; clamped SwiGLU; score rounded once to f32).
+ * f16 scale; clamped SwiGLU; each f32 step of the score correctly rounded).
  */
 #ifndef MOE_ORACLE_H
 #define MOE_ORACLE_H
@@ -38,9 +38,10 @@ typedef struct {
 
 /* per-token flags written by orc_route */
 #define ORC_FLAG_NONFINITE 2   /* a logit or key was NaN or infinite        */
-#define ORC_FLAG_NEAR_MID  4   /* a score lay within 2^-46 (relative) of an
-                                  f32 rounding midpoint: the once-rounded
-                                  score is not certain at f64 precision     */
+#define ORC_FLAG_NEAR_MID  4   /* a step of a score's f32 chain lay within
+                                  2^-56 (relative) of an f32 rounding
+                                  midpoint: its rounding is not certain at
+                                  long-double precision                     */
 
 uint16_t orc_bf16_from_f32(float x);
 double orc_bf16_to_f64(uint16_t h);
@@ -61,6 +62,10 @@ float orc_score(float logit, float temp, int *near_mid);
 int orc_route(const orc_cfg *c, const float *logits, const float *bias, int m,
               int32_t *picks, float *weights, float *scores, int32_t *flags);
 double orc_swiglu(double g, double u, double limit);
+int orc_plan(int m, int k, int n, const int32_t *picks, const float *weights,
+             const int32_t *flags, const int32_t *slot_row, uint64_t base,
+             uint64_t slot_bytes, uint64_t gate_off, uint64_t up_off, uint64_t down_off,
+             int32_t *hdr, float *plan_w, int32_t *plan_rows, uint64_t *ptrs);
 
 void orc_expert_token(const orc_cfg *c, const uint8_t *gate, const uint8_t *up,
                       const uint8_t *down, const uint8_t *x_q8, float *g, float *u,

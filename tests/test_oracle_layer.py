@@ -19,18 +19,40 @@ def _bf16_vals(bits):
     return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-@pytest.mark.parametrize("limit", [0.0, 7.0, 1.5])
-def test_swiglu_closed_form(limit):
+# Clamped SwiGLU, h = silu(min(g, L)) * clamp(u, -L, L), silu(z) = z / (1 + e^-z),
+# no clamp for L <= 0 (page moe_v41.rs, MoeV41Cfg swiglu_limit). Values worked
+# by hand from e^-1 = 0.36787944117144232160, e = 2.71828182845904523536,
+# e^-2 = 0.13533528323661269189, e^-7 = 0.00091188196555451621,
+# e^-10 = 0.00004539992976248485, e^-3 = 0.04978706836786394298:
+SWIGLU_CASES = [
+    # g, u, L, h
+    (1.0, 1.0, 7.0, 0.73105857863000487925),       # 1 / (1 + e^-1)
+    (-1.0, 2.0, 7.0, -0.53788284273999024150),     # -2 / (1 + e)
+    (10.0, 3.0, 7.0, 20.980867924917586447),       # g clamped to 7: 3 * 7 / (1 + e^-7)
+    (7.0, 7.0, 7.0, 48.955358491474368377),        # g and u at the limit: 7 * 7 / (1 + e^-7)
+    (2.0, 9.0, 7.0, 12.331159091690354217),        # u clamped to +7: 7 * 2 / (1 + e^-2)
+    (2.0, -9.0, 7.0, -12.331159091690354217),      # u clamped to -7
+    (10.0, 3.0, 0.0, 29.998638063938926968),       # L = 0: no clamp, 3 * 10 / (1 + e^-10)
+    (10.0, 3.0, -1.0, 29.998638063938926968),      # L < 0: no clamp
+    (-30.0, 2.0, 7.0, -5.6145737813035793723e-12),  # g below -L is not clamped: 2 * -30 / (1 + e^30)
+    (0.0, 5.0, 7.0, 0.0),
+    (3.0, -20.0, 1.5, -1.8395425714356982341),     # both clamped: -1.5 * 1.5 / (1 + e^-1.5)
+]
+
+
+@pytest.mark.parametrize("g,u,limit,h", SWIGLU_CASES)
+def test_swiglu_hand_worked_values(g, u, limit, h):
+    assert oracle.swiglu(g, u, limit) == pytest.approx(h, rel=1e-14, abs=1e-300)
+
+
+def test_swiglu_clamp_bounds():
+    """With L >= 1, |h| <= L^2 (silu(z) <= z for z > 0, |silu(z)| < 0.28 for
+    z < 0); without a clamp h grows with g u."""
     rng = np.random.default_rng(30)
-    for g, u in list(rng.standard_normal((200, 2)) * 6) + [(10.0, 3.0), (3.0, -20.0), (-30.0, 2.0)]:
-        gg, uu = g, u
-        if limit > 0:
-            gg = min(g, limit)
-            uu = min(max(u, -limit), limit)
-        want = gg / (1.0 + math.exp(-gg)) * uu
-        assert oracle.swiglu(g, u, limit) == pytest.approx(want, rel=1e-15, abs=1e-300)
-        if limit >= 1:
-            assert abs(oracle.swiglu(g, u, limit)) <= limit * limit
+    for g, u in rng.standard_normal((400, 2)) * 12:
+        assert abs(oracle.swiglu(g, u, 7.0)) <= 49.0
+        assert abs(oracle.swiglu(g, u, 1.5)) <= 2.25
+    assert oracle.swiglu(40.0, 40.0, 0.0) > 1500.0
 
 
 def _dense(blocks, rows, nb, q3):

@@ -185,3 +185,56 @@ def test_weight_tolerance_covers_logit_perturbations(temp):
         assert_weights_close(cfg, w1[0], w0[0], dl_real)
         checked += 1
     assert checked >= 30
+
+
+def _golden_plan():
+    rows = {}
+    with open(os.path.join(GOLD, "plan_m2.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                key, *vals = line.split()
+                rows[key] = vals
+    return rows
+
+
+def test_plan_layout_golden_m2():
+    """The two-token header / plan / pointer table worked by hand
+    (tests/golden/plan_m2.txt) against the oracle's plan."""
+    g = _golden_plan()
+    m, k, n = int(g["m"][0]), int(g["k"][0]), int(g["n"][0])
+    picks = np.array([[int(v) for v in g[f"picks{t}"]] for t in range(m)], np.int32)
+    weights = np.array([[float(v) for v in g[f"weights{t}"]] for t in range(m)], np.float32)
+    slots = np.array([int(v) for v in g["slots"]], np.int32)
+    arena = [int(v, 16) for v in g["arena"]]
+    hdr, pw, pr, ptrs, ne = oracle.plan(picks, weights, None, slots, arena, n)
+    hw = 1 + 3 * k
+    for t in range(m):
+        assert [int(v) for v in hdr[t * hw:(t + 1) * hw]] == [int(v, 0) for v in g[f"row{t}"]], t
+    po, cap = m * hw, m * k
+    assert ne == int(g["ne"][0]) == hdr[po]
+    assert list(hdr[po + 1:po + 2 + ne]) == [int(v) for v in g["pair_start"]]
+    assert list(hdr[po + 2 + cap:po + 2 + cap + ne]) == [int(v) for v in g["plan_expert"]]
+    # words the layout leaves unused are not written
+    assert list(hdr[po + 2 + ne:po + 2 + cap]) == [-7] * (cap - ne)
+    assert list(hdr[po + 2 + cap + ne:]) == [-7] * (cap - ne)
+    assert list(pr) == [int(v) for v in g["plan_rows"]]
+    assert list(pw) == [float(v) for v in g["plan_w"]]
+    for which, off in (("gate", 0), ("up", cap), ("down", 2 * cap)):
+        assert [int(v) for v in ptrs[off:off + ne]] == [int(v, 16) for v in g[which]], which
+
+
+def test_plan_flags_and_single_token():
+    """At m = 1 the layout is the pages' own (1 + 3k header words, then the
+    plan's ne and its one-pair-per-expert starts); the non-finite flag
+    carries into the status word."""
+    picks = np.array([[4, 0, 2]], np.int32)
+    weights = np.array([[0.5, 0.25, 0.25]], np.float32)
+    slots = np.array([3, -1, 1, -1, 0], np.int32)
+    hdr, pw, pr, ptrs, ne = oracle.plan(picks, weights, np.array([2]), slots, (0, 0x100, 0, 0x10, 0x20), 5)
+    assert hdr[0] == 2                          # non-finite; every pick resident
+    assert list(hdr[7:10]) == [3, 1, 0]         # slots of 0, 2, 4 in ascending id
+    hdr2 = oracle.plan(np.array([[1, 4, 2]], np.int32), weights, None, slots, (0, 0x100, 0, 0x10, 0x20), 5)[0]
+    assert hdr2[0] == 1 and list(hdr2[7:10]) == [0, 1, 0]  # expert 1 missing: slot 0 and the miss bit
+    assert ne == 3 and list(hdr[11:15]) == [0, 1, 2, 3]
+    assert len(hdr) == 18 and list(hdr[15:18]) == [0, 2, 4]
+    assert list(pw) == [0.25, 0.25, 0.5] and list(pr) == [0, 0, 0]
