@@ -9,12 +9,12 @@
 // module doc and fn route_select_launch). No CTA ever waits on another.
 //
 // Selection (page spark_model/layers/moe_v41.rs, fn softplus and
-// fn route_from_logits): score = f32(sqrt(softplus(l / temp))), key = score +
-// bias, stable descending order, top k, weights renormalised in f32. The
-// score is the correctly rounded f32 of the exact value, evaluated in the
-// router epilogue, where every CTA takes a few of the rows, in float-float
-// single precision with a double-precision fallback near rounding midpoints
-// (FP64 is a slow pipe on GB300). The selecting CTA is latency-bound: it reads everything it needs in
+// fn route_from_logits): score = the f32 chain sqrt(ln_1p(exp(l / temp))),
+// each step correctly rounded, key = score + bias, stable descending order,
+// top k, weights renormalised in f32. The score is evaluated in the router
+// epilogue, where every CTA takes a few of the rows, in float-float single
+// precision with double-precision fallbacks near rounding midpoints (FP64 is
+// a slow pipe on GB300). The selecting CTA is latency-bound: it reads everything it needs in
 // one round of loads, ranks each token with one warp (k rounds of a warp-wide
 // maximum over 64-bit sortable values), and only stores afterwards.
 #pragma once
@@ -42,32 +42,28 @@ struct RouteArgs {
     int32_t *plan_rows;
     unsigned long long *ptrs;
     uint32_t *ctrl;  // [MOE_CTRL_TICKET], [MOE_CTRL_STATUS]
+    unsigned long long wait_ns;  // bound on each wait
 };
 
-// ------------------------------------------------------------------ scores
-
-// The score as defined: the f32 rounding of sqrt(softplus(t)), t = f32(l / temp),
-// softplus(x) = x for x > 20. Evaluated in f64 (CUDA's exp, log1p, sqrt) and
-// rounded once: the f64 chain's error is far below half an f32 ulp, so the
-// rounding equals the exact one except within ~2^-50 of an f32 midpoint.
-__device__ __noinline__ float score_exact(float l, float temp)
-{
-    const float t = __fdiv_rn(l, temp);
-    const double sp = t > 20.0f ? (double)t : log1p(exp((double)t));
-    return __double2float_rn(sqrt(sp));
-}
-
-// ------------------------------------------------------------------ the score without FP64
+// ------------------------------------------------------------------ the score
 //
-// The same correctly rounded score in single precision (FP64 is a slow pipe
-// on GB300: the double-precision chain above costs microseconds of latency).
-// A candidate s comes from CUDA's expf / log1pf / sqrtf (a few ulp off);
-// then, for each midpoint m between two neighbouring f32 values, the exact
-// score S satisfies S >= m  <=>  softplus(t) >= m^2  <=>  e^t >= expm1(m^2)
-// (both sides increasing), and e^t and expm1(m^2) are evaluated in
-// float-float (pairs of f32, unevaluated sums hi + lo: Dekker's and Knuth's
-// exact sum and product) to about 2^-39 relative. A decision closer than
-// 2^-37 relative, or t below -170, goes to the double-precision path.
+// Page moe_v41.rs, fn softplus and fn route_from_logits: the score is the f32
+// chain t.exp().ln_1p().sqrt() (t itself in place of the first two steps for
+// t > 20), t = f32(l / temp). Each step is taken as a correctly rounded f32
+// operation:
+//   e = RN(e^t),  p = RN(ln(1 + e)),  s = RN(sqrt(p)).
+// sqrt is the IEEE operation. For e and p, CUDA's expf / log1pf give a
+// candidate within two ulp, and the rounding is decided exactly against the
+// midpoints m between neighbouring f32 values:
+//   e:  e^t >= m
+//   p:  ln(1 + e) >= m  <=>  e >= e^m - 1   (both sides increasing)
+// Level 1 evaluates e^t and e^m - 1 in float-float single precision (pairs of
+// f32, unevaluated sums hi + lo; Dekker's and Knuth's exact sum and product)
+// to about 2^-41 relative: FP64 is a slow pipe on GB300. A decision closer
+// than 2^-37 relative goes to level 2, CUDA's double-precision exp / log1p
+// (error below 2^-51), and one closer than 2^-48 there to level 3, e^x in
+// double-double (Taylor series after a reduction by ln 2, about 2^-100),
+// decided at 2^-70.
 
 struct ff {
     float hi, lo;
@@ -172,145 +168,266 @@ __constant__ float2 c_exp2_32[32] = {
 // 2^q for q in [-126, 127], exactly
 __device__ __forceinline__ float pow2i(int q) { return __int_as_float((q + 127) << 23); }
 
-// One step of the Horner chains below
-__device__ __forceinline__ ff horner_step(ff p, ff r, bool ser, ff c0, ff c1)
+// x 2^n for |n| <= 252, exact when the result is a normal f32 (two exact
+// power-of-two steps, so that 2^n itself need not be representable)
+__device__ __forceinline__ float scale2(float x, int n)
 {
-    return ff_add(ff_mul(p, r), ser ? c1 : c0);
+    const int h = n / 2;
+    return __fmul_rn(__fmul_rn(x, pow2i(h)), pow2i(n - h));
 }
 
-// Tang's table-driven reduction of x (|x| < 120): k = round(x 32 / ln2),
-// x = k ln2 / 32 + r with ln2 / 32 in three parts, the first with 12
-// significant bits so that k times it is exact; |r| < 0.011. Returns r; j =
-// k mod 32, q = floor(k / 32): e^x = 2^q 2^(j / 32) e^r.
+__device__ __forceinline__ ff ff_neg(ff a) { return {-a.hi, -a.lo}; }
+
+// Tang's table-driven reduction of x (|x.hi| <= 110): k = round(x 32 / ln2),
+// x = k ln2 / 32 + r with ln2 / 32 in three parts (k times the first two
+// formed exactly as float-float products), |r| < 0.0109. Returns r; j = k
+// mod 32, q = floor(k / 32): e^x = 2^q 2^(j / 32) e^r.
 __device__ __forceinline__ ff tang_reduce(ff x, int &j, int &q)
 {
     const float P1 = 0x1.62ep-6f, P2 = 0x1.0bfbe8p-20f, P3 = 0x1.cf79acp-45f;
-    const float kf = rintf(x.hi * 0x1.715476p+5f);
+    const float kf = rintf(__fmul_rn(x.hi, 0x1.715476p+5f));
     const int k = (int)kf;
     j = k & 31;
     q = k >> 5;  // arithmetic shift: floor
-    ff r = ff_two_sum(x.hi, -kf * P1);  // kf * P1 is exact
-    r = ff_add(r, {x.lo, 0.0f});
-    const ff k2 = ff_two_prod(kf, P2);
-    r = ff_add(r, {-k2.hi, -k2.lo});
-    return ff_add(r, {-kf * P3, 0.0f});
+    ff r = ff_add(x, ff_neg(ff_two_prod(kf, P1)));
+    r = ff_add(r, ff_neg(ff_two_prod(kf, P2)));
+    return ff_add(r, {-__fmul_rn(kf, P3), 0.0f});
 }
 
-// For t in [-40, 20]: the candidate s and its neighbours s_-2 .. s_+2 (f32
-// steps), the four midpoints m_i between them, and five independent values
-// in float-float: e^t and expm1(m_i^2). The number c of
-// midpoints below the exact score places it: the rounding is s_c (c = 1..3).
-// e^x by Tang's reduction and the Taylor series of e^r to r^5 / 5!
-// (remainder below 2^-48), times 2^(j/32) from the table and 2^q; expm1(M)
-// below 2^-6: M times the series of (e^M - 1) / M to M^5 / 6! (remainder
-// below 2^-48), else e^M - 1 (e^M - 1 >= 2^-6: at most 6 bits lost). Returns
-// -1 when a decision is closer than 2^-37 relative or the candidate is off by
-// two steps.
-// The five values are independent until the decision, so they run one a
-// lane: lane v (0..4) of a converged group of five lanes that share t (mask
-// gmask, first lane src0) evaluates value v -- e^t for v = 0, expm1 of the
-// squared midpoint between candidates v - 1 and v for v > 0 -- then every
-// lane of the group gathers the five and takes the same decision.
-__device__ __noinline__ float score_ff(float t, int v, unsigned gmask, int src0)
+// e^x = 2^q P, P in [0.98, 2] as float-float: 2^(j/32) from the table times
+// the Taylor series of e^r to r^5 / 5! (remainder below 2^-48)
+__device__ ff exp_ff(ff x, int &q)
 {
-    const float s = sqrtf(log1pf(expf(t)));
-    const unsigned sb = __float_as_uint(s);  // positive and normal: +-1 on the bits steps one f32
-    ff x = {t, 0.0f};
-    if (v > 0) {
-        const float lo = __uint_as_float(sb + v - 3), hi = __uint_as_float(sb + v - 2);
-        const ff m = {hi, __fmul_rn(__fsub_rn(lo, hi), 0.5f)};  // exact midpoint
-        x = ff_mul(m, m);
-    }
-    const bool ser = v > 0 && x.hi < 0x1.0p-6f;
-    int j = 0, q = 0;
-    const ff r = ser ? x : tang_reduce(x, j, q);
-    ff p = ff_inv_fact(ser ? 6 : 5);
-#pragma unroll 1
-    for (int n = 4; n >= 0; --n)
-        p = horner_step(p, r, ser, ff_inv_fact(n), ff_inv_fact(n + 1));
-    ff val;
-    if (ser) {
-        val = ff_mul(p, x);
-    } else {
-        const float2 tj = c_exp2_32[j];
-        const ff e = ff_mul({tj.x, tj.y}, p);
-        const float sc = pow2i(q);
-        val = {__fmul_rn(e.hi, sc), __fmul_rn(e.lo, sc)};
-        if (v > 0)
-            val = ff_add(val, {-1.0f, 0.0f});
-    }
-    float vh[5], vl[5];
-#pragma unroll
-    for (int i = 0; i < 5; ++i) {
-        vh[i] = __shfl_sync(gmask, val.hi, src0 + i);
-        vl[i] = __shfl_sync(gmask, val.lo, src0 + i);
-    }
-    const float tol = 0x1.0p-37f * vh[0];
-    int c = 0;
-    bool sure = true;
-#pragma unroll
-    for (int i = 1; i < 5; ++i) {
-        const ff D = ff_add({vh[0], vl[0]}, {-vh[i], -vl[i]});
-        sure = sure && fabsf(D.hi) > tol;
-        c += D.hi > 0.0f;
-    }
-    if (!sure || c == 0 || c == 4)
-        return -1.0f;
-    return __uint_as_float(sb + (c == 1 ? -1 : (c == 2 ? 0 : 1)));
-}
-
-// For t in [-170, -40]: softplus(t) = e^t (1 - e^t / 2 + ...) with e^t below
-// 4.2e-18, so S = e^(t/2) (1 + d), |d| < 2^-59, far inside the 2^-37 margin:
-// S rounds as e^(t/2) does. e^(t/2) = 2^q 2^(j/32) e^r (as in score_ff),
-// compared with the midpoints scaled by 2^-q (exact), so that nothing
-// underflows. Returns -1 when a decision is too close or the candidate is
-// off by two steps.
-__device__ __noinline__ float score_ff_tiny(float t)
-{
-    const float h = __fmul_rn(t, 0.5f);  // exact
-    const float s = expf(h);
-    const unsigned sb = __float_as_uint(s);
-    float sv[5];
-#pragma unroll
-    for (int i = 0; i < 5; ++i)
-        sv[i] = __uint_as_float(sb + i - 2);
-    int j, q;
-    const ff r = tang_reduce({h, 0.0f}, j, q);
+    int j;
+    const ff r = tang_reduce(x, j, q);
     ff p = ff_inv_fact(5);
 #pragma unroll 1
     for (int n = 4; n >= 0; --n)
         p = ff_add(ff_mul(p, r), ff_inv_fact(n));
     const float2 tj = c_exp2_32[j];
-    p = ff_mul({tj.x, tj.y}, p);
-    const float sc = pow2i(-q);
-    const float tol = 0x1.0p-37f * p.hi;
-    int c = 0;
+    return ff_mul({tj.x, tj.y}, p);
+}
+
+// e^m - 1 for m in [2^-26, 21]: below 1/8 the series m (1 + m/2! + ... +
+// m^8/9!) (remainder below 2^-48 relative), else e^m - 1 (e^m - 1 >= 1/8
+// loses at most 3.1 bits to the cancellation)
+__device__ ff expm1_ff(ff m)
+{
+    if (m.hi < 0.125f) {
+        ff p = ff_inv_fact(9);
+#pragma unroll 1
+        for (int n = 8; n >= 1; --n)
+            p = ff_add(ff_mul(p, m), ff_inv_fact(n));
+        return ff_mul(p, m);
+    }
+    int q;
+    const ff P = exp_ff(m, q);
+    const float sc = pow2i(q);  // q <= 30
+    return ff_add({__fmul_rn(P.hi, sc), __fmul_rn(P.lo, sc)}, {-1.0f, 0.0f});
+}
+
+// ---- levels 2 and 3 (rare: a decision within 2^-37 of a midpoint)
+
+struct dd {
+    double hi, lo;
+};
+
+__device__ __forceinline__ dd dd_two_sum(double a, double b)
+{
+    const double s = __dadd_rn(a, b);
+    const double bb = __dsub_rn(s, a);
+    return {s, __dadd_rn(__dsub_rn(a, __dsub_rn(s, bb)), __dsub_rn(b, bb))};
+}
+
+__device__ __forceinline__ dd dd_fast_two_sum(double a, double b)  // |a| >= |b|
+{
+    const double s = __dadd_rn(a, b);
+    return {s, __dsub_rn(b, __dsub_rn(s, a))};
+}
+
+__device__ __forceinline__ dd dd_add(dd a, dd b)
+{
+    const dd s = dd_two_sum(a.hi, b.hi);
+    const dd t = dd_two_sum(a.lo, b.lo);
+    dd u = dd_fast_two_sum(s.hi, __dadd_rn(s.lo, t.hi));
+    return dd_fast_two_sum(u.hi, __dadd_rn(u.lo, t.lo));
+}
+
+__device__ __forceinline__ dd dd_mul(dd a, dd b)
+{
+    const double p = __dmul_rn(a.hi, b.hi);
+    const double e = __fma_rn(a.hi, b.hi, -p);
+    return dd_fast_two_sum(p, __fma_rn(a.hi, b.lo, __fma_rn(a.lo, b.hi, e)));
+}
+
+// a / n for a small positive integer n: the remainder of the rounded
+// quotient is exact (one fma), and carries the low part
+__device__ __forceinline__ dd dd_div_int(dd a, double n)
+{
+    const double q1 = __ddiv_rn(a.hi, n);
+    const double rem = __fma_rn(-q1, n, a.hi);
+    return dd_fast_two_sum(q1, __ddiv_rn(__dadd_rn(rem, a.lo), n));
+}
+
+// e^x in double-double for |x| <= 110: k = round(x / ln2), r = x - k ln2
+// with ln2 = L1 + L2 + L3 (L1 of 32 bits, so k L1 is exact; k L2 an exact
+// double-double product), |r| <= 0.35; e^r = 1 + r (1 + r/2 (1 + r/3 (... (1
+// + r/24)))), remainder below 2^-120; times 2^k (exact).
+__device__ __noinline__ dd exp_dd(double x)
+{
+    const double L1 = 0x1.62e42fee00000p-1, L2 = 0x1.a39ef35793c76p-33, L3 = 0x1.cc01f97b57a08p-87;
+    const double k = rint(__dmul_rn(x, 0x1.71547652b82fep+0));
+    dd r = dd_two_sum(x, -__dmul_rn(k, L1));
+    const double p2 = __dmul_rn(k, L2);
+    r = dd_add(r, {-p2, -__fma_rn(k, L2, -p2)});
+    r = dd_add(r, {-__dmul_rn(k, L3), 0.0});
+    dd p = {1.0, 0.0};
+#pragma unroll 1
+    for (int n = 24; n >= 1; --n)
+        p = dd_add({1.0, 0.0}, dd_div_int(dd_mul(r, p), (double)n));
+    const int ki = (int)k;
+    const double s1 = __longlong_as_double((long long)(1023 + ki / 2) << 52);
+    const double s2 = __longlong_as_double((long long)(1023 + ki - ki / 2) << 52);
+    return {__dmul_rn(__dmul_rn(p.hi, s1), s2), __dmul_rn(__dmul_rn(p.lo, s1), s2)};
+}
+
+// The nearest f32 of an exact value V known through `above(m)` = (V > m) for
+// a midpoint m, with `sure` cleared when the comparison is too close: the
+// candidate c (V's rounding at a precision far above f32) and its two
+// neighbours, decided against the two midpoints around c.
+template <typename Above>
+__device__ __forceinline__ float decide_near(float c, Above above, bool &sure)
+{
+    const unsigned cb = __float_as_uint(c);
+    const float lo = cb > 0u ? __uint_as_float(cb - 1u) : c, hi = __uint_as_float(cb + 1u);
+    const double mlo = 0.5 * ((double)lo + (double)c), mhi = 0.5 * ((double)c + (double)hi);  // exact
+    bool s1 = true, s2 = true;
+    const bool a_hi = above(mhi, s1);
+    const bool a_lo = above(mlo, s2);
+    sure = s1 && s2 && (lo != c || a_lo);
+    return a_hi ? hi : (a_lo ? c : lo);
+}
+
+// RN(e^t) for t in [-104, 20] at levels 2 and 3
+__device__ __noinline__ float exp_rn_slow(float t)
+{
+    const double E = exp((double)t);
+    bool sure;
+    const float c = __double2float_rn(E);
+    float r = decide_near(c, [&](double m, bool &ok) {
+        ok = fabs(E - m) > 0x1.0p-48 * E;
+        return E > m;
+    }, sure);
+    if (sure)
+        return r;
+    const dd E3 = exp_dd((double)t);
+    return decide_near(c, [&](double m, bool &ok) {
+        const dd D = dd_add(E3, {-m, 0.0});
+        ok = fabs(D.hi) > 0x1.0p-70 * m;
+        return D.hi > 0.0;
+    }, sure);
+}
+
+// RN(ln(1 + y)) for y in [2^-25, e^20] at levels 2 and 3 (level 3 compares
+// y with e^m - 1 for the midpoints m)
+__device__ __noinline__ float log1p_rn_slow(float y)
+{
+    const double L = log1p((double)y);
+    bool sure;
+    const float c = __double2float_rn(L);
+    float r = decide_near(c, [&](double m, bool &ok) {
+        ok = fabs(L - m) > 0x1.0p-48 * L;
+        return L > m;
+    }, sure);
+    if (sure)
+        return r;
+    return decide_near(c, [&](double m, bool &ok) {
+        const dd X = dd_add(exp_dd(m), {-1.0, 0.0});
+        const dd D = dd_add({(double)y, 0.0}, {-X.hi, -X.lo});
+        ok = fabs(D.hi) > 0x1.0p-70 * (double)y;
+        return D.hi > 0.0;
+    }, sure);
+}
+
+// ---- level 1
+
+// RN(e^t) for t in [-104, 20] in float-float: the candidate c = expf(t) and
+// its neighbours c_-2 .. c_+2 (f32 steps), the four midpoints between them
+// scaled by 2^-q (exact: c 2^-q is near P), compared with P = e^t 2^-q. The
+// number n of midpoints below e^t places it: the rounding is c_(n-2) for n
+// = 1..3. Returns false when a decision is closer than 2^-37 relative or c
+// is off by two steps.
+__device__ __forceinline__ bool exp_rn_ff(float t, float &out)
+{
+    const unsigned cb = max(__float_as_uint(expf(t)), 2u);
+    int q;
+    const ff P = exp_ff({t, 0.0f}, q);
+    const float tol = 0x1.0p-37f * P.hi;
+    int n = 0;
     bool sure = true;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const float mh = __fmul_rn(__fsub_rn(sv[i], sv[i + 1]), 0.5f);  // the midpoint is sv[i + 1] + mh
-        const ff D = ff_add(p, {-__fmul_rn(sv[i + 1], sc), -__fmul_rn(mh, sc)});
+        const float a = __uint_as_float(cb + i - 2), b = __uint_as_float(cb + i - 1);
+        const ff M = {scale2(b, -q), scale2(__fsub_rn(a, b), -q - 1)};  // (a + b) / 2 2^-q
+        const ff D = ff_add(P, ff_neg(M));
         sure = sure && fabsf(D.hi) > tol;
-        c += D.hi > 0.0f;
+        n += D.hi > 0.0f;
     }
-    if (!sure || c == 0 || c == 4)
-        return -1.0f;
-    return c == 1 ? sv[1] : (c == 2 ? sv[2] : sv[3]);
+    if (!sure || n == 0 || n == 4)
+        return false;
+    out = __uint_as_float(cb - 2 + n);
+    return true;
 }
 
-// The routing score of l on a group of five converged lanes that share l
-// (v = 0..4, mask gmask, first lane src0): sqrt for t > 20, f64 below -170
-// (and NaN), else the float-float paths (score_ff: one value a lane) with
-// the f64 fallback; every lane of the group returns the score.
+// RN(ln(1 + y)) for y in [2^-25, e^20] in float-float, on a converged group
+// of four lanes (mask gmask, first lane src0, this lane's place v): the
+// candidate c = log1pf(y) and its neighbours c_-2 .. c_+2; lane v evaluates
+// e^m_v - 1 for the midpoint m_v between c_(v-2) and c_(v-1); the group
+// gathers the four and compares each with y. Returns false as exp_rn_ff.
+__device__ __forceinline__ bool log1p_rn_ff(float y, int v, unsigned gmask, int src0, float &out)
+{
+    const unsigned cb = __float_as_uint(log1pf(y));
+    const float a = __uint_as_float(cb + v - 2), b = __uint_as_float(cb + v - 1);
+    const ff X = expm1_ff({b, __fmul_rn(__fsub_rn(a, b), 0.5f)});  // the exact midpoint
+    const float tol = 0x1.0p-37f * y;
+    int n = 0;
+    bool sure = true;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float xh = __shfl_sync(gmask, X.hi, src0 + i), xl = __shfl_sync(gmask, X.lo, src0 + i);
+        const ff D = ff_add({y, 0.0f}, {-xh, -xl});
+        sure = sure && fabsf(D.hi) > tol;
+        n += D.hi > 0.0f;
+    }
+    if (!sure || n == 0 || n == 4)
+        return false;
+    out = __uint_as_float(cb - 2 + n);
+    return true;
+}
+
+// The routing score of l on a converged group of four lanes that share l
+// (v = 0..3, mask gmask, first lane src0); every lane returns it.
+// ln(1 + e) rounds to e itself below 2^-25 (ln(1 + e) = e (1 - e/2 + ...)
+// lies within e/2 < 2^-26 relative of e, closer than any midpoint).
+__device__ __noinline__ float score_chain(float t, int v, unsigned gmask, int src0)
+{
+    float e = 0.0f;  // e^t < 2^-150 below t = -104: rounds to 0
+    if (t >= -104.0f && !exp_rn_ff(t, e))
+        e = exp_rn_slow(t);
+    float p = e;
+    if (e >= 0x1.0p-25f && !log1p_rn_ff(e, v, gmask, src0, p))
+        p = log1p_rn_slow(e);
+    return __fsqrt_rn(p);
+}
+
 __device__ __forceinline__ float score_fast(float l, float temp, int v, unsigned gmask, int src0)
 {
     const float t = __fdiv_rn(l, temp);
     if (t > 20.0f)
         return __fsqrt_rn(t);
-    if (!(t >= -170.0f))
-        return score_exact(l, temp);
-    const float s = t >= -40.0f ? score_ff(t, v, gmask, src0) : score_ff_tiny(t);
-    return s > 0.0f ? s : score_exact(l, temp);
+    if (t != t)
+        return t;
+    return score_chain(t, v, gmask, src0);
 }
 
 // ------------------------------------------------------------------ sortable keys
@@ -654,7 +771,7 @@ __global__ void __launch_bounds__(256) moe_router_kernel(RouteArgs a)
             s4[i] = __ldcg(gx + i);
     }
     __syncthreads();
-    const bool ok = nrows <= 0 || mbar_wait(bar, 0, a.ctrl + MOE_CTRL_STATUS);
+    const bool ok = nrows <= 0 || mbar_wait(bar, 0, a.ctrl + MOE_CTRL_STATUS, a.wait_ns);
     if (__syncthreads_and(ok) == 0)
         return;
     // logits: one warp per row, all tokens at once; lane j takes the 16-byte
@@ -696,14 +813,14 @@ __global__ void __launch_bounds__(256) moe_router_kernel(RouteArgs a)
         }
     });
     __syncthreads();
-    // one score a warp first (lane groups of five, lane-major over the
+    // one score a warp first (lane groups of four, lane-major over the
     // warps): the scores take different paths by range, and paths in one
-    // warp would run one after another; a group computes one score, the five
-    // chains of its float-float range one a lane
-    const int nw = blockDim.x >> 5, grp = lane / 5, gv = lane - 5 * grp;
-    if (grp < 6) {
-        const unsigned gmask = 0x1Fu << (5 * grp);
-        for (int i = warp + nw * grp; i < nrows * m; i += nw * 6) {
+    // warp would run one after another; a group computes one score, the four
+    // midpoint tests of its float-float log1p step one a lane
+    const int nw = blockDim.x >> 5, grp = lane >> 2, gv = lane & 3;
+    {
+        const unsigned gmask = 0xFu << (4 * grp);
+        for (int i = warp + nw * grp; i < nrows * m; i += nw * 8) {
             const int r = i / m, t = i % m;
             const float l = red[i];
             const size_t o = (size_t)t * a.n + row0 + r;
@@ -712,7 +829,7 @@ __global__ void __launch_bounds__(256) moe_router_kernel(RouteArgs a)
             if (a.do_select) {
                 // the exact score of this row, here: a few lanes of every CTA
                 // in parallel instead of the selecting CTA
-                const float sc = score_fast(l, a.temp, gv, gmask, 5 * grp);
+                const float sc = score_fast(l, a.temp, gv, gmask, 4 * grp);
                 if (gv == 0) {
                     a.scores[o] = sc;
                     a.keys[o] = __fadd_rn(sc, s_bias[r]);
@@ -760,13 +877,13 @@ __global__ void __launch_bounds__(256) moe_select_kernel(RouteArgs a)
     for (int e = threadIdx.x; e < a.n; e += blockDim.x)
         slot[e] = __ldg(a.slot_row + e);
     {
-        // a group of five lanes a score (six groups a warp)
-        const int lane = threadIdx.x & 31, grp = lane / 5, gv = lane - 5 * grp;
-        const int ng = (int)(blockDim.x >> 5) * 6;
-        if (grp < 6) {
-            const unsigned gmask = 0x1Fu << (5 * grp);
-            for (int i = (int)(threadIdx.x >> 5) * 6 + grp; i < (int)mn; i += ng) {
-                const float s = score_fast(a.logits[i], a.temp, gv, gmask, 5 * grp);
+        // a group of four lanes a score (eight groups a warp)
+        const int lane = threadIdx.x & 31, grp = lane >> 2, gv = lane & 3;
+        const int ng = (int)(blockDim.x >> 5) * 8;
+        {
+            const unsigned gmask = 0xFu << (4 * grp);
+            for (int i = (int)(threadIdx.x >> 5) * 8 + grp; i < (int)mn; i += ng) {
+                const float s = score_fast(a.logits[i], a.temp, gv, gmask, 4 * grp);
                 if (gv == 0) {
                     sc[i] = s;
                     ky[i] = __fadd_rn(s, __ldg(a.bias + i % a.n));
@@ -778,7 +895,7 @@ __global__ void __launch_bounds__(256) moe_select_kernel(RouteArgs a)
     select_and_plan<false>(a, a.logits, sc, ky, slot, smem);
 }
 
-#define MOE_SCORES_PER_CTA 48  // eight warps of six five-lane groups
+#define MOE_SCORES_PER_CTA 64  // eight warps of eight four-lane groups
 
 struct ScoreArgs {
     const float *logits;
@@ -787,15 +904,15 @@ struct ScoreArgs {
     int count;
 };
 
-// the routing score of each of count logits: a group of five lanes each
-// (six groups a warp, MOE_SCORES_PER_CTA a CTA of 256 threads)
+// the routing score of each of count logits: a group of four lanes each
+// (eight groups a warp, MOE_SCORES_PER_CTA a CTA of 256 threads)
 __global__ void moe_score_kernel(ScoreArgs a)
 {
     pdl_wait();
-    const int lane = threadIdx.x & 31, grp = lane / 5, gv = lane - 5 * grp;
-    const int i = blockIdx.x * MOE_SCORES_PER_CTA + (int)(threadIdx.x >> 5) * 6 + grp;
-    if (grp < 6 && i < a.count) {
-        const float s = score_fast(a.logits[i], a.temp, gv, 0x1Fu << (5 * grp), 5 * grp);
+    const int lane = threadIdx.x & 31, grp = lane >> 2, gv = lane & 3;
+    const int i = blockIdx.x * MOE_SCORES_PER_CTA + (int)(threadIdx.x >> 5) * 8 + grp;
+    if (i < a.count) {
+        const float s = score_fast(a.logits[i], a.temp, gv, 0xFu << (4 * grp), 4 * grp);
         if (gv == 0)
             a.scores[i] = s;
     }

@@ -132,41 +132,25 @@ def _same_f32_bits(got, want):
 
 
 def _check_selection(cfg, logits, bias, slot_row, m, arena_tuple, hdr, pw, pr, ptrs):
-    """The device header / plan / pointer table against the oracle chain on the same logits."""
+    """The device header / plan / pointer table against the oracle's (selection
+    and plan layout) on the same logits: every word the layout defines."""
     k, n = cfg.topk, cfg.n_routed
     picks, weights, _, flags = oracle.route(ocfg(cfg), logits, bias)
-    base, sb, go, uo, do = arena_tuple
-    hw = 1 + 3 * k
+    rhdr, rpw, rpr, rptrs, ne = oracle.plan(picks[:m], weights[:m], flags[:m], slot_row, arena_tuple, n)
+    hw, cap = 1 + 3 * k, m * k
+    po = m * hw
     for t in range(m):
         row = hdr[t * hw:(t + 1) * hw]
-        assert list(row[1:1 + k]) == list(picks[t]), (t, row[1:1 + k], picks[t])
-        _same_f32_bits(row[1 + k:1 + 2 * k].view(np.float32), weights[t])
-        st = int(flags[t]) & moe.MOE_HDR_NONFINITE
-        srt = sorted(int(e) for e in picks[t])
-        slots = [int(slot_row[e]) for e in srt]
-        if any(s < 0 for s in slots):
-            st |= moe.MOE_HDR_MISS
-        assert int(row[0]) == st, (t, row[0], st)
-        assert list(row[1 + 2 * k:]) == [max(s, 0) for s in slots]
-    # the plan: distinct experts ascending, pairs grouped by expert, tokens ascending
-    plan = sorted({int(e) for t in range(m) for e in picks[t]})
-    po = m * hw
-    ne = int(hdr[po])
-    assert ne == len(plan)
-    cap = m * k
-    assert list(hdr[po + 2 + cap:po + 2 + cap + ne]) == plan
-    pairs = [(e, t) for e in plan for t in range(m) if e in set(int(v) for v in picks[t])]
-    starts = [0]
-    for e in plan:
-        starts.append(starts[-1] + sum(1 for p in pairs if p[0] == e))
-    assert list(hdr[po + 1:po + 2 + ne]) == starts
-    assert list(pr[:cap]) == [t for _, t in pairs]
-    wmap = {(int(picks[t][i]), t): weights[t][i] for t in range(m) for i in range(k)}
-    _same_f32_bits(pw[:cap], np.array([wmap[p] for p in pairs], np.float32))
-    for p, e in enumerate(plan):
-        s = max(int(slot_row[e]), 0)
-        b = base + s * sb
-        assert int(ptrs[p]) == b + go and int(ptrs[cap + p]) == b + uo and int(ptrs[2 * cap + p]) == b + do
+        assert list(row[:1 + k]) == list(rhdr[t * hw:t * hw + 1 + k]), (t, row, rhdr[t * hw:(t + 1) * hw])
+        _same_f32_bits(row[1 + k:1 + 2 * k].view(np.float32), rhdr[t * hw + 1 + k:t * hw + 1 + 2 * k].view(np.float32))
+        assert list(row[1 + 2 * k:]) == list(rhdr[t * hw + 1 + 2 * k:(t + 1) * hw]), t
+    assert int(hdr[po]) == ne
+    assert list(hdr[po + 1:po + 2 + ne]) == list(rhdr[po + 1:po + 2 + ne])
+    assert list(hdr[po + 2 + cap:po + 2 + cap + ne]) == list(rhdr[po + 2 + cap:po + 2 + cap + ne])
+    assert list(pr[:cap]) == list(rpr)
+    _same_f32_bits(pw[:cap], rpw)
+    for off in (0, cap, 2 * cap):
+        assert list(ptrs[off:off + ne]) == list(rptrs[off:off + ne])
 
 
 def _arena(size=1 << 20):
@@ -178,8 +162,8 @@ def _arena(size=1 << 20):
 # ------------------------------------------------------------------ the score
 
 def _oracle_scores(logits, temp):
-    """The oracle's exact scores (long double, correctly rounded) and the
-    mask of values within 2^-46 relative of an f32 rounding midpoint."""
+    """The oracle's scores (the f32 chain, each step rounded from long double)
+    and the mask of scores with a step within 2^-56 of an f32 midpoint."""
     n = 1024
     lg = np.asarray(logits, np.float32)
     pad = (-len(lg)) % n
@@ -196,18 +180,20 @@ def _oracle_scores(logits, temp):
 @pytest.mark.parametrize("temp", [1.0, 0.7])
 def test_route_scores_are_correctly_rounded(temp):
     """Page moe_v41.rs fn softplus / fn route_from_logits: the score is the
-    f32 rounding of the exact sqrt(softplus(l / temp)); the device's
-    float-float evaluation (double precision near midpoints) equals the
-    oracle's long-double rounding bit for bit."""
+    f32 chain sqrt(ln_1p(exp(l / temp))), each step correctly rounded; the
+    device's float-float decisions (double and double-double precision near
+    midpoints) equal the oracle's long-double roundings bit for bit."""
     rng = np.random.default_rng(11)
     parts = [rng.normal(0.0, 3.0, 1 << 19),
              rng.uniform(-60.0, 30.0, 1 << 18),
              rng.uniform(19.9, 20.1, 1 << 14) * temp,       # around the x > 20 cut
-             rng.uniform(-40.5, -39.5, 1 << 14) * temp,     # where softplus becomes e^t to f32 precision
-             rng.uniform(-175.0, -40.0, 1 << 16) * temp,    # the e^(t/2) path and below it
-             rng.uniform(-171.0, -169.0, 1 << 12) * temp,
+             rng.uniform(-17.6, -17.0, 1 << 14) * temp,     # e around 2^-25: ln(1 + e) rounds to e below
+             rng.uniform(-104.5, -86.0, 1 << 16) * temp,    # e^t subnormal, and rounding to 0 below -103.97
+             rng.uniform(-175.0, -40.0, 1 << 15) * temp,
+             rng.uniform(-1.0, 1.0, 1 << 14) * 2.0 ** -20,  # e near 1
              rng.normal(0.0, 1e-3, 1 << 14),
-             np.array([0.0, -0.0, 20.0 * temp, -40.0 * temp, 1e-30, -1e-30, 88.0, -88.0, 300.0, -300.0])]
+             np.array([0.0, -0.0, 20.0 * temp, -104.0 * temp, -103.97 * temp, 1e-30, -1e-30, 88.0, -88.0,
+                       300.0, -300.0, np.inf, -np.inf])]
     lg = np.concatenate(parts).astype(np.float32)
     d_in = torch.from_numpy(lg).cuda()
     d_out = torch.full_like(d_in, float("nan"))

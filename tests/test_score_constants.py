@@ -1,8 +1,9 @@
-"""The constants of the device's float-float score (page moe_v41.rs fn
-softplus: the score is evaluated as e^t against expm1(m^2)): each 1/n! pair
-is the exact rational rounded to f32 twice, and the three parts of ln 2
-(Cody and Waite's reduction) add up to ln 2 with the first part short
-enough for k * part exact. Read from the kernel source, checked against
+"""The constants of the device's score chain (page moe_v41.rs fn softplus:
+e^t and ln(1 + e) rounded to f32, decided against e^t and e^m - 1 at
+midpoints m): each 1/n! pair is the exact rational rounded to f32 twice; the
+float-float parts of ln 2 / 32 and the double-double parts of ln 2 (Cody and
+Waite's reduction) add up to the constant, the first double part short enough
+for k times it to be exact. Read from the kernel source, checked against
 exact arithmetic."""
 import math
 import os
@@ -19,7 +20,7 @@ def _f32(x):
 
 
 def _ln2():
-    return sum(Fraction(1, k * 2 ** k) for k in range(1, 300))  # ln 2 = sum 1 / (k 2^k)
+    return sum(Fraction(1, k * 2 ** k) for k in range(1, 400))  # ln 2 = sum 1 / (k 2^k)
 
 
 def test_inverse_factorials_are_exact_float_float_pairs():
@@ -36,15 +37,31 @@ def test_inverse_factorials_are_exact_float_float_pairs():
 
 
 def test_ln2_over_32_parts():
-    """Tang's reduction x = k ln2 / 32 + r: the three parts add up to ln 2 / 32
-    and the first is short enough that k times it is exact for |k| < 4096."""
+    """Tang's reduction x = k ln2 / 32 + r (|k| <= 5100 for |x| <= 110): the
+    three f32 parts add up to ln 2 / 32 within 2^-70, so k times the error
+    stays below 2^-57 (k P1 and k P2 are formed as exact float-float
+    products)."""
     src = open(SRC).read()
     m = re.search(r"P1 = ([0-9a-fx.p-]+)f, P2 = ([0-9a-fx.p-]+)f, P3 = ([0-9a-fx.p-]+)f", src)
     p1, p2, p3 = (Fraction(float.fromhex(g)) for g in m.groups())
-    assert abs(p1 + p2 + p3 - _ln2() / 32) < Fraction(1, 2 ** 70)  # x 4096 still below 2^-58
-    for k in (-4095, -3001, -17, 1, 2047, 4095):
-        assert Fraction(_f32(k * float(p1))) == k * p1
-    assert p1.numerator.bit_length() <= 12 and p1.denominator & (p1.denominator - 1) == 0
+    assert abs(p1 + p2 + p3 - _ln2() / 32) < Fraction(1, 2 ** 70)
+    for p in (p1, p2, p3):
+        assert Fraction(_f32(float(p))) == p
+
+
+def test_ln2_double_double_parts():
+    """The level-3 reduction x = k ln2 + r (|k| <= 160): L1 + L2 + L3 = ln 2
+    within 2^-130, and L1 has at most 32 significant bits, so k L1 is an
+    exact double for |k| < 2^21."""
+    src = open(SRC).read()
+    m = re.search(r"L1 = ([0-9a-fx.p+-]+), L2 = ([0-9a-fx.p+-]+), L3 = ([0-9a-fx.p+-]+);", src)
+    l1, l2, l3 = (Fraction(float.fromhex(g)) for g in m.groups())
+    assert abs(l1 + l2 + l3 - _ln2()) < Fraction(1, 2 ** 130)
+    num = l1.numerator
+    while num % 2 == 0:
+        num //= 2
+    assert num.bit_length() <= 32
+    assert l1.denominator & (l1.denominator - 1) == 0
 
 
 def test_exp2_table():
