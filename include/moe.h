@@ -126,16 +126,17 @@ int moe_quantize_q8_1(const moe_cfg *cfg, const void *x_dev, int m, void *out_de
                       moe_stream_t stream);
 
 /* Device selection ([moe_v41] fn route_from_logits; [route] fn
- * route_select_launch, module doc): per token, scores s = f32(sqrt(
- * softplus(l / temp))) (softplus(x) = x for x > 20), picks = the top k of
+ * route_select_launch, module doc): per token, scores s = the f32 chain
+ * sqrt(ln_1p(exp(t))), t = l / temp, each step correctly rounded (t itself
+ * in place of ln_1p(exp(t)) for t > 20; [moe_v41] fn softplus), picks = the top k of
  * s + bias with ties to the lower id, weights = picked scores divided by
  * (their f32 sum in pick order + 1e-20) when norm_topk_prob and k > 1, times
  * route_scale; then the plan, the plan weights and rows (pair-major:
  * experts ascending, tokens ascending within one), and the pointer table
  * ptrs[0..cap) gate, [cap..2cap) up, [2cap..3cap) down with cap = m * topk,
  * pointer = base + slot * slot_bytes + offset, slot -1 -> slot 0 and the
- * MOE_HDR_MISS bit. Picks are bit-identical to the definition; the score is
- * evaluated so its f32 rounding is exact (double-checked in f64).
+ * MOE_HDR_MISS bit. Scores, picks and weights are bit-identical to the
+ * definition (each rounding of the score decided exactly).
  * logits_dev f32 [m, n_routed]; bias_dev f32 [n_routed]; slot_row_dev i32
  * [n_routed]; arena by value (host struct, device base); header_dev i32
  * [moe_header_words]; plan_w_dev f32 [m*topk]; plan_rows_dev i32 [m*topk];
@@ -146,12 +147,13 @@ int moe_route_select(const moe_cfg *cfg, const float *logits_dev, const float *b
                      uint64_t *ptrs_dev, moe_stream_t stream);
 
 /* The routing score of each logit ([moe_v41] fn softplus, fn
- * route_from_logits): scores[i] = the f32 rounding of the exact
- * sqrt(softplus(t)), t = f32(logits[i] / gate_temp), softplus(x) = x for
- * x > 20, else ln(1 + e^x) -- the score the router and the selection use.
- * Evaluated in float-float single precision, in double precision when that
- * cannot decide the rounding. logits_dev, scores_dev f32 [count], count >= 0
- * (0: nothing is launched). */
+ * route_from_logits): t = f32(logits[i] / gate_temp); for t > 20
+ * scores[i] = f32(sqrt(t)), else e = f32(e^t), p = f32(ln(1 + e)),
+ * scores[i] = f32(sqrt(p)), each rounding to nearest as a correctly rounded
+ * operation -- the score the router and the selection use. The roundings
+ * are decided in float-float single precision, in double and then
+ * double-double precision when that cannot decide them. logits_dev,
+ * scores_dev f32 [count], count >= 0 (0: nothing is launched). */
 int moe_route_scores(const moe_cfg *cfg, const float *logits_dev, int count, float *scores_dev,
                      moe_stream_t stream);
 
@@ -197,8 +199,11 @@ int moe_layer_step(const moe_cfg *cfg, const moe_layer *layer, const moe_arena *
  * The workspace is a 4 MiB array in the library's device memory, one per
  * device. The first call on a device (with that device current) looks it up
  * with cudaGetSymbolAddress and zeroes it; make that first call before any
- * stream capture. Every call clears the array's control words and counters
- * on `stream` first, then runs the same kernels as moe_layer_step.
+ * stream capture (a first call on a capturing stream returns
+ * MOE_EUNSUPPORTED). The looked-up address is kept for the life of the
+ * process: do not use this call across cudaDeviceReset of that device.
+ * Every call clears the array's control words and counters on `stream`
+ * first, then runs the same kernels as moe_layer_step.
  * Arguments as moe_layer_step; status_host: NULL, or a host word that
  * receives the workspace status (MOE_WS_*) of this call once `stream`
  * reaches the end of the call (pinned memory keeps the copy asynchronous).
@@ -241,6 +246,25 @@ int moe_workspace_view(const moe_cfg *cfg, void *ws_dev, moe_ws_view *view);
 /* Reads the workspace status word (MOE_WS_* bits) to a host variable; this
  * synchronises `stream`. */
 int moe_read_status(void *ws_dev, uint32_t *status_host, moe_stream_t stream);
+
+/* Sets the bound, in nanoseconds, on every wait inside the kernels (a wait
+ * on a shared-memory barrier, on another CTA's count, or on the selection's
+ * plan) for the calls enqueued after it; a graph keeps the bound it was
+ * captured with. 0 restores the default of 2 s. Process-wide. When a wait
+ * runs out, the kernel records MOE_WS_TIMEOUT in the workspace status and
+ * returns instead of waiting on (page step_seg.rs has no counterpart: a
+ * device wait there is unbounded). */
+int moe_set_wait_limit_ns(uint64_t ns);
+
+/* Failure-handling check, not a step of the layer: launches the two expert
+ * kernels of a layer step as moe_layer_step does, but with no router kernel
+ * before them, so the gate/up producers' bounded wait for the selection's
+ * plan-ready word can only end by running out. header_dev must hold an empty
+ * plan (zeros: ne = 0), so that no expert is read. After the stream reaches
+ * it, the workspace status has MOE_WS_TIMEOUT and the workspace must be
+ * initialised again (moe_workspace_init). x_dev bf16 [m, dim]. */
+int moe_expert_step_unreleased(const moe_cfg *cfg, const void *x_dev, const int32_t *header_dev, int m,
+                               void *ws_dev, moe_stream_t stream);
 
 /* Slot-table update ([route] fn slot_table_update, struct Kernels
  * slot_table_set): for each of n (layer, expert, slot) int32 triples,

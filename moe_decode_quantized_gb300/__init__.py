@@ -26,7 +26,8 @@ SLOT_TABLE_LAYERS = 64
 __all__ = ["Config", "Arena", "Layer", "MoeError", "header_words", "workspace_bytes",
            "workspace_init", "router_logits", "quantize_q8_1", "route_select", "expert_step",
            "swiglu_q8", "layer_step", "host_io_bytes", "layer_step_host", "workspace_view",
-           "read_status", "layer_step_profiled", "layer_step_static", "route_scores", "slot_table_set", "dedupe_triples", "parse_header", "Graph"]
+           "read_status", "layer_step_profiled", "layer_step_static", "route_scores", "set_wait_limit_ns",
+           "expert_step_unreleased", "slot_table_set", "dedupe_triples", "parse_header", "Graph"]
 
 
 class MoeError(RuntimeError):
@@ -165,8 +166,20 @@ def layer_step_static(cfg: Config, layer: Layer, arena: Arena, x, residual, x_ne
                                             _stream(stream)))
 
 
+def set_wait_limit_ns(ns: int):
+    """Bound (ns) on every wait inside kernels enqueued from now on; 0 = 2 s."""
+    _check(_lib.moe().moe_set_wait_limit_ns(int(ns)))
+
+
+def expert_step_unreleased(cfg: Config, x, header, m: int, ws, stream=None):
+    """The expert kernels with no router before them: their wait for the plan
+    can only run out (a failure-handling check; see include/moe.h)."""
+    _check(_lib.moe().moe_expert_step_unreleased(C.byref(cfg.c()), _ptr(x), _ptr(header), m, _ptr(ws),
+                                                 _stream(stream)))
+
+
 def route_scores(cfg: Config, logits, scores, count: int, stream=None):
-    """scores[i] = f32(sqrt(softplus(logits[i] / gate_temp))), correctly rounded."""
+    """scores[i] = the f32 chain sqrt(ln_1p(exp(logits[i] / gate_temp))), each step correctly rounded."""
     _check(_lib.moe().moe_route_scores(C.byref(cfg.c()), _ptr(logits), count, _ptr(scores), _stream(stream)))
 
 

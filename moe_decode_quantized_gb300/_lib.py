@@ -71,6 +71,8 @@ MOE_SYMBOLS = {
     "moe_graph_launch_host": (C.c_int, [P, P, P, P, P, P, P]),
     "moe_layer_step_profiled": (C.c_int, [C.POINTER(MoeCfg), C.POINTER(MoeLayer), C.POINTER(MoeArena), P,
                                           P, P, P, C.c_int, P, P, P]),
+    "moe_set_wait_limit_ns": (C.c_int, [U64]),
+    "moe_expert_step_unreleased": (C.c_int, [C.POINTER(MoeCfg), P, P, C.c_int, P, P]),
     "moe_last_error": (C.c_char_p, []),
 }
 

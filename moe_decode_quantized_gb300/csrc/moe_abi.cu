@@ -2,6 +2,7 @@
 // documented in include/moe.h): argument checks, workspace layout, launch
 // geometry, programmatic dependent launch between the three kernels of a
 // layer step, and CUDA-graph capture of whole multi-layer steps.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -81,6 +82,9 @@ struct DevInfo {
 
 std::mutex g_mu;
 DevInfo g_dev[64];
+
+// bound on every wait inside the kernels launched from now on (nanoseconds)
+std::atomic<unsigned long long> g_wait_ns{MOE_WAIT_NS};
 
 int dev_info(DevInfo **out)
 {
@@ -258,6 +262,7 @@ RouteArgs route_args(const moe_cfg &c, int m)
     a.route_scale = c.route_scale;
     a.norm = c.norm_topk_prob != 0;
     a.k = c.topk;
+    a.wait_ns = g_wait_ns.load();
     return a;
 }
 
@@ -287,7 +292,7 @@ int launch_experts(const moe_cfg &c, int m, const Geo &G, const Bufs &B, const u
                    const unsigned long long *ptrs, const float *plan_w, const int32_t *plan_rows,
                    const int32_t *hdr, const uint16_t *w1, const uint16_t *w3, const uint16_t *w2,
                    float *acc, float *residual, uint16_t *x_next, cudaStream_t s, bool pdl_gateup,
-                   cudaEvent_t *ev = nullptr)
+                   cudaEvent_t *ev = nullptr, bool plan_hint = false)
 {
     const int k = c.topk, cap = m * k;
     GArgs ga{};
@@ -298,8 +303,9 @@ int launch_experts(const moe_cfg &c, int m, const Geo &G, const Bufs &B, const u
     ga.hs = B.hs;
     ga.sd = B.sd;
     ga.limit = c.swiglu_limit;
+    ga.wait_ns = g_wait_ns.load();
     ga.w2r = G.w2r;
-    ga.plan_hint = pdl_gateup ? 1 : 0;  // only a layer step's router raises the hint
+    ga.plan_hint = (pdl_gateup || plan_hint) ? 1 : 0;  // only a layer step's router raises the hint
     ga.stage_x = G.stage_x ? 1 : 0;
     ga.hdr = hdr;
     ga.ptrs = ptrs;
@@ -339,6 +345,7 @@ int launch_experts(const moe_cfg &c, int m, const Geo &G, const Bufs &B, const u
     da.rgcnt = B.rgcnt;
     da.status = B.ctrl + MOE_CTRL_STATUS;
     da.limit = c.swiglu_limit;
+    da.wait_ns = g_wait_ns.load();
     da.dim = c.dim;
     da.inter = c.inter;
     da.m = m;
@@ -428,7 +435,9 @@ void *g_static_ptr[64];  // per device ordinal, under g_mu
 
 // Address of this device's copy of g_static_ws. The first call on a device
 // (with that device current) looks the symbol up and zeroes the whole array
-// on `s`, as moe_workspace_init does for a caller's workspace.
+// on `s`, as moe_workspace_init does for a caller's workspace; that set-up
+// must not be recorded into a graph, so a first call made while `s` is being
+// captured is refused.
 int static_ws(cudaStream_t s, void **out)
 {
     int d = 0;
@@ -437,6 +446,12 @@ int static_ws(cudaStream_t s, void **out)
         return fail(MOE_EUNSUPPORTED, "device ordinal %d", d);
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_static_ptr[d]) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        CUDA_OK(cudaStreamIsCapturing(s, &cs));
+        if (cs != cudaStreamCaptureStatusNone)
+            return fail(MOE_EUNSUPPORTED,
+                        "moe_layer_step_static: the first call on a device sets up the static workspace and "
+                        "must be made outside stream capture");
         void *p = nullptr;
         CUDA_OK(cudaGetSymbolAddress(&p, g_static_ws));
         CUDA_OK(cudaMemsetAsync(p, 0, MOE_STATIC_WS_BYTES, s));
@@ -520,6 +535,32 @@ int moe_read_status(void *ws, uint32_t *status, moe_stream_t stream)
                             (cudaStream_t)stream));
     CUDA_OK(cudaStreamSynchronize((cudaStream_t)stream));
     return MOE_OK;
+}
+
+int moe_set_wait_limit_ns(uint64_t ns)
+{
+    g_wait_ns.store(ns == 0 ? MOE_WAIT_NS : (unsigned long long)ns);
+    return MOE_OK;
+}
+
+int moe_expert_step_unreleased(const moe_cfg *cfg, const void *x, const int32_t *header, int m, void *ws,
+                               moe_stream_t stream)
+{
+    int rc = check_cfg(cfg);
+    if (rc || (rc = check_m(cfg, m)))
+        return rc;
+    if (m < 1 || !x || !header || !ws || !aligned16(x))
+        return fail(MOE_EINVAL, "moe_expert_step_unreleased: bad arguments");
+    DevInfo *I;
+    if ((rc = dev_info(&I)))
+        return rc;
+    Geo G;
+    if ((rc = geometry(*cfg, m, false, *I, G)))
+        return rc;
+    const Bufs B = ws_bufs(*cfg, ws);
+    return launch_experts(*cfg, m, G, B, static_cast<const uint16_t *>(x), B.ptrs, B.plan_w, B.plan_rows, header,
+                          nullptr, nullptr, nullptr, B.acc, nullptr, nullptr, (cudaStream_t)stream, false, nullptr,
+                          true);
 }
 
 int moe_router_logits(const moe_cfg *cfg, const void *x, const void *w, float *logits, int m,

@@ -5,8 +5,9 @@
 // form) into shared memory, L2 eviction-priority hints, and programmatic
 // dependent launch (griddepcontrol) so a kernel's independent prologue runs
 // while its predecessor drains. Every wait on an mbarrier is bounded: after
-// MOE_WAIT_NS of wall time the waiting thread records MOE_WS_TIMEOUT in the
-// workspace status word and the kernel unwinds instead of hanging.
+// the kernel's wait_ns of wall time (MOE_WAIT_NS unless the host set another
+// bound) the waiting thread records MOE_WS_TIMEOUT in the workspace status
+// word and the kernel unwinds instead of hanging.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -19,7 +20,7 @@
 #define MOE_Q2K_BYTES 84      // Q2_K super-block
 #define MOE_Q3K_BYTES 110     // Q3_K super-block
 #define MOE_Q8_BYTES 36       // q8_1 block of 32
-#define MOE_WAIT_NS 2000000000ull  // 2 s bound on any single wait
+#define MOE_WAIT_NS 2000000000ull  // default bound on any single wait: 2 s
 
 // one Q2_K task = 128 super-blocks of one matrix (10752 B); one Q3_K task =
 // 64 super-blocks (7040 B). Both sizes are multiples of 16 so the bulk copies
@@ -140,8 +141,9 @@ __device__ __forceinline__ uint64_t globaltimer()
 }
 
 // Waits for the phase with `parity` of `bar` to complete. Returns false after
-// MOE_WAIT_NS and records MOE_WS_TIMEOUT in *status.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status)
+// wait_ns nanoseconds and records MOE_WS_TIMEOUT in *status.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status,
+                                          unsigned long long wait_ns)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -149,7 +151,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
     for (uint32_t i = 0;; ++i) {
         if (mbar_try_wait(bar, parity))
             return true;
-        if ((i & 63u) == 63u && globaltimer() - t0 > MOE_WAIT_NS) {
+        if ((i & 63u) == 63u && globaltimer() - t0 > wait_ns) {
             atomicOr(status, (uint32_t)MOE_WS_TIMEOUT);
             return false;
         }

@@ -329,6 +329,7 @@ struct Ring {
     uint8_t *stage;
     uint32_t stage_bytes;
     int S;
+    unsigned long long wait_ns;  // bound on each wait
     __device__ uint8_t *at(int slot) const { return stage + (size_t)slot * stage_bytes; }
 };
 
@@ -340,7 +341,7 @@ __device__ __forceinline__ bool ring_issue(const Ring &r, int i, const Task &t, 
 {
     const int slot = i % r.S;
     const uint32_t round = (uint32_t)(i / r.S);
-    if (round > 0 && !mbar_wait(&r.empty[slot], (round - 1) & 1u, status))
+    if (round > 0 && !mbar_wait(&r.empty[slot], (round - 1) & 1u, status, r.wait_ns))
         return false;
     Task tt = t;
     tt.seq = i;
@@ -381,10 +382,12 @@ __host__ __device__ inline size_t ring_head_bytes(int S)
     return align_up(ring_pc_off(S) + sizeof(PlanCache), 128);
 }
 
-__device__ __forceinline__ Ring ring_carve(uint8_t *smem, int S, uint32_t stage_bytes, size_t stage_off)
+__device__ __forceinline__ Ring ring_carve(uint8_t *smem, int S, uint32_t stage_bytes, size_t stage_off,
+                                           unsigned long long wait_ns)
 {
     Ring r;
     r.S = S;
+    r.wait_ns = wait_ns;
     r.full = reinterpret_cast<uint64_t *>(smem);
     r.empty = r.full + S;
     r.desc = reinterpret_cast<Task *>(smem + ring_desc_off(S));
@@ -407,7 +410,7 @@ __device__ __forceinline__ int ring_grab(const Ring &r)
 // descriptor only after the slot's previous task was consumed, so once the
 // stamp reads j the barrier's current phase is task j's and the parity wait
 // is unambiguous (a parity wait cannot tell a phase two ahead from the one
-// just completed). Bounded like every wait; false after MOE_WAIT_NS.
+// just completed). Bounded like every wait; false after r.wait_ns.
 __device__ __forceinline__ bool ring_acquire(const Ring &r, int j, uint32_t *status)
 {
     const int slot = j % r.S;
@@ -416,13 +419,13 @@ __device__ __forceinline__ bool ring_acquire(const Ring &r, int j, uint32_t *sta
         const uint64_t t0 = globaltimer();
         while (*seq != j) {
             __nanosleep(64);
-            if (globaltimer() - t0 > MOE_WAIT_NS) {
+            if (globaltimer() - t0 > r.wait_ns) {
                 atomicOr(status, (uint32_t)MOE_WS_TIMEOUT);
                 return false;
             }
         }
     }
-    return mbar_wait(&r.full[slot], (uint32_t)(j / r.S) & 1u, status);
+    return mbar_wait(&r.full[slot], (uint32_t)(j / r.S) & 1u, status, r.wait_ns);
 }
 
 // the producer warp caches the plan (all 32 lanes load in parallel, one
@@ -490,6 +493,7 @@ struct GArgs {
     // selection's plan-ready hint
     uint32_t *gctr;
     float limit;
+    unsigned long long wait_ns;  // bound on each wait
     int plan_hint;  // the plan comes from the selection in this stream (its hint at gctr[5])
     int stage_x;    // bf16 x and hs staged in shared memory (few tokens); else read from L2
     int dim, inter, m, k, cap, plan_off, S, w2r;
@@ -544,7 +548,7 @@ __device__ bool g_load_hs(const GArgs &a, const Ring &ring, uint16_t *hs_s, int 
         const uint64_t t0 = globaltimer();
         while (ld_acquire_gpu(a.gctr + 4) < target) {
             __nanosleep(128);
-            if (globaltimer() - t0 > MOE_WAIT_NS) {
+            if (globaltimer() - t0 > a.wait_ns) {
                 atomicOr(a.status, (uint32_t)MOE_WS_TIMEOUT);
                 ok = false;
                 break;
@@ -580,7 +584,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
     extern __shared__ __align__(1024) uint8_t smem[];
     const bool shared = a.w1 != nullptr;
     const bool stage = a.stage_x != 0;
-    const Ring ring = ring_carve(smem, a.S, a.stage_bytes, g_stage_off(a.S, a.m, a.dim, a.inter, shared, stage));
+    const Ring ring = ring_carve(smem, a.S, a.stage_bytes, g_stage_off(a.S, a.m, a.dim, a.inter, shared, stage), a.wait_ns);
     uint8_t *act = smem + g_act_off(a.S);
     uint16_t *xs = reinterpret_cast<uint16_t *>(smem + g_xs_off(a.S, a.m, a.dim));  // staged only
     uint16_t *hs_s = reinterpret_cast<uint16_t *>(smem + g_hs_off(a.S, a.m, a.dim, stage));  // staged only
@@ -680,7 +684,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
                     hint = __shfl_sync(0xffffffffu, hint, 0);
                     if (hint != 0u)
                         break;  // W2 entirely after the routed work
-                    if (done >= (uint32_t)inter || globaltimer() - t0 > MOE_WAIT_NS) {
+                    if (done >= (uint32_t)inter || globaltimer() - t0 > a.wait_ns) {
                         g_load_hs(a, ring, hs_s, lane);  // acquires; times out itself
                         have_hs = true;
                         break;
@@ -724,7 +728,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
                 const uint64_t t0 = globaltimer();
                 while (ld_acquire_gpu(a.gctr + 5) == 0u) {
                     __nanosleep(64);
-                    if (globaltimer() - t0 > MOE_WAIT_NS) {
+                    if (globaltimer() - t0 > a.wait_ns) {
                         if (lane == 0)
                             atomicOr(a.status, (uint32_t)MOE_WS_TIMEOUT);
                         break;
@@ -947,7 +951,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
                         const uint64_t t0 = globaltimer();
                         while (*f == 0) {
                             __nanosleep(64);
-                            if (globaltimer() - t0 > MOE_WAIT_NS) {
+                            if (globaltimer() - t0 > a.wait_ns) {
                                 atomicOr(a.status, (uint32_t)MOE_WS_TIMEOUT);
                                 break;
                             }
@@ -1019,6 +1023,7 @@ struct DArgs {
     uint16_t *x_next;             // [m, dim] or NULL
     uint32_t *rgcnt, *status;
     float limit;
+    unsigned long long wait_ns;  // bound on each wait
     int has_shared;  // add sd to the routed sum
     // own_rows > 0: each CTA owns a range of row groups of the output (at
     // most own_rows rows), takes every plan expert's down rows of them,
@@ -1146,7 +1151,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     const bool shared = a.has_shared != 0;
-    const Ring ring = ring_carve(smem, a.S, a.stage_bytes, d_stage_off(a.S, a.pair_cap, a.dim, a.inter, a.own_rows));
+    const Ring ring = ring_carve(smem, a.S, a.stage_bytes, d_stage_off(a.S, a.pair_cap, a.dim, a.inter, a.own_rows), a.wait_ns);
     float *s_own = reinterpret_cast<float *>(smem + d_own_off(a.S, a.pair_cap, a.dim, a.inter));
     int *s_rows = reinterpret_cast<int *>(smem + d_small_off(a.S));
     float *s_w = reinterpret_cast<float *>(s_rows + D_SW);

@@ -14,8 +14,9 @@ import oracle
 from moe_decode_quantized_gb300 import synth
 from moe_decode_quantized_gb300.workload import Workload, bf16_tensor, x_tensor
 
-from helpers import (GU_RTOL, OUT_RTOL, THREADS, assert_bf16_within_one_ulp, assert_weights_close, bf16_vals, decode_cfg, expert_image, gpu, near_tie,
-                     new_header, ocfg, oracle_layer, parse_all, rel_inf, tiny_cfg, tiny_workload)
+from helpers import (GU_RTOL, OUT_RTOL, THREADS, bf16_vals, compare_layer as _compare_layer, decode_cfg,
+                     expert_image, gpu, near_tie, new_header, ocfg, rel_inf, run_layer as _run_layer, tiny_cfg,
+                     tiny_workload, ws_view as _view)
 
 pytestmark = gpu
 
@@ -28,52 +29,6 @@ def decode_wl():
     yield wl
     del wl
     torch.cuda.empty_cache()
-
-
-def _view(wl, cfg, name, count, dtype=torch.float32):
-    v = moe.workspace_view(cfg, wl.ws)
-    off = v[name] - wl.ws.data_ptr()
-    nbytes = count * torch.tensor([], dtype=dtype).element_size()
-    return wl.ws[off:off + nbytes].view(dtype).cpu().numpy()
-
-
-def _run_layer(wl, cfg, l, x, m, residual=None):
-    res = torch.zeros((m, cfg.dim), dtype=torch.float32, device="cuda") if residual is None else residual
-    xn = torch.empty_like(x)
-    hdr = new_header(cfg, m)
-    moe.layer_step(cfg, wl.layer(l), wl.arena, x, res, xn, hdr, m, wl.ws)
-    torch.cuda.synchronize()
-    assert moe.read_status(wl.ws) == 0
-    return res, xn, hdr
-
-
-def _compare_layer(wl, cfg, x_bits, m, res, xn, hdr, residual0=None, l=0):
-    ref = oracle_layer(wl, cfg, l, x_bits, residual0)
-    h = hdr.cpu().numpy()
-    ws_logits = _view(wl, cfg, "logits", m * cfg.n_routed).reshape(m, cfg.n_routed)
-    compared = 0
-    acc = _view(wl, cfg, "acc", m * cfg.dim).reshape(m, cfg.dim)
-    for t, (st, picks, w) in enumerate(parse_all(cfg, h, m)):
-        if near_tie(cfg, ref["logits"], wl.host_bias(l), t):
-            continue  # the picks may legitimately differ; reported by the test below
-        assert list(picks) == list(ref["picks"][t]), (t, picks, ref["picks"][t])
-        # the weights: bit-exact on the device's logits (below), and against the
-        # oracle's within what the logits' own difference allows
-        dl = float(np.abs(ws_logits[t].astype(np.float64) - ref["logits"][t]).max())
-        assert_weights_close(cfg, w, ref["weights"][t], dl)
-        assert rel_inf(acc[t], ref["acc"][t]) <= OUT_RTOL, (t, rel_inf(acc[t], ref["acc"][t]))
-        compared += 1
-    assert compared >= max(1, m - 1)
-    # selection on the device's own logits is exact (the device_route_check design)
-    opicks, oweights, _, _ = oracle.route(ocfg(cfg), ws_logits, wl.host_bias(l))
-    for t, (st, picks, w) in enumerate(parse_all(cfg, h, m)):
-        assert list(picks) == list(opicks[t])
-        np.testing.assert_array_equal(w.view(np.uint32), oweights[t].view(np.uint32))
-    r = res.cpu().numpy()
-    assert rel_inf(r, ref["residual"]) <= OUT_RTOL
-    assert_bf16_within_one_ulp(xn.cpu().numpy().view(np.uint16), ref["x_next"],
-                               OUT_RTOL * np.abs(ref["residual"]).max())
-    return ref
 
 
 # ------------------------------------------------------------------ tiny layer

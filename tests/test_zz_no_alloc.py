@@ -1,10 +1,11 @@
 """moe_layer_step_static: the layer step on the library's own static device
 workspace, for callers that cannot allocate device memory.
 
-The pages have no counterpart of this call; it must give what
-moe_layer_step gives on a workspace of the caller's. This file is named to be
-collected last, so that the static array has already seen other calls' data
-(and the tests here also pass alone)."""
+The pages have no counterpart of this call; it must give exactly what
+moe_layer_step gives on a workspace of the caller's (the kernels are
+deterministic, so bit for bit), and it must not allocate device memory. This
+file is named to be collected last, so that the static array has already
+seen other calls' data (and the tests here also pass alone)."""
 import numpy as np
 import pytest
 import torch
@@ -13,7 +14,7 @@ import moe_decode_quantized_gb300 as moe
 from moe_decode_quantized_gb300 import synth
 from moe_decode_quantized_gb300.workload import Workload, bf16_tensor
 
-from helpers import OUT_RTOL, decode_cfg, new_header, rel_inf, tiny_cfg, tiny_workload
+from helpers import decode_cfg, new_header, tiny_cfg, tiny_workload
 
 STATIC_WS_BYTES = 4 << 20
 
@@ -61,12 +62,20 @@ def _compare(cfg, wl, m, x0, r0):
     ref = _two_steps(with_ws, cfg, x0, r0, m)
     got = _two_steps(static, cfg, x0, r0, m)
     for (xr, rr, hr), (xg, rg, hg) in zip(ref, got):
-        assert torch.equal(hr, hg)  # picks, weights and slots exact
-        assert rel_inf(rg.cpu().numpy(), rr.cpu().numpy()) <= OUT_RTOL
-        xr32 = xr.view(torch.int16).to(torch.int32) << 16
-        xg32 = xg.view(torch.int16).to(torch.int32) << 16
-        assert rel_inf(xg32.view(torch.float32).cpu().numpy(), xr32.view(torch.float32).cpu().numpy()) <= OUT_RTOL
+        assert torch.equal(hr, hg)  # picks, weights and slots
+        assert torch.equal(rg, rr)  # the same kernels on the same inputs: bit for bit
+        assert torch.equal(xg, xr)
     assert moe.read_status(wl.ws) == 0
+
+    # no device allocation: with every buffer in place and the array set up by
+    # the calls above, further calls leave the device's free memory unchanged
+    x, res, xn, hdr = x0.clone(), r0.clone(), torch.empty_like(x0), new_header(cfg, m)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(4):
+        moe.layer_step_static(cfg, ly, wl.arena, x, res, xn, hdr, m, status)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
 
 
 @pytest.mark.gpu
