@@ -9,8 +9,9 @@ Default workload (one GPU): the single-token decode layer -- dim 4096, inter
 arena), top 6, bf16 router and bf16 shared expert -- stacked as 8 independent
 layers captured in one CUDA graph. A step is one replay: one token through the
 8 layers (865 MB of distinct weights, far above the 129 MB L2, so nothing is
-served from L2 between steps). value = token-layer steps per second over all
-ranks.
+served from L2 between steps); the steps take 64 distinct tokens in turn, so
+the picks change from step to step. value = token-layer steps per second over
+all ranks.
 
 Other workloads (--workload): batch8 (the same layers at m = 8 tokens),
 chain40 (40 stacked layers, one token, one replay = one 40-layer decode step;
@@ -47,6 +48,9 @@ WORKLOADS = {
     "batch8": (8, 8, "decode tokens/s per MoE layer step (1 GB300), m=8", "token-layer steps/s"),
     "chain40": (1, 40, "decode tokens/s, 40-layer MoE decode step (1 GB300)", "tokens/s"),
 }
+
+
+NX = 64  # distinct tokens the timed steps rotate through
 
 
 def decode_cfg(m, n_routed=384):
@@ -246,13 +250,17 @@ def run_ours(args):
     headers = torch.zeros(L * hw, dtype=torch.int32, device="cuda")
     graph = moe.Graph(cfg, layers, wl.arena, m, x_a, x_b, residual, headers, wl.ws)
     stream = torch.cuda.current_stream()
-    # every step is a new token: x restored from x0 and the residual zeroed
-    # before each replay (the synthetic layers carry no normalisation, so a
-    # residual carried from step to step would grow without bound)
-    x0 = x_a.clone()
+    # the steps rotate through NX distinct tokens held on the device: step i
+    # copies token i % NX into the graph's input and zeroes the residual before
+    # the replay (the synthetic layers carry no normalisation, so a residual
+    # carried from step to step would grow without bound), so routing and the
+    # picked slots vary from step to step
+    xs = torch.stack([x_tensor(rank, 1000 + i, m, cfg.dim) for i in range(NX)])
+    it = [0]
 
     def step():
-        x_a.copy_(x0)
+        x_a.copy_(xs[it[0] % NX])
+        it[0] += 1
         residual.zero_()
         graph.launch()
 
@@ -291,27 +299,28 @@ def run_ours(args):
     ne = float(np.mean(ne_list))
 
     # e2e: the same replays through the host-buffer C-ABI call (pinned buffers,
-    # H2D of the token's x and residual, D2H of x, residual and the headers)
-    xh = x0.cpu().pin_memory()  # the token's x and residual, the same each step
+    # H2D of the token's x and residual, D2H of x, residual and the headers),
+    # the tokens rotating through the same NX rows, here in host memory
+    xhs = xs.cpu().pin_memory()
     rh = torch.zeros_like(residual, device="cpu").pin_memory()
-    xo = torch.empty_like(xh).pin_memory()
+    xo = torch.empty_like(xhs[0]).pin_memory()
     ro = torch.empty_like(rh).pin_memory()
     hh = torch.zeros(L * hw, dtype=torch.int32).pin_memory()
-    for _ in range(max(1, args.warmup)):
-        graph.launch_host(xh, rh, xo, ro, hh)
+    for i in range(max(1, args.warmup)):
+        graph.launch_host(xhs[i % NX], rh, xo, ro, hh)
     torch.cuda.synchronize()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.perf_counter()
     e0.record(stream)
-    for _ in range(args.steps):
-        graph.launch_host(xh, rh, xo, ro, hh)
+    for i in range(args.steps):
+        graph.launch_host(xhs[i % NX], rh, xo, ro, hh)
     e1.record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     barrier(world)
     e_units, e_secs = aggregate(units_local, max(e0.elapsed_time(e1) / 1e3, wall), world)
-    h2d = xh.numel() * xh.element_size() + rh.numel() * rh.element_size()
+    h2d = xo.numel() * xo.element_size() + rh.numel() * rh.element_size()
     d2h = h2d + hh.numel() * 4
 
     # per-kernel durations (router+select, gate/up, down) with CUDA events on the
@@ -362,8 +371,8 @@ def run_ours(args):
                 "workload": f"{args.workload}: MoE decode layer dim 4096, inter 2048, {cfg.n_routed} routed experts top 6 "
                             f"(Q2_K gate/up, Q3_K down), bf16 router + bf16 shared expert, m={m}",
                 "layers_per_step": L, "tokens_per_layer_step": m, "graph": "CUDA graph, PDL-chained kernels",
-                "token": "a new token every step: x restored and the residual zeroed on the device inside the "
-                         "timed region (two copies a step)",
+                "token": f"{NX} distinct tokens in turn: step i copies token i % {NX} (resident on the device) "
+                         "into the graph's input and zeroes the residual inside the timed region (two copies a step)",
                 "l2": f"inputs larger than L2: {L} distinct layers, {L * layer_bytes / 1e6:.0f} MB per step",
                 "parallelism": f"replicas x{world}",
                 "distinct_experts_per_layer_step": ne,

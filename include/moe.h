@@ -80,16 +80,24 @@ typedef struct {
     uint64_t slot_bytes, gate_off, up_off, down_off;
 } moe_arena;
 
+/* Formats of the shared expert ([moe_v41] struct MoeV41LayerWeights: "bf16
+ * or the GGUF's Q2_K (w1, w3) / Q3_K (w2) blocks on the routed experts'
+ * kernels"). */
+#define MOE_SHARED_BF16 0   /* w1, w3 bf16 [inter, dim]; w2 bf16 [dim, inter]   */
+#define MOE_SHARED_KQUANT 1 /* w1, w3 Q2_K [inter, dim]; w2 Q3_K [dim, inter],
+                               laid out as a routed expert's gate, up, down   */
+
 /* One layer's resident weights ([moe_v41] struct MoeV41LayerWeights), all
  * device pointers: router_w bf16 [n_routed, dim] row-major; bias f32
  * [n_routed]; slot_row i32 [n_routed] (this layer's slot-table row, -1 = not
- * resident); sh_w1, sh_w3 bf16 [inter, dim] and sh_w2 bf16 [dim, inter] (the
- * shared expert; all three NULL = no shared expert). 16-byte aligned. */
+ * resident); sh_w1, sh_w3, sh_w2 the shared expert in format sh_format
+ * (MOE_SHARED_*; all three NULL = no shared expert). 16-byte aligned. */
 typedef struct {
     const void *router_w;
     const float *bias;
     const int32_t *slot_row;
     const void *sh_w1, *sh_w3, *sh_w2;
+    int32_t sh_format;
 } moe_layer;
 
 /* Words (int32) of the route header for m tokens. Layout, k = topk:
@@ -179,7 +187,10 @@ int moe_swiglu_q8(const moe_cfg *cfg, const float *g_dev, const float *u_dev, in
 
 /* One whole MoE layer step for m tokens ([moe_v41] module doc and fn
  * shared_side; [route] module doc): router logits, selection, routed experts,
- * the bf16 shared expert (gs, us = W1 x, W3 x; hs = bf16(SwiGLU); sd = W2 hs),
+ * the shared expert (bf16: gs, us = W1 x, W3 x; hs = bf16(SwiGLU); sd = W2 hs;
+ * K-quant: gs, us = Q2_K(W1, W3) . q8_1(x), hs = SwiGLU in f32, sd =
+ * Q3_K(W2) . q8_1(hs), as a routed expert of weight 1 -- [moe_v41] struct
+ * MoeV41 sh_q8),
  * acc = routed sum (ascending id) + sd added last, residual += acc,
  * x_next = bf16 round-to-nearest-even of residual ([moe_v41] fn bf16_bytes).
  * Launched as three kernels chained with programmatic dependent launch.

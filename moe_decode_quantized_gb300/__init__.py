@@ -21,6 +21,8 @@ MOE_HDR_NONFINITE = 2
 MOE_WS_TIMEOUT = 1
 MOE_WS_PLAN = 2
 MOE_WS_TRIPLE = 4
+MOE_SHARED_BF16 = 0
+MOE_SHARED_KQUANT = 1
 SLOT_TABLE_LAYERS = 64
 
 __all__ = ["Config", "Arena", "Layer", "MoeError", "header_words", "workspace_bytes",
@@ -96,17 +98,20 @@ class Arena:
 
 @dataclass
 class Layer:
-    """One layer's resident weights (page spark_model/layers/moe_v41.rs, MoeV41LayerWeights)."""
+    """One layer's resident weights (page spark_model/layers/moe_v41.rs, MoeV41LayerWeights).
+    sh_format: MOE_SHARED_BF16 (bf16 w1, w3, w2) or MOE_SHARED_KQUANT (Q2_K w1,
+    w3 and Q3_K w2 blocks, laid out as a routed expert's gate, up, down)."""
     router_w: object
     bias: object
     slot_row: object
     sh_w1: object = None
     sh_w3: object = None
     sh_w2: object = None
+    sh_format: int = 0
 
     def c(self) -> _lib.MoeLayer:
         return _lib.MoeLayer(_ptr(self.router_w), _ptr(self.bias), _ptr(self.slot_row), _ptr(self.sh_w1),
-                             _ptr(self.sh_w3), _ptr(self.sh_w2))
+                             _ptr(self.sh_w3), _ptr(self.sh_w2), int(self.sh_format))
 
 
 def header_words(cfg: Config, m: int) -> int:

@@ -32,7 +32,7 @@ class MoeArena(C.Structure):
 
 class MoeLayer(C.Structure):
     _fields_ = [("router_w", P), ("bias", P), ("slot_row", P), ("sh_w1", P), ("sh_w3", P),
-                ("sh_w2", P)]
+                ("sh_w2", P), ("sh_format", C.c_int32)]
 
 
 class MoeWsView(C.Structure):

@@ -155,7 +155,8 @@ int stages_fit(size_t fixed, uint32_t stage, int cap, size_t limit)
     return S;
 }
 
-int geometry(const moe_cfg &c, int m, bool shared, const DevInfo &I, Geo &G)
+// sk: the shared expert's kind (0 none, 1 bf16, 2 K-quant)
+int geometry(const moe_cfg &c, int m, int sk, const DevInfo &I, Geo &G)
 {
     const int n = c.n_routed, dim = c.dim, inter = c.inter, k = c.topk;
     const size_t limit = (size_t)I.smem_optin;
@@ -166,23 +167,27 @@ int geometry(const moe_cfg &c, int m, bool shared, const DevInfo &I, Geo &G)
     G.r_grid = (n + G.r_rows - 1) / G.r_rows;
     G.r_smem = router_smem(G.r_rows, dim, m, c.n_routed);
     G.grid = I.sms;
-    // gate/up: stages of max(one Q2_K task, one shared W1 or W3 row, one W2 row);
-    // w2r W2 rows a task, as many as a stage holds (<= 4, dividing dim)
+    // gate/up: stages of max(one Q2_K task, one bf16 shared W1 or W3 row, one
+    // bf16 W2 row); w2r bf16 W2 rows a task, as many as a stage holds (<= 4,
+    // dividing dim). K-quant shared tasks are a routed task's size (W1, W3)
+    // or a down task's (W2)
     size_t gst = (size_t)MOE_G_TASK_SB * MOE_Q2K_BYTES;
-    if (shared)
+    if (sk == 1)
         gst = std::max(gst, std::max((size_t)dim * 2, (size_t)inter * 2));
+    if (sk == 2)
+        gst = std::max(gst, (size_t)MOE_D_TASK_SB * MOE_Q3K_BYTES);
     G.g_stage = (uint32_t)align_up(gst, 128);
     G.w2r = 1;
-    while (shared && G.w2r < 4 && (size_t)G.w2r * 2 * inter * 2 <= G.g_stage && dim % (G.w2r * 2) == 0)
+    while (sk == 1 && G.w2r < 4 && (size_t)G.w2r * 2 * inter * 2 <= G.g_stage && dim % (G.w2r * 2) == 0)
         G.w2r *= 2;
     // bf16 x and hs in shared memory for up to two tokens; beyond, the ring
     // keeps the room and the consumers read them from L2
     G.stage_x = g_stage_x(m);
     size_t g_fixed = align_up((size_t)m * act_row_bytes(dim), 128) +
-                     (G.stage_x ? align_up((size_t)m * dim * 2, 128) : 0) +
-                     (shared && G.stage_x ? align_up((size_t)m * inter * 2, 128) : 0) + g_pair_bytes(shared);
+                     (G.stage_x ? align_up((size_t)m * dim * 2, 128) : 0) + g_hs_bytes(m, inter, sk, G.stage_x) +
+                     g_pair_bytes(sk);
     G.g_S = stages_fit(g_fixed, G.g_stage, 32, limit);
-    G.g_smem = g_smem_bytes(G.g_S, m, dim, inter, shared, G.stage_x, G.g_stage);
+    G.g_smem = g_smem_bytes(G.g_S, m, dim, inter, sk, G.stage_x, G.g_stage);
     // down: stages of one Q3_K task (the shared expert is done by the gate/up kernel)
     G.d_stage = (uint32_t)align_up((size_t)MOE_D_TASK_SB * MOE_Q3K_BYTES, 128);
     const int tpr = dim / down_rows_per_task(inter);
@@ -222,7 +227,7 @@ struct Bufs {
     float *plan_w;
     int32_t *plan_rows;
     unsigned long long *ptrs;
-    float *g, *u, *h, *gs, *us, *down, *sd, *acc;
+    float *g, *u, *h, *gs, *us, *hsf, *down, *sd, *acc;
     uint16_t *hs;
     uint32_t *ctrl, *rgcnt;
 };
@@ -246,6 +251,7 @@ Bufs ws_bufs(const moe_cfg &c, void *ws)
     B.gs = reinterpret_cast<float *>(b + L.gs);
     B.us = reinterpret_cast<float *>(b + L.us);
     B.hs = reinterpret_cast<uint16_t *>(b + L.hs);
+    B.hsf = reinterpret_cast<float *>(b + L.hsf);
     B.down = reinterpret_cast<float *>(b + L.down);
     B.sd = reinterpret_cast<float *>(b + L.sd);
     B.acc = reinterpret_cast<float *>(b + L.acc);
@@ -290,7 +296,7 @@ int check_arena(const moe_arena *ar)
 // prologue reads x before its own wait).
 int launch_experts(const moe_cfg &c, int m, const Geo &G, const Bufs &B, const uint16_t *x,
                    const unsigned long long *ptrs, const float *plan_w, const int32_t *plan_rows,
-                   const int32_t *hdr, const uint16_t *w1, const uint16_t *w3, const uint16_t *w2,
+                   const int32_t *hdr, int sk, const void *w1, const void *w3, const void *w2,
                    float *acc, float *residual, uint16_t *x_next, cudaStream_t s, bool pdl_gateup,
                    cudaEvent_t *ev = nullptr, bool plan_hint = false)
 {
@@ -300,7 +306,9 @@ int launch_experts(const moe_cfg &c, int m, const Geo &G, const Bufs &B, const u
     ga.w1 = w1;
     ga.w3 = w3;
     ga.w2 = w2;
+    ga.sk = sk;
     ga.hs = B.hs;
+    ga.hsf = B.hsf;
     ga.sd = B.sd;
     ga.limit = c.swiglu_limit;
     ga.wait_ns = g_wait_ns.load();
@@ -370,9 +378,9 @@ int layer_step(const moe_cfg &c, const moe_layer &ly, const moe_arena &ar, const
     int rc = dev_info(&I);
     if (rc)
         return rc;
-    const bool shared = ly.sh_w1 != nullptr;
+    const int sk = ly.sh_w1 == nullptr ? 0 : (ly.sh_format == MOE_SHARED_KQUANT ? 2 : 1);
     Geo G;
-    if ((rc = geometry(c, m, shared, *I, G)))
+    if ((rc = geometry(c, m, sk, *I, G)))
         return rc;
     const Bufs B = ws_bufs(c, ws);
     RouteArgs ra = route_args(c, m);
@@ -398,9 +406,8 @@ int layer_step(const moe_cfg &c, const moe_layer &ly, const moe_arena &ar, const
         return rc;
     if (ev)
         CUDA_OK(cudaEventRecord(ev[1], s));
-    return launch_experts(c, m, G, B, static_cast<const uint16_t *>(x), B.ptrs, B.plan_w, B.plan_rows, hdr,
-                          static_cast<const uint16_t *>(ly.sh_w1), static_cast<const uint16_t *>(ly.sh_w3),
-                          static_cast<const uint16_t *>(ly.sh_w2), B.acc, residual,
+    return launch_experts(c, m, G, B, static_cast<const uint16_t *>(x), B.ptrs, B.plan_w, B.plan_rows, hdr, sk,
+                          ly.sh_w1, ly.sh_w3, ly.sh_w2, B.acc, residual,
                           static_cast<uint16_t *>(x_next), s, pdl, ev ? ev + 2 : nullptr);
 }
 
@@ -413,6 +420,8 @@ int check_layer(const moe_cfg &c, const moe_layer *ly)
         return fail(MOE_EINVAL, "shared expert: sh_w1, sh_w3 and sh_w2 must be all set or all NULL");
     if (!aligned16(ly->router_w) || (all && (!aligned16(ly->sh_w1) || !aligned16(ly->sh_w3) || !aligned16(ly->sh_w2))))
         return fail(MOE_EINVAL, "router and shared-expert weights must be 16-byte aligned");
+    if (ly->sh_format != MOE_SHARED_BF16 && ly->sh_format != MOE_SHARED_KQUANT)
+        return fail(MOE_EINVAL, "sh_format (%d) must be MOE_SHARED_BF16 or MOE_SHARED_KQUANT", ly->sh_format);
     (void)c;
     return MOE_OK;
 }
@@ -555,11 +564,11 @@ int moe_expert_step_unreleased(const moe_cfg *cfg, const void *x, const int32_t 
     if ((rc = dev_info(&I)))
         return rc;
     Geo G;
-    if ((rc = geometry(*cfg, m, false, *I, G)))
+    if ((rc = geometry(*cfg, m, 0, *I, G)))
         return rc;
     const Bufs B = ws_bufs(*cfg, ws);
     return launch_experts(*cfg, m, G, B, static_cast<const uint16_t *>(x), B.ptrs, B.plan_w, B.plan_rows, header,
-                          nullptr, nullptr, nullptr, B.acc, nullptr, nullptr, (cudaStream_t)stream, false, nullptr,
+                          0, nullptr, nullptr, nullptr, B.acc, nullptr, nullptr, (cudaStream_t)stream, false, nullptr,
                           true);
 }
 
@@ -577,7 +586,7 @@ int moe_router_logits(const moe_cfg *cfg, const void *x, const void *w, float *l
     if ((rc = dev_info(&I)))
         return rc;
     Geo G;
-    if ((rc = geometry(*cfg, m, false, *I, G)))
+    if ((rc = geometry(*cfg, m, 0, *I, G)))
         return rc;
     RouteArgs a = route_args(*cfg, m);
     a.x = static_cast<const uint16_t *>(x);
@@ -686,11 +695,11 @@ int moe_expert_step(const moe_cfg *cfg, const void *x, const uint64_t *ptrs, con
     if ((rc = dev_info(&I)))
         return rc;
     Geo G;
-    if ((rc = geometry(*cfg, m, false, *I, G)))
+    if ((rc = geometry(*cfg, m, 0, *I, G)))
         return rc;
     const Bufs B = ws_bufs(*cfg, ws);
     return launch_experts(*cfg, m, G, B, static_cast<const uint16_t *>(x),
-                          reinterpret_cast<const unsigned long long *>(ptrs), plan_w, plan_rows, header, nullptr,
+                          reinterpret_cast<const unsigned long long *>(ptrs), plan_w, plan_rows, header, 0, nullptr,
                           nullptr, nullptr, acc, nullptr, nullptr, (cudaStream_t)stream, false);
 }
 

@@ -43,7 +43,8 @@ namespace moe {
 // ------------------------------------------------------------------ layout
 
 struct WsLayout {
-    size_t ctrl, rgcnt, logits, scores, keys, plan_w, plan_rows, ptrs, g, u, h, gs, us, hs, down, sd, acc, total;
+    size_t ctrl, rgcnt, logits, scores, keys, plan_w, plan_rows, ptrs, g, u, h, gs, us, hs, hsf, down, sd, acc,
+        total;
 };
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -73,6 +74,7 @@ inline WsLayout ws_layout(const moe_cfg &c)
     L.gs = take(sizeof(float) * M * c.inter);
     L.us = take(sizeof(float) * M * c.inter);
     L.hs = take(sizeof(uint16_t) * M * c.inter);  // bf16 SwiGLU of the shared expert
+    L.hsf = take(sizeof(float) * M * c.inter);    // f32 SwiGLU of a K-quant shared expert
     L.down = take(sizeof(float) * cap * c.dim);
     L.sd = take(sizeof(float) * M * c.dim);
     L.acc = take(sizeof(float) * M * c.dim);

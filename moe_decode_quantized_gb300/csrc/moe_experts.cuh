@@ -38,7 +38,8 @@
 namespace moe {
 
 struct __align__(16) Task {
-    int kind;   // 0 end, 1 routed, 2 shared W1 or W3 row (gate/up), 3 shared W2 rows (gate/up)
+    int kind;   // 0 end, 1 routed; gate/up kernel, shared expert: bf16 2 W1 or W3 row, 3 W2 rows;
+                // K-quant 4 W1 and W3 rows, 5 W2 rows
     int p;      // plan expert (routed); 0 W1, 1 W3 (shared row)
     int row;    // first row (routed) or the row (shared)
     int pair0, npair;
@@ -478,14 +479,16 @@ __device__ __forceinline__ void cache_plan(const Ring &r, const int32_t *hdr, in
 
 struct GArgs {
     const uint16_t *x;                 // bf16 [m, dim]
-    const uint16_t *w1, *w3;           // shared expert bf16 [inter, dim] (NULL: none)
-    const uint16_t *w2;                // shared expert bf16 [dim, inter]
+    const void *w1, *w3;               // shared expert [inter, dim], bf16 or Q2_K (NULL: none)
+    const void *w2;                    // shared expert [dim, inter], bf16 or Q3_K
+    int sk;                            // shared expert: 0 none, 1 bf16, 2 Q2_K / Q3_K
     const int32_t *hdr;                // route header (plan tail at plan_off)
     const unsigned long long *ptrs;    // [3][cap]
     const int32_t *plan_rows;          // [cap]
     float *g, *u, *h;                  // [cap, inter]: h = SwiGLU(g, u)
     float *gs, *us;                    // [m, inter]
-    uint16_t *hs;                      // [m, inter] bf16(SwiGLU(gs, us))
+    uint16_t *hs;                      // [m, inter] bf16(SwiGLU(gs, us)) (bf16 shared expert)
+    float *hsf;                        // [m, inter] SwiGLU(gs, us) (K-quant shared expert)
     float *sd;                         // [m, dim] W2 hs
     uint32_t *status;
     // [0] shared row-task counter, [1] routed-task counter, [2] exit ticket,
@@ -519,27 +522,37 @@ struct PairCell {
 };
 #define MOE_PAIR_CELLS 32  // more than the pairs one ring holds
 static_assert(MOE_G_CHUNK % 2 == 0, "a chunk holds whole shared-row pairs");
-__host__ __device__ inline size_t g_pair_bytes(bool shared)
+// sk: the shared expert's kind (0 none, 1 bf16, 2 K-quant). The hs area holds
+// bf16 hs (staged, bf16) or q8_1(hs) in the activation layout (K-quant).
+__host__ __device__ inline size_t g_pair_bytes(int sk)
 {
-    return shared ? align_up(sizeof(PairCell) * MOE_PAIR_CELLS, 128) : 0;
+    return sk == 1 ? align_up(sizeof(PairCell) * MOE_PAIR_CELLS, 128) : 0;
 }
-__host__ __device__ inline size_t g_pair_off(int S, int m, int dim, int inter, bool shared, bool stage)
+__host__ __device__ inline size_t g_hs_bytes(int m, int inter, int sk, bool stage)
 {
-    return g_hs_off(S, m, dim, stage) + (shared && stage ? align_up((size_t)m * inter * 2, 128) : 0);
+    if (sk == 2)
+        return align_up((size_t)m * act_row_bytes(inter), 128);
+    return sk == 1 && stage ? align_up((size_t)m * inter * 2, 128) : 0;
 }
-__host__ __device__ inline size_t g_stage_off(int S, int m, int dim, int inter, bool shared, bool stage)
+__host__ __device__ inline size_t g_pair_off(int S, int m, int dim, int inter, int sk, bool stage)
 {
-    return g_pair_off(S, m, dim, inter, shared, stage) + g_pair_bytes(shared);
+    return g_hs_off(S, m, dim, stage) + g_hs_bytes(m, inter, sk, stage);
 }
-__host__ __device__ inline size_t g_smem_bytes(int S, int m, int dim, int inter, bool shared, bool stage,
+__host__ __device__ inline size_t g_stage_off(int S, int m, int dim, int inter, int sk, bool stage)
+{
+    return g_pair_off(S, m, dim, inter, sk, stage) + g_pair_bytes(sk);
+}
+__host__ __device__ inline size_t g_smem_bytes(int S, int m, int dim, int inter, int sk, bool stage,
                                                uint32_t stage_bytes)
 {
-    return g_stage_off(S, m, dim, inter, shared, stage) + (size_t)S * stage_bytes + 16;
+    return g_stage_off(S, m, dim, inter, sk, stage) + (size_t)S * stage_bytes + 16;
 }
 
 // The producer warp: waits (bounded) until every hs row of the shared
-// expert is done grid-wide, copies hs into shared memory and raises the CTA's
-// flag (2 instead of 1 after a timeout, so that no consumer waits forever).
+// expert is done grid-wide, copies hs into shared memory (bf16) or builds
+// q8_1(hs) there (K-quant: four lanes a block, as the activation of the
+// Q3_K W2 rows), and raises the CTA's flag (2 instead of 1 after a timeout,
+// so that no consumer waits forever).
 __device__ bool g_load_hs(const GArgs &a, const Ring &ring, uint16_t *hs_s, int lane)
 {
     const uint32_t target = (uint32_t)a.inter;
@@ -557,7 +570,21 @@ __device__ bool g_load_hs(const GArgs &a, const Ring &ring, uint16_t *hs_s, int 
     }
     // every lane polled itself: its loads below come after its own acquire
     // (unstaged, the consumers read hs from L2 once the flag is up)
-    const int n16 = a.stage_x ? a.m * a.inter / 8 : 0;
+    if (a.sk == 2) {
+        // m * inter / 8 lane items (a multiple of 32): the whole warp calls
+        // q8_block_quad together
+        uint8_t *hact = reinterpret_cast<uint8_t *>(hs_s);
+        const int nbi = a.inter / MOE_QK, bpr = a.inter / 32;
+        const size_t arow = act_row_bytes(a.inter);
+        for (int i = lane; i < a.m * a.inter / 8; i += 32) {
+            const int b = i >> 2, sub = i & 3, t = b / bpr, bi = b - t * bpr;
+            const float4 *h4 = reinterpret_cast<const float4 *>(a.hsf + (size_t)t * a.inter + bi * 32 + 8 * sub);
+            const float4 p = __ldcg(h4), q = __ldcg(h4 + 1);
+            const float v[8] = {p.x, p.y, p.z, p.w, q.x, q.y, q.z, q.w};
+            q8_block_quad(v, sub, hact + t * arow, nbi, bi, false);
+        }
+    }
+    const int n16 = a.stage_x && a.sk == 1 ? a.m * a.inter / 8 : 0;
     const uint4 *src = reinterpret_cast<const uint4 *>(a.hs);
     uint4 *dst = reinterpret_cast<uint4 *>(hs_s);
     for (int i0 = lane; i0 < n16; i0 += 32 * 8) {
@@ -582,22 +609,24 @@ __device__ bool g_load_hs(const GArgs &a, const Ring &ring, uint16_t *hs_s, int 
 __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
-    const bool shared = a.w1 != nullptr;
+    const bool shared = a.sk != 0, kq = a.sk == 2;
     const bool stage = a.stage_x != 0;
-    const Ring ring = ring_carve(smem, a.S, a.stage_bytes, g_stage_off(a.S, a.m, a.dim, a.inter, shared, stage), a.wait_ns);
+    const Ring ring = ring_carve(smem, a.S, a.stage_bytes, g_stage_off(a.S, a.m, a.dim, a.inter, a.sk, stage), a.wait_ns);
     uint8_t *act = smem + g_act_off(a.S);
     uint16_t *xs = reinterpret_cast<uint16_t *>(smem + g_xs_off(a.S, a.m, a.dim));  // staged only
-    uint16_t *hs_s = reinterpret_cast<uint16_t *>(smem + g_hs_off(a.S, a.m, a.dim, stage));  // staged only
-    PairCell *cells = reinterpret_cast<PairCell *>(smem + g_pair_off(a.S, a.m, a.dim, a.inter, shared, stage));
+    uint16_t *hs_s = reinterpret_cast<uint16_t *>(smem + g_hs_off(a.S, a.m, a.dim, stage));  // staged (bf16) or q8_1 (K-quant)
+    PairCell *cells = reinterpret_cast<PairCell *>(smem + g_pair_off(a.S, a.m, a.dim, a.inter, a.sk, stage));
     // 16-byte chunk i of bf16 x / of hs: shared memory when staged, else L2
     // (kStage: the staging of the token count g_stage_x, known where M is)
     const uint4 *x4s = reinterpret_cast<const uint4 *>(xs), *x4g = reinterpret_cast<const uint4 *>(a.x);
     const uint4 *h4s = reinterpret_cast<const uint4 *>(hs_s), *h4g = reinterpret_cast<const uint4 *>(a.hs);
+    const uint8_t *hact = reinterpret_cast<const uint8_t *>(hs_s);  // K-quant: q8_1(hs) rows
+    const int nbi = a.inter / MOE_QK;  // super-blocks of a W2 (K-quant) row
     auto ldx = [&](size_t i) { return stage ? x4s[i] : __ldcg(x4g + i); };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int dim = a.dim, inter = a.inter, nb = dim / MOE_QK;
     const size_t arow = act_row_bytes(dim);
-    if (shared && threadIdx.x < MOE_PAIR_CELLS)
+    if (a.sk == 1 && threadIdx.x < MOE_PAIR_CELLS)
         cells[threadIdx.x].cnt = 0;
     ring_init(ring);
     __syncthreads();
@@ -614,16 +643,19 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
         bool ok = true;
         int w2_pending = -1;  // W2 left for after the routed work: a chunk taken, or -2 (none taken)
         bool have_hs = false;
+        // W2 tasks: w2r bf16 rows, or (K-quant) the Q3_K rows of 64 super-blocks
+        const int w2rows = kq ? down_rows_per_task(inter) : a.w2r;
+        const uint32_t w2bytes = kq ? (uint32_t)(w2rows * nbi * MOE_Q3K_BYTES) : (uint32_t)a.w2r * inter * 2u;
         auto issue_w2 = [&](int c0, int c1) {
             for (int b = c0; b < c1 && ok; b += P) {
                 const int j = b + lane;
                 bool mine = true;
                 if (issuer && j < c1) {
                     Task t{};
-                    t.kind = 3;
-                    t.row = j * a.w2r;
-                    mine = ring_issue(ring, base + (j - c0), t, a.w2 + (size_t)t.row * inter,
-                                      (uint32_t)a.w2r * inter * 2u, pol, a.status);
+                    t.kind = kq ? 5 : 3;
+                    t.row = j * w2rows;
+                    mine = ring_issue(ring, base + (j - c0), t, static_cast<const char *>(a.w2) + (size_t)j * w2bytes,
+                                      w2bytes, pol, a.status);
                 }
                 ok = __all_sync(0xffffffffu, mine);
             }
@@ -631,12 +663,16 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
         };
         if (shared) {
             // The shared expert depends only on x: all of it runs before the
-            // wait. (1) Rows: task 2i is W1 row i, task 2i + 1 is W3 row i (one
-            // row a stage, so the stages fit the routed tasks); of the two
-            // consumers of row i the one that finishes second writes
+            // wait. (1) Rows. bf16: task 2i is W1 row i, task 2i + 1 is W3 row
+            // i (one row a stage, so the stages fit the routed tasks); of the
+            // two consumers of row i the one that finishes second writes
             // hs[i] = bf16(SwiGLU). pair0 carries the CTA's pair sequence
-            // number (its meeting cell).
-            const int nsh = 2 * inter;
+            // number (its meeting cell). K-quant: task i is rows rt i .. of
+            // W1 and the same rows of W3 (Q2_K, as a routed task), whose
+            // consumer writes gs, us and hs = SwiGLU for every token.
+            const int rt = gate_rows_per_task(dim);
+            const uint32_t kbytes = (uint32_t)(rt * nb * MOE_Q2K_BYTES);
+            const int nsh = kq ? inter / rt : 2 * inter;
             int pseq = 0;
             unsigned nxt = 0;
             if (lane == 0)
@@ -651,13 +687,21 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
                 for (int b = c0; b < c1 && ok; b += P) {
                     const int j = b + lane;
                     bool mine = true;
-                    if (issuer && j < c1) {
+                    if (issuer && j < c1 && kq) {
+                        Task t{};
+                        t.kind = 4;
+                        t.row = j * rt;
+                        mine = ring_issue(ring, base + (j - c0), t, static_cast<const char *>(a.w1) + (size_t)j * kbytes,
+                                          kbytes, pol, a.status,
+                                          static_cast<const char *>(a.w3) + (size_t)j * kbytes, kbytes);
+                    } else if (issuer && j < c1) {
                         Task t{};
                         t.kind = 2;
                         t.row = j >> 1;
                         t.p = j & 1;  // 0: W1 (gate), 1: W3 (up)
                         t.pair0 = pseq + ((j - c0) >> 1);
-                        mine = ring_issue(ring, base + (j - c0), t, (t.p ? a.w3 : a.w1) + (size_t)t.row * dim,
+                        mine = ring_issue(ring, base + (j - c0), t,
+                                          static_cast<const uint16_t *>(t.p ? a.w3 : a.w1) + (size_t)t.row * dim,
                                           (uint32_t)dim * 2u, pol, a.status);
                     }
                     ok = __all_sync(0xffffffffu, mine);
@@ -665,13 +709,14 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
                 base += c1 - c0;
                 pseq += (c1 - c0) >> 1;
             }
-            // (2) W2, w2r rows a task, against hs. This warp polls (bounded)
-            // two words: every hs row done grid-wide -> it loads hs into
-            // shared memory and issues W2; the selection's plan-ready hint ->
+            // (2) W2 against hs. This warp polls (bounded) two words: every
+            // hs row done grid-wide -> it loads hs into shared memory (bf16)
+            // or builds q8_1(hs) there (K-quant) and issues W2; the
+            // selection's plan-ready hint ->
             // the routed work goes first and W2 (or its rest) after it. No W2
             // task is issued before hs is in shared memory, so nothing queued
             // ahead of a routed task ever waits.
-            const int nw2 = dim / a.w2r;
+            const int nw2 = dim / w2rows;
             {
                 const uint64_t t0 = globaltimer();
                 for (;;) {
@@ -785,7 +830,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
         if (w2_pending != -1) {
             // the rest of W2, hs first if it is not in shared memory yet (the
             // routed tasks ahead of it never wait)
-            const int nw2 = dim / a.w2r;
+            const int nw2 = dim / w2rows;
             if (!have_hs)
                 g_load_hs(a, ring, hs_s, lane);
             int c0 = w2_pending;
@@ -941,9 +986,51 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
                     }
                 }
             });
+        } else if (t.kind == 4) {
+            // K-quant shared rows t.row .. t.row + rt of W1, then the same rows
+            // of W3 (Q2_K, lanes laid out as in a routed task), for every
+            // token: gs, us and hs = SwiGLU(gs, us) in f32; then the task's
+            // rows are counted done grid-wide (release, after every lane's
+            // stores)
+            constexpr int PER = MOE_G_TASK_SB / 32;
+            const int blk = lane % nb;
+#pragma unroll 1
+            for (int tt = 0; tt < a.m; ++tt) {
+                const uint8_t *xr = act + tt * arow;
+                const int4 *xq = reinterpret_cast<const int4 *>(xr + blk * MOE_SEG_Q_BYTES);
+                const float4 *rec = reinterpret_cast<const float4 *>(xr + nb * MOE_SEG_Q_BYTES) +
+                                    blk * (MOE_SEG_REC_FLOATS / 4);
+                float v[PER];
+#pragma unroll
+                for (int q = 0; q < PER; ++q)
+                    v[q] = q2k_dot(reinterpret_cast<const uint32_t *>(st + (size_t)(lane + 32 * q) * MOE_Q2K_BYTES),
+                                   xq, rec);
+                for (int o = nb >> 1; o > 0; o >>= 1) {
+#pragma unroll
+                    for (int q = 0; q < PER; ++q)
+                        v[q] += __shfl_xor_sync(0xffffffffu, v[q], o);
+                }
+                if (blk == 0) {
+                    const size_t o = (size_t)tt * inter + t.row;
+#pragma unroll
+                    for (int q = 0; q < PER / 2; ++q) {
+                        const int r = (lane + 32 * q) / nb;
+                        a.gs[o + r] = v[q];
+                        a.us[o + r] = v[q + PER / 2];
+                        a.hsf[o + r] = swiglu_f32(v[q], v[q + PER / 2], a.limit);
+                    }
+                }
+            }
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&ring.empty[slot]);
+                red_add_release_gpu(a.gctr + 4, (unsigned)gate_rows_per_task(dim));
+            }
         } else {
-            // w2r rows of W2 against every token's hs (in shared memory once
-            // the producer has loaded it)
+            // W2 rows against every token's hs: bf16 (staged or from L2), or
+            // (K-quant) Q3_K against q8_1(hs), both in shared memory once the
+            // producer has them there
             if (!hs_seen) {
                 if (lane == 0) {
                     volatile int *f = &ring.pc->hs_ready;
@@ -961,6 +1048,36 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
                 }
                 __syncwarp();
                 hs_seen = true;
+            }
+            if (t.kind == 5) {
+                // 64 Q3_K super-blocks: rows t.row .. of W2, lanes laid out as
+                // in a down task, one token at a time
+                constexpr int PER = MOE_D_TASK_SB / 32;
+                const int blk = lane % nbi;
+                const size_t arow_i = act_row_bytes(inter);
+#pragma unroll 1
+                for (int tt = 0; tt < a.m; ++tt) {
+                    const uint8_t *xr = hact + tt * arow_i;
+                    const int4 *xq = reinterpret_cast<const int4 *>(xr + blk * MOE_SEG_Q_BYTES);
+                    const float4 *rec = reinterpret_cast<const float4 *>(xr + nbi * MOE_SEG_Q_BYTES) +
+                                        blk * (MOE_SEG_REC_FLOATS / 4);
+                    float v[PER];
+                    q3k_dot_multi<PER>(st, lane, xq, rec, v);
+                    for (int o = nbi >> 1; o > 0; o >>= 1) {
+#pragma unroll
+                        for (int q = 0; q < PER; ++q)
+                            v[q] += __shfl_xor_sync(0xffffffffu, v[q], o);
+                    }
+                    if (blk == 0) {
+#pragma unroll
+                        for (int q = 0; q < PER; ++q)
+                            a.sd[(size_t)tt * dim + t.row + (lane + 32 * q) / nbi] = v[q];
+                    }
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&ring.empty[slot]);
+                continue;
             }
             with_m(a.m, [&](auto MC) {
                 constexpr int M = decltype(MC)::value;

@@ -89,7 +89,7 @@ def lib():
             L.orc_shared_token.argtypes = [C.POINTER(Cfg), P, P, P, P, P, P, P, P, C.c_int]
             L.orc_layer.restype = C.c_int
             L.orc_layer.argtypes = [C.POINTER(Cfg), C.c_int, P, P, P, P, C.c_uint64, C.c_uint64,
-                                    C.c_uint64, P, P, P, P, P, P, P, P, P, P, P, C.c_int]
+                                    C.c_uint64, P, P, P, C.c_int, P, P, P, P, P, P, P, P, C.c_int]
             _lib = L
     return _lib
 
@@ -298,11 +298,13 @@ def shared_token(c: Cfg, w1, w3, w2, x_bf16, threads: int = 1):
 
 
 def layer(c: Cfg, x_bf16, router_w, bias, experts: dict, offsets, shared=None, residual=None,
-          threads: int = 1):
+          threads: int = 1, shared_kquant: bool = False):
     """One layer step over m tokens.
 
     experts: {expert id: slot image (uint8)}; offsets = (gate_off, up_off, down_off);
-    shared = (w1, w3, w2) bf16 bit arrays or None; residual f32 (m, dim) (default zeros).
+    shared = (w1, w3, w2) bf16 bit arrays, or with shared_kquant the Q2_K w1,
+    w3 and Q3_K w2 blocks as uint8 arrays, or None; residual f32 (m, dim)
+    (default zeros).
     Returns dict(logits, picks, weights, flags, acc, sd, residual, x_next).
     """
     x = _u16(x_bf16)
@@ -320,12 +322,12 @@ def layer(c: Cfg, x_bf16, router_w, bias, experts: dict, offsets, shared=None, r
     acc = np.zeros((m, c.dim), np.float32)
     sd = np.zeros((m, c.dim), np.float32)
     if shared is not None:
-        w1, w3, w2 = (_u16(a) for a in shared)
+        w1, w3, w2 = (_u8(a) if shared_kquant else _u16(a) for a in shared)
     else:
         w1 = w3 = w2 = None
     rc = lib().orc_layer(C.byref(c), m, _p(x), _p(w), _p(b), C.cast(table, C.c_void_p),
                          int(offsets[0]), int(offsets[1]), int(offsets[2]), _p(w1), _p(w3), _p(w2),
-                         _p(res), _p(xn), _p(logits), _p(picks), _p(weights), _p(flags), _p(acc),
+                         int(bool(shared_kquant)), _p(res), _p(xn), _p(logits), _p(picks), _p(weights), _p(flags), _p(acc),
                          _p(sd), threads)
     if rc != 0:
         raise KeyError("oracle layer: a picked expert has no host image")

@@ -678,7 +678,8 @@ void orc_shared_token(const orc_cfg *c, const uint16_t *w1, const uint16_t *w3,
 
 /* -------------------------------------------------------------------- layer */
 
-/* One MoE layer step:
+/* One MoE layer step (sh_kquant: the shared expert's w1, w3 are Q2_K and w2
+ * Q3_K blocks, passed through the uint16_t pointers as raw bytes):
  *   logits, picks, weights as above; per token the plan = its picks in
  *   ascending expert id (moe_v41/device_route.rs, fn device_route_check:
  *   plan weights in ascending id);
@@ -689,7 +690,7 @@ void orc_shared_token(const orc_cfg *c, const uint16_t *w1, const uint16_t *w3,
 int orc_layer(const orc_cfg *c, int m, const uint16_t *x, const uint16_t *router_w,
               const float *bias, const uint8_t *const *experts, uint64_t gate_off,
               uint64_t up_off, uint64_t down_off, const uint16_t *sh_w1,
-              const uint16_t *sh_w3, const uint16_t *sh_w2, float *residual,
+              const uint16_t *sh_w3, const uint16_t *sh_w2, int sh_kquant, float *residual,
               uint16_t *x_next, float *logits, int32_t *picks, float *weights,
               int32_t *flags, float *acc, float *sd, int threads)
 {
@@ -740,7 +741,16 @@ int orc_layer(const orc_cfg *c, int m, const uint16_t *x, const uint16_t *router
         }
         if (rc)
             break;
-        if (sh_w1 && sh_w3 && sh_w2) {
+        if (sh_w1 && sh_w3 && sh_w2 && sh_kquant) {
+            /* the shared expert on the routed experts' kernels (moe_v41.rs
+             * MoeV41LayerWeights: Q2_K w1, w3 and Q3_K w2; struct MoeV41
+             * sh_q8: its own q8_1 of the SwiGLU output): the routed
+             * expert's arithmetic, weight 1, added after the routed sum */
+            orc_expert_token(c, (const uint8_t *)sh_w1, (const uint8_t *)sh_w3,
+                             (const uint8_t *)sh_w2, xq, NULL, NULL, NULL, NULL, s, threads);
+            for (int r = 0; r < dim; r++)
+                a[r] = a[r] + s[r];
+        } else if (sh_w1 && sh_w3 && sh_w2) {
             orc_shared_token(c, sh_w1, sh_w3, sh_w2, xt, NULL, NULL, NULL, s, threads);
             for (int r = 0; r < dim; r++)
                 a[r] = a[r] + s[r];

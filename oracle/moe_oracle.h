@@ -77,13 +77,15 @@ void orc_shared_token(const orc_cfg *c, const uint16_t *w1, const uint16_t *w3,
 /* One layer step over m tokens. experts[e] = the host image of expert e's
  * slot (gate at gate_off, up at up_off, down at down_off), NULL when absent
  * (an absent pick is an error, return -1). sh_w* may be NULL (no shared
- * expert). residual is updated in place; x_next = bf16(residual). Optional
+ * expert); bf16 matrices, or with sh_kquant Q2_K (w1, w3) and Q3_K (w2)
+ * blocks run as a routed expert of weight 1. residual is updated in place;
+ * x_next = bf16(residual). Optional
  * outputs (NULL to skip): logits [m,n], picks/weights [m,k], flags [m],
  * acc [m,dim], sd [m,dim]. */
 int orc_layer(const orc_cfg *c, int m, const uint16_t *x, const uint16_t *router_w,
               const float *bias, const uint8_t *const *experts, uint64_t gate_off,
               uint64_t up_off, uint64_t down_off, const uint16_t *sh_w1,
-              const uint16_t *sh_w3, const uint16_t *sh_w2, float *residual,
+              const uint16_t *sh_w3, const uint16_t *sh_w2, int sh_kquant, float *residual,
               uint16_t *x_next, float *logits, int32_t *picks, float *weights,
               int32_t *flags, float *acc, float *sd, int threads);
 

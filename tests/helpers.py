@@ -40,9 +40,10 @@ def ocfg(cfg: moe.Config):
                       cfg.route_scale, cfg.swiglu_limit)
 
 
-def tiny_workload(cfg, seed=0, n_layers=1, shared=False):
+def tiny_workload(cfg, seed=0, n_layers=1, shared=False, shared_kquant=False):
     """The tiny layer: experts quantised from N(0, 0.02) with the oracle's quantisers."""
-    wl = Workload(cfg, n_layers=n_layers, seed=seed, shared=shared, fill_experts=False)
+    wl = Workload(cfg, n_layers=n_layers, seed=seed, shared=shared, fill_experts=False,
+                  shared_kquant=shared_kquant)
     wl.images = {}
     for l in range(n_layers):
         for e in range(cfg.n_routed):
@@ -136,7 +137,7 @@ def oracle_layer(wl, cfg, l, x_bits, residual=None):
     experts = {int(e): expert_image(wl, l, int(e)) for e in np.unique(picks)}
     out = oracle.layer(oc, x_bits, router, bias, experts,
                        (wl.shape.gate_off, wl.shape.up_off, wl.shape.down_off), wl.host_shared(l),
-                       residual, threads=THREADS)
+                       residual, threads=THREADS, shared_kquant=getattr(wl, "shared_kquant", False))
     out["experts"] = experts
     return out
 

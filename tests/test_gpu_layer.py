@@ -242,3 +242,37 @@ def test_invalid_arguments_are_rejected_before_launch(decode_wl):
     bad = moe.Arena(decode_wl.arena_t.data_ptr() + 4, decode_wl.arena.slot_bytes, 0, 0, 0)
     with pytest.raises(moe.MoeError):
         moe.layer_step(cfg, decode_wl.layer(0), bad, x, res, x, hdr, 1, decode_wl.ws)
+
+
+# ------------------------------------------------------------------ K-quant shared expert
+
+@pytest.mark.parametrize("m", [1, 2, 3])
+def test_tiny_layer_kquant_shared(m):
+    """Page moe_v41.rs MoeV41LayerWeights: the shared w1, w3 as Q2_K and w2 as
+    Q3_K blocks on the routed experts' kernels (struct MoeV41 sh_q8: its own
+    q8_1 of the SwiGLU output), added after the routed sum."""
+    cfg = tiny_cfg(m)
+    wl = tiny_workload(cfg, seed=60 + m, shared=True, shared_kquant=True)
+    x_bits = synth.x_bf16(60 + m, 0, m, cfg.dim)
+    res, xn, hdr = _run_layer(wl, cfg, 0, bf16_tensor(x_bits, "cuda"), m)
+    _compare_layer(wl, cfg, x_bits, m, res, xn, hdr)
+    # the shared expert's own intermediates against the oracle's routed-expert math
+    gs = _view(wl, cfg, "gs", m * cfg.inter).reshape(m, cfg.inter)
+    sd = _view(wl, cfg, "sd", m * cfg.dim).reshape(m, cfg.dim)
+    w1, w3, w2 = wl.host_shared(0)
+    for t in range(m):
+        xq = oracle.quant_q8_1(bf16_vals(x_bits[t]))
+        ref = oracle.expert_token(ocfg(cfg), w1, w3, w2, xq)
+        assert rel_inf(gs[t], ref["g"]) <= GU_RTOL
+        assert rel_inf(sd[t], ref["down"]) <= OUT_RTOL
+
+
+@pytest.mark.parametrize("m", [1, 8])
+def test_decode_layer_kquant_shared(m):
+    cfg = decode_cfg(m)
+    wl = Workload(cfg, n_layers=1, seed=64, shared=True, shared_kquant=True)
+    x_bits = synth.x_bf16(64, 1, m, cfg.dim)
+    res, xn, hdr = _run_layer(wl, cfg, 0, bf16_tensor(x_bits, "cuda"), m)
+    _compare_layer(wl, cfg, x_bits, m, res, xn, hdr)
+    del wl
+    torch.cuda.empty_cache()

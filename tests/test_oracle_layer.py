@@ -162,6 +162,29 @@ def test_layer_accumulates_in_ascending_id_then_shared():
         np.testing.assert_array_equal(out["acc"][t], acc)
 
 
+def test_layer_kquant_shared_expert_is_a_routed_expert_of_weight_one():
+    """Page moe_v41.rs MoeV41LayerWeights: the shared w1, w3 may be Q2_K and w2
+    Q3_K blocks, run on the routed experts' kernels (struct MoeV41: sh_q8, its
+    own q8_1 of the SwiGLU output). acc = the routed sum in ascending id, then
+    the shared expert's down output (weight 1) added last; its blocks are
+    checked against dense matmuls by test_expert_chain_against_dense_matmul."""
+    c, shp, experts, x, w, b = _tiny_layer(45, k=2)
+    img = np.frombuffer(synth.expert_bytes(45, 0, 999, shp), np.uint8)
+    sh = (img[shp.gate_off:shp.gate_off + shp.gate_bytes], img[shp.up_off:shp.up_off + shp.up_bytes],
+          img[shp.down_off:shp.down_off + shp.down_bytes])
+    res0 = np.full((2, 256), 0.5, np.float32)
+    out = oracle.layer(c, x, w, b, experts, (shp.gate_off, shp.up_off, shp.down_off), sh, res0,
+                       shared_kquant=True)
+    base = oracle.layer(c, x, w, b, experts, (shp.gate_off, shp.up_off, shp.down_off), None, res0)
+    for t in range(2):
+        xq = oracle.quant_q8_1(_bf16_vals(x[t]).astype(np.float32))
+        sd = oracle.expert_token(c, sh[0], sh[1], sh[2], xq)["down"]
+        np.testing.assert_array_equal(out["acc"][t], (base["acc"][t] + sd).astype(np.float32))
+        np.testing.assert_array_equal(out["sd"][t], sd)
+        np.testing.assert_array_equal(out["residual"][t], (res0[t] + out["acc"][t]).astype(np.float32))
+    assert np.abs(sd).max() > 0
+
+
 def test_layer_missing_expert_is_an_error():
     c, shp, experts, x, w, b = _tiny_layer(43)
     with pytest.raises(KeyError):
