@@ -330,6 +330,49 @@ int moe_layer_step_profiled(const moe_cfg *cfg, const moe_layer *layer, const mo
                             const void *x_dev, float *residual_dev, void *x_next_dev, int32_t *header_dev,
                             int m, void *ws_dev, moe_stream_t stream, float *ms_host);
 
+/* Dense GEMM on the tensor cores (tcgen05.mma, f32 accumulator in tensor
+ * memory, operands by TMA): d[n * ldd + r] = sum_k a[r, k] * b[n, k], a bf16
+ * [M, K] and b bf16 [N, K] row-major (bf16 products exact, f32 sums) --
+ * the contraction of the router and of the bf16 shared expert when many
+ * tokens run at once ([moe_v41] struct Kernels gemm / gemm_f32out). K a
+ * positive multiple of 64, ldd >= M, a and b 16-byte aligned with row
+ * strides K * 2 a multiple of 16. Device pointers. */
+int moe_gemm_bf16(const void *a_dev, const void *b_dev, float *d_dev, int M, int N, int K, int ldd,
+                  moe_stream_t stream);
+
+/* The batched (prefill) arm: one MoE layer step for m tokens at once
+ * ([moe_v41] struct Kernels gather, scatter_add, sum_rows, quant_d2s6 /
+ * quant_d4, mmq_q2k_*, mmq_q3k_*, gemm; struct MoeV41 a_rows, a_q8: an
+ * expert group's gathered rows and their q8_1 activations). The arithmetic
+ * is moe_layer_step's; the routed experts run as GEMMs over each expert's
+ * group of tokens, on tensor cores:
+ *   logits = router GEMM; scores, picks and weights as the decode selection;
+ *   pairs (token, pick) grouped by expert in ascending id, tokens ascending;
+ *   per expert g, u = Q2_K(gate, up) . q8_1(x) over its group, h = SwiGLU,
+ *   q8_1(h), down = Q3_K(down) . q8_1(h), each times the pair's weight;
+ *   the bf16 shared expert as dense GEMMs; acc = the pairs in ascending
+ *   expert id then sd; residual += acc; x_next = bf16(residual).
+ * The GEMM operands are the dequantised weights and the dequantised q8_1
+ * activations rounded to fp16 (the products then differ from the exact
+ * dequantise-then-dot by about 2^-12 relative per operand); accumulation
+ * f32. Shapes: dim a multiple of 1024, inter of 2048 (the row strides of
+ * the Q2_K / Q3_K blocks must be multiples of 16 bytes for TMA), the shared
+ * expert bf16 or absent, 0 <= m <= 65536 (cfg->max_tokens is not used).
+ * arena_slots: slots in the arena (the tensor maps cover that many). x_dev
+ * bf16 [m, dim]; residual_dev f32 [m, dim] (in/out); x_next_dev bf16
+ * [m, dim]; picks_dev i32 [m, topk], weights_dev f32 [m, topk] (pick
+ * order); ws_dev: moe_prefill_workspace_bytes bytes (no initialisation
+ * needed). Errors: MOE_EUNSUPPORTED for the shapes above; a picked expert
+ * whose slot is -1 uses slot 0 and sets MOE_WS_PLAN (moe_prefill_status). */
+int moe_prefill_workspace_bytes(const moe_cfg *cfg, int m, size_t *bytes);
+int moe_prefill_step(const moe_cfg *cfg, const moe_layer *layer, const moe_arena *arena, int64_t arena_slots,
+                     const void *x_dev, float *residual_dev, void *x_next_dev, int32_t *picks_dev,
+                     float *weights_dev, int m, void *ws_dev, size_t ws_bytes, moe_stream_t stream);
+
+/* The status word (MOE_WS_* bits) of the last moe_prefill_step on ws_dev;
+ * synchronises `stream`. */
+int moe_prefill_status(const moe_cfg *cfg, int m, void *ws_dev, uint32_t *status_host, moe_stream_t stream);
+
 /* Last error message of the calling thread ("" if none). */
 const char *moe_last_error(void);
 

@@ -29,7 +29,7 @@ __all__ = ["Config", "Arena", "Layer", "MoeError", "header_words", "workspace_by
            "workspace_init", "router_logits", "quantize_q8_1", "route_select", "expert_step",
            "swiglu_q8", "layer_step", "host_io_bytes", "layer_step_host", "workspace_view",
            "read_status", "layer_step_profiled", "layer_step_static", "route_scores", "set_wait_limit_ns",
-           "expert_step_unreleased", "slot_table_set", "dedupe_triples", "parse_header", "Graph"]
+           "expert_step_unreleased", "gemm_bf16", "prefill_workspace_bytes", "prefill_step", "prefill_status", "slot_table_set", "dedupe_triples", "parse_header", "Graph"]
 
 
 class MoeError(RuntimeError):
@@ -247,6 +247,31 @@ def parse_header(cfg: Config, header_host: np.ndarray, m: int, t: int):
                                        C.c_void_p(st.ctypes.data), C.c_void_p(picks.ctypes.data),
                                        C.c_void_p(w.ctypes.data)))
     return int(st[0]), picks, w
+
+
+def gemm_bf16(a, b, d, M: int, N: int, K: int, ldd: int, stream=None):
+    """d[n * ldd + r] = sum_k a[r, k] b[n, k] on the tensor cores (bf16 in, f32 out)."""
+    _check(_lib.moe().moe_gemm_bf16(_ptr(a), _ptr(b), _ptr(d), M, N, K, ldd, _stream(stream)))
+
+
+def prefill_workspace_bytes(cfg: Config, m: int) -> int:
+    b = C.c_size_t(0)
+    _check(_lib.moe().moe_prefill_workspace_bytes(C.byref(cfg.c()), m, C.byref(b)))
+    return b.value
+
+
+def prefill_step(cfg: Config, layer: Layer, arena: Arena, arena_slots: int, x, residual, x_next, picks, weights,
+                 m: int, ws, stream=None):
+    """The batched (prefill) layer step for m tokens (include/moe.h, moe_prefill_step)."""
+    _check(_lib.moe().moe_prefill_step(C.byref(cfg.c()), C.byref(layer.c()), C.byref(arena.c()), int(arena_slots),
+                                       _ptr(x), _ptr(residual), _ptr(x_next), _ptr(picks), _ptr(weights), m,
+                                       _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def prefill_status(cfg: Config, m: int, ws, stream=None) -> int:
+    s = C.c_uint32(0)
+    _check(_lib.moe().moe_prefill_status(C.byref(cfg.c()), m, _ptr(ws), C.byref(s), _stream(stream)))
+    return s.value
 
 
 class Graph:

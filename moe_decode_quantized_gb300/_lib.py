@@ -73,6 +73,11 @@ MOE_SYMBOLS = {
                                           P, P, P, C.c_int, P, P, P]),
     "moe_set_wait_limit_ns": (C.c_int, [U64]),
     "moe_expert_step_unreleased": (C.c_int, [C.POINTER(MoeCfg), P, P, C.c_int, P, P]),
+    "moe_gemm_bf16": (C.c_int, [P, P, P, C.c_int, C.c_int, C.c_int, C.c_int, P]),
+    "moe_prefill_workspace_bytes": (C.c_int, [C.POINTER(MoeCfg), C.c_int, C.POINTER(SZ)]),
+    "moe_prefill_step": (C.c_int, [C.POINTER(MoeCfg), C.POINTER(MoeLayer), C.POINTER(MoeArena), C.c_int64, P, P,
+                                   P, P, P, C.c_int, P, SZ, P]),
+    "moe_prefill_status": (C.c_int, [C.POINTER(MoeCfg), C.c_int, P, C.POINTER(C.c_uint32), P]),
     "moe_last_error": (C.c_char_p, []),
 }
 

@@ -14,6 +14,7 @@
 #include "moe_route.cuh"
 #include "moe_experts.cuh"
 #include "moe_slot.cuh"
+#include "moe_prefill.cuh"
 
 using namespace moe;
 
@@ -80,6 +81,13 @@ struct DevInfo {
     bool attrs = false;
 };
 
+template <int AK>
+int tc_attr(int smem_optin)
+{
+    CUDA_OK(cudaFuncSetAttribute(moe_tc_gemm<AK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin));
+    return MOE_OK;
+}
+
 std::mutex g_mu;
 DevInfo g_dev[64];
 
@@ -101,6 +109,9 @@ int dev_info(DevInfo **out)
         CUDA_OK(cudaFuncSetAttribute(moe_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
         CUDA_OK(cudaFuncSetAttribute(moe_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
         CUDA_OK(cudaFuncSetAttribute(moe_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
+        int rc = tc_attr<0>(I.smem_optin);
+        if (rc || (rc = tc_attr<1>(I.smem_optin)) || (rc = tc_attr<2>(I.smem_optin)))
+            return rc;
         I.attrs = true;
     }
     *out = &I;
@@ -468,6 +479,170 @@ int static_ws(cudaStream_t s, void **out)
     }
     *out = g_static_ptr[d];
     return MOE_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps (TMA descriptors)
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// the driver's cuTensorMapEncodeTiled, looked up once through the runtime
+// (the library links no driver library)
+int encode_tiled(EncodeTiledFn *out)
+{
+    static EncodeTiledFn fn = nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        CUDA_OK(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q));
+        if (q != cudaDriverEntryPointSuccess || !p)
+            return fail(MOE_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+        fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    *out = fn;
+    return MOE_OK;
+}
+
+// rows x inner 16-bit elements, row stride row_bytes; boxes of box_rows rows
+// x 64 elements, 128-byte swizzle (the SW128 K-major operand layout)
+int map_rows16(CUtensorMap *m, bool bf16, const void *base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+               uint32_t box_rows)
+{
+    EncodeTiledFn fn;
+    int rc = encode_tiled(&fn);
+    if (rc)
+        return rc;
+    const cuuint64_t dims[2] = {inner, rows}, strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {64, box_rows}, es[2] = {1, 1};
+    const CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                          const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(MOE_ECUDA, "cuTensorMapEncodeTiled (2-D, %llu x %llu) failed: %d", (unsigned long long)rows,
+                    (unsigned long long)inner, (int)r);
+    return MOE_OK;
+}
+
+// The expert arena's blocks of one matrix kind as u32 elements [slot][row]
+// [row_bytes / 4]; boxes of 128 rows x raw_row bytes of one slot.
+int map_arena(CUtensorMap *m, const void *base, uint64_t row_bytes, uint64_t rows, uint64_t slots,
+              uint64_t slot_bytes, uint32_t raw_row)
+{
+    EncodeTiledFn fn;
+    int rc = encode_tiled(&fn);
+    if (rc)
+        return rc;
+    const cuuint64_t dims[3] = {row_bytes / 4, rows, slots}, strides[2] = {row_bytes, slot_bytes};
+    const cuuint32_t box[3] = {raw_row / 4, TC_M, 1}, es[3] = {1, 1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(MOE_ECUDA, "cuTensorMapEncodeTiled (arena, %llu slots) failed: %d", (unsigned long long)slots,
+                    (int)r);
+    return MOE_OK;
+}
+
+// ------------------------------------------------------------------ prefill
+
+struct PfLayout {
+    size_t logits, scores, flags, cnt, off, pair_tok, pair_w, pick_pair, tasks, ntasks, status, xhat, xhat_lo, xg,
+        xg_lo, g, u, hh, dw, gs, us, hs, sd, acc, total;
+    int P, max_tasks;
+};
+
+PfLayout pf_layout(const moe_cfg &c, int m)
+{
+    PfLayout L{};
+    const size_t M = (size_t)m, P = M * c.topk, n = c.n_routed;
+    L.P = (int)P;
+    L.max_tasks = (int)std::min<size_t>(n, P) + (int)(P / TC_NT) + 1;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+    L.logits = take(4 * M * n);
+    L.scores = take(4 * M * n);
+    L.flags = take(4 * M);
+    L.cnt = take(4 * n);
+    L.off = take(4 * (n + 1));
+    L.pair_tok = take(4 * P);
+    L.pair_w = take(4 * P);
+    L.pick_pair = take(4 * P);
+    L.tasks = take(sizeof(TcTask) * (size_t)L.max_tasks);
+    L.ntasks = take(4);
+    L.status = take(4);
+    L.xhat = take(2 * M * c.dim);
+    L.xhat_lo = take(2 * M * c.dim);
+    L.xg = take(2 * P * c.dim);
+    L.xg_lo = take(2 * P * c.dim);
+    L.g = take(4 * P * c.inter);
+    L.u = take(4 * P * c.inter);
+    L.hh = take(2 * P * c.inter);
+    L.dw = take(4 * P * c.dim);
+    L.gs = take(4 * M * c.inter);
+    L.us = take(4 * M * c.inter);
+    L.hs = take(2 * M * c.inter);
+    L.sd = take(4 * M * c.dim);
+    L.acc = take(4 * M * c.dim);
+    L.total = off;
+    return L;
+}
+
+#define MOE_PREFILL_MAX_TOKENS 65536
+
+int check_prefill(const moe_cfg *c, int m)
+{
+    if (m < 0 || m > MOE_PREFILL_MAX_TOKENS)
+        return fail(MOE_EINVAL, "prefill: m (%d) must be in [0, %d]", m, MOE_PREFILL_MAX_TOKENS);
+    if (c->dim % 1024 || c->inter % 2048)
+        return fail(MOE_EUNSUPPORTED,
+                    "prefill: dim (%d) must be a multiple of 1024 and inter (%d) of 2048 (TMA row strides of "
+                    "the Q2_K / Q3_K blocks)",
+                    c->dim, c->inter);
+    return MOE_OK;
+}
+
+// one GEMM of the prefill: D[M x N] = A . B^T, out[col * ldo + row]
+template <int AK>
+int launch_tc(const CUtensorMap &am, const CUtensorMap &bm, const CUtensorMap &bm_lo, const TcArgs &a, dim3 grid,
+              cudaStream_t s)
+{
+    if (grid.x == 0 || grid.y == 0)
+        return MOE_OK;
+    moe_tc_gemm<AK><<<grid, TC_THREADS, tc_smem_bytes(tc_parts(AK), a.S, a.SR, a.raw_bytes), s>>>(am, bm, bm_lo, a);
+    CUDA_OK(cudaGetLastError());
+    return MOE_OK;
+}
+
+TcArgs tc_args(int M, int N, int K, float *out, int ldo, uint32_t *status)
+{
+    TcArgs a{};
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.out = out;
+    a.ldo = ldo;
+    a.S = 4;
+    a.SR = 0;
+    const int kc = K / TC_KC;  // K-chunks: split over up to four accumulators, evenly
+    a.ksplit = kc % 4 == 0 ? 4 : (kc % 2 == 0 ? 2 : 1);
+    a.status = status;
+    a.wait_ns = g_wait_ns.load();
+    return a;
+}
+
+// bf16 GEMM out[n * ldo + r] = sum_k A[r, k] B[n, k] (A [M, K], B [N, K] row-major bf16)
+int gemm_bf16(const void *A, const void *B, float *out, int M, int N, int K, int ldo, uint32_t *status,
+              cudaStream_t s)
+{
+    CUtensorMap am, bm;
+    int rc = map_rows16(&am, true, A, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, TC_M);
+    if (rc || (rc = map_rows16(&bm, true, B, (uint64_t)K, (uint64_t)N, (uint64_t)K * 2, TC_BROWS)))
+        return rc;
+    const TcArgs a = tc_args(M, N, K, out, ldo, status);
+    return launch_tc<0>(am, bm, bm, a, dim3((N + TC_NT - 1) / TC_NT, (M + TC_M - 1) / TC_M), s);
 }
 
 struct GraphObj {
@@ -950,6 +1125,176 @@ int moe_layer_step_profiled(const moe_cfg *cfg, const moe_layer *layer, const mo
     CUDA_OK(cudaEventSynchronize(ev[3]));
     for (int i = 0; i < 3; ++i)
         CUDA_OK(cudaEventElapsedTime(&ms[i], ev[i], ev[i + 1]));
+    return MOE_OK;
+}
+
+int moe_gemm_bf16(const void *a, const void *b, float *d, int M, int N, int K, int ldd, moe_stream_t stream)
+{
+    if (!a || !b || !d || M < 0 || N < 0 || K <= 0 || K % TC_KC || ldd < M || !aligned16(a) || !aligned16(b))
+        return fail(MOE_EINVAL, "moe_gemm_bf16: bad arguments (K a positive multiple of 64, ldd >= M, 16-byte "
+                                "aligned operands)");
+    if (M == 0 || N == 0)
+        return MOE_OK;
+    DevInfo *I;
+    int rc = dev_info(&I);
+    if (rc)
+        return rc;
+    return gemm_bf16(a, b, d, M, N, K, ldd, nullptr, (cudaStream_t)stream);
+}
+
+int moe_prefill_workspace_bytes(const moe_cfg *cfg, int m, size_t *bytes)
+{
+    int rc = check_cfg(cfg);
+    if (rc || (rc = check_prefill(cfg, m)))
+        return rc;
+    if (!bytes)
+        return fail(MOE_EINVAL, "bytes is NULL");
+    *bytes = pf_layout(*cfg, m).total;
+    return MOE_OK;
+}
+
+int moe_prefill_step(const moe_cfg *cfg, const moe_layer *layer, const moe_arena *arena, int64_t arena_slots,
+                     const void *x, float *residual, void *x_next, int32_t *picks, float *weights, int m,
+                     void *ws, size_t ws_bytes, moe_stream_t stream)
+{
+    int rc = check_cfg(cfg);
+    if (rc || (rc = check_prefill(cfg, m)) || (rc = check_arena(arena)) || (rc = check_layer(*cfg, layer)))
+        return rc;
+    if (layer->sh_w1 && layer->sh_format != MOE_SHARED_BF16)
+        return fail(MOE_EUNSUPPORTED, "prefill: the shared expert must be bf16");
+    if (m == 0)
+        return MOE_OK;
+    if (!x || !residual || !x_next || !picks || !weights || !ws || arena_slots < 1 || !aligned16(x))
+        return fail(MOE_EINVAL, "moe_prefill_step: a buffer is NULL, arena_slots < 1 or x not 16-byte aligned");
+    const PfLayout L = pf_layout(*cfg, m);
+    if (ws_bytes < L.total)
+        return fail(MOE_EINVAL, "moe_prefill_step: workspace of %zu bytes, %zu needed", ws_bytes, L.total);
+    DevInfo *I;
+    if ((rc = dev_info(&I)))
+        return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    const int n = cfg->n_routed, k = cfg->topk, dim = cfg->dim, inter = cfg->inter, P = L.P;
+    char *w = static_cast<char *>(ws);
+    float *logits = reinterpret_cast<float *>(w + L.logits), *scores = reinterpret_cast<float *>(w + L.scores);
+    int32_t *flags = reinterpret_cast<int32_t *>(w + L.flags), *cnt = reinterpret_cast<int32_t *>(w + L.cnt);
+    int32_t *off = reinterpret_cast<int32_t *>(w + L.off), *pair_tok = reinterpret_cast<int32_t *>(w + L.pair_tok);
+    float *pair_w = reinterpret_cast<float *>(w + L.pair_w);
+    int32_t *pick_pair = reinterpret_cast<int32_t *>(w + L.pick_pair);
+    TcTask *tasks = reinterpret_cast<TcTask *>(w + L.tasks);
+    int32_t *ntasks = reinterpret_cast<int32_t *>(w + L.ntasks);
+    uint32_t *status = reinterpret_cast<uint32_t *>(w + L.status);
+    __half *xhat = reinterpret_cast<__half *>(w + L.xhat), *xg = reinterpret_cast<__half *>(w + L.xg);
+    __half *xhat_lo = reinterpret_cast<__half *>(w + L.xhat_lo), *xg_lo = reinterpret_cast<__half *>(w + L.xg_lo);
+    __half *hh = reinterpret_cast<__half *>(w + L.hh);
+    float *g = reinterpret_cast<float *>(w + L.g), *u = reinterpret_cast<float *>(w + L.u);
+    float *dw = reinterpret_cast<float *>(w + L.dw), *gs = reinterpret_cast<float *>(w + L.gs);
+    float *us = reinterpret_cast<float *>(w + L.us), *sd = reinterpret_cast<float *>(w + L.sd);
+    float *acc = reinterpret_cast<float *>(w + L.acc);
+    uint16_t *hs = reinterpret_cast<uint16_t *>(w + L.hs);
+    CUDA_OK(cudaMemsetAsync(status, 0, 4, s));
+    // router logits [m, n] on tensor cores, the scores, each token's picks
+    if ((rc = gemm_bf16(layer->router_w, x, logits, n, m, dim, n, status, s)))
+        return rc;
+    ScoreArgs sa{logits, scores, cfg->gate_temp, m * n};
+    if ((rc = launch(moe_score_kernel, dim3((m * n + MOE_SCORES_PER_CTA - 1) / MOE_SCORES_PER_CTA), dim3(256), 0,
+                     s, false, sa)))
+        return rc;
+    PTopArgs ta{logits, scores, layer->bias, picks, flags, weights, m, n, k, cfg->norm_topk_prob != 0,
+                cfg->route_scale};
+    moe_prefill_topk_kernel<<<(m + 7) / 8, 256, 0, s>>>(ta);
+    CUDA_OK(cudaGetLastError());
+    // pairs grouped by expert, the column tasks of the routed GEMMs
+    PPlanArgs pa{picks, weights, layer->slot_row, m, n, k, cnt, off, pair_tok, pair_w, pick_pair, tasks, ntasks,
+                 status};
+    moe_prefill_plan_kernel<<<1, 1024, 0, s>>>(pa);
+    CUDA_OK(cudaGetLastError());
+    // q8_1 of x, dequantised to fp16, gathered into pair order
+    const int nbx = m * dim / 32;
+    moe_prefill_xhat_kernel<<<(nbx + 7) / 8, 256, 0, s>>>(static_cast<const uint16_t *>(x), nbx, xhat, xhat_lo);
+    const size_t gthreads = (size_t)P * (dim / 8);
+    moe_prefill_gather_kernel<<<(unsigned)((gthreads + 255) / 256), 256, 0, s>>>(
+        reinterpret_cast<const uint4 *>(xhat), pair_tok, P, dim / 8, reinterpret_cast<uint4 *>(xg));
+    moe_prefill_gather_kernel<<<(unsigned)((gthreads + 255) / 256), 256, 0, s>>>(
+        reinterpret_cast<const uint4 *>(xhat_lo), pair_tok, P, dim / 8, reinterpret_cast<uint4 *>(xg_lo));
+    CUDA_OK(cudaGetLastError());
+    // routed gate and up: Q2_K rows (4 super-blocks a raw stage) x the groups' rows
+    const char *ab = static_cast<const char *>(arena->base);
+    const uint64_t q2row = (uint64_t)dim / 256 * MOE_Q2K_BYTES, q3row = (uint64_t)inter / 256 * MOE_Q3K_BYTES;
+    CUtensorMap gmap, umap, dmap, xmap, xlmap, hmap;
+    if ((rc = map_arena(&gmap, ab + arena->gate_off, q2row, inter, arena_slots, arena->slot_bytes,
+                        4 * MOE_Q2K_BYTES)) ||
+        (rc = map_arena(&umap, ab + arena->up_off, q2row, inter, arena_slots, arena->slot_bytes,
+                        4 * MOE_Q2K_BYTES)) ||
+        (rc = map_arena(&dmap, ab + arena->down_off, q3row, dim, arena_slots, arena->slot_bytes,
+                        8 * MOE_Q3K_BYTES)) ||
+        (rc = map_rows16(&xmap, false, xg, dim, P, (uint64_t)dim * 2, TC_BROWS)) ||
+        (rc = map_rows16(&xlmap, false, xg_lo, dim, P, (uint64_t)dim * 2, TC_BROWS)) ||
+        (rc = map_rows16(&hmap, false, hh, inter, P, (uint64_t)inter * 2, TC_BROWS)))
+        return rc;
+    TcArgs ga = tc_args(inter, P, dim, g, inter, status);
+    ga.tasks = tasks;
+    ga.ntasks = ntasks;
+    ga.raw_row = 4 * MOE_Q2K_BYTES;
+    ga.rk = 1024;
+    ga.S = 2;
+    ga.SR = 2;
+    ga.raw_bytes = (uint32_t)(TC_M * ga.raw_row);
+    if ((rc = launch_tc<1>(gmap, xmap, xlmap, ga, dim3(L.max_tasks, inter / TC_M), s)))
+        return rc;
+    ga.out = u;
+    if ((rc = launch_tc<1>(umap, xmap, xlmap, ga, dim3(L.max_tasks, inter / TC_M), s)))
+        return rc;
+    // h = SwiGLU(g, u), its q8_1, dequantised to fp16
+    const int nbh = P * inter / 32;
+    moe_prefill_swiglu_kernel<<<(nbh + 7) / 8, 256, 0, s>>>(g, u, nbh, cfg->swiglu_limit, hh);
+    CUDA_OK(cudaGetLastError());
+    // routed down: Q3_K rows (8 super-blocks a raw stage), times each pair's weight
+    TcArgs da = tc_args(dim, P, inter, dw, dim, status);
+    da.colw = pair_w;
+    da.tasks = tasks;
+    da.ntasks = ntasks;
+    da.raw_row = 8 * MOE_Q3K_BYTES;
+    da.rk = 2048;
+    da.S = 3;
+    da.SR = 1;
+    da.raw_bytes = (uint32_t)(TC_M * da.raw_row);
+    if ((rc = launch_tc<2>(dmap, hmap, hmap, da, dim3(L.max_tasks, dim / TC_M), s)))
+        return rc;
+    // the bf16 shared expert as dense GEMMs
+    const float *sdp = nullptr;
+    if (layer->sh_w1) {
+        if ((rc = gemm_bf16(layer->sh_w1, x, gs, inter, m, dim, inter, status, s)) ||
+            (rc = gemm_bf16(layer->sh_w3, x, us, inter, m, dim, inter, status, s)))
+            return rc;
+        const size_t ns = (size_t)m * inter;
+        moe_prefill_shared_swiglu_kernel<<<(unsigned)((ns + 255) / 256), 256, 0, s>>>(gs, us, ns, cfg->swiglu_limit,
+                                                                                       hs);
+        CUDA_OK(cudaGetLastError());
+        if ((rc = gemm_bf16(layer->sh_w2, hs, sd, dim, m, inter, dim, status, s)))
+            return rc;
+        sdp = sd;
+    }
+    // acc (pairs in ascending expert id, then sd), residual, x_next
+    const size_t nf = (size_t)m * dim;
+    moe_prefill_finish_kernel<<<(unsigned)((nf + 255) / 256), 256, 0, s>>>(
+        dw, picks, pick_pair, k, sdp, acc, residual, static_cast<uint16_t *>(x_next), m, dim);
+    CUDA_OK(cudaGetLastError());
+    (void)cnt;
+    (void)off;
+    return MOE_OK;
+}
+
+int moe_prefill_status(const moe_cfg *cfg, int m, void *ws, uint32_t *status_host, moe_stream_t stream)
+{
+    int rc = check_cfg(cfg);
+    if (rc || (rc = check_prefill(cfg, m)))
+        return rc;
+    if (!ws || !status_host)
+        return fail(MOE_EINVAL, "moe_prefill_status: bad arguments");
+    const PfLayout L = pf_layout(*cfg, m);
+    CUDA_OK(cudaMemcpyAsync(status_host, static_cast<char *>(ws) + L.status, 4, cudaMemcpyDeviceToHost,
+                            (cudaStream_t)stream));
+    CUDA_OK(cudaStreamSynchronize((cudaStream_t)stream));
     return MOE_OK;
 }
 
