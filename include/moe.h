@@ -369,6 +369,16 @@ int moe_prefill_step(const moe_cfg *cfg, const moe_layer *layer, const moe_arena
                      const void *x_dev, float *residual_dev, void *x_next_dev, int32_t *picks_dev,
                      float *weights_dev, int m, void *ws_dev, size_t ws_bytes, moe_stream_t stream);
 
+/* Measurement entry point: moe_prefill_step with CUDA events between its
+ * stages on `stream`; synchronises `stream` and writes milliseconds to
+ * ms_host[0..8]: router GEMM; scores, top-k and grouping; q8_1 of x and the
+ * gathers; gate GEMM; up GEMM; SwiGLU + q8_1(h); down GEMM; shared expert
+ * (three GEMMs and its SwiGLU); finish. */
+int moe_prefill_step_profiled(const moe_cfg *cfg, const moe_layer *layer, const moe_arena *arena,
+                              int64_t arena_slots, const void *x_dev, float *residual_dev, void *x_next_dev,
+                              int32_t *picks_dev, float *weights_dev, int m, void *ws_dev, size_t ws_bytes,
+                              moe_stream_t stream, float *ms_host);
+
 /* The status word (MOE_WS_* bits) of the last moe_prefill_step on ws_dev;
  * synchronises `stream`. */
 int moe_prefill_status(const moe_cfg *cfg, int m, void *ws_dev, uint32_t *status_host, moe_stream_t stream);

@@ -29,7 +29,7 @@ __all__ = ["Config", "Arena", "Layer", "MoeError", "header_words", "workspace_by
            "workspace_init", "router_logits", "quantize_q8_1", "route_select", "expert_step",
            "swiglu_q8", "layer_step", "host_io_bytes", "layer_step_host", "workspace_view",
            "read_status", "layer_step_profiled", "layer_step_static", "route_scores", "set_wait_limit_ns",
-           "expert_step_unreleased", "gemm_bf16", "prefill_workspace_bytes", "prefill_step", "prefill_status", "slot_table_set", "dedupe_triples", "parse_header", "Graph"]
+           "expert_step_unreleased", "gemm_bf16", "prefill_workspace_bytes", "prefill_step", "prefill_step_profiled", "prefill_status", "slot_table_set", "dedupe_triples", "parse_header", "Graph"]
 
 
 class MoeError(RuntimeError):
@@ -266,6 +266,17 @@ def prefill_step(cfg: Config, layer: Layer, arena: Arena, arena_slots: int, x, r
     _check(_lib.moe().moe_prefill_step(C.byref(cfg.c()), C.byref(layer.c()), C.byref(arena.c()), int(arena_slots),
                                        _ptr(x), _ptr(residual), _ptr(x_next), _ptr(picks), _ptr(weights), m,
                                        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def prefill_step_profiled(cfg: Config, layer: Layer, arena: Arena, arena_slots: int, x, residual, x_next, picks,
+                          weights, m: int, ws, stream=None):
+    """-> ms of the nine stages of one prefill step (include/moe.h, moe_prefill_step_profiled)."""
+    ms = np.zeros(9, np.float32)
+    _check(_lib.moe().moe_prefill_step_profiled(C.byref(cfg.c()), C.byref(layer.c()), C.byref(arena.c()),
+                                                int(arena_slots), _ptr(x), _ptr(residual), _ptr(x_next), _ptr(picks),
+                                                _ptr(weights), m, _ptr(ws), ws.numel() * ws.element_size(),
+                                                _stream(stream), C.c_void_p(ms.ctypes.data)))
+    return ms
 
 
 def prefill_status(cfg: Config, m: int, ws, stream=None) -> int:

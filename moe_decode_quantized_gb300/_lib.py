@@ -77,6 +77,8 @@ MOE_SYMBOLS = {
     "moe_prefill_workspace_bytes": (C.c_int, [C.POINTER(MoeCfg), C.c_int, C.POINTER(SZ)]),
     "moe_prefill_step": (C.c_int, [C.POINTER(MoeCfg), C.POINTER(MoeLayer), C.POINTER(MoeArena), C.c_int64, P, P,
                                    P, P, P, C.c_int, P, SZ, P]),
+    "moe_prefill_step_profiled": (C.c_int, [C.POINTER(MoeCfg), C.POINTER(MoeLayer), C.POINTER(MoeArena),
+                                            C.c_int64, P, P, P, P, P, C.c_int, P, SZ, P, P]),
     "moe_prefill_status": (C.c_int, [C.POINTER(MoeCfg), C.c_int, P, C.POINTER(C.c_uint32), P]),
     "moe_last_error": (C.c_char_p, []),
 }

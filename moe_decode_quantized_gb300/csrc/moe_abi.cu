@@ -605,13 +605,20 @@ int check_prefill(const moe_cfg *c, int m)
 }
 
 // one GEMM of the prefill: D[M x N] = A . B^T, out[col * ldo + row]
+// the B ring takes the shared memory the A stages and raw stages leave (up
+// to TC_SB_MAX full-width stages)
 template <int AK>
-int launch_tc(const CUtensorMap &am, const CUtensorMap &bm, const CUtensorMap &bm_lo, const TcArgs &a, dim3 grid,
-              cudaStream_t s)
+int launch_tc(const CUtensorMap &am, const CUtensorMap &bm, const CUtensorMap &bm_lo, TcArgs a, dim3 grid,
+              cudaStream_t s, int smem_optin)
 {
     if (grid.x == 0 || grid.y == 0)
         return MOE_OK;
-    moe_tc_gemm<AK><<<grid, TC_THREADS, tc_smem_bytes(tc_parts(AK), a.S, a.SR, a.raw_bytes), s>>>(am, bm, bm_lo, a);
+    const size_t fixed = tc_smem_bytes(AK, a.S, a.SR, a.raw_bytes, 0);
+    const size_t full = (size_t)TC_SB_MAX * tc_parts(AK) * TC_NT * 128;
+    if ((size_t)smem_optin < fixed + 2 * tc_parts(AK) * TC_NT * 128)
+        return fail(MOE_EUNSUPPORTED, "prefill GEMM: %zu bytes of shared memory needed", fixed);
+    a.b_buf = (uint32_t)std::min(full, ((size_t)smem_optin - fixed) / 2048 * 2048);
+    moe_tc_gemm<AK><<<grid, TC_THREADS, fixed + a.b_buf, s>>>(am, bm, bm_lo, a);
     CUDA_OK(cudaGetLastError());
     return MOE_OK;
 }
@@ -624,7 +631,7 @@ TcArgs tc_args(int M, int N, int K, float *out, int ldo, uint32_t *status)
     a.K = K;
     a.out = out;
     a.ldo = ldo;
-    a.S = 4;
+    a.S = 3;
     a.SR = 0;
     const int kc = K / TC_KC;  // K-chunks: split over up to four accumulators, evenly
     a.ksplit = kc % 4 == 0 ? 4 : (kc % 2 == 0 ? 2 : 1);
@@ -635,14 +642,14 @@ TcArgs tc_args(int M, int N, int K, float *out, int ldo, uint32_t *status)
 
 // bf16 GEMM out[n * ldo + r] = sum_k A[r, k] B[n, k] (A [M, K], B [N, K] row-major bf16)
 int gemm_bf16(const void *A, const void *B, float *out, int M, int N, int K, int ldo, uint32_t *status,
-              cudaStream_t s)
+              cudaStream_t s, int smem_optin)
 {
     CUtensorMap am, bm;
     int rc = map_rows16(&am, true, A, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, TC_M);
     if (rc || (rc = map_rows16(&bm, true, B, (uint64_t)K, (uint64_t)N, (uint64_t)K * 2, TC_BROWS)))
         return rc;
     const TcArgs a = tc_args(M, N, K, out, ldo, status);
-    return launch_tc<0>(am, bm, bm, a, dim3((N + TC_NT - 1) / TC_NT, (M + TC_M - 1) / TC_M), s);
+    return launch_tc<0>(am, bm, bm, a, dim3((N + TC_NT - 1) / TC_NT, (M + TC_M - 1) / TC_M), s, smem_optin);
 }
 
 struct GraphObj {
@@ -1139,7 +1146,7 @@ int moe_gemm_bf16(const void *a, const void *b, float *d, int M, int N, int K, i
     int rc = dev_info(&I);
     if (rc)
         return rc;
-    return gemm_bf16(a, b, d, M, N, K, ldd, nullptr, (cudaStream_t)stream);
+    return gemm_bf16(a, b, d, M, N, K, ldd, nullptr, (cudaStream_t)stream, I->smem_optin);
 }
 
 int moe_prefill_workspace_bytes(const moe_cfg *cfg, int m, size_t *bytes)
@@ -1153,9 +1160,12 @@ int moe_prefill_workspace_bytes(const moe_cfg *cfg, int m, size_t *bytes)
     return MOE_OK;
 }
 
-int moe_prefill_step(const moe_cfg *cfg, const moe_layer *layer, const moe_arena *arena, int64_t arena_slots,
-                     const void *x, float *residual, void *x_next, int32_t *picks, float *weights, int m,
-                     void *ws, size_t ws_bytes, moe_stream_t stream)
+}  // extern "C"
+
+namespace {
+static int prefill_step(const moe_cfg *cfg, const moe_layer *layer, const moe_arena *arena, int64_t arena_slots,
+                        const void *x, float *residual, void *x_next, int32_t *picks, float *weights, int m,
+                        void *ws, size_t ws_bytes, moe_stream_t stream, cudaEvent_t *ev)
 {
     int rc = check_cfg(cfg);
     if (rc || (rc = check_prefill(cfg, m)) || (rc = check_arena(arena)) || (rc = check_layer(*cfg, layer)))
@@ -1191,10 +1201,14 @@ int moe_prefill_step(const moe_cfg *cfg, const moe_layer *layer, const moe_arena
     float *us = reinterpret_cast<float *>(w + L.us), *sd = reinterpret_cast<float *>(w + L.sd);
     float *acc = reinterpret_cast<float *>(w + L.acc);
     uint16_t *hs = reinterpret_cast<uint16_t *>(w + L.hs);
+    // stage boundaries for the profiled variant
+    auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], s) : cudaSuccess; };
     CUDA_OK(cudaMemsetAsync(status, 0, 4, s));
+    CUDA_OK(mark(0));
     // router logits [m, n] on tensor cores, the scores, each token's picks
-    if ((rc = gemm_bf16(layer->router_w, x, logits, n, m, dim, n, status, s)))
+    if ((rc = gemm_bf16(layer->router_w, x, logits, n, m, dim, n, status, s, I->smem_optin)))
         return rc;
+    CUDA_OK(mark(1));
     ScoreArgs sa{logits, scores, cfg->gate_temp, m * n};
     if ((rc = launch(moe_score_kernel, dim3((m * n + MOE_SCORES_PER_CTA - 1) / MOE_SCORES_PER_CTA), dim3(256), 0,
                      s, false, sa)))
@@ -1208,6 +1222,7 @@ int moe_prefill_step(const moe_cfg *cfg, const moe_layer *layer, const moe_arena
                  status};
     moe_prefill_plan_kernel<<<1, 1024, 0, s>>>(pa);
     CUDA_OK(cudaGetLastError());
+    CUDA_OK(mark(2));
     // q8_1 of x, dequantised to fp16, gathered into pair order
     const int nbx = m * dim / 32;
     moe_prefill_xhat_kernel<<<(nbx + 7) / 8, 256, 0, s>>>(static_cast<const uint16_t *>(x), nbx, xhat, xhat_lo);
@@ -1217,6 +1232,7 @@ int moe_prefill_step(const moe_cfg *cfg, const moe_layer *layer, const moe_arena
     moe_prefill_gather_kernel<<<(unsigned)((gthreads + 255) / 256), 256, 0, s>>>(
         reinterpret_cast<const uint4 *>(xhat_lo), pair_tok, P, dim / 8, reinterpret_cast<uint4 *>(xg_lo));
     CUDA_OK(cudaGetLastError());
+    CUDA_OK(mark(3));
     // routed gate and up: Q2_K rows (4 super-blocks a raw stage) x the groups' rows
     const char *ab = static_cast<const char *>(arena->base);
     const uint64_t q2row = (uint64_t)dim / 256 * MOE_Q2K_BYTES, q3row = (uint64_t)inter / 256 * MOE_Q3K_BYTES;
@@ -1236,18 +1252,22 @@ int moe_prefill_step(const moe_cfg *cfg, const moe_layer *layer, const moe_arena
     ga.ntasks = ntasks;
     ga.raw_row = 4 * MOE_Q2K_BYTES;
     ga.rk = 1024;
-    ga.S = 2;
+    ga.S = 4;  // A stages in TMEM: 4 x 64 columns (hi and lo) beside two accumulators
     ga.SR = 2;
+    ga.ksplit = 2;
     ga.raw_bytes = (uint32_t)(TC_M * ga.raw_row);
-    if ((rc = launch_tc<1>(gmap, xmap, xlmap, ga, dim3(L.max_tasks, inter / TC_M), s)))
+    if ((rc = launch_tc<1>(gmap, xmap, xlmap, ga, dim3(L.max_tasks, inter / TC_M), s, I->smem_optin)))
         return rc;
+    CUDA_OK(mark(4));
     ga.out = u;
-    if ((rc = launch_tc<1>(umap, xmap, xlmap, ga, dim3(L.max_tasks, inter / TC_M), s)))
+    if ((rc = launch_tc<1>(umap, xmap, xlmap, ga, dim3(L.max_tasks, inter / TC_M), s, I->smem_optin)))
         return rc;
+    CUDA_OK(mark(5));
     // h = SwiGLU(g, u), its q8_1, dequantised to fp16
     const int nbh = P * inter / 32;
     moe_prefill_swiglu_kernel<<<(nbh + 7) / 8, 256, 0, s>>>(g, u, nbh, cfg->swiglu_limit, hh);
     CUDA_OK(cudaGetLastError());
+    CUDA_OK(mark(6));
     // routed down: Q3_K rows (8 super-blocks a raw stage), times each pair's weight
     TcArgs da = tc_args(dim, P, inter, dw, dim, status);
     da.colw = pair_w;
@@ -1255,32 +1275,77 @@ int moe_prefill_step(const moe_cfg *cfg, const moe_layer *layer, const moe_arena
     da.ntasks = ntasks;
     da.raw_row = 8 * MOE_Q3K_BYTES;
     da.rk = 2048;
-    da.S = 3;
+    da.S = 8;  // A stages in TMEM: 8 x 32 columns beside two accumulators
     da.SR = 1;
+    da.ksplit = 2;
     da.raw_bytes = (uint32_t)(TC_M * da.raw_row);
-    if ((rc = launch_tc<2>(dmap, hmap, hmap, da, dim3(L.max_tasks, dim / TC_M), s)))
+    if ((rc = launch_tc<2>(dmap, hmap, hmap, da, dim3(L.max_tasks, dim / TC_M), s, I->smem_optin)))
         return rc;
+    CUDA_OK(mark(7));
     // the bf16 shared expert as dense GEMMs
     const float *sdp = nullptr;
     if (layer->sh_w1) {
-        if ((rc = gemm_bf16(layer->sh_w1, x, gs, inter, m, dim, inter, status, s)) ||
-            (rc = gemm_bf16(layer->sh_w3, x, us, inter, m, dim, inter, status, s)))
+        if ((rc = gemm_bf16(layer->sh_w1, x, gs, inter, m, dim, inter, status, s, I->smem_optin)) ||
+            (rc = gemm_bf16(layer->sh_w3, x, us, inter, m, dim, inter, status, s, I->smem_optin)))
             return rc;
         const size_t ns = (size_t)m * inter;
         moe_prefill_shared_swiglu_kernel<<<(unsigned)((ns + 255) / 256), 256, 0, s>>>(gs, us, ns, cfg->swiglu_limit,
                                                                                        hs);
         CUDA_OK(cudaGetLastError());
-        if ((rc = gemm_bf16(layer->sh_w2, hs, sd, dim, m, inter, dim, status, s)))
+        if ((rc = gemm_bf16(layer->sh_w2, hs, sd, dim, m, inter, dim, status, s, I->smem_optin)))
             return rc;
         sdp = sd;
     }
+    CUDA_OK(mark(8));
     // acc (pairs in ascending expert id, then sd), residual, x_next
     const size_t nf = (size_t)m * dim;
     moe_prefill_finish_kernel<<<(unsigned)((nf + 255) / 256), 256, 0, s>>>(
         dw, picks, pick_pair, k, sdp, acc, residual, static_cast<uint16_t *>(x_next), m, dim);
     CUDA_OK(cudaGetLastError());
+    CUDA_OK(mark(9));
     (void)cnt;
     (void)off;
+    return MOE_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int moe_prefill_step(const moe_cfg *cfg, const moe_layer *layer, const moe_arena *arena, int64_t arena_slots,
+                     const void *x, float *residual, void *x_next, int32_t *picks, float *weights, int m,
+                     void *ws, size_t ws_bytes, moe_stream_t stream)
+{
+    return prefill_step(cfg, layer, arena, arena_slots, x, residual, x_next, picks, weights, m, ws, ws_bytes, stream,
+                        nullptr);
+}
+
+int moe_prefill_step_profiled(const moe_cfg *cfg, const moe_layer *layer, const moe_arena *arena,
+                              int64_t arena_slots, const void *x, float *residual, void *x_next, int32_t *picks,
+                              float *weights, int m, void *ws, size_t ws_bytes, moe_stream_t stream, float *ms)
+{
+    if (!ms)
+        return fail(MOE_EINVAL, "moe_prefill_step_profiled: ms is NULL");
+    thread_local cudaEvent_t ev[10] = {};
+    thread_local int ev_dev = -1;
+    int d = 0;
+    CUDA_OK(cudaGetDevice(&d));
+    if (ev_dev != d) {
+        for (int i = 0; i < 10; ++i)
+            CUDA_OK(cudaEventCreate(&ev[i]));
+        ev_dev = d;
+    }
+    int rc = prefill_step(cfg, layer, arena, arena_slots, x, residual, x_next, picks, weights, m, ws, ws_bytes,
+                          stream, ev);
+    if (rc)
+        return rc;
+    if (m == 0) {
+        for (int i = 0; i < 9; ++i)
+            ms[i] = 0.0f;
+        return MOE_OK;
+    }
+    CUDA_OK(cudaEventSynchronize(ev[9]));
+    for (int i = 0; i < 9; ++i)
+        CUDA_OK(cudaEventElapsedTime(&ms[i], ev[i], ev[i + 1]));
     return MOE_OK;
 }
 

@@ -14,9 +14,13 @@
 //   AK = 2  A dequantised from Q3_K blocks  -- routed down
 // For AK > 0 a producer warp streams the raw blocks of 128 weight rows with
 // 3-D TMA loads (u32 elements over [slot][row][bytes] of the expert arena)
-// and four worker warps turn them into fp16 operand tiles in the 128-byte
-// swizzled layout (each weight d * sc * q - dmin * m or d * sc * q in f32,
-// then rounded to fp16); B is the group's activation rows, fp16, by TMA.
+// and eight worker warps turn them into fp16 A operands held in tensor
+// memory (each thread a row -- its TMEM lane -- written with tcgen05.st; each
+// weight d * sc * q - dmin * m or d * sc * q in f32, then rounded to fp16),
+// which the MMAs read from TMEM: the large operand never passes through
+// shared memory, whose bandwidth would otherwise bound the kernel (fp16 tiles
+// written once and read by every MMA). B is the group's activation rows,
+// fp16, by TMA.
 // gate and up (AK = 1) split both operands into fp16 pairs hi + lo (22
 // significant bits: the dequantised q8_1 activation, 18 bits, exactly; the
 // weight to 2^-23) and accumulate hi.hi + hi.lo + lo.hi, so g and u are as
@@ -27,8 +31,9 @@
 // (about 2e-5 relative over K = 4096), so K is split over up to four
 // accumulators in TMEM (4 x 128 columns) whose results the epilogue adds in
 // f32, in order; over K = 4096 that keeps the router logits within 1e-5.
-// One warp issues the MMAs; the four worker warps are the epilogue (TMEM ->
-// registers -> global).
+// One warp issues the MMAs; the eight worker warps (two a scheduler: the
+// dequantisation is a chain of dependent integer and float steps) are also
+// the epilogue (TMEM -> registers -> global).
 #pragma once
 #include "moe_tc.cuh"
 #include "moe_route.cuh"
@@ -38,9 +43,13 @@ namespace moe {
 #define TC_M 128        // rows of a tile (weights)
 #define TC_NT 128       // columns (tokens) of a tile, at most
 #define TC_KC 64        // K per stage (one 128-byte swizzle atom of 16-bit elements)
-#define TC_THREADS 192  // warps 0-3 workers / epilogue, 4 producer, 5 MMA
+#define TC_WORKERS 8    // worker warps: two threads a tile row (one 32-weight group each)
+#define TC_THREADS ((TC_WORKERS + 3) * 32)  // warps 0-7 workers / epilogue, 8 and 9 producers, 10 MMA
 #define TC_BROWS 16     // rows of a B TMA box
-#define TC_TMEM_COLS 512  // TMEM columns a CTA holds: up to 4 accumulators of TC_NT columns
+#define TC_TMEM_COLS 512  // TMEM columns a CTA holds: up to 4 accumulators of TC_NT columns (dense),
+                          // or 2 accumulators and the A stages from column 256 (K-quant)
+#define TC_TA0 256        // first TMEM column of the K-quant A stages
+#define TC_SB_MAX 16      // stages of the B ring, at most
 
 // a column task of the routed GEMMs: the expert's slot, its first pair and
 // the number of its pairs in this tile
@@ -60,6 +69,7 @@ struct TcArgs {
     uint32_t raw_bytes;     // AK > 0: bytes of one raw stage (128 rows x raw_row)
     int rk;                 // AK > 0: K per raw stage
     int ksplit;             // K split over this many accumulators (1, 2 or 4), added in f32 at the end
+    uint32_t b_buf;         // bytes of the B ring (a multiple of 2048)
     uint32_t *status;
     unsigned long long wait_ns;
 };
@@ -67,10 +77,11 @@ struct TcArgs {
 // operands of a stage: hi and lo tiles for the split GEMM (gate, up)
 __host__ __device__ constexpr int tc_parts(int AK) { return AK == 1 ? 2 : 1; }
 
-__host__ __device__ inline size_t tc_smem_bytes(int parts, int S, int SR, uint32_t raw_bytes)
+// AK = 0 keeps its A stages in shared memory, the K-quant kernels in TMEM
+__host__ __device__ inline size_t tc_smem_bytes(int AK, int S, int SR, uint32_t raw_bytes, uint32_t b_buf)
 {
-    // 1024 alignment slack, A and B stages (16 KB a part each), raw stages, barriers + TMEM address
-    return 1024 + (size_t)S * 2 * parts * 16384 + (size_t)SR * raw_bytes + 256;
+    // 1024 alignment slack, A stages (16 KB), raw stages, the B ring, barriers + TMEM address
+    return 1024 + (AK == 0 ? (size_t)S * 16384 : 0) + (size_t)SR * raw_bytes + b_buf + 512;
 }
 
 // f32 pair -> fp16 pairs hi (the rounding) and lo (the rounding of the rest)
@@ -83,49 +94,45 @@ __device__ __forceinline__ void split_half2(float a, float b, uint32_t &hi, uint
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
-// Q2_K: 64 weights (quarter kq of the super-block at blk) of one row -> 32
-// words of fp16 pairs (hi) and of the pairs' remainders (lo), element order.
-// w = d sc q - dmin m (one f32 rounding).
-__device__ __forceinline__ void dq_q2k_quarter(const uint8_t *blk, int kq, uint32_t (&o)[32], uint32_t (&ol)[32])
+// Q2_K: the 32 weights of group gi (0, 1) of quarter kq of the super-block at
+// blk (elements 32 gi .. 32 gi + 31 of the quarter) of one row -> 16 words of
+// fp16 pairs (hi) and of the pairs' remainders (lo), element order.
+// w = d sc q - dmin m (one f32 rounding). A weight takes one of four values a
+// sub-block (q = 0..3): their hi and lo halves form two 8-byte tables, and a
+// byte permute with a selector made from two quants (one multiply-add) fetches
+// a pair of weights.
+__device__ __forceinline__ void dq_q2k_group(const uint8_t *blk, int kq, int gi, uint32_t (&o)[16], uint32_t (&ol)[16])
 {
     const uint32_t *bw = reinterpret_cast<const uint32_t *>(blk);  // 4-byte aligned (84-byte blocks)
-    const uint32_t scw = bw[kq];                                   // scales of sub-blocks 4 kq .. 4 kq + 3
+    const uint32_t scw = bw[kq] >> (16 * gi);                      // scales of sub-blocks 4 kq + 2 gi, + 1
     const uint32_t dd = bw[20];
     const float d = f16_bits_to_f32(dd), dmin = f16_bits_to_f32(dd >> 16);
-    float ds[4], dm[4];
+    uint32_t th[2][2], tl[2][2];  // [sub-block][q >> 1]: halves of q = 0, 1 and q = 2, 3
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 2; ++u) {
         const uint32_t sc = (scw >> (8 * u)) & 0xFFu;
-        ds[u] = d * (float)(sc & 15u);
-        dm[u] = dmin * (float)(sc >> 4);
+        const float ds = d * (float)(sc & 15u), dm = dmin * (float)(sc >> 4);
+        split_half2(-dm, fmaf(1.0f, ds, -dm), th[u][0], tl[u][0]);
+        split_half2(fmaf(2.0f, ds, -dm), fmaf(3.0f, ds, -dm), th[u][1], tl[u][1]);
     }
-    const int half = kq >> 1, g0 = 2 * (kq & 1);
-    uint32_t W[8];
+    const int half = kq >> 1, sh = 2 * (2 * (kq & 1) + gi);
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-        W[i] = bw[4 + 8 * half + i];
-#pragma unroll
-    for (int gi = 0; gi < 2; ++gi) {
-#pragma unroll
-        for (int wi = 0; wi < 8; ++wi) {
-            const uint32_t qq = (W[wi] >> (2 * (g0 + gi))) & 0x03030303u;
-            const int u = 2 * gi + (wi >> 2);
-            float f[4];
-#pragma unroll
-            for (int b = 0; b < 4; ++b)  // 2^23 + q exactly, then q
-                f[b] = __uint_as_float(__byte_perm(qq, 0x4B000000u, b | 0x7440)) - 8388608.0f;
-            split_half2(fmaf(f[0], ds[u], -dm[u]), fmaf(f[1], ds[u], -dm[u]), o[16 * gi + 2 * wi],
-                        ol[16 * gi + 2 * wi]);
-            split_half2(fmaf(f[2], ds[u], -dm[u]), fmaf(f[3], ds[u], -dm[u]), o[16 * gi + 2 * wi + 1],
-                        ol[16 * gi + 2 * wi + 1]);
-        }
+    for (int wi = 0; wi < 8; ++wi) {
+        const uint32_t qq = (bw[4 + 8 * half + wi] >> sh) & 0x03030303u;  // four quants, one a byte
+        const int u = wi >> 2;
+        // selector of halfwords q_a, q_b: nibbles 2 q_a, 2 q_a + 1, 2 q_b, 2 q_b + 1
+        const uint32_t s01 = (qq & 0x0303u) * 0x22u + 0x1010u, s23 = (qq >> 16) * 0x22u + 0x1010u;
+        o[2 * wi] = __byte_perm(th[u][0], th[u][1], s01);
+        o[2 * wi + 1] = __byte_perm(th[u][0], th[u][1], s23);
+        ol[2 * wi] = __byte_perm(tl[u][0], tl[u][1], s01);
+        ol[2 * wi + 1] = __byte_perm(tl[u][0], tl[u][1], s23);
     }
 }
 
-// Q3_K: 64 weights (quarter kq) of one row from a 110-byte block at a 2-byte
-// aligned address. w = d * (scale - 32) * q (exact in f32), q = low2 | hbit
-// << 2 minus 4.
-__device__ __forceinline__ void dq_q3k_quarter(const uint8_t *blk, int kq, uint32_t (&o)[32])
+// Q3_K: the 32 weights of group gi of quarter kq of one row from a 110-byte
+// block at a 2-byte aligned address. w = d * (scale - 32) * q (exact in
+// f32), q = low2 | hbit << 2 minus 4.
+__device__ __forceinline__ void dq_q3k_group(const uint8_t *blk, int kq, int gi, uint32_t (&o)[16])
 {
     const uintptr_t a = reinterpret_cast<uintptr_t>(blk);
     const uint32_t *W = reinterpret_cast<const uint32_t *>(a & ~(uintptr_t)3);
@@ -142,30 +149,27 @@ __device__ __forceinline__ void dq_q3k_quarter(const uint8_t *blk, int kq, uint3
     const float d = f16_bits_to_f32(word(27));
     const uint32_t scb[3] = {s0, s1, s2};
     auto sbyte = [&](int i) { return (scb[i >> 2] >> (8 * (i & 3))) & 0xFFu; };
-    float ds[4];
+    float ds[2];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const int i = 4 * kq + u;  // sub-block
+    for (int u = 0; u < 2; ++u) {
+        const int i = 4 * kq + 2 * gi + u;  // sub-block
         const uint32_t lo4 = i < 8 ? (sbyte(i) & 15u) : (sbyte(i - 8) >> 4);
         const uint32_t hi2 = (sbyte(8 + (i & 3)) >> (2 * (i >> 2))) & 3u;
         ds[u] = d * (float)((int)(lo4 | (hi2 << 4)) - 32);
     }
+    const int g = g0 + gi, hsh = 4 * half + g;  // weight j: bit j / 32 of hmask[j % 32]
 #pragma unroll
-    for (int gi = 0; gi < 2; ++gi) {
-        const int g = g0 + gi, hsh = 4 * half + g;  // weight j: bit j / 32 of hmask[j % 32]
+    for (int wi = 0; wi < 8; ++wi) {
+        const uint32_t v = ((qv[wi] >> (2 * g)) & 0x03030303u) | (((hm[wi] >> hsh) & 0x01010101u) << 2);
+        const int u = wi >> 2;
+        float f[4];
 #pragma unroll
-        for (int wi = 0; wi < 8; ++wi) {
-            const uint32_t v = ((qv[wi] >> (2 * g)) & 0x03030303u) | (((hm[wi] >> hsh) & 0x01010101u) << 2);
-            const int u = 2 * gi + (wi >> 2);
-            float f[4];
-#pragma unroll
-            for (int b = 0; b < 4; ++b)  // 2^23 + v exactly, then v - 4
-                f[b] = __uint_as_float(__byte_perm(v, 0x4B000000u, b | 0x7440)) - 8388612.0f;
-            const __half2 h01 = __floats2half2_rn(f[0] * ds[u], f[1] * ds[u]);
-            const __half2 h23 = __floats2half2_rn(f[2] * ds[u], f[3] * ds[u]);
-            o[16 * gi + 2 * wi] = *reinterpret_cast<const uint32_t *>(&h01);
-            o[16 * gi + 2 * wi + 1] = *reinterpret_cast<const uint32_t *>(&h23);
-        }
+        for (int b = 0; b < 4; ++b)  // 2^23 + v exactly, then v - 4
+            f[b] = __uint_as_float(__byte_perm(v, 0x4B000000u, b | 0x7440)) - 8388612.0f;
+        const __half2 h01 = __floats2half2_rn(f[0] * ds[u], f[1] * ds[u]);
+        const __half2 h23 = __floats2half2_rn(f[2] * ds[u], f[3] * ds[u]);
+        o[2 * wi] = *reinterpret_cast<const uint32_t *>(&h01);
+        o[2 * wi + 1] = *reinterpret_cast<const uint32_t *>(&h23);
     }
 }
 
@@ -183,16 +187,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const __grid_constant__ CUtensorMap bmap_lo, TcArgs a)
 {
     constexpr int PARTS = tc_parts(AK);
-    constexpr uint32_t STG = PARTS * 16384u;  // bytes of a stage's A (or B) tiles: hi, then lo
+    constexpr uint32_t TAC = 32 * PARTS;  // TMEM columns of a K-quant A stage: 64 fp16 a row, hi then lo
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int S = a.S, SR = a.SR;
-    uint8_t *sa = smem;                    // S x STG
-    uint8_t *sb = smem + (size_t)S * STG;  // S x STG
-    uint8_t *sraw = sb + (size_t)S * STG;  // SR x raw_bytes
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sraw + (size_t)SR * a.raw_bytes);
-    uint64_t *full_a = bars, *full_b = bars + S, *empty = bars + 2 * S, *raw_full = bars + 3 * S;
-    uint64_t *raw_empty = raw_full + SR, *done = raw_empty + SR;
+    uint8_t *sa = smem;                                           // AK = 0: S x 16 KB
+    uint8_t *sraw = sa + (AK == 0 ? (size_t)S * 16384 : 0);      // SR x raw_bytes
+    uint8_t *sb = sraw + (size_t)SR * a.raw_bytes;  // the B ring, b_buf bytes
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sb + a.b_buf);
+    uint64_t *full_a = bars, *empty_a = bars + S, *full_b = bars + 2 * S, *empty_b = full_b + TC_SB_MAX;
+    uint64_t *raw_full = empty_b + TC_SB_MAX, *raw_empty = raw_full + SR, *done = raw_empty + SR;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -209,21 +213,28 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         c0 = t.c0;
         ncols = t.ncols;
     }
-    const int nb16 = (ncols + TC_BROWS - 1) / TC_BROWS;  // B boxes a stage
+    const int nb16 = (ncols + TC_BROWS - 1) / TC_BROWS;  // B boxes a stage and part
     const int n_mma = nb16 * TC_BROWS;                   // MMA N (a multiple of 16)
     const uint32_t idesc = mma_idesc(TC_M, n_mma, AK == 0);
     const int KC = a.K / TC_KC;
-    const int per_raw = AK == 0 ? 1 : a.rk / TC_KC;     // operand stages a raw stage feeds
+    const int per_raw = AK == 0 ? 1 : a.rk / TC_KC;     // A stages a raw stage feeds
+    // the B ring holds as many stages as the tile's columns allow: narrow
+    // groups keep many loads in flight
+    const uint32_t bpart = (uint32_t)nb16 * TC_BROWS * 128u, bstage = PARTS * bpart;
+    const int SB = max(1, min(TC_SB_MAX, (int)(a.b_buf / bstage)));
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(&full_a[s], AK == 0 ? 1 : 128);
+            mbar_init(&full_a[s], AK == 0 ? 1 : TC_WORKERS);  // one arrival a worker warp
+            mbar_init(&empty_a[s], 1);
+        }
+        for (int s = 0; s < SB; ++s) {
             mbar_init(&full_b[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty_b[s], 1);
         }
         for (int r = 0; r < SR; ++r) {
             mbar_init(&raw_full[r], 1);
-            mbar_init(&raw_empty[r], 128);
+            mbar_init(&raw_empty[r], TC_WORKERS);
         }
         mbar_init(done, 1);
         fence_barrier_init();
@@ -236,13 +247,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const uint32_t tmem = *tmem_slot;
     bool dead = false;
 
-    if (warp == 4) {
-        // ---------------- producer: B boxes (and A, or the raw blocks)
+    if (warp == TC_WORKERS) {
+        // ---------------- producers: this warp the A side (A tiles, or the
+        // raw blocks), the next the B ring, each on its own barriers
         if (lane == 0) {
             tma_prefetch_map(&amap);
-            tma_prefetch_map(&bmap);
-            if constexpr (PARTS == 2)
-                tma_prefetch_map(&bmap_lo);
             for (int kc = 0; kc < KC; ++kc) {
                 if constexpr (AK > 0) {
                     if (kc % per_raw == 0) {
@@ -253,53 +262,71 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         tma_load_3d(sraw + (size_t)r * a.raw_bytes, &amap, rc * (a.raw_row / 4), m0, slot,
                                     &raw_full[r]);
                     }
-                }
-                const int s = kc % S;
-                if (kc >= S)
-                    tc_wait(&empty[s], (uint32_t)((kc / S - 1) & 1), a, dead);
-                if constexpr (AK == 0) {
+                } else {
+                    const int s = kc % S;
+                    if (kc >= S)
+                        tc_wait(&empty_a[s], (uint32_t)((kc / S - 1) & 1), a, dead);
                     mbar_arrive_expect_tx(&full_a[s], 16384u);
-                    tma_load_2d(sa + (size_t)s * STG, &amap, kc * TC_KC, m0, &full_a[s]);
-                }
-                mbar_arrive_expect_tx(&full_b[s], (uint32_t)PARTS * nb16 * TC_BROWS * 128u);
-                for (int i = 0; i < nb16; ++i) {
-                    tma_load_2d(sb + (size_t)s * STG + i * TC_BROWS * 128, &bmap, kc * TC_KC, c0 + i * TC_BROWS,
-                                &full_b[s]);
-                    if constexpr (PARTS == 2)
-                        tma_load_2d(sb + (size_t)s * STG + 16384 + i * TC_BROWS * 128, &bmap_lo, kc * TC_KC,
-                                    c0 + i * TC_BROWS, &full_b[s]);
+                    tma_load_2d(sa + (size_t)s * 16384, &amap, kc * TC_KC, m0, &full_a[s]);
                 }
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == TC_WORKERS + 1) {
+        if (lane == 0) {
+            tma_prefetch_map(&bmap);
+            if constexpr (PARTS == 2)
+                tma_prefetch_map(&bmap_lo);
+            for (int kc = 0; kc < KC; ++kc) {
+                const int s = kc % SB;
+                if (kc >= SB)
+                    tc_wait(&empty_b[s], (uint32_t)((kc / SB - 1) & 1), a, dead);
+                uint8_t *dst = sb + (size_t)s * bstage;
+                mbar_arrive_expect_tx(&full_b[s], bstage);
+                for (int i = 0; i < nb16; ++i) {
+                    tma_load_2d(dst + i * TC_BROWS * 128, &bmap, kc * TC_KC, c0 + i * TC_BROWS, &full_b[s]);
+                    if constexpr (PARTS == 2)
+                        tma_load_2d(dst + bpart + i * TC_BROWS * 128, &bmap_lo, kc * TC_KC, c0 + i * TC_BROWS,
+                                    &full_b[s]);
+                }
+            }
+        }
+    } else if (warp == TC_WORKERS + 2) {
         // ---------------- MMA issuer
         if (lane == 0) {
             const int kper = KC / a.ksplit;  // K-chunks an accumulator takes
             for (int kc = 0; kc < KC; ++kc) {
-                const int s = kc % S;
-                const uint32_t ph = (uint32_t)((kc / S) & 1);
+                const int s = kc % S, t = kc % SB;
+                tc_wait(&full_a[s], (uint32_t)((kc / S) & 1), a, dead);
+                tc_wait(&full_b[t], (uint32_t)((kc / SB) & 1), a, dead);
+                tc_fence_after();
                 const uint32_t acc = tmem + (uint32_t)(kc / kper) * TC_NT;
                 const bool first = kc % kper == 0;
-                tc_wait(&full_a[s], ph, a, dead);
-                tc_wait(&full_b[s], ph, a, dead);
-                tc_fence_after();
-                const uint64_t ad = sw128_desc(sa + (size_t)s * STG), bd = sw128_desc(sb + (size_t)s * STG);
+                const uint64_t bd = sw128_desc(sb + (size_t)t * bstage);
+                if constexpr (AK == 0) {
+                    const uint64_t ad = sw128_desc(sa + (size_t)s * 16384);
 #pragma unroll
-                for (int k = 0; k < TC_KC / 16; ++k) {  // K = 16 a step: 32 bytes further in the swizzle atom
-                    mma_f16(acc, ad + 2 * k, bd + 2 * k, idesc, !first || k > 0);
-                    if constexpr (PARTS == 2) {  // + hi . lo + lo . hi (lo tiles 16 KB after the hi tiles)
-                        mma_f16(acc, ad + 2 * k, bd + (16384 >> 4) + 2 * k, idesc, true);
-                        mma_f16(acc, ad + (16384 >> 4) + 2 * k, bd + 2 * k, idesc, true);
+                    for (int k = 0; k < TC_KC / 16; ++k)  // K = 16 a step: 32 bytes further in the swizzle atom
+                        mma_f16(acc, ad + 2 * k, bd + 2 * k, idesc, !first || k > 0);
+                } else {
+                    const uint32_t ta = tmem + TC_TA0 + (uint32_t)s * TAC;  // A in TMEM: 8 columns a K = 16 step
+#pragma unroll
+                    for (int k = 0; k < TC_KC / 16; ++k) {
+                        mma_f16_ts(acc, ta + 8 * k, bd + 2 * k, idesc, !first || k > 0);
+                        if constexpr (PARTS == 2) {  // + hi . lo + lo . hi (lo parts after the hi parts)
+                            mma_f16_ts(acc, ta + 8 * k, bd + (bpart >> 4) + 2 * k, idesc, true);
+                            mma_f16_ts(acc, ta + 32 + 8 * k, bd + 2 * k, idesc, true);
+                        }
                     }
                 }
-                mma_commit(&empty[s]);
+                mma_commit(&empty_a[s]);
+                mma_commit(&empty_b[t]);
             }
             mma_commit(done);
         }
     } else {
         // ---------------- workers (AK > 0): raw blocks -> fp16 operand tiles
         if constexpr (AK > 0) {
-            const int r = threadIdx.x;  // the tile row this thread builds
+            const int r = threadIdx.x & (TC_M - 1), gi = threadIdx.x >> 7;  // tile row, 32-weight group
             const int bbytes = AK == 1 ? MOE_Q2K_BYTES : MOE_Q3K_BYTES;
             for (int kc = 0; kc < KC; ++kc) {
                 const int rc = kc / per_raw, ri = rc % SR, q = kc % per_raw;
@@ -307,36 +334,38 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     tc_wait(&raw_full[ri], (uint32_t)((rc / SR) & 1), a, dead);
                 const int s = kc % S;
                 if (kc >= S)
-                    tc_wait(&empty[s], (uint32_t)((kc / S - 1) & 1), a, dead);
+                    tc_wait(&empty_a[s], (uint32_t)((kc / S - 1) & 1), a, dead);
                 const uint8_t *blk = sraw + (size_t)ri * a.raw_bytes + (size_t)r * a.raw_row + (q >> 2) * bbytes;
-                uint32_t o[32];
-                uint8_t *tile = sa + (size_t)s * STG;
+                // this thread's row of the stage: TMEM lane r, columns 16 gi .. (hi), + 32 (lo)
+                const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + TC_TA0 + (uint32_t)s * TAC +
+                                    16u * (uint32_t)gi;
+                uint32_t o[16];
                 if constexpr (AK == 1) {
-                    uint32_t ol[32];
-                    dq_q2k_quarter(blk, q & 3, o, ol);
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4 *>(tile + 16384 + sw128_offset(r, 8 * c)) =
-                            make_uint4(ol[4 * c], ol[4 * c + 1], ol[4 * c + 2], ol[4 * c + 3]);
+                    uint32_t ol[16];
+                    dq_q2k_group(blk, q & 3, gi, o, ol);
+                    tmem_st16(ta, o);
+                    tmem_st16(ta + 32, ol);
                 } else {
-                    dq_q3k_quarter(blk, q & 3, o);
+                    dq_q3k_group(blk, q & 3, gi, o);
+                    tmem_st16(ta, o);
                 }
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<uint4 *>(tile + sw128_offset(r, 8 * c)) =
-                        make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-                fence_proxy_async_smem();  // generic-proxy writes before the MMA reads them
-                mbar_arrive(&full_a[s]);
-                if (q == per_raw - 1)
-                    mbar_arrive(&raw_empty[ri]);
+                tmem_st_wait();
+                tc_fence_before();  // the stores before the arrival the MMA thread acquires
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&full_a[s]);
+                    if (q == per_raw - 1)
+                        mbar_arrive(&raw_empty[ri]);
+                }
             }
         }
-        // ---------------- epilogue: row m0 + threadIdx.x, columns 32 at a time
+        // ---------------- epilogue: row m0 + 32 (warp % 4) + lane (the TMEM lane
+        // quadrant of the warp), column blocks of 32 shared by warps w, w + 4
         tc_wait(done, 0, a, dead);
         tc_fence_after();
-        const int row = m0 + (int)threadIdx.x;
-        const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-        for (int cb = 0; cb < ncols; cb += 32) {
+        const int row = m0 + 32 * (warp & 3) + lane;
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        for (int cb = 32 * (warp >> 2); cb < ncols; cb += 32 * (TC_WORKERS / 4)) {
             float v[32];
             tmem_ld32(lane_addr + (uint32_t)cb, v);
             for (int j = 1; j < a.ksplit; ++j) {
