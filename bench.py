@@ -15,7 +15,8 @@ all ranks.
 
 Other workloads (--workload): batch8 (the same layers at m = 8 tokens),
 chain40 (40 stacked layers, one token, one replay = one 40-layer decode step;
-tokens/s).
+tokens/s), prefill (512 tokens through one layer on the tensor-core arm,
+correction bias ~U(-1, 1); tokens/s).
 
 --impl reference times the CPU oracle (oracle/, plain C, f64) on the same
 workload and metric: each step one token through one layer, on the host cores.
@@ -47,6 +48,9 @@ WORKLOADS = {
     "decode": (1, 8, "decode tokens/s per MoE layer step (1 GB300)", "token-layer steps/s"),
     "batch8": (8, 8, "decode tokens/s per MoE layer step (1 GB300), m=8", "token-layer steps/s"),
     "chain40": (1, 40, "decode tokens/s, 40-layer MoE decode step (1 GB300)", "tokens/s"),
+    # the batched (prefill) arm: 512 tokens through one layer, expert load
+    # skewed by a correction bias ~U(-1, 1)
+    "prefill": (512, 1, "prefill tokens/s through one MoE layer, 512 tokens (1 GB300)", "tokens/s"),
 }
 
 
@@ -180,7 +184,7 @@ def hbm_peak():
 
 # ------------------------------------------------------------------ CPU oracle (baseline leg)
 
-def oracle_sample(cfg, m, budget_s, seed=1000, max_steps=10 ** 9, warmup=0):
+def oracle_sample(cfg, m, budget_s, seed=1000, max_steps=10 ** 9, warmup=0, bias_range=(-0.1, 0.1)):
     """The oracle as it stands, on host cores: one layer step per iteration over
     the same synthetic decode layer. Returns (steps, seconds, threads, sample text)."""
     import numpy as np
@@ -192,7 +196,7 @@ def oracle_sample(cfg, m, budget_s, seed=1000, max_steps=10 ** 9, warmup=0):
     oc = oracle.cfg(cfg.dim, cfg.inter, cfg.n_routed, cfg.topk, cfg.norm_topk_prob, cfg.gate_temp,
                     cfg.route_scale, cfg.swiglu_limit)
     router = synth.router_bf16(seed, 0, cfg.n_routed, cfg.dim)
-    bias = synth.bias_f32(seed, 0, cfg.n_routed)
+    bias = synth.bias_f32(seed, 0, cfg.n_routed, *bias_range)
     shared = synth.shared_bf16(seed, 0, cfg.dim, cfg.inter)
     cache = {}
     done, spent, i = 0, 0.0, 0
@@ -216,8 +220,8 @@ def oracle_sample(cfg, m, budget_s, seed=1000, max_steps=10 ** 9, warmup=0):
             continue
         spent += dt
         done += 1
-    sample = (f"{done} layer steps of the {m}-token decode layer (dim {cfg.dim}, inter {cfg.inter}, "
-              f"{cfg.n_routed}x{cfg.topk}, shared expert), oracle.layer timed, {threads} threads")
+    sample = (f"{done} layer steps of {m} tokens through the decode layer (dim {cfg.dim}, inter {cfg.inter}, "
+              f"{cfg.n_routed}x{cfg.topk}, shared expert, bias U{bias_range}), oracle.layer timed, {threads} threads")
     return done, spent, threads, sample
 
 
@@ -401,6 +405,159 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------ the prefill arm
+
+PREFILL_BIAS = (-1.0, 1.0)
+PREFILL_STAGES = ["router", "select_plan", "xhat_gather", "gate", "up", "swiglu_q8", "down", "shared", "finish"]
+
+
+def run_prefill(args):
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    from moe_decode_quantized_gb300 import build as mbuild
+    mbuild.build()
+    import moe_decode_quantized_gb300 as moe
+    from moe_decode_quantized_gb300.workload import Workload, x_tensor
+
+    m, _, metric, unit = WORKLOADS["prefill"]
+    cfg = decode_cfg(1, args.experts)
+    wl = Workload(cfg, n_layers=1, seed=rank, shared=True, bias_range=PREFILL_BIAS)
+    nb = 4  # distinct batches the steps take in turn
+    xs = torch.stack([x_tensor(rank, 3000 + i, m, cfg.dim) for i in range(nb)])
+    res = torch.zeros((m, cfg.dim), dtype=torch.float32, device="cuda")
+    xn = torch.empty_like(xs[0])
+    picks = torch.zeros((m, cfg.topk), dtype=torch.int32, device="cuda")
+    weights = torch.zeros((m, cfg.topk), dtype=torch.float32, device="cuda")
+    ws = torch.empty(moe.prefill_workspace_bytes(cfg, m), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    it = [0]
+
+    def step():
+        res.zero_()
+        moe.prefill_step(cfg, wl.layer(0), wl.arena, cfg.n_routed, xs[it[0] % nb], res, xn, picks, weights, m, ws)
+        it[0] += 1
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.soak:
+        for _ in range(10):
+            step()
+        torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    if moe.prefill_status(cfg, m, ws):
+        raise RuntimeError("prefill status set after the timed region")
+    units, secs = aggregate(float(args.steps * m), ms / 1e3, world)
+
+    # stages with CUDA events on the launching stream, the batches in turn
+    st = np.mean([moe.prefill_step_profiled(cfg, wl.layer(0), wl.arena, cfg.n_routed, xs[i % nb], res, xn,
+                                            picks, weights, m, ws) for i in range(2 * nb)], axis=0)
+    used = len(np.unique(picks.cpu().numpy()))
+    dim, inter, P = cfg.dim, cfg.inter, m * cfg.topk
+    q2 = inter * (dim // 256) * 84
+    q3 = dim * (inter // 256) * 110
+    # algorithmic bytes and flops of the three routed GEMMs: the picked
+    # experts' blocks once, the group rows (fp16 hi + lo for gate / up) once,
+    # the outputs once; flops of the products the layer defines
+    gemm_bytes = {"gate": used * q2 + P * dim * 4 + P * inter * 4, "up": used * q2 + P * dim * 4 + P * inter * 4,
+                  "down": used * q3 + P * inter * 2 + P * dim * 4}
+    gemm_flops = {"gate": 2.0 * P * inter * dim, "up": 2.0 * P * inter * dim, "down": 2.0 * P * dim * inter}
+    idx = {n: i for i, n in enumerate(PREFILL_STAGES)}
+    st = [float(v) for v in st]
+    dom = max(gemm_bytes, key=lambda n: st[idx[n]])
+    dur = st[idx[dom]] * 1e-3
+    peak, peak_kind = hbm_peak()
+    achieved = gemm_bytes[dom] / dur / 1e9
+    try:
+        bf16_peak = float(json.load(open(PEAKS))["bf16_tflops"])
+    except (OSError, ValueError, KeyError):
+        bf16_peak = 1900.0
+
+    # e2e: x from pinned host memory in, the residual back, every step
+    xh = xs.cpu().pin_memory()
+    rh = torch.empty_like(res, device="cpu").pin_memory()
+    xd = torch.empty_like(xs[0])
+    for i in range(max(1, args.warmup)):
+        xd.copy_(xh[i % nb], non_blocking=True)
+        res.zero_()
+        moe.prefill_step(cfg, wl.layer(0), wl.arena, cfg.n_routed, xd, res, xn, picks, weights, m, ws)
+        rh.copy_(res, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record(stream)
+    for i in range(args.steps):
+        xd.copy_(xh[i % nb], non_blocking=True)
+        res.zero_()
+        moe.prefill_step(cfg, wl.layer(0), wl.arena, cfg.n_routed, xd, res, xn, picks, weights, m, ws)
+        rh.copy_(res, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier(world)
+    e_units, e_secs = aggregate(float(args.steps * m), max(e0.elapsed_time(e1) / 1e3, wall), world)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        n, spent, thr, sample = oracle_sample(cfg, 4, args.cpu_budget, bias_range=PREFILL_BIAS)
+        cpu = {"value": n * 4 / spent, "unit": unit, "cores": thr, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        out = {
+            "metric": metric, "value": units / secs, "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16 router / shared GEMMs; routed Q2_K / Q3_K dequantised to fp16 (gate / up as hi + lo "
+                     "pairs), f32 accumulate in TMEM",
+            "data": "synthetic (seeded SplitMix64: random Q2_K/Q3_K blocks, bf16 ~N(0,0.02) router and shared "
+                    "expert, x ~N(0,1), correction bias ~U(-1,1))",
+            "config": {
+                "workload": f"prefill: {m} tokens through one MoE layer (dim 4096, inter 2048, {cfg.n_routed} "
+                            "routed experts top 6, Q2_K gate/up, Q3_K down, bf16 router + bf16 shared expert)",
+                "tokens_per_step": m, "batches": f"{nb} distinct batches in turn",
+                "experts_read_per_step": used,
+                "l2": f"inputs larger than L2: {used} experts' blocks ({used * (2 * q2 + q3) / 1e6:.0f} MB) "
+                      "plus the 50 MB shared expert per step",
+                "parallelism": f"replicas x{world}",
+                "stages_us": {n: float(v * 1e3) for n, v in zip(PREFILL_STAGES, st)},
+            },
+            "roofline": {"bound": "hbm", "kernel": f"moe_tc_gemm ({dom})", "achieved": achieved, "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                         "algorithmic_bytes": gemm_bytes[dom], "avg_launch_us": dur * 1e6,
+                         "tensor_tflops": gemm_flops[dom] / dur / 1e12,
+                         "tensor_frac_of_bf16_peak": gemm_flops[dom] / dur / 1e12 / bf16_peak,
+                         "timing": "CUDA events between the prefill stages on the launching stream"},
+            "e2e": {"value": e_units / e_secs, "unit": unit, "h2d_bytes_per_step": m * cfg.dim * 2,
+                    "d2h_bytes_per_step": m * cfg.dim * 4},
+            "gpu_launches": args.steps * 17,  # router, scores, top-k, plan, x_hat, 2 gathers, gate, up, SwiGLU, down, 3 shared GEMMs, its SwiGLU, finish
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 # ------------------------------------------------------------------ reference arm (the oracle)
 
 def run_reference(args):
@@ -409,8 +566,11 @@ def run_reference(args):
         return  # under torchrun only rank 0 runs the CPU reference
     m, L, metric, unit = WORKLOADS[args.workload]
     cfg = decode_cfg(m)
+    bias = (-0.1, 0.1)
+    if args.workload == "prefill":  # each step a bounded sample: 4 of the 512 tokens
+        m, bias = 4, PREFILL_BIAS
     n, spent, thr, sample = oracle_sample(cfg, m, budget_s=0.0, max_steps=args.steps,
-                                          warmup=args.warmup)
+                                          warmup=args.warmup, bias_range=bias)
     value = n * m / spent
     if args.workload == "chain40":
         value = value / (args.layers or L)
@@ -444,6 +604,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "prefill":
+        run_prefill(args)
     else:
         run_ours(args)
 
