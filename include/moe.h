@@ -299,17 +299,38 @@ int moe_dedupe_triples(int32_t *triples_host, int n, int *n_out);
 int moe_parse_header(const moe_cfg *cfg, const int32_t *header_host, int m, int t,
                      int32_t *status_host, int32_t *picks_host, float *weights_host);
 
+/* Options of moe_graph_create. */
+#define MOE_GRAPH_SNAPSHOTS 1       /* copy each layer's input (x and residual) to snapshot memory
+                                       before the layer, inside the graph ([step_seg] module doc:
+                                       a snapshot a layer, ~75 KB there), so the step can be rerun
+                                       from a layer (moe_graph_rerun_from, moe_graph_step_cached) */
+#define MOE_GRAPH_EAGER_FALLBACK 2  /* if capture or instantiation fails, the object runs the layers
+                                       eagerly instead ([step_seg] fn close_or_disable: graph mode off) */
+#define MOE_GRAPH_TEST_FAIL_CAPTURE 4 /* failure-handling check: treat the capture as failed (no capture
+                                       is attempted), to exercise MOE_GRAPH_EAGER_FALLBACK */
+
 /* A whole-step CUDA graph ([step_seg] module doc: the step captured once and
  * replayed, one read-back of the headers per launch): n_layers layer steps
  * chained, layer l reading x from x_a (l even) or x_b (l odd) and writing the
  * other, except that the last layer writes x_a, so each launch continues from
  * the previous launch's output; residual_dev carries between layers; layer
  * l's header lands at headers_dev + l * moe_header_words(cfg, m). layers is a
- * host array of n_layers structs (its device pointers are baked in); every
- * buffer must outlive the graph. */
+ * host array of n_layers structs (copied; their device pointers are baked
+ * in); every buffer must outlive the graph. snap_dev: moe_graph_snapshot_bytes
+ * of device memory with MOE_GRAPH_SNAPSHOTS, else may be NULL. flags:
+ * MOE_GRAPH_*. Without MOE_GRAPH_EAGER_FALLBACK a failed capture returns
+ * MOE_ECAPTURE and no object. */
+int moe_graph_snapshot_bytes(const moe_cfg *cfg, int m, int n_layers, size_t *bytes);
 int moe_graph_create(const moe_cfg *cfg, const moe_layer *layers, int n_layers,
                      const moe_arena *arena, int m, void *x_a_dev, void *x_b_dev,
-                     float *residual_dev, int32_t *headers_dev, void *ws_dev, void **graph);
+                     float *residual_dev, int32_t *headers_dev, void *ws_dev, void *snap_dev,
+                     unsigned flags, void **graph);
+/* *eager = 1 when the object runs its layers eagerly (capture failed). */
+int moe_graph_is_eager(void *graph, int *eager);
+/* Restores layer `layer`'s snapshot into that layer's input buffers and runs
+ * layers layer .. n_layers - 1 eagerly on `stream` (snapshots refreshed on
+ * the way). Needs MOE_GRAPH_SNAPSHOTS. */
+int moe_graph_rerun_from(void *graph, int layer, moe_stream_t stream);
 int moe_graph_launch(void *graph, moe_stream_t stream);
 int moe_graph_destroy(void *graph);
 
@@ -382,6 +403,55 @@ int moe_prefill_step_profiled(const moe_cfg *cfg, const moe_layer *layer, const 
 /* The status word (MOE_WS_* bits) of the last moe_prefill_step on ws_dev;
  * synchronises `stream`. */
 int moe_prefill_status(const moe_cfg *cfg, int m, void *ws_dev, uint32_t *status_host, moe_stream_t stream);
+
+/* Expert residency ([moe_v41] module doc: the ExpertLru gathers the picked
+ * experts' raw slices into device-visible slots, misses read from the
+ * source; [route] module doc and fn slot_table_update: the host touches the
+ * picks, fetches the misses and uploads the slot changes to the device
+ * table). A cache owns n_slots slots of the arena for layers 0 .. n_layers-1
+ * of the slot table at slot_table_dev ([64][n_routed], row l for layer l; NULL
+ * keeps the table on the host only), least recently used out first, and
+ * fetches a missing expert with fetch(user, layer, expert, slot address,
+ * slot_bytes, stream) -- which must enqueue the copy of the expert's slot
+ * image on `stream` and return 0. Creating the cache marks every entry of its
+ * rows not resident (-1). */
+typedef int (*moe_expert_fetch_fn)(void *user, int layer, int expert, void *slot_dev, uint64_t slot_bytes,
+                                   moe_stream_t stream);
+int moe_cache_create(int n_layers, int n_routed, int n_slots, const moe_arena *arena, int32_t *slot_table_dev,
+                     moe_expert_fetch_fn fetch, void *user, void **cache);
+int moe_cache_destroy(void *cache);
+/* Makes the experts (host array of n ids of one layer; repeats allowed)
+ * resident: hits become most recently used, misses take the least recently
+ * used slots (their previous experts marked -1) and are fetched; the changed
+ * table rows are uploaded on `stream`. *n_fetched (may be NULL) = misses.
+ * MOE_EUNSUPPORTED when more distinct experts are asked at once than slots. */
+int moe_cache_ensure(void *cache, int layer, const int32_t *experts_host, int n, int *n_fetched,
+                     moe_stream_t stream);
+/* The slot of (layer, expert), -1 when not resident. */
+int moe_cache_slot_of(void *cache, int layer, int expert, int32_t *slot);
+int moe_cache_stats(void *cache, uint64_t *hits, uint64_t *misses, uint64_t *evictions);
+
+/* An expert source over host memory: images_host[layer * n_routed + expert]
+ * = host address of that expert's slot image (image_bytes; pinned memory
+ * keeps the copies asynchronous). moe_fetch_host_images is its fetch
+ * function (pass the source as `user`). */
+int moe_host_source_create(const void *const *images_host, int n_layers, int n_routed, uint64_t image_bytes,
+                           void **source);
+int moe_host_source_destroy(void *source);
+int moe_fetch_host_images(void *source, int layer, int expert, void *slot_dev, uint64_t slot_bytes,
+                          moe_stream_t stream);
+
+/* One launch of a graph with snapshots whose layers take their experts from
+ * a cache (layer l using row l of the cache's table): launch, read the
+ * headers; at the first layer whose header has MOE_HDR_MISS, make that
+ * layer's picks resident, restore its snapshot and run the rest eagerly,
+ * layer by layer, a layer with a miss fetched and rerun from its snapshot
+ * ([step_seg] module doc and fn step_seg: restore, the layer's ffn eagerly,
+ * eager to the end). On return (the stream synchronised) the graph's buffers
+ * hold the result and headers_host (host, n_layers header rows) the final
+ * headers; *layers_rerun (may be NULL) = layers run again. */
+int moe_graph_step_cached(void *graph, void *cache, int32_t *headers_host, int *layers_rerun,
+                          moe_stream_t stream);
 
 /* Last error message of the calling thread ("" if none). */
 const char *moe_last_error(void);

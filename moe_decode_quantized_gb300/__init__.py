@@ -23,13 +23,17 @@ MOE_WS_PLAN = 2
 MOE_WS_TRIPLE = 4
 MOE_SHARED_BF16 = 0
 MOE_SHARED_KQUANT = 1
+MOE_GRAPH_SNAPSHOTS = 1
+MOE_GRAPH_EAGER_FALLBACK = 2
+MOE_GRAPH_TEST_FAIL_CAPTURE = 4
 SLOT_TABLE_LAYERS = 64
 
 __all__ = ["Config", "Arena", "Layer", "MoeError", "header_words", "workspace_bytes",
            "workspace_init", "router_logits", "quantize_q8_1", "route_select", "expert_step",
            "swiglu_q8", "layer_step", "host_io_bytes", "layer_step_host", "workspace_view",
            "read_status", "layer_step_profiled", "layer_step_static", "route_scores", "set_wait_limit_ns",
-           "expert_step_unreleased", "gemm_bf16", "prefill_workspace_bytes", "prefill_step", "prefill_step_profiled", "prefill_status", "slot_table_set", "dedupe_triples", "parse_header", "Graph"]
+           "expert_step_unreleased", "gemm_bf16", "prefill_workspace_bytes", "prefill_step", "prefill_step_profiled", "prefill_status", "graph_snapshot_bytes", "HostSource",
+           "ExpertCache", "slot_table_set", "dedupe_triples", "parse_header", "Graph"]
 
 
 class MoeError(RuntimeError):
@@ -112,6 +116,85 @@ class Layer:
     def c(self) -> _lib.MoeLayer:
         return _lib.MoeLayer(_ptr(self.router_w), _ptr(self.bias), _ptr(self.slot_row), _ptr(self.sh_w1),
                              _ptr(self.sh_w3), _ptr(self.sh_w2), int(self.sh_format))
+
+
+class HostSource:
+    """Expert slot images in host memory (include/moe.h, moe_host_source_create):
+    images[layer][expert] -> a host array (pinned torch tensor or numpy), kept alive here."""
+
+    def __init__(self, images, n_layers: int, n_routed: int, image_bytes: int):
+        self._keep = images
+        ptrs = (C.c_void_p * (n_layers * n_routed))()
+        for l in range(n_layers):
+            for e in range(n_routed):
+                img = images[l][e]
+                ptrs[l * n_routed + e] = img.data_ptr() if hasattr(img, "data_ptr") else img.ctypes.data
+        h = C.c_void_p()
+        _check(_lib.moe().moe_host_source_create(C.cast(ptrs, C.c_void_p), n_layers, n_routed, image_bytes,
+                                                 C.byref(h)))
+        self._h = h
+
+    def close(self):
+        if self._h:
+            _lib.moe().moe_host_source_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class ExpertCache:
+    """LRU expert slots over an arena (include/moe.h, moe_cache_create). source:
+    a HostSource (its fetch runs in the library), or a Python callable
+    fetch(layer, expert, slot_address, slot_bytes, stream) -> int, or None."""
+
+    def __init__(self, n_layers: int, n_routed: int, n_slots: int, arena: Arena, slot_table=None, source=None):
+        lib = _lib.moe()
+        self._keep = (arena, slot_table, source)
+        if isinstance(source, HostSource):
+            fn = C.cast(lib.moe_fetch_host_images, C.c_void_p)
+            user = source._h
+        elif source is not None:
+            self._cb = _lib.FETCH_FN(lambda u, l, e, d, b, s: int(source(l, e, d, b, s)))
+            fn = C.cast(self._cb, C.c_void_p)
+            user = None
+        else:
+            fn, user = None, None
+        h = C.c_void_p()
+        _check(lib.moe_cache_create(n_layers, n_routed, n_slots, C.byref(arena.c()), _ptr(slot_table), fn, user,
+                                    C.byref(h)))
+        self._h = h
+
+    def ensure(self, layer: int, experts, stream=None) -> int:
+        e = np.ascontiguousarray(experts, dtype=np.int32)
+        n = C.c_int(0)
+        _check(_lib.moe().moe_cache_ensure(self._h, layer, C.c_void_p(e.ctypes.data), e.size, C.byref(n),
+                                           _stream(stream)))
+        return n.value
+
+    def slot_of(self, layer: int, expert: int) -> int:
+        sl = C.c_int32(0)
+        _check(_lib.moe().moe_cache_slot_of(self._h, layer, expert, C.byref(sl)))
+        return sl.value
+
+    def stats(self):
+        h, m, ev = C.c_uint64(0), C.c_uint64(0), C.c_uint64(0)
+        _check(_lib.moe().moe_cache_stats(self._h, C.byref(h), C.byref(m), C.byref(ev)))
+        return h.value, m.value, ev.value
+
+    def close(self):
+        if self._h:
+            _lib.moe().moe_cache_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def header_words(cfg: Config, m: int) -> int:
@@ -285,17 +368,42 @@ def prefill_status(cfg: Config, m: int, ws, stream=None) -> int:
     return s.value
 
 
-class Graph:
-    """A captured multi-layer step (include/moe.h, moe_graph_create)."""
+def graph_snapshot_bytes(cfg: Config, m: int, n_layers: int) -> int:
+    b = C.c_size_t(0)
+    _check(_lib.moe().moe_graph_snapshot_bytes(C.byref(cfg.c()), m, n_layers, C.byref(b)))
+    return b.value
 
-    def __init__(self, cfg: Config, layers, arena: Arena, m: int, x_a, x_b, residual, headers, ws):
+
+class Graph:
+    """A captured multi-layer step (include/moe.h, moe_graph_create). snapshots:
+    device memory of graph_snapshot_bytes (with MOE_GRAPH_SNAPSHOTS in flags)."""
+
+    def __init__(self, cfg: Config, layers, arena: Arena, m: int, x_a, x_b, residual, headers, ws, snapshots=None,
+                 flags: int = 0):
         arr = (_lib.MoeLayer * len(layers))(*[ly.c() for ly in layers])
-        self._keep = (layers, arena, x_a, x_b, residual, headers, ws)
+        self._keep = (layers, arena, x_a, x_b, residual, headers, ws, snapshots)
         h = C.c_void_p()
         _check(_lib.moe().moe_graph_create(C.byref(cfg.c()), C.cast(arr, C.c_void_p), len(layers),
                                            C.byref(arena.c()), m, _ptr(x_a), _ptr(x_b), _ptr(residual),
-                                           _ptr(headers), _ptr(ws), C.byref(h)))
+                                           _ptr(headers), _ptr(ws), _ptr(snapshots), flags, C.byref(h)))
         self._h = h
+
+    @property
+    def eager(self) -> bool:
+        e = C.c_int(0)
+        _check(_lib.moe().moe_graph_is_eager(self._h, C.byref(e)))
+        return bool(e.value)
+
+    def rerun_from(self, layer: int, stream=None):
+        _check(_lib.moe().moe_graph_rerun_from(self._h, layer, _stream(stream)))
+
+    def step_cached(self, cache: "ExpertCache", headers_host: np.ndarray, stream=None) -> int:
+        """One launch with misses fetched and the rest rerun (moe_graph_step_cached);
+        -> layers rerun. headers_host: int32 numpy array of the graph's header rows."""
+        n = C.c_int(0)
+        _check(_lib.moe().moe_graph_step_cached(self._h, cache._h, C.c_void_p(headers_host.ctypes.data),
+                                                C.byref(n), _stream(stream)))
+        return n.value
 
     def launch(self, stream=None):
         _check(_lib.moe().moe_graph_launch(self._h, _stream(stream)))

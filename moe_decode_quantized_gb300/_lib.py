@@ -40,6 +40,9 @@ class MoeWsView(C.Structure):
                 ("gs", P), ("us", P), ("down", P), ("sd", P), ("acc", P), ("status", P)]
 
 
+# the type of an expert fetch callback (include/moe.h, moe_expert_fetch_fn)
+FETCH_FN = C.CFUNCTYPE(C.c_int, C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_uint64, C.c_void_p)
+
 # name -> (restype, argtypes); every symbol include/moe.h declares
 MOE_SYMBOLS = {
     "moe_header_words": (C.c_int, [C.POINTER(MoeCfg), C.c_int]),
@@ -64,8 +67,20 @@ MOE_SYMBOLS = {
     "moe_slot_table_set": (C.c_int, [P, C.c_int, P, C.c_int, P, P]),
     "moe_dedupe_triples": (C.c_int, [P, C.c_int, C.POINTER(C.c_int)]),
     "moe_parse_header": (C.c_int, [C.POINTER(MoeCfg), P, C.c_int, C.c_int, P, P, P]),
+    "moe_graph_snapshot_bytes": (C.c_int, [C.POINTER(MoeCfg), C.c_int, C.c_int, C.POINTER(SZ)]),
     "moe_graph_create": (C.c_int, [C.POINTER(MoeCfg), P, C.c_int, C.POINTER(MoeArena), C.c_int, P,
-                                   P, P, P, P, C.POINTER(P)]),
+                                   P, P, P, P, P, C.c_uint, C.POINTER(P)]),
+    "moe_graph_is_eager": (C.c_int, [P, C.POINTER(C.c_int)]),
+    "moe_graph_rerun_from": (C.c_int, [P, C.c_int, P]),
+    "moe_cache_create": (C.c_int, [C.c_int, C.c_int, C.c_int, C.POINTER(MoeArena), P, P, P, C.POINTER(P)]),
+    "moe_cache_destroy": (C.c_int, [P]),
+    "moe_cache_ensure": (C.c_int, [P, C.c_int, P, C.c_int, C.POINTER(C.c_int), P]),
+    "moe_cache_slot_of": (C.c_int, [P, C.c_int, C.c_int, C.POINTER(C.c_int32)]),
+    "moe_cache_stats": (C.c_int, [P, C.POINTER(U64), C.POINTER(U64), C.POINTER(U64)]),
+    "moe_host_source_create": (C.c_int, [P, C.c_int, C.c_int, U64, C.POINTER(P)]),
+    "moe_host_source_destroy": (C.c_int, [P]),
+    "moe_fetch_host_images": (C.c_int, [P, C.c_int, C.c_int, P, U64, P]),
+    "moe_graph_step_cached": (C.c_int, [P, P, P, C.POINTER(C.c_int), P]),
     "moe_graph_launch": (C.c_int, [P, P]),
     "moe_graph_destroy": (C.c_int, [P]),
     "moe_graph_launch_host": (C.c_int, [P, P, P, P, P, P, P]),

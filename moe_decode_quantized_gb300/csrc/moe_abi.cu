@@ -15,6 +15,7 @@
 #include "moe_experts.cuh"
 #include "moe_slot.cuh"
 #include "moe_prefill.cuh"
+#include "moe_runtime.cuh"
 
 using namespace moe;
 
@@ -652,13 +653,125 @@ int gemm_bf16(const void *A, const void *B, float *out, int M, int N, int K, int
     return launch_tc<0>(am, bm, bm, a, dim3((N + TC_NT - 1) / TC_NT, (M + TC_M - 1) / TC_M), s, smem_optin);
 }
 
+// A multi-layer step: the captured graph, and what its eager form needs (the
+// layers, buffers and per-layer snapshots), used when capture failed and the
+// object runs eagerly, and to rerun the step from a layer.
 struct GraphObj {
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
-    void *x_a = nullptr;
+    bool eager = false;
+    moe_cfg cfg{};
+    std::vector<moe_layer> layers;
+    moe_arena arena{};
+    int m = 0, n_layers = 0, hw = 0;
+    void *x_a = nullptr, *x_b = nullptr, *ws = nullptr;
     float *residual = nullptr;
     int32_t *headers = nullptr;
-    size_t x_bytes = 0, res_bytes = 0, hdr_bytes = 0;
+    char *snap = nullptr;  // per layer: its input x (bf16) then the residual (f32), or NULL
+    size_t x_bytes = 0, res_bytes = 0, hdr_bytes = 0, snap_stride = 0;
+
+    void *x_in(int l) const { return (l % 2 == 0) ? x_a : x_b; }
+    void *x_out(int l) const { return (l == n_layers - 1) ? x_a : ((l % 2 == 0) ? x_b : x_a); }
+};
+
+size_t snapshot_stride(const moe_cfg &c, int m)
+{
+    return align_up((size_t)m * c.dim * 2, 256) + align_up((size_t)m * c.dim * 4, 256);
+}
+
+// layers `from` .. the last, each preceded by the copy of its input into its
+// snapshot (when the object keeps snapshots)
+int run_layers(GraphObj &G, int from, cudaStream_t s)
+{
+    for (int l = from; l < G.n_layers; ++l) {
+        if (G.snap) {
+            char *sn = G.snap + (size_t)l * G.snap_stride;
+            CUDA_OK(cudaMemcpyAsync(sn, G.x_in(l), G.x_bytes, cudaMemcpyDeviceToDevice, s));
+            CUDA_OK(cudaMemcpyAsync(sn + align_up(G.x_bytes, 256), G.residual, G.res_bytes, cudaMemcpyDeviceToDevice,
+                                    s));
+        }
+        const int rc = layer_step(G.cfg, G.layers[l], G.arena, G.x_in(l), G.residual, G.x_out(l),
+                                  G.headers + (size_t)l * G.hw, G.m, G.ws, s);
+        if (rc)
+            return rc;
+    }
+    return MOE_OK;
+}
+
+// the inputs of layer l back from its snapshot
+int restore_snapshot(GraphObj &G, int l, cudaStream_t s)
+{
+    const char *sn = G.snap + (size_t)l * G.snap_stride;
+    CUDA_OK(cudaMemcpyAsync(G.x_in(l), sn, G.x_bytes, cudaMemcpyDeviceToDevice, s));
+    CUDA_OK(cudaMemcpyAsync(G.residual, sn + align_up(G.x_bytes, 256), G.res_bytes, cudaMemcpyDeviceToDevice, s));
+    return MOE_OK;
+}
+
+// The picks of every token of layer l (header in host memory) made resident.
+int cache_ensure(ExpertCache &C, int layer, const int32_t *experts, int n, int *n_fetched, cudaStream_t s)
+{
+    if (layer < 0 || layer >= C.n_layers || n < 0 || (n > 0 && !experts))
+        return fail(MOE_EINVAL, "moe_cache_ensure: layer %d outside [0, %d) or bad experts", layer, C.n_layers);
+    std::vector<int> req;
+    for (int i = 0; i < n; ++i) {
+        const int e = experts[i];
+        if (e < 0 || e >= C.n_routed)
+            return fail(MOE_EINVAL, "moe_cache_ensure: expert %d outside [0, %d)", e, C.n_routed);
+        bool seen = false;
+        for (int r : req)
+            seen = seen || r == e;
+        if (!seen)
+            req.push_back(e);
+    }
+    if ((int)req.size() > C.n_slots)
+        return fail(MOE_EUNSUPPORTED, "moe_cache_ensure: %d experts at once, the cache holds %d slots", (int)req.size(),
+                    C.n_slots);
+    const size_t base = (size_t)layer * C.n_routed;
+    // the hits first: most recently used, so no victim below is one of them
+    for (int e : req)
+        if (C.table[base + e] >= 0) {
+            ++C.hits;
+            C.touch(C.table[base + e]);
+        }
+    std::vector<char> dirty(C.n_layers, 0);
+    int fetched = 0;
+    for (int e : req) {
+        if (C.table[base + e] >= 0)
+            continue;
+        ++C.misses;
+        const int v = C.lru.back();
+        if (C.owner[v] >= 0) {  // evict the least recently used expert
+            ++C.evictions;
+            C.table[(size_t)C.owner[v]] = -1;
+            dirty[C.owner[v] / C.n_routed] = 1;
+        }
+        C.owner[v] = (int64_t)(base + e);
+        C.table[base + e] = v;
+        dirty[layer] = 1;
+        C.touch(v);
+        if (C.fetch) {
+            const int rc = C.fetch(C.user, layer, e, const_cast<char *>(C.arena_base) + (size_t)v * C.slot_bytes,
+                                   C.slot_bytes, (moe_stream_t)s);
+            if (rc)
+                return fail(MOE_ECUDA, "moe_cache_ensure: the expert source failed (%d) for layer %d expert %d", rc,
+                            layer, e);
+        }
+        ++fetched;
+    }
+    if (C.table_dev)
+        for (int l = 0; l < C.n_layers; ++l)
+            if (dirty[l])  // pageable source: the copy has taken the row when the call returns
+                CUDA_OK(cudaMemcpyAsync(C.table_dev + (size_t)l * C.n_routed, C.table.data() + (size_t)l * C.n_routed,
+                                        sizeof(int32_t) * C.n_routed, cudaMemcpyHostToDevice, s));
+    if (n_fetched)
+        *n_fetched = fetched;
+    return MOE_OK;
+}
+
+struct HostSource {
+    std::vector<const void *> images;  // [layer * n_routed + expert]
+    int n_routed = 0;
+    uint64_t image_bytes = 0;
 };
 
 }  // namespace
@@ -1026,69 +1139,121 @@ int moe_parse_header(const moe_cfg *cfg, const int32_t *hdr, int m, int t, int32
     return MOE_OK;
 }
 
+int moe_graph_snapshot_bytes(const moe_cfg *cfg, int m, int n_layers, size_t *bytes)
+{
+    int rc = check_cfg(cfg);
+    if (rc || (rc = check_m(cfg, m)))
+        return rc;
+    if (n_layers < 1 || !bytes)
+        return fail(MOE_EINVAL, "moe_graph_snapshot_bytes: bad arguments");
+    *bytes = snapshot_stride(*cfg, m) * (size_t)n_layers;
+    return MOE_OK;
+}
+
 int moe_graph_create(const moe_cfg *cfg, const moe_layer *layers, int n_layers, const moe_arena *arena, int m,
-                     void *x_a, void *x_b, float *residual, int32_t *headers, void *ws, void **graph)
+                     void *x_a, void *x_b, float *residual, int32_t *headers, void *ws, void *snap, unsigned flags,
+                     void **graph)
 {
     int rc = check_cfg(cfg);
     if (rc || (rc = check_m(cfg, m)) || (rc = check_arena(arena)))
         return rc;
     if (!layers || n_layers < 1 || !x_a || !x_b || !residual || !headers || !ws || !graph || m < 1)
         return fail(MOE_EINVAL, "moe_graph_create: bad arguments");
+    if ((flags & MOE_GRAPH_SNAPSHOTS) && !snap)
+        return fail(MOE_EINVAL, "moe_graph_create: MOE_GRAPH_SNAPSHOTS needs snapshot memory");
     for (int l = 0; l < n_layers; ++l)
         if ((rc = check_layer(*cfg, &layers[l])))
             return rc;
     DevInfo *I;
     if ((rc = dev_info(&I)))
         return rc;
-    cudaStream_t cs;
-    CUDA_OK(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking));
     GraphObj *G = new GraphObj;
-    const int hw = header_words(m, cfg->topk);
-    cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
-    if (e == cudaSuccess) {
-        for (int l = 0; l < n_layers && rc == MOE_OK; ++l) {
-            const void *xin = (l % 2 == 0) ? x_a : x_b;
-            void *xout = (l == n_layers - 1) ? x_a : ((l % 2 == 0) ? x_b : x_a);
-            rc = layer_step(*cfg, layers[l], *arena, xin, residual, xout, headers + (size_t)l * hw, m, ws, cs);
+    G->cfg = *cfg;
+    G->layers.assign(layers, layers + n_layers);
+    G->arena = *arena;
+    G->m = m;
+    G->n_layers = n_layers;
+    G->hw = header_words(m, cfg->topk);
+    G->x_a = x_a;
+    G->x_b = x_b;
+    G->ws = ws;
+    G->residual = residual;
+    G->headers = headers;
+    G->snap = (flags & MOE_GRAPH_SNAPSHOTS) ? static_cast<char *>(snap) : nullptr;
+    G->snap_stride = snapshot_stride(*cfg, m);
+    G->x_bytes = (size_t)m * cfg->dim * 2;
+    G->res_bytes = (size_t)m * cfg->dim * 4;
+    G->hdr_bytes = sizeof(int32_t) * (size_t)G->hw * n_layers;
+    cudaError_t e = cudaSuccess;
+    if (flags & MOE_GRAPH_TEST_FAIL_CAPTURE) {
+        e = cudaErrorStreamCaptureUnsupported;  // as if the capture had failed
+    } else {
+        cudaStream_t cs;
+        CUDA_OK(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking));
+        e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+        if (e == cudaSuccess) {
+            rc = run_layers(*G, 0, cs);
+            cudaGraph_t g = nullptr;
+            cudaError_t e2 = cudaStreamEndCapture(cs, &g);
+            if (rc == MOE_OK && e2 == cudaSuccess) {
+                G->graph = g;
+                e = cudaGraphInstantiate(&G->exec, g, 0);
+            } else {
+                if (g)
+                    cudaGraphDestroy(g);
+                e = e2 != cudaSuccess ? e2 : cudaErrorUnknown;
+            }
         }
-        cudaGraph_t g = nullptr;
-        cudaError_t e2 = cudaStreamEndCapture(cs, &g);
-        if (rc == MOE_OK && e2 == cudaSuccess) {
-            G->graph = g;
-            e = cudaGraphInstantiate(&G->exec, g, 0);
-        } else {
-            if (g)
-                cudaGraphDestroy(g);
-            e = e2 != cudaSuccess ? e2 : cudaErrorUnknown;
-        }
+        cudaStreamDestroy(cs);
     }
-    cudaStreamDestroy(cs);
     if (rc != MOE_OK || e != cudaSuccess) {
         if (G->exec)
             cudaGraphExecDestroy(G->exec);
         if (G->graph)
             cudaGraphDestroy(G->graph);
-        delete G;
-        cudaGetLastError();
-        if (rc != MOE_OK)
-            return fail(MOE_ECAPTURE, "graph capture failed: %s", g_err);
-        return fail(MOE_ECAPTURE, "graph capture failed: %s", cudaGetErrorString(e));
+        G->exec = nullptr;
+        G->graph = nullptr;
+        if (e != cudaErrorStreamCaptureUnsupported || !(flags & MOE_GRAPH_TEST_FAIL_CAPTURE))
+            cudaGetLastError();
+        if (!(flags & MOE_GRAPH_EAGER_FALLBACK)) {
+            delete G;
+            if (rc != MOE_OK)
+                return fail(MOE_ECAPTURE, "graph capture failed: %s", g_err);
+            return fail(MOE_ECAPTURE, "graph capture failed: %s", cudaGetErrorString(e));
+        }
+        G->eager = true;  // graph mode off: every launch runs the layers eagerly
     }
-    G->x_a = x_a;
-    G->residual = residual;
-    G->headers = headers;
-    G->x_bytes = (size_t)m * cfg->dim * 2;
-    G->res_bytes = (size_t)m * cfg->dim * 4;
-    G->hdr_bytes = sizeof(int32_t) * (size_t)hw * n_layers;
     *graph = G;
     return MOE_OK;
+}
+
+int moe_graph_is_eager(void *graph, int *eager)
+{
+    if (!graph || !eager)
+        return fail(MOE_EINVAL, "moe_graph_is_eager: bad arguments");
+    *eager = static_cast<GraphObj *>(graph)->eager ? 1 : 0;
+    return MOE_OK;
+}
+
+int moe_graph_rerun_from(void *graph, int layer, moe_stream_t stream)
+{
+    if (!graph)
+        return fail(MOE_EINVAL, "graph is NULL");
+    GraphObj *G = static_cast<GraphObj *>(graph);
+    if (!G->snap || layer < 0 || layer >= G->n_layers)
+        return fail(MOE_EINVAL, "moe_graph_rerun_from: no snapshots, or layer %d outside [0, %d)", layer, G->n_layers);
+    const int rc = restore_snapshot(*G, layer, (cudaStream_t)stream);
+    return rc ? rc : run_layers(*G, layer, (cudaStream_t)stream);
 }
 
 int moe_graph_launch(void *graph, moe_stream_t stream)
 {
     if (!graph)
         return fail(MOE_EINVAL, "graph is NULL");
-    CUDA_OK(cudaGraphLaunch(static_cast<GraphObj *>(graph)->exec, (cudaStream_t)stream));
+    GraphObj *G = static_cast<GraphObj *>(graph);
+    if (G->eager)
+        return run_layers(*G, 0, (cudaStream_t)stream);
+    CUDA_OK(cudaGraphLaunch(G->exec, (cudaStream_t)stream));
     return MOE_OK;
 }
 
@@ -1101,7 +1266,13 @@ int moe_graph_launch_host(void *graph, const void *x_host, const float *residual
     cudaStream_t s = (cudaStream_t)stream;
     CUDA_OK(cudaMemcpyAsync(G->x_a, x_host, G->x_bytes, cudaMemcpyHostToDevice, s));
     CUDA_OK(cudaMemcpyAsync(G->residual, residual_host, G->res_bytes, cudaMemcpyHostToDevice, s));
-    CUDA_OK(cudaGraphLaunch(G->exec, s));
+    if (G->eager) {
+        const int rc = run_layers(*G, 0, s);
+        if (rc)
+            return rc;
+    } else {
+        CUDA_OK(cudaGraphLaunch(G->exec, s));
+    }
     CUDA_OK(cudaMemcpyAsync(x_out_host, G->x_a, G->x_bytes, cudaMemcpyDeviceToHost, s));
     CUDA_OK(cudaMemcpyAsync(residual_out_host, G->residual, G->res_bytes, cudaMemcpyDeviceToHost, s));
     CUDA_OK(cudaMemcpyAsync(headers_host, G->headers, G->hdr_bytes, cudaMemcpyDeviceToHost, s));
@@ -1360,6 +1531,173 @@ int moe_prefill_status(const moe_cfg *cfg, int m, void *ws, uint32_t *status_hos
     CUDA_OK(cudaMemcpyAsync(status_host, static_cast<char *>(ws) + L.status, 4, cudaMemcpyDeviceToHost,
                             (cudaStream_t)stream));
     CUDA_OK(cudaStreamSynchronize((cudaStream_t)stream));
+    return MOE_OK;
+}
+
+int moe_cache_create(int n_layers, int n_routed, int n_slots, const moe_arena *arena, int32_t *slot_table_dev,
+                     moe_expert_fetch_fn fetch, void *user, void **cache)
+{
+    if (n_layers < 1 || n_layers > MOE_SLOT_TABLE_LAYERS || n_routed < 1 || n_routed > MOE_MAX_ROUTED ||
+        n_slots < 1 || !arena || !cache)
+        return fail(MOE_EINVAL, "moe_cache_create: bad arguments");
+    ExpertCache *C = new ExpertCache;
+    C->init(n_layers, n_routed, n_slots, arena, slot_table_dev, fetch, user);
+    if (slot_table_dev)
+        CUDA_OK(cudaMemcpy(slot_table_dev, C->table.data(), sizeof(int32_t) * C->table.size(),
+                           cudaMemcpyHostToDevice));
+    *cache = C;
+    return MOE_OK;
+}
+
+int moe_cache_destroy(void *cache)
+{
+    delete static_cast<ExpertCache *>(cache);
+    return MOE_OK;
+}
+
+int moe_cache_ensure(void *cache, int layer, const int32_t *experts_host, int n, int *n_fetched, moe_stream_t stream)
+{
+    if (!cache)
+        return fail(MOE_EINVAL, "cache is NULL");
+    return cache_ensure(*static_cast<ExpertCache *>(cache), layer, experts_host, n, n_fetched, (cudaStream_t)stream);
+}
+
+int moe_cache_slot_of(void *cache, int layer, int expert, int32_t *slot)
+{
+    if (!cache || !slot)
+        return fail(MOE_EINVAL, "moe_cache_slot_of: bad arguments");
+    ExpertCache *C = static_cast<ExpertCache *>(cache);
+    if (layer < 0 || layer >= C->n_layers || expert < 0 || expert >= C->n_routed)
+        return fail(MOE_EINVAL, "moe_cache_slot_of: (%d, %d) outside the table", layer, expert);
+    *slot = C->table[(size_t)layer * C->n_routed + expert];
+    return MOE_OK;
+}
+
+int moe_cache_stats(void *cache, uint64_t *hits, uint64_t *misses, uint64_t *evictions)
+{
+    if (!cache)
+        return fail(MOE_EINVAL, "cache is NULL");
+    ExpertCache *C = static_cast<ExpertCache *>(cache);
+    if (hits)
+        *hits = C->hits;
+    if (misses)
+        *misses = C->misses;
+    if (evictions)
+        *evictions = C->evictions;
+    return MOE_OK;
+}
+
+int moe_host_source_create(const void *const *images_host, int n_layers, int n_routed, uint64_t image_bytes,
+                           void **source)
+{
+    if (!images_host || n_layers < 1 || n_routed < 1 || image_bytes == 0 || !source)
+        return fail(MOE_EINVAL, "moe_host_source_create: bad arguments");
+    HostSource *H = new HostSource;
+    H->images.assign(images_host, images_host + (size_t)n_layers * n_routed);
+    H->n_routed = n_routed;
+    H->image_bytes = image_bytes;
+    *source = H;
+    return MOE_OK;
+}
+
+int moe_host_source_destroy(void *source)
+{
+    delete static_cast<HostSource *>(source);
+    return MOE_OK;
+}
+
+int moe_fetch_host_images(void *source, int layer, int expert, void *slot_dev, uint64_t slot_bytes, moe_stream_t stream)
+{
+    HostSource *H = static_cast<HostSource *>(source);
+    if (!H || !slot_dev || H->image_bytes > slot_bytes)
+        return MOE_EINVAL;
+    const void *img = H->images[(size_t)layer * H->n_routed + expert];
+    if (!img)
+        return MOE_EINVAL;
+    return cudaMemcpyAsync(slot_dev, img, H->image_bytes, cudaMemcpyHostToDevice, (cudaStream_t)stream) == cudaSuccess
+               ? MOE_OK
+               : MOE_ECUDA;
+}
+
+// the distinct picks of every token of one layer's header
+static std::vector<int32_t> header_picks(const int32_t *h, int m, int k)
+{
+    std::vector<int32_t> v;
+    for (int t = 0; t < m; ++t)
+        for (int i = 0; i < k; ++i)
+            v.push_back(h[(size_t)t * (1 + 3 * k) + 1 + i]);
+    return v;
+}
+
+static bool header_miss(const int32_t *h, int m, int k)
+{
+    for (int t = 0; t < m; ++t)
+        if (h[(size_t)t * (1 + 3 * k)] & MOE_HDR_MISS)
+            return true;
+    return false;
+}
+
+int moe_graph_step_cached(void *graph, void *cache, int32_t *headers_host, int *layers_rerun, moe_stream_t stream)
+{
+    if (!graph || !cache || !headers_host)
+        return fail(MOE_EINVAL, "moe_graph_step_cached: bad arguments");
+    GraphObj *G = static_cast<GraphObj *>(graph);
+    ExpertCache *C = static_cast<ExpertCache *>(cache);
+    if (!G->snap)
+        return fail(MOE_EINVAL, "moe_graph_step_cached: the graph keeps no snapshots (MOE_GRAPH_SNAPSHOTS)");
+    if (C->n_layers < G->n_layers || C->n_routed != G->cfg.n_routed)
+        return fail(MOE_EINVAL, "moe_graph_step_cached: the cache covers %d layers of %d experts", C->n_layers,
+                    C->n_routed);
+    for (int l = 0; l < G->n_layers; ++l)
+        if (!C->table_dev || G->layers[l].slot_row != C->table_dev + (size_t)l * C->n_routed)
+            return fail(MOE_EINVAL, "moe_graph_step_cached: layer %d does not use row %d of the cache's table", l, l);
+    cudaStream_t s = (cudaStream_t)stream;
+    const int k = G->cfg.topk, m = G->m, hw = G->hw;
+    int rc = moe_graph_launch(graph, stream);
+    if (rc)
+        return rc;
+    CUDA_OK(cudaMemcpyAsync(headers_host, G->headers, G->hdr_bytes, cudaMemcpyDeviceToHost, s));
+    CUDA_OK(cudaStreamSynchronize(s));
+    int first = -1;
+    for (int l = 0; l < G->n_layers && first < 0; ++l)
+        if (header_miss(headers_host + (size_t)l * hw, m, k))
+            first = l;
+    if (layers_rerun)
+        *layers_rerun = 0;
+    if (first < 0)
+        return MOE_OK;
+    // from the first layer with a miss: its picks made resident, its input
+    // back from the snapshot, then layer by layer eagerly, each layer's
+    // misses fetched and the layer run again from its snapshot
+    for (int l = first; l < G->n_layers; ++l) {
+        int32_t *h = headers_host + (size_t)l * hw;
+        for (int attempt = 0;; ++attempt) {
+            if (attempt > 0 || l == first) {
+                const std::vector<int32_t> p = header_picks(h, m, k);
+                if ((rc = cache_ensure(*C, l, p.data(), (int)p.size(), nullptr, s)))
+                    return rc;
+                if ((rc = restore_snapshot(*G, l, s)))
+                    return rc;
+            }
+            if (G->snap) {
+                char *sn = G->snap + (size_t)l * G->snap_stride;
+                CUDA_OK(cudaMemcpyAsync(sn, G->x_in(l), G->x_bytes, cudaMemcpyDeviceToDevice, s));
+                CUDA_OK(cudaMemcpyAsync(sn + align_up(G->x_bytes, 256), G->residual, G->res_bytes,
+                                        cudaMemcpyDeviceToDevice, s));
+            }
+            if ((rc = layer_step(G->cfg, G->layers[l], G->arena, G->x_in(l), G->residual, G->x_out(l),
+                                 G->headers + (size_t)l * hw, m, G->ws, s)))
+                return rc;
+            CUDA_OK(cudaMemcpyAsync(h, G->headers + (size_t)l * hw, sizeof(int32_t) * hw, cudaMemcpyDeviceToHost, s));
+            CUDA_OK(cudaStreamSynchronize(s));
+            if (!header_miss(h, m, k))
+                break;
+            if (attempt >= 1)
+                return fail(MOE_EUNSUPPORTED, "moe_graph_step_cached: layer %d still misses after a fetch", l);
+        }
+    }
+    if (layers_rerun)
+        *layers_rerun = G->n_layers - first;
     return MOE_OK;
 }
 
