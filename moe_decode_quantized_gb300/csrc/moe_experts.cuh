@@ -228,13 +228,21 @@ __device__ __forceinline__ float q2k_dot(const uint32_t *blk, const int4 *xq, co
 }
 
 // PER Q3_K super-blocks of one lane sharing the same activation columns
-// (as q3k_dot, the activation's quants and scale records loaded once)
+// (the activation's quants and scale records loaded once). Q3_K: 32 bytes
+// of high bits (bit 4h + g of byte b: value 128h + 32g + b), 64 bytes of
+// 2-bit lows (field g of byte 32h + b), 12 bytes of 6-bit scales, f16 d;
+// the value is low + 4 high - 4. Per 16-value sub-block the integer sum
+//   t = sum low x + 4 sum high x - 4 sum x
+// takes two dp4a a weight word: the low field masked in place (4^g low) and
+// the high bit masked in place (2^(4h + g) high), both shifted out of the
+// sums afterwards (exact: each sum is a multiple of its power of two); the
+// top field and the top high bit give unsigned bytes.
 template <int PER>
 __device__ __forceinline__ void q3k_dot_multi(const uint8_t *st, int lane, const int4 *xq, const float4 *rec,
                                               float (&out)[PER])
 {
     const uint32_t *W[PER];
-    uint32_t sh[PER], hm[PER][8], scw[PER][3];
+    uint32_t sh[PER], hm[PER][8], S[PER][4];
     float d[PER], acc[PER];
 #pragma unroll
     for (int q = 0; q < PER; ++q) {
@@ -249,9 +257,15 @@ __device__ __forceinline__ void q3k_dot_multi(const uint8_t *st, int lane, const
         for (int i = 0; i < 8; ++i)
             hm[q][i] = __funnelshift_r(w[i], w[i + 1], sh[q]);
         const uint32_t w24 = W[q][24], w25 = W[q][25], w26 = W[q][26], w27 = W[q][27];
-        scw[q][0] = __funnelshift_r(w24, w25, sh[q]);
-        scw[q][1] = __funnelshift_r(w25, w26, sh[q]);
-        scw[q][2] = __funnelshift_r(w26, w27, sh[q]);
+        const uint32_t s0 = __funnelshift_r(w24, w25, sh[q]), s1 = __funnelshift_r(w25, w26, sh[q]),
+                       s2 = __funnelshift_r(w26, w27, sh[q]);
+        // the 16 scales as bytes (0 .. 63): the low nibbles of bytes 0-7 are
+        // scales 0-7, their high nibbles scales 8-15; byte 8 + j holds the
+        // top two bits of scales j, j + 4, j + 8, j + 12
+        S[q][0] = (s0 & 0x0F0F0F0Fu) | ((s2 << 4) & 0x30303030u);
+        S[q][1] = (s1 & 0x0F0F0F0Fu) | ((s2 << 2) & 0x30303030u);
+        S[q][2] = ((s0 >> 4) & 0x0F0F0F0Fu) | (s2 & 0x30303030u);
+        S[q][3] = ((s1 >> 4) & 0x0F0F0F0Fu) | ((s2 >> 2) & 0x30303030u);
         d[q] = f16_bits_to_f32(w27 >> sh[q]);
         acc[q] = 0.0f;
     }
@@ -277,29 +291,29 @@ __device__ __forceinline__ void q3k_dot_multi(const uint8_t *st, int lane, const
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
             const int4 xa = xq[8 * h + 2 * g], xb = xq[8 * h + 2 * g + 1];
-            const int qsh = 2 * g, hsh = 4 * h + g;
+            const int hsh = 4 * h + g;
+            const uint32_t lm = 0x03030303u << (2 * g), hmk = 0x01010101u << hsh;
             const int i0 = 8 * h + 2 * g, i1 = i0 + 1;
+            const int xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
 #pragma unroll
             for (int q = 0; q < PER; ++q) {
-                int v[8];
+                int sl[2], shh[2];
 #pragma unroll
-                for (int w = 0; w < 8; ++w)
-                    v[w] = (int)(((qv[q][w] >> qsh) & 0x03030303u) | (((hm[q][w] >> hsh) & 0x01010101u) << 2));
-                int s0 = __dp4a(v[0], xa.x, 0);
-                s0 = __dp4a(v[1], xa.y, s0);
-                s0 = __dp4a(v[2], xa.z, s0);
-                s0 = __dp4a(v[3], xa.w, s0);
-                int s1 = __dp4a(v[4], xb.x, 0);
-                s1 = __dp4a(v[5], xb.y, s1);
-                s1 = __dp4a(v[6], xb.z, s1);
-                s1 = __dp4a(v[7], xb.w, s1);
-                // 6-bit scales i0, i1: low 4 bits from byte i (i < 8) or the high
-                // nibble of byte i - 8; high 2 bits at 2 * (i / 4) in byte 8 + i % 4
-                const int sc0 = (int)((i0 < 8 ? (byte_of(scw[q], i0) & 15u) : (byte_of(scw[q], i0 - 8) >> 4)) |
-                                      (((byte_of(scw[q], 8 + (i0 & 3)) >> (2 * (i0 >> 2))) & 3u) << 4)) - 32;
-                const int sc1 = (int)((i1 < 8 ? (byte_of(scw[q], i1) & 15u) : (byte_of(scw[q], i1 - 8) >> 4)) |
-                                      (((byte_of(scw[q], 8 + (i1 & 3)) >> (2 * (i1 >> 2))) & 3u) << 4)) - 32;
-                const int isum = sc0 * (s0 - 4 * sq[2 * g]) + sc1 * (s1 - 4 * sq[2 * g + 1]);
+                for (int b = 0; b < 2; ++b) {
+                    int a0 = 0, a1 = 0;
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const uint32_t lo = qv[q][4 * b + w] & lm, hi = hm[q][4 * b + w] & hmk;
+                        a0 = g == 3 ? dp4a_us(lo, xv[4 * b + w], a0) : __dp4a((int)lo, xv[4 * b + w], a0);
+                        a1 = hsh == 7 ? dp4a_us(hi, xv[4 * b + w], a1) : __dp4a((int)hi, xv[4 * b + w], a1);
+                    }
+                    sl[b] = a0 >> (2 * g);
+                    shh[b] = a1 >> hsh;
+                }
+                const int t0 = sl[0] + 4 * shh[0] - 4 * sq[2 * g], t1 = sl[1] + 4 * shh[1] - 4 * sq[2 * g + 1];
+                const int sc0 = (int)__byte_perm(S[q][i0 >> 2], 0u, 0x4440u + (unsigned)(i0 & 3)) - 32;
+                const int sc1 = (int)__byte_perm(S[q][i1 >> 2], 0u, 0x4440u + (unsigned)(i1 & 3)) - 32;
+                const int isum = sc0 * t0 + sc1 * t1;
                 acc[q] = fmaf(d8[4 * h + g], (float)isum, acc[q]);
             }
         }
@@ -1201,10 +1215,15 @@ __device__ __forceinline__ void d_task(const DRange &R, int tix, int &p, int &gr
     }
 }
 
-__device__ __forceinline__ DRange d_range(const DArgs &a)
+// ps: the plan's pair starts as cached by cache_plan (clamped, ne at
+// ps_ne), or NULL to read them from the header
+__device__ __forceinline__ DRange d_range(const DArgs &a, const int *ps = nullptr, int ps_ne = 0)
 {
+    auto start = [&](int i) {  // pair start of plan expert i (i <= ne)
+        return ps ? ps[i] : min(max(__ldcg(a.hdr + a.plan_off + 1 + i), 0), a.cap);
+    };
     DRange r;
-    r.ne = min(max(__ldcg(a.hdr + a.plan_off), 0), a.cap);
+    r.ne = ps ? ps_ne : min(max(__ldcg(a.hdr + a.plan_off), 0), a.cap);
     r.tpr = a.dim / down_rows_per_task(a.inter);
     r.Tr = r.ne * r.tpr;
     r.own = a.own_rows > 0;
@@ -1215,7 +1234,7 @@ __device__ __forceinline__ DRange d_range(const DArgs &a)
         r.lo = 0;
         r.hi = r.ne * r.ng;
         r.pair_lo = 0;
-        r.pair_hi = r.hi > 0 ? min(max(__ldcg(a.hdr + a.plan_off + 1 + r.ne), 0), a.cap) : 0;
+        r.pair_hi = r.hi > 0 ? start(r.ne) : 0;
         return r;
     }
     r.lo = (int)((long long)blockIdx.x * r.Tr / gridDim.x);
@@ -1223,8 +1242,8 @@ __device__ __forceinline__ DRange d_range(const DArgs &a)
     r.pair_lo = r.pair_hi = 0;
     if (r.lo < r.hi) {
         const int p_lo = r.lo / r.tpr, p_hi = (r.hi - 1) / r.tpr;
-        r.pair_lo = min(max(__ldcg(a.hdr + a.plan_off + 1 + p_lo), 0), a.cap);
-        r.pair_hi = min(max(__ldcg(a.hdr + a.plan_off + 2 + p_hi), r.pair_lo), a.cap);
+        r.pair_lo = start(p_lo);
+        r.pair_hi = min(max(start(p_hi + 1), r.pair_lo), a.cap);
     }
     return r;
 }
@@ -1280,15 +1299,16 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
     const size_t arow = act_row_bytes(inter);
     ring_init(ring);
     __syncthreads();
-    const DRange R = d_range(a);
 
     if (warp == MOE_CONSUMER_WARPS) {
         // ---------------- producer warp: everything it loads depends only on
-        // the pointer table, so the whole range is issued before the wait;
-        // MOE_PRODUCER_LANES lanes issue consecutive tasks in parallel
+        // the pointer table, so the whole range is issued before the wait,
+        // after one round of loads (the plan, its range from the cached
+        // copy); MOE_PRODUCER_LANES lanes issue consecutive tasks in parallel
         pdl_launch_dependents();
         cache_plan(ring, a.hdr, a.plan_off, a.plan_rows, a.ptrs, a.cap, 2, 1);
         const PlanCache &pc = *ring.pc;
+        const DRange R = d_range(a, pc.pair_start, pc.ne);
         const uint64_t pol = policy_evict_first();
         const int P = min(MOE_PRODUCER_LANES, ring.S);
         const bool issuer = lane < P;
@@ -1332,6 +1352,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
         }
         return;
     }
+    const DRange R = d_range(a);
 
     // ---------------- consumers: wait for h; build the activations
     pdl_launch_dependents();

@@ -463,30 +463,47 @@ struct SelectSmem {
     int first[MOE_MAX_TOKENS * MOE_MAX_TOPK], ent[MOE_MAX_TOKENS * MOE_MAX_TOPK];
 };
 
+// the largest of PL (a power of two) values, as a balanced tree
+template <int PL>
+__device__ __forceinline__ unsigned long long lane_max(const unsigned long long (&v)[PL])
+{
+    unsigned long long t[PL];
+#pragma unroll
+    for (int i = 0; i < PL; ++i)
+        t[i] = v[i];
+#pragma unroll
+    for (int w = PL / 2; w >= 1; w /= 2)
+#pragma unroll
+        for (int i = 0; i < w; ++i)
+            t[i] = max(t[i], t[i + w]);
+    return t[0];
+}
+
 // k rounds of the warp-wide maximum over PL values per lane (distinct; 0
 // marks an empty place and ranks last): out[r] = the r-th largest, written
-// by lane 0. The lane holding the winner removes it and rescans its values.
+// by lane 0. A round reduces the high words; the low words only when more
+// than one lane holds the largest high word (equal keys). The lane holding
+// the winner removes it and takes the maximum of the rest.
 template <int PL>
 __device__ __forceinline__ void warp_topk(unsigned long long (&v)[PL], int k, unsigned long long *out)
 {
+    const unsigned full = 0xffffffffu;
     const int lane = threadIdx.x & 31;
-    unsigned long long best = 0ull;
-#pragma unroll
-    for (int i = 0; i < PL; ++i)
-        best = max(best, v[i]);
+    unsigned long long best = lane_max<PL>(v);
     for (int r = 0; r < k; ++r) {
-        const unsigned hi = __reduce_max_sync(0xffffffffu, (unsigned)(best >> 32));
-        const unsigned lo = __reduce_max_sync(0xffffffffu, (unsigned)(best >> 32) == hi ? (unsigned)best : 0u);
+        const unsigned bh = (unsigned)(best >> 32);
+        const unsigned hi = __reduce_max_sync(full, bh);
+        const unsigned tied = __ballot_sync(full, bh == hi);
+        const unsigned lo = (tied & (tied - 1u)) == 0u ? __shfl_sync(full, (unsigned)best, __ffs(tied) - 1)
+                                                       : __reduce_max_sync(full, bh == hi ? (unsigned)best : 0u);
         const unsigned long long win = ((unsigned long long)hi << 32) | lo;
         if (lane == 0)
             out[r] = win;
         if (win != 0ull && best == win) {
-            best = 0ull;
 #pragma unroll
-            for (int i = 0; i < PL; ++i) {
+            for (int i = 0; i < PL; ++i)
                 v[i] = v[i] == win ? 0ull : v[i];
-                best = max(best, v[i]);
-            }
+            best = lane_max<PL>(v);
         }
     }
 }
