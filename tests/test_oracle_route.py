@@ -238,3 +238,23 @@ def test_plan_flags_and_single_token():
     assert ne == 3 and list(hdr[11:15]) == [0, 1, 2, 3]
     assert len(hdr) == 18 and list(hdr[15:18]) == [0, 2, 4]
     assert list(pw) == [0.25, 0.25, 0.5] and list(pr) == [0, 0, 0]
+
+
+def test_pick_comparison_allows_an_order_swap_only_between_near_equal_keys():
+    """The GPU tests compare picks in order, except where two of the k best
+    keys are closer than the logit tolerance can resolve: then as a set, with
+    the weights matched by pick."""
+    from helpers import match_picks, near_tie, order_near_tie, tiny_cfg
+    cfg = tiny_cfg(1)  # 16 experts, top 2
+    bias = np.zeros(16, np.float32)
+    logits = np.zeros((1, 16), np.float32)
+    logits[0, 3], logits[0, 7] = 2.0, np.float32(2.0) + np.float32(2.0 ** -22)
+    assert order_near_tie(cfg, logits, bias, 0) and not near_tie(cfg, logits, bias, 0)
+    w, rw = match_picks(cfg, [3, 7], [0.4, 0.6], [7, 3], [0.6, 0.4], logits, bias, 0)
+    assert w.tolist() == rw.tolist()
+    with pytest.raises(AssertionError):
+        match_picks(cfg, [3, 8], [0.4, 0.6], [7, 3], [0.6, 0.4], logits, bias, 0)
+    logits[0, 7] = 3.0  # well separated: the order itself must match
+    assert not order_near_tie(cfg, logits, bias, 0)
+    with pytest.raises(AssertionError):
+        match_picks(cfg, [3, 7], [0.4, 0.6], [7, 3], [0.6, 0.4], logits, bias, 0)
