@@ -165,10 +165,11 @@ __device__ __forceinline__ uint32_t byte_of(const uint32_t *w, int i) { return (
 // Q2_K super-block (84 bytes, 4-byte aligned in shared memory) against a
 // q8_1 segment: d * sum_b d8_b (sc_2b dot_2b + sc_2b+1 dot_2b+1)
 //               - dmin * sum_s min_s * d8 * sum(q8 of s)
-// The 2-bit fields g < 3 of a byte are masked in place (value 4^g q <= 48,
-// still a non-negative signed byte) and the 4^g is shifted out of the
-// integer sum afterwards (exact: the sum is a multiple of 4^g), which saves a
-// shift per weight word; field 3 is shifted down first.
+// The 2-bit fields of a byte are masked in place (value 4^g q) and the 4^g
+// is shifted out of the integer sum afterwards (exact: the sum is a multiple
+// of 4^g), which saves a shift per weight word; fields 0-2 stay below 128
+// (signed bytes), field 3 reaches 0xC0 and its products take the bytes as
+// unsigned.
 // sum of the four products of unsigned bytes of a and signed bytes of b, plus c
 __device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c)
 {
