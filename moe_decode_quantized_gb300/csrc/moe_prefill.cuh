@@ -25,7 +25,9 @@
 // significant bits: the dequantised q8_1 activation, 18 bits, exactly; the
 // weight to 2^-23) and accumulate hi.hi + hi.lo + lo.hi, so g and u are as
 // exact as f32 sums allow -- h is quantised to q8_1 again, and g, u a few
-// 2^-12 off would move some of its roundings. down (AK = 2) takes single
+// 2^-12 off would move some of its roundings. Up to 64 columns, hi.hi and
+// hi.lo are one MMA over the B stage's hi and lo rows side by side: an
+// M = 128 MMA takes as long for 16 columns as for 128. down (AK = 2) takes single
 // fp16 parts (about 2^-12 relative per operand): its output is only summed.
 // The tensor cores' f32 accumulation is coarser than a sequential f32 sum
 // (about 2e-5 relative over K = 4096), so K is split over up to four
@@ -216,6 +218,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int nb16 = (ncols + TC_BROWS - 1) / TC_BROWS;  // B boxes a stage and part
     const int n_mma = nb16 * TC_BROWS;                   // MMA N (a multiple of 16)
     const uint32_t idesc = mma_idesc(TC_M, n_mma, AK == 0);
+    // split GEMM over at most 64 columns: the B stage holds the hi rows and
+    // then the lo rows, so one MMA of 2 n_mma columns computes hi.hi and hi.lo
+    // side by side in the accumulator (an M = 128 MMA costs the same up to
+    // N = 128); the epilogue adds the two halves
+    const bool cat = PARTS == 2 && 2 * n_mma <= TC_NT;
+    const uint32_t idesc2 = mma_idesc(TC_M, 2 * n_mma, false);
     const int KC = a.K / TC_KC;
     const int per_raw = AK == 0 ? 1 : a.rk / TC_KC;     // A stages a raw stage feeds
     // the B ring holds as many stages as the tile's columns allow: narrow
@@ -309,12 +317,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         mma_f16(acc, ad + 2 * k, bd + 2 * k, idesc, !first || k > 0);
                 } else {
                     const uint32_t ta = tmem + TC_TA0 + (uint32_t)s * TAC;  // A in TMEM: 8 columns a K = 16 step
+                    if (cat) {
 #pragma unroll
-                    for (int k = 0; k < TC_KC / 16; ++k) {
-                        mma_f16_ts(acc, ta + 8 * k, bd + 2 * k, idesc, !first || k > 0);
-                        if constexpr (PARTS == 2) {  // + hi . lo + lo . hi (lo parts after the hi parts)
-                            mma_f16_ts(acc, ta + 8 * k, bd + (bpart >> 4) + 2 * k, idesc, true);
+                        for (int k = 0; k < TC_KC / 16; ++k) {
+                            // hi . [hi | lo] over 2 n_mma columns, then + lo . hi
+                            mma_f16_ts(acc, ta + 8 * k, bd + 2 * k, idesc2, !first || k > 0);
                             mma_f16_ts(acc, ta + 32 + 8 * k, bd + 2 * k, idesc, true);
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < TC_KC / 16; ++k) {
+                            mma_f16_ts(acc, ta + 8 * k, bd + 2 * k, idesc, !first || k > 0);
+                            if constexpr (PARTS == 2) {  // + hi . lo + lo . hi (lo parts after the hi parts)
+                                mma_f16_ts(acc, ta + 8 * k, bd + (bpart >> 4) + 2 * k, idesc, true);
+                                mma_f16_ts(acc, ta + 32 + 8 * k, bd + 2 * k, idesc, true);
+                            }
                         }
                     }
                 }
@@ -368,9 +385,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int cb = 32 * (warp >> 2); cb < ncols; cb += 32 * (TC_WORKERS / 4)) {
             float v[32];
             tmem_ld32(lane_addr + (uint32_t)cb, v);
+            if (cat) {  // + the hi . lo half
+                float w[32];
+                tmem_ld32(lane_addr + (uint32_t)(n_mma + cb), w);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    v[i] = __fadd_rn(v[i], w[i]);
+            }
             for (int j = 1; j < a.ksplit; ++j) {
                 float w[32];
                 tmem_ld32(lane_addr + (uint32_t)(j * TC_NT + cb), w);
+                if (cat) {
+                    float w2[32];
+                    tmem_ld32(lane_addr + (uint32_t)(j * TC_NT + n_mma + cb), w2);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        w[i] = __fadd_rn(w[i], w2[i]);
+                }
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
                     v[i] = __fadd_rn(v[i], w[i]);
