@@ -1409,11 +1409,11 @@ static int prefill_step(const moe_cfg *cfg, const moe_layer *layer, const moe_ar
     const uint64_t q2row = (uint64_t)dim / 256 * MOE_Q2K_BYTES, q3row = (uint64_t)inter / 256 * MOE_Q3K_BYTES;
     CUtensorMap gmap, umap, dmap, xmap, xlmap, hmap;
     if ((rc = map_arena(&gmap, ab + arena->gate_off, q2row, inter, arena_slots, arena->slot_bytes,
-                        4 * MOE_Q2K_BYTES)) ||
+                        tc_raw_blocks(1) * MOE_Q2K_BYTES)) ||
         (rc = map_arena(&umap, ab + arena->up_off, q2row, inter, arena_slots, arena->slot_bytes,
-                        4 * MOE_Q2K_BYTES)) ||
+                        tc_raw_blocks(1) * MOE_Q2K_BYTES)) ||
         (rc = map_arena(&dmap, ab + arena->down_off, q3row, dim, arena_slots, arena->slot_bytes,
-                        8 * MOE_Q3K_BYTES)) ||
+                        tc_raw_blocks(2) * MOE_Q3K_BYTES)) ||
         (rc = map_rows16(&xmap, false, xg, dim, P, (uint64_t)dim * 2, TC_BROWS)) ||
         (rc = map_rows16(&xlmap, false, xg_lo, dim, P, (uint64_t)dim * 2, TC_BROWS)) ||
         (rc = map_rows16(&hmap, false, hh, inter, P, (uint64_t)inter * 2, TC_BROWS)))
@@ -1421,8 +1421,8 @@ static int prefill_step(const moe_cfg *cfg, const moe_layer *layer, const moe_ar
     TcArgs ga = tc_args(inter, P, dim, g, inter, status);
     ga.tasks = tasks;
     ga.ntasks = ntasks;
-    ga.raw_row = 4 * MOE_Q2K_BYTES;
-    ga.rk = 1024;
+    ga.raw_row = tc_raw_blocks(1) * MOE_Q2K_BYTES;
+    ga.rk = tc_raw_blocks(1) * 256;
     ga.S = 4;  // A stages in TMEM: 4 x 64 columns (hi and lo) beside two accumulators
     ga.SR = 2;
     ga.ksplit = 2;
@@ -1444,8 +1444,8 @@ static int prefill_step(const moe_cfg *cfg, const moe_layer *layer, const moe_ar
     da.colw = pair_w;
     da.tasks = tasks;
     da.ntasks = ntasks;
-    da.raw_row = 8 * MOE_Q3K_BYTES;
-    da.rk = 2048;
+    da.raw_row = tc_raw_blocks(2) * MOE_Q3K_BYTES;
+    da.rk = tc_raw_blocks(2) * 256;
     da.S = 8;  // A stages in TMEM: 8 x 32 columns beside two accumulators
     da.SR = 1;
     da.ksplit = 2;

@@ -96,17 +96,72 @@ __device__ __forceinline__ void split_half2(float a, float b, uint32_t &hi, uint
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
-// Q2_K: the 32 weights of group gi (0, 1) of quarter kq of the super-block at
-// blk (elements 32 gi .. 32 gi + 31 of the quarter) of one row -> 16 words of
-// fp16 pairs (hi) and of the pairs' remainders (lo), element order.
+// super-blocks of a row in one raw stage: Q2_K 4 (K = 1024 a stage), Q3_K 8 (K = 2048)
+__host__ __device__ constexpr int tc_raw_blocks(int AK) { return AK == 1 ? 4 : 8; }
+__host__ __device__ constexpr int tc_block_bytes(int AK) { return AK == 1 ? MOE_Q2K_BYTES : MOE_Q3K_BYTES; }
+__host__ __device__ constexpr int tc_block_words(int AK) { return AK == 1 ? 21 : 28; }
+
+// The words of super-block b of a raw-stage row (16-byte aligned; its
+// stride, 336 or 880 bytes, an odd number of 16-byte units, so the eight
+// rows of a quarter warp fall in distinct bank groups) by 16-byte loads:
+// word i = bytes 4 i .. 4 i + 3 of the block, bytes past its end read as 0.
+// O, the block's byte offset, is a constant, so the byte alignment (blocks
+// of 84 or 110 bytes) costs shifts between registers only.
+template <int O, int BB, int NW>
+__device__ __forceinline__ void tc_block_words_at(const uint8_t *row, uint32_t (&E)[NW])
+{
+    constexpr int off = O & 15, nch = (off + BB + 15) / 16, w0 = off >> 2, sh = (off & 3) * 8;
+    uint32_t C[4 * nch];
+    const uint4 *p = reinterpret_cast<const uint4 *>(row + (O & ~15));
+#pragma unroll
+    for (int c = 0; c < nch; ++c) {
+        const uint4 v = p[c];
+        C[4 * c] = v.x;
+        C[4 * c + 1] = v.y;
+        C[4 * c + 2] = v.z;
+        C[4 * c + 3] = v.w;
+    }
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+        const int w = w0 + i;
+        const uint32_t lo = w < 4 * nch ? C[w] : 0u, hi = w + 1 < 4 * nch ? C[w + 1] : 0u;
+        E[i] = sh ? __funnelshift_r(lo, hi, sh) : lo;
+    }
+}
+
+template <int AK>
+__device__ __forceinline__ void tc_load_block(const uint8_t *row, int b, uint32_t (&E)[tc_block_words(AK)])
+{
+    constexpr int BB = tc_block_bytes(AK), NW = tc_block_words(AK);
+    switch (b) {
+    case 0: tc_block_words_at<0 * BB, BB, NW>(row, E); break;
+    case 1: tc_block_words_at<1 * BB, BB, NW>(row, E); break;
+    case 2: tc_block_words_at<2 * BB, BB, NW>(row, E); break;
+    case 3: tc_block_words_at<3 * BB, BB, NW>(row, E); break;
+    default:
+        if constexpr (tc_raw_blocks(AK) == 8) {
+            switch (b) {
+            case 4: tc_block_words_at<4 * BB, BB, NW>(row, E); break;
+            case 5: tc_block_words_at<5 * BB, BB, NW>(row, E); break;
+            case 6: tc_block_words_at<6 * BB, BB, NW>(row, E); break;
+            default: tc_block_words_at<7 * BB, BB, NW>(row, E); break;
+            }
+        }
+    }
+}
+
+// Q2_K: the 32 weights of group gi (0, 1) of quarter KQ of a super-block
+// (its 21 words bw: scales 0-3, quants 4-19, d and dmin 20) -- elements
+// 32 gi .. 32 gi + 31 of the quarter -- to 16 words of fp16 pairs (hi) and of
+// the pairs' remainders (lo), element order.
 // w = d sc q - dmin m (one f32 rounding). A weight takes one of four values a
 // sub-block (q = 0..3): their hi and lo halves form two 8-byte tables, and a
 // byte permute with a selector made from two quants (one multiply-add) fetches
 // a pair of weights.
-__device__ __forceinline__ void dq_q2k_group(const uint8_t *blk, int kq, int gi, uint32_t (&o)[16], uint32_t (&ol)[16])
+template <int KQ>
+__device__ __forceinline__ void dq_q2k_group(const uint32_t (&bw)[21], int gi, uint32_t (&o)[16], uint32_t (&ol)[16])
 {
-    const uint32_t *bw = reinterpret_cast<const uint32_t *>(blk);  // 4-byte aligned (84-byte blocks)
-    const uint32_t scw = bw[kq] >> (16 * gi);                      // scales of sub-blocks 4 kq + 2 gi, + 1
+    const uint32_t scw = bw[KQ] >> (16 * gi);  // scales of sub-blocks 4 KQ + 2 gi, + 1
     const uint32_t dd = bw[20];
     const float d = f16_bits_to_f32(dd), dmin = f16_bits_to_f32(dd >> 16);
     uint32_t th[2][2], tl[2][2];  // [sub-block][q >> 1]: halves of q = 0, 1 and q = 2, 3
@@ -117,7 +172,8 @@ __device__ __forceinline__ void dq_q2k_group(const uint8_t *blk, int kq, int gi,
         split_half2(-dm, fmaf(1.0f, ds, -dm), th[u][0], tl[u][0]);
         split_half2(fmaf(2.0f, ds, -dm), fmaf(3.0f, ds, -dm), th[u][1], tl[u][1]);
     }
-    const int half = kq >> 1, sh = 2 * (2 * (kq & 1) + gi);
+    constexpr int half = KQ >> 1;
+    const int sh = 2 * (2 * (KQ & 1) + gi);
 #pragma unroll
     for (int wi = 0; wi < 8; ++wi) {
         const uint32_t qq = (bw[4 + 8 * half + wi] >> sh) & 0x03030303u;  // four quants, one a byte
@@ -131,38 +187,28 @@ __device__ __forceinline__ void dq_q2k_group(const uint8_t *blk, int kq, int gi,
     }
 }
 
-// Q3_K: the 32 weights of group gi of quarter kq of one row from a 110-byte
-// block at a 2-byte aligned address. w = d * (scale - 32) * q (exact in
-// f32), q = low2 | hbit << 2 minus 4.
-__device__ __forceinline__ void dq_q3k_group(const uint8_t *blk, int kq, int gi, uint32_t (&o)[16])
+// Q3_K: the 32 weights of group gi of quarter KQ of one row's super-block
+// (its 28 words w: hmask 0-7, quants 8-23, scales 24-26, d the low half of
+// 27). w = d * (scale - 32) * q (exact in f32), q = low2 | hbit << 2 minus 4.
+template <int KQ>
+__device__ __forceinline__ void dq_q3k_group(const uint32_t (&w)[28], int gi, uint32_t (&o)[16])
 {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(blk);
-    const uint32_t *W = reinterpret_cast<const uint32_t *>(a & ~(uintptr_t)3);
-    const uint32_t sh = (uint32_t)(a & 3) * 8u;
-    auto word = [&](int i) { return __funnelshift_r(W[i], W[i + 1], sh); };
-    uint32_t hm[8], qv[8];
-    const int half = kq >> 1, g0 = 2 * (kq & 1);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        hm[i] = word(i);
-        qv[i] = word(8 + 8 * half + i);
-    }
-    const uint32_t s0 = word(24), s1 = word(25), s2 = word(26);
-    const float d = f16_bits_to_f32(word(27));
-    const uint32_t scb[3] = {s0, s1, s2};
-    auto sbyte = [&](int i) { return (scb[i >> 2] >> (8 * (i & 3))) & 0xFFu; };
+    constexpr int half = KQ >> 1, g0 = 2 * (KQ & 1);
+    const float d = f16_bits_to_f32(w[27]);
     float ds[2];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-        const int i = 4 * kq + 2 * gi + u;  // sub-block
-        const uint32_t lo4 = i < 8 ? (sbyte(i) & 15u) : (sbyte(i - 8) >> 4);
-        const uint32_t hi2 = (sbyte(8 + (i & 3)) >> (2 * (i >> 2))) & 3u;
+        // sub-block 4 KQ + j: low four bits in byte j of scale word KQ (KQ < 2,
+        // low nibbles) or KQ - 2 (high nibbles), high two in byte j of word 2
+        const int j = 2 * gi + u;
+        const uint32_t lo4 = KQ < 2 ? (w[24 + KQ] >> (8 * j)) & 15u : (w[24 + (KQ & 1)] >> (8 * j + 4)) & 15u;
+        const uint32_t hi2 = (w[26] >> (8 * j + 2 * KQ)) & 3u;
         ds[u] = d * (float)((int)(lo4 | (hi2 << 4)) - 32);
     }
     const int g = g0 + gi, hsh = 4 * half + g;  // weight j: bit j / 32 of hmask[j % 32]
 #pragma unroll
     for (int wi = 0; wi < 8; ++wi) {
-        const uint32_t v = ((qv[wi] >> (2 * g)) & 0x03030303u) | (((hm[wi] >> hsh) & 0x01010101u) << 2);
+        const uint32_t v = ((w[8 + 8 * half + wi] >> (2 * g)) & 0x03030303u) | (((w[wi] >> hsh) & 0x01010101u) << 2);
         const int u = wi >> 2;
         float f[4];
 #pragma unroll
@@ -181,6 +227,34 @@ __device__ __forceinline__ void tc_wait(uint64_t *bar, uint32_t parity, const Tc
 {
     if (!dead && !mbar_wait(bar, parity, a.status, a.wait_ns))
         dead = true;
+}
+
+// one quarter of a super-block (K-chunk kc): this thread's 32 weights into
+// A stage kc % S in TMEM, then the warp's arrival on its full barrier
+template <int AK, int KQ>
+__device__ __forceinline__ void tc_quarter(const uint32_t (&E)[tc_block_words(AK)], int kc, int S, int gi,
+                                           uint32_t ta0, uint32_t tac, uint64_t *full_a, uint64_t *empty_a,
+                                           const TcArgs &a, bool &dead)
+{
+    const int s = kc % S;
+    if (kc >= S)
+        tc_wait(&empty_a[s], (uint32_t)((kc / S - 1) & 1), a, dead);
+    const uint32_t ta = ta0 + (uint32_t)s * tac;
+    uint32_t o[16];
+    if constexpr (AK == 1) {
+        uint32_t ol[16];
+        dq_q2k_group<KQ>(E, gi, o, ol);
+        tmem_st16(ta, o);
+        tmem_st16(ta + 32, ol);
+    } else {
+        dq_q3k_group<KQ>(E, gi, o);
+        tmem_st16(ta, o);
+    }
+    tmem_st_wait();
+    tc_fence_before();  // the stores before the arrival the MMA thread acquires
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0)
+        mbar_arrive(&full_a[s]);
 }
 
 template <int AK>
@@ -344,36 +418,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // ---------------- workers (AK > 0): raw blocks -> fp16 operand tiles
         if constexpr (AK > 0) {
             const int r = threadIdx.x & (TC_M - 1), gi = threadIdx.x >> 7;  // tile row, 32-weight group
-            const int bbytes = AK == 1 ? MOE_Q2K_BYTES : MOE_Q3K_BYTES;
-            for (int kc = 0; kc < KC; ++kc) {
-                const int rc = kc / per_raw, ri = rc % SR, q = kc % per_raw;
-                if (q == 0)
+            constexpr int NB = tc_raw_blocks(AK);
+            // this thread's row of a stage: TMEM lane r, columns 16 gi .. (hi), + 32 (lo)
+            const uint32_t ta0 = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + TC_TA0 + 16u * (uint32_t)gi;
+            for (int kb = 0; kb < KC / 4; ++kb) {  // super-blocks along K, four K-chunks each
+                const int rc = kb / NB, ri = rc % SR, b = kb % NB;
+                if (b == 0)
                     tc_wait(&raw_full[ri], (uint32_t)((rc / SR) & 1), a, dead);
-                const int s = kc % S;
-                if (kc >= S)
-                    tc_wait(&empty_a[s], (uint32_t)((kc / S - 1) & 1), a, dead);
-                const uint8_t *blk = sraw + (size_t)ri * a.raw_bytes + (size_t)r * a.raw_row + (q >> 2) * bbytes;
-                // this thread's row of the stage: TMEM lane r, columns 16 gi .. (hi), + 32 (lo)
-                const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + TC_TA0 + (uint32_t)s * TAC +
-                                    16u * (uint32_t)gi;
-                uint32_t o[16];
-                if constexpr (AK == 1) {
-                    uint32_t ol[16];
-                    dq_q2k_group(blk, q & 3, gi, o, ol);
-                    tmem_st16(ta, o);
-                    tmem_st16(ta + 32, ol);
-                } else {
-                    dq_q3k_group(blk, q & 3, gi, o);
-                    tmem_st16(ta, o);
-                }
-                tmem_st_wait();
-                tc_fence_before();  // the stores before the arrival the MMA thread acquires
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&full_a[s]);
-                    if (q == per_raw - 1)
+                uint32_t E[tc_block_words(AK)];
+                tc_load_block<AK>(sraw + (size_t)ri * a.raw_bytes + (size_t)r * a.raw_row, b, E);
+                if (b == NB - 1) {  // the raw stage is all in registers: release it
+                    __syncwarp();
+                    if (lane == 0)
                         mbar_arrive(&raw_empty[ri]);
                 }
+                tc_quarter<AK, 0>(E, 4 * kb, S, gi, ta0, TAC, full_a, empty_a, a, dead);
+                tc_quarter<AK, 1>(E, 4 * kb + 1, S, gi, ta0, TAC, full_a, empty_a, a, dead);
+                tc_quarter<AK, 2>(E, 4 * kb + 2, S, gi, ta0, TAC, full_a, empty_a, a, dead);
+                tc_quarter<AK, 3>(E, 4 * kb + 3, S, gi, ta0, TAC, full_a, empty_a, a, dead);
             }
         }
         // ---------------- epilogue: row m0 + 32 (warp % 4) + lane (the TMEM lane
