@@ -229,16 +229,23 @@ __device__ __forceinline__ void tc_wait(uint64_t *bar, uint32_t parity, const Tc
         dead = true;
 }
 
-// one quarter of a super-block (K-chunk kc): this thread's 32 weights into
-// A stage kc % S in TMEM, then the warp's arrival on its full barrier
+// K-chunk j's MMAs done: barrier mdone[j % D] (one commit a chunk), phase j / D
+__device__ __forceinline__ void tc_wait_chunk(uint64_t *mdone, int D, int j, const TcArgs &a, bool &dead)
+{
+    tc_wait(&mdone[j % D], (uint32_t)((j / D) & 1), a, dead);
+}
+
+// one quarter of a super-block (K-chunk kc): once chunk kc - S has freed A
+// stage kc % S, this thread's 32 weights into it in TMEM, then the warp's
+// arrival on its full barrier
 template <int AK, int KQ>
 __device__ __forceinline__ void tc_quarter(const uint32_t (&E)[tc_block_words(AK)], int kc, int S, int gi,
-                                           uint32_t ta0, uint32_t tac, uint64_t *full_a, uint64_t *empty_a,
+                                           uint32_t ta0, uint32_t tac, uint64_t *full_a, uint64_t *mdone, int D,
                                            const TcArgs &a, bool &dead)
 {
     const int s = kc % S;
     if (kc >= S)
-        tc_wait(&empty_a[s], (uint32_t)((kc / S - 1) & 1), a, dead);
+        tc_wait_chunk(mdone, D, kc - S, a, dead);
     const uint32_t ta = ta0 + (uint32_t)s * tac;
     uint32_t o[16];
     if constexpr (AK == 1) {
@@ -271,8 +278,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     uint8_t *sraw = sa + (AK == 0 ? (size_t)S * 16384 : 0);      // SR x raw_bytes
     uint8_t *sb = sraw + (size_t)SR * a.raw_bytes;  // the B ring, b_buf bytes
     uint64_t *bars = reinterpret_cast<uint64_t *>(sb + a.b_buf);
-    uint64_t *full_a = bars, *empty_a = bars + S, *full_b = bars + 2 * S, *empty_b = full_b + TC_SB_MAX;
-    uint64_t *raw_full = empty_b + TC_SB_MAX, *raw_empty = raw_full + SR, *done = raw_empty + SR;
+    uint64_t *full_a = bars, *mdone = bars + S, *full_b = mdone + TC_SB_MAX;
+    uint64_t *raw_full = full_b + TC_SB_MAX, *raw_empty = raw_full + SR, *done = raw_empty + SR;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -304,16 +311,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // groups keep many loads in flight
     const uint32_t bpart = (uint32_t)nb16 * TC_BROWS * 128u, bstage = PARTS * bpart;
     const int SB = max(1, min(TC_SB_MAX, (int)(a.b_buf / bstage)));
+    // One barrier ring tells both the A side (S stages) and the B side (SB
+    // stages) which chunks' MMAs are done: a waiter for chunk j has already
+    // seen chunk j - D done (it waited for it, or for a later one, before
+    // filling the stage now being refilled) and no MMA of chunk j + D can run
+    // before the waiter's own next stage, so parity j / D is unambiguous.
+    const int D = max(S, SB);  // S <= TC_SB_MAX
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
+        for (int s = 0; s < S; ++s)
             mbar_init(&full_a[s], AK == 0 ? 1 : TC_WORKERS);  // one arrival a worker warp
-            mbar_init(&empty_a[s], 1);
-        }
-        for (int s = 0; s < SB; ++s) {
+        for (int j = 0; j < D; ++j)
+            mbar_init(&mdone[j], 1);
+        for (int s = 0; s < SB; ++s)
             mbar_init(&full_b[s], 1);
-            mbar_init(&empty_b[s], 1);
-        }
         for (int r = 0; r < SR; ++r) {
             mbar_init(&raw_full[r], 1);
             mbar_init(&raw_empty[r], TC_WORKERS);
@@ -347,7 +358,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 } else {
                     const int s = kc % S;
                     if (kc >= S)
-                        tc_wait(&empty_a[s], (uint32_t)((kc / S - 1) & 1), a, dead);
+                        tc_wait_chunk(mdone, D, kc - S, a, dead);
                     mbar_arrive_expect_tx(&full_a[s], 16384u);
                     tma_load_2d(sa + (size_t)s * 16384, &amap, kc * TC_KC, m0, &full_a[s]);
                 }
@@ -361,7 +372,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             for (int kc = 0; kc < KC; ++kc) {
                 const int s = kc % SB;
                 if (kc >= SB)
-                    tc_wait(&empty_b[s], (uint32_t)((kc / SB - 1) & 1), a, dead);
+                    tc_wait_chunk(mdone, D, kc - SB, a, dead);
                 uint8_t *dst = sb + (size_t)s * bstage;
                 mbar_arrive_expect_tx(&full_b[s], bstage);
                 for (int i = 0; i < nb16; ++i) {
@@ -409,8 +420,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         }
                     }
                 }
-                mma_commit(&empty_a[s]);
-                mma_commit(&empty_b[t]);
+                mma_commit(&mdone[kc % D]);  // frees A stage s and B stage t
             }
             mma_commit(done);
         }
@@ -432,10 +442,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     if (lane == 0)
                         mbar_arrive(&raw_empty[ri]);
                 }
-                tc_quarter<AK, 0>(E, 4 * kb, S, gi, ta0, TAC, full_a, empty_a, a, dead);
-                tc_quarter<AK, 1>(E, 4 * kb + 1, S, gi, ta0, TAC, full_a, empty_a, a, dead);
-                tc_quarter<AK, 2>(E, 4 * kb + 2, S, gi, ta0, TAC, full_a, empty_a, a, dead);
-                tc_quarter<AK, 3>(E, 4 * kb + 3, S, gi, ta0, TAC, full_a, empty_a, a, dead);
+                tc_quarter<AK, 0>(E, 4 * kb, S, gi, ta0, TAC, full_a, mdone, D, a, dead);
+                tc_quarter<AK, 1>(E, 4 * kb + 1, S, gi, ta0, TAC, full_a, mdone, D, a, dead);
+                tc_quarter<AK, 2>(E, 4 * kb + 2, S, gi, ta0, TAC, full_a, mdone, D, a, dead);
+                tc_quarter<AK, 3>(E, 4 * kb + 3, S, gi, ta0, TAC, full_a, mdone, D, a, dead);
             }
         }
         // ---------------- epilogue: row m0 + 32 (warp % 4) + lane (the TMEM lane
