@@ -229,23 +229,36 @@ __device__ __forceinline__ void tc_wait(uint64_t *bar, uint32_t parity, const Tc
         dead = true;
 }
 
-// K-chunk j's MMAs done: barrier mdone[j % D] (one commit a chunk), phase j / D
-__device__ __forceinline__ void tc_wait_chunk(uint64_t *mdone, int D, int j, const TcArgs &a, bool &dead)
-{
-    tc_wait(&mdone[j % D], (uint32_t)((j / D) & 1), a, dead);
-}
+// Position i in a ring of n barriers: barrier i % n, phase parity (i / n) & 1,
+// stepped by one (the loops of one thread stay free of divisions by the
+// run-time ring sizes, which cost a chain of dependent instructions each)
+struct RingPos {
+    int slot = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void next(int n)
+    {
+        if (++slot == n) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+};
 
-// one quarter of a super-block (K-chunk kc): once chunk kc - S has freed A
-// stage kc % S, this thread's 32 weights into it in TMEM, then the warp's
-// arrival on its full barrier
+// one quarter of a super-block (K-chunk kc): once chunk kc - S (position
+// `done_pos` of the completion ring of D barriers) has freed A stage `st`,
+// this thread's 32 weights into it in TMEM, then the warp's arrival on its
+// full barrier
 template <int AK, int KQ>
 __device__ __forceinline__ void tc_quarter(const uint32_t (&E)[tc_block_words(AK)], int kc, int S, int gi,
                                            uint32_t ta0, uint32_t tac, uint64_t *full_a, uint64_t *mdone, int D,
-                                           const TcArgs &a, bool &dead)
+                                           RingPos &st, RingPos &done_pos, const TcArgs &a, bool &dead)
 {
-    const int s = kc % S;
-    if (kc >= S)
-        tc_wait_chunk(mdone, D, kc - S, a, dead);
+    const int s = st.slot;
+    if (kc >= S) {
+        tc_wait(&mdone[done_pos.slot], done_pos.phase, a, dead);
+        done_pos.next(D);
+    }
+    st.next(S);
     const uint32_t ta = ta0 + (uint32_t)s * tac;
     uint32_t o[16];
     if constexpr (AK == 1) {
@@ -345,22 +358,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // raw blocks), the next the B ring, each on its own barriers
         if (lane == 0) {
             tma_prefetch_map(&amap);
-            for (int kc = 0; kc < KC; ++kc) {
-                if constexpr (AK > 0) {
-                    if (kc % per_raw == 0) {
-                        const int rc = kc / per_raw, r = rc % SR;
-                        if (rc >= SR)
-                            tc_wait(&raw_empty[r], (uint32_t)((rc / SR - 1) & 1), a, dead);
-                        mbar_arrive_expect_tx(&raw_full[r], a.raw_bytes);
-                        tma_load_3d(sraw + (size_t)r * a.raw_bytes, &amap, rc * (a.raw_row / 4), m0, slot,
-                                    &raw_full[r]);
+            RingPos pf, pw;  // the stage being filled; the one being waited for
+            if constexpr (AK > 0) {
+                for (int rc = 0; rc < KC / per_raw; ++rc) {  // raw stages
+                    if (rc >= SR) {
+                        tc_wait(&raw_empty[pw.slot], pw.phase, a, dead);
+                        pw.next(SR);
                     }
-                } else {
-                    const int s = kc % S;
-                    if (kc >= S)
-                        tc_wait_chunk(mdone, D, kc - S, a, dead);
-                    mbar_arrive_expect_tx(&full_a[s], 16384u);
-                    tma_load_2d(sa + (size_t)s * 16384, &amap, kc * TC_KC, m0, &full_a[s]);
+                    mbar_arrive_expect_tx(&raw_full[pf.slot], a.raw_bytes);
+                    tma_load_3d(sraw + (size_t)pf.slot * a.raw_bytes, &amap, rc * (a.raw_row / 4), m0, slot,
+                                &raw_full[pf.slot]);
+                    pf.next(SR);
+                }
+            } else {
+                for (int kc = 0; kc < KC; ++kc) {
+                    if (kc >= S) {  // chunk kc - S done
+                        tc_wait(&mdone[pw.slot], pw.phase, a, dead);
+                        pw.next(D);
+                    }
+                    mbar_arrive_expect_tx(&full_a[pf.slot], 16384u);
+                    tma_load_2d(sa + (size_t)pf.slot * 16384, &amap, kc * TC_KC, m0, &full_a[pf.slot]);
+                    pf.next(S);
                 }
             }
         }
@@ -369,10 +387,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             tma_prefetch_map(&bmap);
             if constexpr (PARTS == 2)
                 tma_prefetch_map(&bmap_lo);
+            RingPos pf, pw;
             for (int kc = 0; kc < KC; ++kc) {
-                const int s = kc % SB;
-                if (kc >= SB)
-                    tc_wait_chunk(mdone, D, kc - SB, a, dead);
+                if (kc >= SB) {  // chunk kc - SB done
+                    tc_wait(&mdone[pw.slot], pw.phase, a, dead);
+                    pw.next(D);
+                }
+                const int s = pf.slot;
+                pf.next(SB);
                 uint8_t *dst = sb + (size_t)s * bstage;
                 mbar_arrive_expect_tx(&full_b[s], bstage);
                 for (int i = 0; i < nb16; ++i) {
@@ -387,13 +409,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // ---------------- MMA issuer
         if (lane == 0) {
             const int kper = KC / a.ksplit;  // K-chunks an accumulator takes
+            RingPos pa, pb, pd;               // A stage, B stage, completion barrier
+            int acc_i = 0, kin = 0;           // accumulator, chunk within it
             for (int kc = 0; kc < KC; ++kc) {
-                const int s = kc % S, t = kc % SB;
-                tc_wait(&full_a[s], (uint32_t)((kc / S) & 1), a, dead);
-                tc_wait(&full_b[t], (uint32_t)((kc / SB) & 1), a, dead);
+                const int s = pa.slot, t = pb.slot;
+                tc_wait(&full_a[s], pa.phase, a, dead);
+                tc_wait(&full_b[t], pb.phase, a, dead);
                 tc_fence_after();
-                const uint32_t acc = tmem + (uint32_t)(kc / kper) * TC_NT;
-                const bool first = kc % kper == 0;
+                const uint32_t acc = tmem + (uint32_t)acc_i * TC_NT;
+                const bool first = kin == 0;
                 const uint64_t bd = sw128_desc(sb + (size_t)t * bstage);
                 if constexpr (AK == 0) {
                     const uint64_t ad = sw128_desc(sa + (size_t)s * 16384);
@@ -420,7 +444,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         }
                     }
                 }
-                mma_commit(&mdone[kc % D]);  // frees A stage s and B stage t
+                mma_commit(&mdone[pd.slot]);  // frees A stage s and B stage t
+                pa.next(S);
+                pb.next(SB);
+                pd.next(D);
+                if (++kin == kper) {
+                    kin = 0;
+                    ++acc_i;
+                }
             }
             mma_commit(done);
         }
@@ -431,21 +462,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             constexpr int NB = tc_raw_blocks(AK);
             // this thread's row of a stage: TMEM lane r, columns 16 gi .. (hi), + 32 (lo)
             const uint32_t ta0 = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + TC_TA0 + 16u * (uint32_t)gi;
+            RingPos pr, ps, pw;  // raw stage; A stage; completion barrier of chunk kc - S
+            int b = 0;           // super-block within the raw stage
             for (int kb = 0; kb < KC / 4; ++kb) {  // super-blocks along K, four K-chunks each
-                const int rc = kb / NB, ri = rc % SR, b = kb % NB;
                 if (b == 0)
-                    tc_wait(&raw_full[ri], (uint32_t)((rc / SR) & 1), a, dead);
+                    tc_wait(&raw_full[pr.slot], pr.phase, a, dead);
                 uint32_t E[tc_block_words(AK)];
-                tc_load_block<AK>(sraw + (size_t)ri * a.raw_bytes + (size_t)r * a.raw_row, b, E);
+                tc_load_block<AK>(sraw + (size_t)pr.slot * a.raw_bytes + (size_t)r * a.raw_row, b, E);
                 if (b == NB - 1) {  // the raw stage is all in registers: release it
                     __syncwarp();
                     if (lane == 0)
-                        mbar_arrive(&raw_empty[ri]);
+                        mbar_arrive(&raw_empty[pr.slot]);
                 }
-                tc_quarter<AK, 0>(E, 4 * kb, S, gi, ta0, TAC, full_a, mdone, D, a, dead);
-                tc_quarter<AK, 1>(E, 4 * kb + 1, S, gi, ta0, TAC, full_a, mdone, D, a, dead);
-                tc_quarter<AK, 2>(E, 4 * kb + 2, S, gi, ta0, TAC, full_a, mdone, D, a, dead);
-                tc_quarter<AK, 3>(E, 4 * kb + 3, S, gi, ta0, TAC, full_a, mdone, D, a, dead);
+                tc_quarter<AK, 0>(E, 4 * kb, S, gi, ta0, TAC, full_a, mdone, D, ps, pw, a, dead);
+                tc_quarter<AK, 1>(E, 4 * kb + 1, S, gi, ta0, TAC, full_a, mdone, D, ps, pw, a, dead);
+                tc_quarter<AK, 2>(E, 4 * kb + 2, S, gi, ta0, TAC, full_a, mdone, D, ps, pw, a, dead);
+                tc_quarter<AK, 3>(E, 4 * kb + 3, S, gi, ta0, TAC, full_a, mdone, D, ps, pw, a, dead);
+                if (++b == NB) {
+                    b = 0;
+                    pr.next(SR);
+                }
             }
         }
         // ---------------- epilogue: row m0 + 32 (warp % 4) + lane (the TMEM lane
