@@ -135,6 +135,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// n / d and n % d for a divisor known only at run time, by one multiply-high
+// with m = ceil(2^32 / d): n m / 2^32 = n / d + n (m d - 2^32) / (d 2^32),
+// and the second term stays below 1 / d while n < 2^32 / d, so the floor is
+// exact there (task and ring indices are far below it). A plain division by
+// a run-time value is a chain of dependent instructions.
+struct FastDiv {
+    uint32_t d = 1, m = 0;
+    __host__ __device__ FastDiv() {}
+    // ceil(2^32 / d) = floor((2^32 - 1) / d) + 1 for every d >= 2 (a 32-bit division)
+    __host__ __device__ explicit FastDiv(uint32_t dv) : d(dv), m(dv > 1 ? 0xFFFFFFFFu / dv + 1u : 0u) {}
+    __device__ __forceinline__ uint32_t div(uint32_t n) const { return d > 1 ? __umulhi(n, m) : n; }
+    __device__ __forceinline__ uint32_t mod(uint32_t n) const { return n - div(n) * d; }
+};
+
 __device__ __forceinline__ uint64_t globaltimer()
 {
     uint64_t t;

@@ -344,7 +344,8 @@ struct Ring {
     PlanCache *pc;
     uint8_t *stage;
     uint32_t stage_bytes;
-    int S;
+    int S;                       // at least 2
+    uint32_t Sm;                 // ceil(2^32 / S): task i's round i / S = umulhi(i, Sm) (FastDiv)
     unsigned long long wait_ns;  // bound on each wait
     __device__ uint8_t *at(int slot) const { return stage + (size_t)slot * stage_bytes; }
 };
@@ -355,8 +356,8 @@ __device__ __forceinline__ bool ring_issue(const Ring &r, int i, const Task &t, 
                                            uint32_t bytes, uint64_t pol, uint32_t *status,
                                            const void *src2 = nullptr, uint32_t bytes2 = 0)
 {
-    const int slot = i % r.S;
-    const uint32_t round = (uint32_t)(i / r.S);
+    const uint32_t round = __umulhi((uint32_t)i, r.Sm);
+    const int slot = i - (int)round * r.S;
     if (round > 0 && !mbar_wait(&r.empty[slot], (round - 1) & 1u, status, r.wait_ns))
         return false;
     Task tt = t;
@@ -403,6 +404,7 @@ __device__ __forceinline__ Ring ring_carve(uint8_t *smem, int S, uint32_t stage_
 {
     Ring r;
     r.S = S;
+    r.Sm = FastDiv((uint32_t)S).m;
     r.wait_ns = wait_ns;
     r.full = reinterpret_cast<uint64_t *>(smem);
     r.empty = r.full + S;
@@ -429,7 +431,8 @@ __device__ __forceinline__ int ring_grab(const Ring &r)
 // just completed). Bounded like every wait; false after r.wait_ns.
 __device__ __forceinline__ bool ring_acquire(const Ring &r, int j, uint32_t *status)
 {
-    const int slot = j % r.S;
+    const uint32_t round = __umulhi((uint32_t)j, r.Sm);
+    const int slot = j - (int)round * r.S;
     volatile const int *seq = &r.desc[slot].seq;
     if (*seq != j) {
         const uint64_t t0 = globaltimer();
@@ -441,7 +444,7 @@ __device__ __forceinline__ bool ring_acquire(const Ring &r, int j, uint32_t *sta
             }
         }
     }
-    return mbar_wait(&r.full[slot], (uint32_t)(j / r.S) & 1u, status, r.wait_ns);
+    return mbar_wait(&r.full[slot], round & 1u, status, r.wait_ns);
 }
 
 // the producer warp caches the plan (all 32 lanes load in parallel, one
@@ -803,6 +806,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
         const PlanCache &pc = *ring.pc;
         const int rt = gate_rows_per_task(dim);
         const int tpe = inter / rt;  // tasks per expert: rt gate rows and the same up rows each
+        const FastDiv tpe_d((uint32_t)tpe);
         const int total = pc.ne * tpe;
         const uint32_t bytes = (uint32_t)(rt * nb * MOE_Q2K_BYTES);  // one matrix's rows
         for (;;) {
@@ -818,8 +822,8 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
                 if (issuer && tix < c1) {
                     Task t{};
                     t.kind = 1;
-                    t.p = tix / tpe;
-                    const int r = tix % tpe;
+                    t.p = (int)tpe_d.div((uint32_t)tix);
+                    const int r = tix - t.p * tpe;
                     t.row = r * rt;
                     t.pair0 = pc.pair_start[t.p];
                     t.npair = pc.pair_start[t.p + 1] - t.pair0;
@@ -901,7 +905,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
     bool hs_seen = false;
     for (;;) {
         const int j = ring_grab(ring);
-        const int slot = j % ring.S;
+        const int slot = j - (int)__umulhi((uint32_t)j, ring.Sm) * ring.S;
         if (!ring_acquire(ring, j, a.status))
             break;
         const Task t = ring.desc[slot];
@@ -1416,7 +1420,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
     const unsigned expected = (unsigned)R.ne;
     for (;;) {
         const int j = ring_grab(ring);
-        const int slot = j % ring.S;
+        const int slot = j - (int)__umulhi((uint32_t)j, ring.Sm) * ring.S;
         if (!ring_acquire(ring, j, a.status))
             break;
         const Task t = ring.desc[slot];
