@@ -552,6 +552,7 @@ __device__ void select_and_plan(const RouteArgs &a, const float *logits, const f
     unsigned long long *val = reinterpret_cast<unsigned long long *>(smem + sel_v_off());
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n = a.n, k = a.k, m = a.m, cap = m * k, mn = m * n;
+    const FastDiv nd((uint32_t)n), kd((uint32_t)k);  // token of entry i, of pair q: one multiply-high each
     float *sco = reinterpret_cast<float *>(val + (size_t)mn);
     if (tid < MOE_MAX_TOKENS)
         sm.flags[tid] = 0;
@@ -571,7 +572,7 @@ __device__ void select_and_plan(const RouteArgs &a, const float *logits, const f
         for (int u = 0; u < SEL_UNROLL; ++u) {
             const int i = b + tid + 256 * u;
             if (i < mn) {
-                const int t = i / n, e = i - t * n;
+                const int t = (int)nd.div((uint32_t)i), e = i - t * n;
                 val[i] = rank_value(kk[u], e);
                 sco[i] = ss[u];
                 if (!isfinite(ll[u]) || !isfinite(kk[u]))
@@ -612,8 +613,8 @@ __device__ void select_and_plan(const RouteArgs &a, const float *logits, const f
                 unsigned long long v[2];
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
-                    const int c = lane + 32 * j;
-                    v[j] = c < nc ? sm.cand[group * gsz + c / k][c % k] : 0ull;
+                    const int c = lane + 32 * j, cw = (int)kd.div((uint32_t)c);
+                    v[j] = c < nc ? sm.cand[group * gsz + cw][c - cw * k] : 0ull;
                 }
                 warp_topk<2>(v, k, fin);
             }
@@ -664,8 +665,8 @@ __device__ void select_and_plan(const RouteArgs &a, const float *logits, const f
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             const int q = lane + 32 * j;
-            eq[j] = q < cap ? sm.pick[q / k][q % k] : 0;
-            tq[j] = q / k;
+            tq[j] = (int)kd.div((uint32_t)q);
+            eq[j] = q < cap ? sm.pick[tq[j]][q - tq[j] * k] : 0;
             if (q < cap)
                 sm.ent[q] = eq[j];
         }
@@ -677,15 +678,19 @@ __device__ void select_and_plan(const RouteArgs &a, const float *logits, const f
             fq[j] = false;
             if (q < cap) {
                 int earlier = 0;
-                for (int q2 = 0; q2 < cap; ++q2) {
-                    const int e2 = sm.ent[q2], t2 = q2 / k;
+                for (int q2 = 0, t2 = 0, r2 = 0; q2 < cap; ++q2) {  // pair q2 = token t2, pick r2
+                    const int e2 = sm.ent[q2];
                     rq[j] += e2 < eq[j] || (e2 == eq[j] && t2 < tq[j]);
                     earlier += e2 == eq[j] && t2 < tq[j];
+                    if (++r2 == k) {
+                        r2 = 0;
+                        ++t2;
+                    }
                 }
                 fq[j] = earlier == 0;
                 sm.first[q] = fq[j];
                 a.plan_rows[rq[j]] = tq[j];
-                a.plan_w[rq[j]] = sm.w[tq[j]][q % k];
+                a.plan_w[rq[j]] = sm.w[tq[j]][q - tq[j] * k];
             }
         }
         __syncwarp();
@@ -837,8 +842,9 @@ __global__ void __launch_bounds__(256) moe_router_kernel(RouteArgs a)
     const int nw = blockDim.x >> 5, grp = lane >> 2, gv = lane & 3;
     {
         const unsigned gmask = 0xFu << (4 * grp);
+        const FastDiv md((uint32_t)m);
         for (int i = warp + nw * grp; i < nrows * m; i += nw * 8) {
-            const int r = i / m, t = i % m;
+            const int r = (int)md.div((uint32_t)i), t = i - r * m;
             const float l = red[i];
             const size_t o = (size_t)t * a.n + row0 + r;
             if (gv == 0)
