@@ -890,9 +890,10 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
     }
     consumers_sync();
     const int nblk = a.m * dim / 32;
+    const FastDiv bpx((uint32_t)(dim / 32));  // 32-value blocks a token row
     for (int i = threadIdx.x; i < nblk * 4; i += MOE_CONSUMER_WARPS * 32) {  // four lanes a block
         const int b = i >> 2, sub = i & 3;
-        const int t = b / (dim / 32), bi = b % (dim / 32);
+        const int t = (int)bpx.div((uint32_t)b), bi = b - t * (dim / 32);
         const uint4 w = ldx(((size_t)t * dim + bi * 32 + 8 * sub) / 8);
         const float v[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
                             bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
@@ -1373,12 +1374,13 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
     constexpr int DQ = 4, CTH = MOE_CONSUMER_WARPS * 32;
     const int np = min(R.pair_hi - R.pair_lo, a.pair_cap);
     const int nq = np * inter / 32 * 4;
+    const FastDiv bpr((uint32_t)(inter / 32));  // 32-value blocks a pair row
     for (int i0 = 0; i0 < nq; i0 += CTH * DQ) {
         float4 hv[DQ][2];
 #pragma unroll
         for (int u = 0; u < DQ; ++u) {
             const int i = i0 + (int)threadIdx.x + CTH * u, b = i >> 2, sub = i & 3;
-            const int pr = b / (inter / 32), bi = b % (inter / 32);
+            const int pr = (int)bpr.div((uint32_t)b), bi = b - pr * (inter / 32);
             const float4 *h4 =
                 reinterpret_cast<const float4 *>(a.h + (size_t)(R.pair_lo + pr) * inter + bi * 32 + 8 * sub);
             const bool in = i < nq;
@@ -1388,7 +1390,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
 #pragma unroll
         for (int u = 0; u < DQ; ++u) {
             const int i = i0 + (int)threadIdx.x + CTH * u, b = i >> 2, sub = i & 3;
-            const int pr = b / (inter / 32), bi = b % (inter / 32);
+            const int pr = (int)bpr.div((uint32_t)b), bi = b - pr * (inter / 32);
             if (i >= nq)
                 continue;
             const float v[8] = {hv[u][0].x, hv[u][0].y, hv[u][0].z, hv[u][0].w,
@@ -1492,11 +1494,12 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
         *s_nfin = 0;
     consumers_sync();
     const int ngroups = dim / rd;
+    const FastDiv tprd((uint32_t)R.tpr);
     auto count_in = [&](int g) {
         // experts p with lo <= p * tpr + g < hi
         const int a0 = R.lo - g, a1 = R.hi - g;
-        const int c0 = a0 <= 0 ? 0 : (a0 + R.tpr - 1) / R.tpr;
-        const int c1 = a1 <= 0 ? 0 : (a1 + R.tpr - 1) / R.tpr;
+        const int c0 = a0 <= 0 ? 0 : (int)tprd.div((uint32_t)(a0 + R.tpr - 1));
+        const int c1 = a1 <= 0 ? 0 : (int)tprd.div((uint32_t)(a1 + R.tpr - 1));
         return max(0, c1 - c0);
     };
     for (int g0 = threadIdx.x; g0 < ngroups; g0 += 2 * CTH) {
