@@ -617,30 +617,72 @@ struct PPlanArgs {
     uint32_t *status;
 };
 
+#define PLAN_SMEM_PICKS 5120  // m * k up to this: the plan is built in shared memory (16-bit indices)
+
 __global__ void __launch_bounds__(1024) moe_prefill_plan_kernel(PPlanArgs a)
 {
     __shared__ int s_cnt[MOE_MAX_ROUTED], s_off[MOE_MAX_ROUTED + 1], s_toff[MOE_MAX_ROUTED + 1];
-    const int tid = threadIdx.x, P = a.m * a.k;
-    for (int e = tid; e < a.n; e += blockDim.x)
+    __shared__ int s_wsum[2][32], s_fill[MOE_MAX_ROUTED];
+    // staged: the picks, each pair's pick (t k + i) and each pick's pair
+    __shared__ uint16_t s_pick[PLAN_SMEM_PICKS], s_qp[PLAN_SMEM_PICKS], s_pp[PLAN_SMEM_PICKS];
+    const int tid = threadIdx.x, P = a.m * a.k, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+    const bool staged = P <= PLAN_SMEM_PICKS;
+    for (int e = tid; e < a.n; e += blockDim.x) {
         s_cnt[e] = 0;
+        s_fill[e] = 0;
+    }
     __syncthreads();
     for (int p = tid; p < P; p += blockDim.x) {
         const int e = a.picks[p];
-        if (e >= 0 && e < a.n)
+        const bool ok = e >= 0 && e < a.n;
+        if (staged)
+            s_pick[p] = ok ? (uint16_t)e : (uint16_t)0xFFFFu;  // n <= 1024
+        if (ok)
             atomicAdd(&s_cnt[e], 1);
     }
     __syncthreads();
-    if (tid == 0) {
-        int acc = 0, tacc = 0;
-        for (int e = 0; e < a.n; ++e) {
-            s_off[e] = acc;
-            s_toff[e] = tacc;
-            acc += s_cnt[e];
-            tacc += (s_cnt[e] + TC_NT - 1) / TC_NT;
+    // offsets: an exclusive scan over the experts of their pair counts and of
+    // their column-task counts (thread e holds expert e; n <= 1024 threads)
+    {
+        const int c = tid < a.n ? s_cnt[tid] : 0, tc = (c + TC_NT - 1) / TC_NT;
+        int ic = c, it = tc;  // inclusive scans within the warp
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int uc = __shfl_up_sync(0xffffffffu, ic, o), ut = __shfl_up_sync(0xffffffffu, it, o);
+            if (lane >= o) {
+                ic += uc;
+                it += ut;
+            }
         }
-        s_off[a.n] = acc;
-        s_toff[a.n] = tacc;
-        *a.ntasks = tacc;
+        if (lane == 31) {
+            s_wsum[0][warp] = ic;
+            s_wsum[1][warp] = it;
+        }
+        __syncthreads();
+        if (warp == 0) {  // scan of the warp totals
+            int wc = lane < nw ? s_wsum[0][lane] : 0, wt = lane < nw ? s_wsum[1][lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int uc = __shfl_up_sync(0xffffffffu, wc, o), ut = __shfl_up_sync(0xffffffffu, wt, o);
+                if (lane >= o) {
+                    wc += uc;
+                    wt += ut;
+                }
+            }
+            s_wsum[0][lane] = wc;  // inclusive totals of warps 0 .. lane
+            s_wsum[1][lane] = wt;
+        }
+        __syncthreads();
+        const int bc = warp > 0 ? s_wsum[0][warp - 1] : 0, bt = warp > 0 ? s_wsum[1][warp - 1] : 0;
+        if (tid < a.n) {
+            s_off[tid] = bc + ic - c;
+            s_toff[tid] = bt + it - tc;
+        }
+        if (tid == a.n - 1) {
+            s_off[a.n] = bc + ic;
+            s_toff[a.n] = bt + it;
+            *a.ntasks = bt + it;
+        }
     }
     __syncthreads();
     for (int e = tid; e <= a.n; e += blockDim.x) {
@@ -654,29 +696,58 @@ __global__ void __launch_bounds__(1024) moe_prefill_plan_kernel(PPlanArgs a)
                 a.tasks[s_toff[e] + j] = TcTask{sl < 0 ? 0 : sl, s_off[e] + j * TC_NT, min(TC_NT, s_cnt[e] - j * TC_NT), 0};
         }
     }
-    // per expert, a warp places its pairs in token order
-    const int warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
-    for (int e = warp; e < a.n; e += nw) {
-        if (s_cnt[e] == 0)
-            continue;
-        int base = s_off[e];
+    // placement, O(m k) by one warp: tokens in rounds of 32 (lane = token),
+    // pick slots in order; lanes with the same expert (one match) take
+    // consecutive places after the expert's running fill. An expert's pairs
+    // end up in (round, slot, lane) order -- deterministic; no result depends
+    // on the order within a group (every pair's column is computed alone).
+    __syncthreads();
+    if (warp == 0) {
         for (int t0 = 0; t0 < a.m; t0 += 32) {
             const int t = t0 + lane;
-            int which = -1;
-            if (t < a.m)
-                for (int i = 0; i < a.k; ++i)
-                    if (a.picks[(size_t)t * a.k + i] == e)
-                        which = i;
-            const unsigned bal = __ballot_sync(0xffffffffu, which >= 0);
-            if (which >= 0) {
-                const int q = base + __popc(bal & ((1u << lane) - 1u));
-                a.pair_tok[q] = t;
-                a.pair_w[q] = a.weights[(size_t)t * a.k + which];
-                a.pick_pair[(size_t)t * a.k + which] = q;
+            for (int i = 0; i < a.k; ++i) {
+                const int pk = t * a.k + i;
+                int e = -1;
+                if (t < a.m) {
+                    e = staged ? (int)s_pick[pk] : __ldg(a.picks + pk);
+                    if (e < 0 || e >= a.n)
+                        e = -1;
+                }
+                const unsigned grp = __match_any_sync(0xffffffffu, e);
+                const int rank = __popc(grp & ((1u << lane) - 1u));
+                const int fill = e >= 0 ? s_fill[e] : 0;
+                __syncwarp();
+                if (e >= 0) {
+                    const int q = s_off[e] + fill + rank;
+                    if (rank == 0)
+                        s_fill[e] = fill + __popc(grp);
+                    if (staged) {
+                        s_qp[q] = (uint16_t)pk;
+                        s_pp[pk] = (uint16_t)q;
+                    } else {
+                        a.pair_tok[q] = t;
+                        a.pair_w[q] = a.weights[pk];
+                        a.pick_pair[pk] = q;
+                    }
+                }
+                __syncwarp();
             }
-            base += __popc(bal);
         }
     }
+    if (!staged)
+        return;
+    // the pair tables from shared memory, in coalesced passes
+    __syncthreads();
+    const int np = s_off[a.n];
+    const FastDiv kd((uint32_t)a.k);
+    for (int q = tid; q < np; q += blockDim.x) {
+        const int pk = s_qp[q];
+        a.pair_tok[q] = (int)kd.div((uint32_t)pk);
+        a.pair_w[q] = a.weights[pk];
+    }
+    for (int p = tid; p < P; p += blockDim.x)
+        if (s_pick[p] != 0xFFFFu)
+            a.pick_pair[p] = s_pp[p];
 }
 
 // ------------------------------------------------------------------ activations
