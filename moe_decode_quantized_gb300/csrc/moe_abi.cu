@@ -1470,8 +1470,15 @@ static int prefill_step(const moe_cfg *cfg, const moe_layer *layer, const moe_ar
     CUDA_OK(mark(8));
     // acc (pairs in ascending expert id, then sd), residual, x_next
     const size_t nf = (size_t)m * dim;
-    moe_prefill_finish_kernel<<<(unsigned)((nf + 255) / 256), 256, 0, s>>>(
-        dw, picks, pick_pair, k, sdp, acc, residual, static_cast<uint16_t *>(x_next), m, dim);
+    const bool v4 = ((reinterpret_cast<uintptr_t>(residual) | reinterpret_cast<uintptr_t>(acc) |
+                      reinterpret_cast<uintptr_t>(dw) | reinterpret_cast<uintptr_t>(sdp)) & 15u) == 0 &&
+                    (reinterpret_cast<uintptr_t>(x_next) & 7u) == 0;  // dim is a multiple of 4
+    if (v4)
+        moe_prefill_finish_kernel<4><<<(unsigned)((nf / 4 + 255) / 256), 256, 0, s>>>(
+            dw, picks, pick_pair, k, sdp, acc, residual, static_cast<uint16_t *>(x_next), m, dim);
+    else
+        moe_prefill_finish_kernel<1><<<(unsigned)((nf + 255) / 256), 256, 0, s>>>(
+            dw, picks, pick_pair, k, sdp, acc, residual, static_cast<uint16_t *>(x_next), m, dim);
     CUDA_OK(cudaGetLastError());
     CUDA_OK(mark(9));
     (void)cnt;

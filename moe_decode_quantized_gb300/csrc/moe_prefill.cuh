@@ -800,36 +800,64 @@ __global__ void moe_prefill_shared_swiglu_kernel(const float *gs, const float *u
 
 // acc[t] = its pairs' weighted down rows in ascending expert id, then sd;
 // residual += acc; x_next = bf16(residual)
+template <int V>
 __global__ void moe_prefill_finish_kernel(const float *dw, const int32_t *picks, const int32_t *pick_pair, int k,
                                           const float *sd, float *acc, float *residual, uint16_t *x_next, int m,
                                           int dim)
 {
-    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    // V consecutive elements of one token a thread (V = 4: 16-byte accesses)
+    const size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * V;
     if (i >= (size_t)m * dim)
         return;
-    const int t = (int)(i / dim), r = (int)(i % dim);
+    const int t = (int)(i / dim), r = (int)(i - (size_t)t * dim);
+    // the token's pairs in ascending expert id (its picks are distinct): a
+    // compare-swap network over MOE_MAX_TOPK slots, absent picks last
     int e[MOE_MAX_TOPK], q[MOE_MAX_TOPK];
-    for (int j = 0; j < k; ++j) {
-        e[j] = __ldg(picks + (size_t)t * k + j);
-        q[j] = min(max(__ldg(pick_pair + (size_t)t * k + j), 0), m * k - 1);
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+        e[j] = j < k ? __ldg(picks + (size_t)t * k + j) : INT_MAX;
+        q[j] = j < k ? min(max(__ldg(pick_pair + (size_t)t * k + j), 0), m * k - 1) : 0;
     }
-    for (int j = 1; j < k; ++j)  // ascending expert id (the picks of a token are distinct)
-        for (int l = j; l > 0 && e[l] < e[l - 1]; --l) {
-            const int te = e[l], tq = q[l];
-            e[l] = e[l - 1];
-            q[l] = q[l - 1];
-            e[l - 1] = te;
-            q[l - 1] = tq;
+#pragma unroll
+    for (int j = 1; j < MOE_MAX_TOPK; ++j)
+#pragma unroll
+        for (int l = j; l > 0; --l)
+            if (e[l] < e[l - 1]) {
+                const int te = e[l], tq = q[l];
+                e[l] = e[l - 1];
+                q[l] = q[l - 1];
+                e[l - 1] = te;
+                q[l - 1] = tq;
+            }
+    float s[V];
+#pragma unroll
+    for (int c = 0; c < V; ++c)
+        s[c] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+        if (j < k) {
+            const float *row = dw + (size_t)q[j] * dim + r;
+            float v[V];
+            if constexpr (V == 4) {
+                const float4 w = *reinterpret_cast<const float4 *>(row);
+                v[0] = w.x, v[1] = w.y, v[2] = w.z, v[3] = w.w;
+            } else {
+                v[0] = row[0];
+            }
+#pragma unroll
+            for (int c = 0; c < V; ++c)
+                s[c] = __fadd_rn(s[c], v[c]);
         }
-    float s = 0.0f;
-    for (int j = 0; j < k; ++j)
-        s = __fadd_rn(s, dw[(size_t)q[j] * dim + r]);
-    if (sd)
-        s = __fadd_rn(s, sd[i]);
-    acc[i] = s;
-    const float res = __fadd_rn(residual[i], s);
-    residual[i] = res;
-    x_next[i] = f32_to_bf16(res);
+    }
+#pragma unroll
+    for (int c = 0; c < V; ++c) {
+        if (sd)
+            s[c] = __fadd_rn(s[c], sd[i + c]);
+        acc[i + c] = s[c];
+        const float res = __fadd_rn(residual[i + c], s[c]);
+        residual[i + c] = res;
+        x_next[i + c] = f32_to_bf16(res);
+    }
 }
 
 }  // namespace moe
