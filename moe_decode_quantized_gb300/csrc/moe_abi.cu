@@ -110,6 +110,8 @@ int dev_info(DevInfo **out)
         CUDA_OK(cudaFuncSetAttribute(moe_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
         CUDA_OK(cudaFuncSetAttribute(moe_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
         CUDA_OK(cudaFuncSetAttribute(moe_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
+        CUDA_OK(cudaFuncSetAttribute(moe_prefill_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     I.smem_optin - 16384));  // beside its static tables
         int rc = tc_attr<0>(I.smem_optin);
         if (rc || (rc = tc_attr<1>(I.smem_optin)) || (rc = tc_attr<2>(I.smem_optin)))
             return rc;
@@ -643,14 +645,21 @@ TcArgs tc_args(int M, int N, int K, float *out, int ldo, uint32_t *status)
 
 // bf16 GEMM out[n * ldo + r] = sum_k A[r, k] B[n, k] (A [M, K], B [N, K] row-major bf16)
 int gemm_bf16(const void *A, const void *B, float *out, int M, int N, int K, int ldo, uint32_t *status,
-              cudaStream_t s, int smem_optin)
+              cudaStream_t s, int smem_optin, int sms)
 {
     CUtensorMap am, bm;
     int rc = map_rows16(&am, true, A, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, TC_M);
     if (rc || (rc = map_rows16(&bm, true, B, (uint64_t)K, (uint64_t)N, (uint64_t)K * 2, TC_BROWS)))
         return rc;
-    const TcArgs a = tc_args(M, N, K, out, ldo, status);
-    return launch_tc<0>(am, bm, bm, a, dim3((N + TC_NT - 1) / TC_NT, (M + TC_M - 1) / TC_M), s, smem_optin);
+    TcArgs a = tc_args(M, N, K, out, ldo, status);
+    // narrower column tiles while the grid still fits one wave: a CTA's time
+    // hardly depends on its width, so a small grid (the router's 3 row
+    // tiles) spreads over more SMs; a second wave would cost a CTA's time
+    const int mt = (M + TC_M - 1) / TC_M;
+    a.nt = TC_NT;
+    while (a.nt > 16 && (long long)mt * ((N + a.nt / 2 - 1) / (a.nt / 2)) <= sms)
+        a.nt /= 2;
+    return launch_tc<0>(am, bm, bm, a, dim3((N + a.nt - 1) / a.nt, mt), s, smem_optin);
 }
 
 // A multi-layer step: the captured graph, and what its eager form needs (the
@@ -1317,7 +1326,7 @@ int moe_gemm_bf16(const void *a, const void *b, float *d, int M, int N, int K, i
     int rc = dev_info(&I);
     if (rc)
         return rc;
-    return gemm_bf16(a, b, d, M, N, K, ldd, nullptr, (cudaStream_t)stream, I->smem_optin);
+    return gemm_bf16(a, b, d, M, N, K, ldd, nullptr, (cudaStream_t)stream, I->smem_optin, I->sms);
 }
 
 int moe_prefill_workspace_bytes(const moe_cfg *cfg, int m, size_t *bytes)
@@ -1377,7 +1386,7 @@ static int prefill_step(const moe_cfg *cfg, const moe_layer *layer, const moe_ar
     CUDA_OK(cudaMemsetAsync(status, 0, 4, s));
     CUDA_OK(mark(0));
     // router logits [m, n] on tensor cores, the scores, each token's picks
-    if ((rc = gemm_bf16(layer->router_w, x, logits, n, m, dim, n, status, s, I->smem_optin)))
+    if ((rc = gemm_bf16(layer->router_w, x, logits, n, m, dim, n, status, s, I->smem_optin, I->sms)))
         return rc;
     CUDA_OK(mark(1));
     ScoreArgs sa{logits, scores, cfg->gate_temp, m * n};
@@ -1391,7 +1400,10 @@ static int prefill_step(const moe_cfg *cfg, const moe_layer *layer, const moe_ar
     // pairs grouped by expert, the column tasks of the routed GEMMs
     PPlanArgs pa{picks, weights, layer->slot_row, m, n, k, cnt, off, pair_tok, pair_w, pick_pair, tasks, ntasks,
                  status};
-    moe_prefill_plan_kernel<<<1, 1024, 0, s>>>(pa);
+    const size_t plan_smem = plan_smem_bytes(n, m * k);
+    if (plan_smem > (size_t)I->smem_optin - 16384)
+        return fail(MOE_EUNSUPPORTED, "prefill plan: %zu bytes of shared memory needed", plan_smem);
+    moe_prefill_plan_kernel<<<1, 1024, plan_smem, s>>>(pa);
     CUDA_OK(cudaGetLastError());
     CUDA_OK(mark(2));
     // q8_1 of x, dequantised to fp16, gathered into pair order
@@ -1456,14 +1468,14 @@ static int prefill_step(const moe_cfg *cfg, const moe_layer *layer, const moe_ar
     // the bf16 shared expert as dense GEMMs
     const float *sdp = nullptr;
     if (layer->sh_w1) {
-        if ((rc = gemm_bf16(layer->sh_w1, x, gs, inter, m, dim, inter, status, s, I->smem_optin)) ||
-            (rc = gemm_bf16(layer->sh_w3, x, us, inter, m, dim, inter, status, s, I->smem_optin)))
+        if ((rc = gemm_bf16(layer->sh_w1, x, gs, inter, m, dim, inter, status, s, I->smem_optin, I->sms)) ||
+            (rc = gemm_bf16(layer->sh_w3, x, us, inter, m, dim, inter, status, s, I->smem_optin, I->sms)))
             return rc;
         const size_t ns = (size_t)m * inter;
         moe_prefill_shared_swiglu_kernel<<<(unsigned)((ns + 255) / 256), 256, 0, s>>>(gs, us, ns, cfg->swiglu_limit,
                                                                                        hs);
         CUDA_OK(cudaGetLastError());
-        if ((rc = gemm_bf16(layer->sh_w2, hs, sd, dim, m, inter, dim, status, s, I->smem_optin)))
+        if ((rc = gemm_bf16(layer->sh_w2, hs, sd, dim, m, inter, dim, status, s, I->smem_optin, I->sms)))
             return rc;
         sdp = sd;
     }

@@ -71,6 +71,7 @@ struct TcArgs {
     uint32_t raw_bytes;     // AK > 0: bytes of one raw stage (128 rows x raw_row)
     int rk;                 // AK > 0: K per raw stage
     int ksplit;             // K split over this many accumulators (1, 2 or 4), added in f32 at the end
+    int nt;                 // AK = 0: columns of a tile (a multiple of 16, <= TC_NT)
     uint32_t b_buf;         // bytes of the B ring (a multiple of 2048)
     uint32_t *status;
     unsigned long long wait_ns;
@@ -299,8 +300,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // the tile: rows m0 .. m0 + 127 of the weights, columns c0 .. c0 + ncols - 1
     int m0 = blockIdx.y * TC_M, c0, ncols, slot = 0;
     if constexpr (AK == 0) {
-        c0 = blockIdx.x * TC_NT;
-        ncols = min(TC_NT, a.N - c0);
+        c0 = blockIdx.x * a.nt;
+        ncols = min(a.nt, a.N - c0);
     } else {
         if ((int)blockIdx.x >= __ldg(a.ntasks))
             return;
@@ -617,28 +618,50 @@ struct PPlanArgs {
     uint32_t *status;
 };
 
-#define PLAN_SMEM_PICKS 5120  // m * k up to this: the plan is built in shared memory (16-bit indices)
+#define PLAN_SMEM_PICKS 5120  // m * k up to this: the pair tables are built in shared memory (16-bit)
+#define PLAN_WARPS 32         // warps of the plan kernel (1024 threads)
+
+// dynamic shared memory of the plan kernel: per warp and expert a count (then
+// a base), and for m * k <= PLAN_SMEM_PICKS the picks and both pair tables
+__host__ __device__ inline size_t plan_smem_bytes(int n, int P)
+{
+    return (size_t)PLAN_WARPS * n * 4 + (P <= PLAN_SMEM_PICKS ? 3 * align_up((size_t)P * 2, 16) : 0);
+}
 
 __global__ void __launch_bounds__(1024) moe_prefill_plan_kernel(PPlanArgs a)
 {
     __shared__ int s_cnt[MOE_MAX_ROUTED], s_off[MOE_MAX_ROUTED + 1], s_toff[MOE_MAX_ROUTED + 1];
-    __shared__ int s_wsum[2][32], s_fill[MOE_MAX_ROUTED];
-    // staged: the picks, each pair's pick (t k + i) and each pick's pair
-    __shared__ uint16_t s_pick[PLAN_SMEM_PICKS], s_qp[PLAN_SMEM_PICKS], s_pp[PLAN_SMEM_PICKS];
+    __shared__ int s_wsum[2][32];
+    extern __shared__ __align__(16) uint8_t plan_dyn[];
     const int tid = threadIdx.x, P = a.m * a.k, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
     const bool staged = P <= PLAN_SMEM_PICKS;
-    for (int e = tid; e < a.n; e += blockDim.x) {
+    int *s_wc = reinterpret_cast<int *>(plan_dyn);  // [PLAN_WARPS][n]
+    uint16_t *s_pick = reinterpret_cast<uint16_t *>(plan_dyn + (size_t)PLAN_WARPS * a.n * 4);
+    uint16_t *s_qp = s_pick + align_up((size_t)P * 2, 16) / 2;  // pair q -> its pick t k + i
+    uint16_t *s_pp = s_qp + align_up((size_t)P * 2, 16) / 2;    // pick -> its pair
+    auto pick_at = [&](int p) {  // expert of pick p, -1 if out of range
+        const int e = staged ? (s_pick[p] == 0xFFFFu ? -1 : (int)s_pick[p]) : __ldg(a.picks + p);
+        return e >= 0 && e < a.n ? e : -1;
+    };
+    for (int e = tid; e < a.n; e += blockDim.x)
         s_cnt[e] = 0;
-        s_fill[e] = 0;
-    }
+    for (int i = tid; i < PLAN_WARPS * a.n; i += blockDim.x)
+        s_wc[i] = 0;
     __syncthreads();
-    for (int p = tid; p < P; p += blockDim.x) {
-        const int e = a.picks[p];
-        const bool ok = e >= 0 && e < a.n;
+    // each warp owns the contiguous picks [R warp, R warp + R): its counts per
+    // expert, and the totals
+    const int R = ((P + PLAN_WARPS - 1) / PLAN_WARPS + 31) / 32 * 32;
+    const int p_lo = min(P, R * warp), p_hi = min(P, R * warp + R);
+    for (int p = p_lo + lane; p < p_hi; p += 32) {
+        int e = __ldg(a.picks + p);
+        if (e < 0 || e >= a.n)
+            e = -1;
         if (staged)
-            s_pick[p] = ok ? (uint16_t)e : (uint16_t)0xFFFFu;  // n <= 1024
-        if (ok)
+            s_pick[p] = e < 0 ? (uint16_t)0xFFFFu : (uint16_t)e;  // n <= 1024
+        if (e >= 0) {
+            atomicAdd(&s_wc[warp * a.n + e], 1);
             atomicAdd(&s_cnt[e], 1);
+        }
     }
     __syncthreads();
     // offsets: an exclusive scan over the experts of their pair counts and of
@@ -675,8 +698,17 @@ __global__ void __launch_bounds__(1024) moe_prefill_plan_kernel(PPlanArgs a)
         __syncthreads();
         const int bc = warp > 0 ? s_wsum[0][warp - 1] : 0, bt = warp > 0 ? s_wsum[1][warp - 1] : 0;
         if (tid < a.n) {
-            s_off[tid] = bc + ic - c;
+            const int off = bc + ic - c;
+            s_off[tid] = off;
             s_toff[tid] = bt + it - tc;
+            // each warp's first place in the expert's group: its offset plus
+            // the counts of the warps before it (whose picks come first)
+            int run = off;
+            for (int w = 0; w < PLAN_WARPS; ++w) {
+                const int cw = s_wc[w * a.n + tid];
+                s_wc[w * a.n + tid] = run;
+                run += cw;
+            }
         }
         if (tid == a.n - 1) {
             s_off[a.n] = bc + ic;
@@ -696,43 +728,31 @@ __global__ void __launch_bounds__(1024) moe_prefill_plan_kernel(PPlanArgs a)
                 a.tasks[s_toff[e] + j] = TcTask{sl < 0 ? 0 : sl, s_off[e] + j * TC_NT, min(TC_NT, s_cnt[e] - j * TC_NT), 0};
         }
     }
-    // placement, O(m k) by one warp: tokens in rounds of 32 (lane = token),
-    // pick slots in order; lanes with the same expert (one match) take
-    // consecutive places after the expert's running fill. An expert's pairs
-    // end up in (round, slot, lane) order -- deterministic; no result depends
-    // on the order within a group (every pair's column is computed alone).
-    __syncthreads();
-    if (warp == 0) {
-        for (int t0 = 0; t0 < a.m; t0 += 32) {
-            const int t = t0 + lane;
-            for (int i = 0; i < a.k; ++i) {
-                const int pk = t * a.k + i;
-                int e = -1;
-                if (t < a.m) {
-                    e = staged ? (int)s_pick[pk] : __ldg(a.picks + pk);
-                    if (e < 0 || e >= a.n)
-                        e = -1;
-                }
-                const unsigned grp = __match_any_sync(0xffffffffu, e);
-                const int rank = __popc(grp & ((1u << lane) - 1u));
-                const int fill = e >= 0 ? s_fill[e] : 0;
-                __syncwarp();
-                if (e >= 0) {
-                    const int q = s_off[e] + fill + rank;
-                    if (rank == 0)
-                        s_fill[e] = fill + __popc(grp);
-                    if (staged) {
-                        s_qp[q] = (uint16_t)pk;
-                        s_pp[pk] = (uint16_t)q;
-                    } else {
-                        a.pair_tok[q] = t;
-                        a.pair_w[q] = a.weights[pk];
-                        a.pick_pair[pk] = q;
-                    }
-                }
-                __syncwarp();
+    // placement: each warp its picks in order, 32 at a time; lanes with the
+    // same expert (one match) take consecutive places after the warp's next
+    // place in that group. Picks are token-major, a token picks an expert at
+    // most once, so each group is in ascending token order.
+    for (int p0 = p_lo; p0 < p_hi; p0 += 32) {
+        const int p = p0 + lane;
+        const int e = p < p_hi ? pick_at(p) : -1;
+        const unsigned grp = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(grp & ((1u << lane) - 1u));
+        const int base = e >= 0 ? s_wc[warp * a.n + e] : 0;
+        __syncwarp();
+        if (e >= 0) {
+            const int q = base + rank;
+            if (rank == 0)
+                s_wc[warp * a.n + e] = base + __popc(grp);
+            if (staged) {
+                s_qp[q] = (uint16_t)p;
+                s_pp[p] = (uint16_t)q;
+            } else {
+                a.pair_tok[q] = p / a.k;
+                a.pair_w[q] = a.weights[p];
+                a.pick_pair[p] = q;
             }
         }
+        __syncwarp();
     }
     if (!staged)
         return;
