@@ -1409,10 +1409,9 @@ static int prefill_step(const moe_cfg *cfg, const moe_layer *layer, const moe_ar
     // q8_1 of x, dequantised to fp16, gathered into pair order
     const int nbx = m * dim / 32;
     moe_prefill_xhat_kernel<<<(nbx + 7) / 8, 256, 0, s>>>(static_cast<const uint16_t *>(x), nbx, xhat, xhat_lo);
-    const size_t gthreads = (size_t)P * (dim / 8);
-    moe_prefill_gather_kernel<<<(unsigned)((gthreads + 255) / 256), 256, 0, s>>>(
+    moe_prefill_gather_kernel<<<(unsigned)P, 128, 0, s>>>(
         reinterpret_cast<const uint4 *>(xhat), pair_tok, P, dim / 8, reinterpret_cast<uint4 *>(xg));
-    moe_prefill_gather_kernel<<<(unsigned)((gthreads + 255) / 256), 256, 0, s>>>(
+    moe_prefill_gather_kernel<<<(unsigned)P, 128, 0, s>>>(
         reinterpret_cast<const uint4 *>(xhat_lo), pair_tok, P, dim / 8, reinterpret_cast<uint4 *>(xg_lo));
     CUDA_OK(cudaGetLastError());
     CUDA_OK(mark(3));
@@ -1448,7 +1447,8 @@ static int prefill_step(const moe_cfg *cfg, const moe_layer *layer, const moe_ar
     CUDA_OK(mark(5));
     // h = SwiGLU(g, u), its q8_1, dequantised to fp16
     const int nbh = P * inter / 32;
-    moe_prefill_swiglu_kernel<<<(nbh + 7) / 8, 256, 0, s>>>(g, u, nbh, cfg->swiglu_limit, hh);
+    moe_prefill_swiglu_kernel<<<(unsigned)(((size_t)nbh * 4 + 255) / 256), 256, 0, s>>>(g, u, nbh, cfg->swiglu_limit,
+                                                                                     hh);
     CUDA_OK(cudaGetLastError());
     CUDA_OK(mark(6));
     // routed down: Q3_K rows (8 super-blocks a raw stage), times each pair's weight

@@ -790,23 +790,52 @@ __global__ void moe_prefill_xhat_kernel(const uint16_t *x, int nblk, __half *xha
 
 __global__ void moe_prefill_gather_kernel(const uint4 *src, const int32_t *pair_tok, int P, int row16, uint4 *dst)
 {
-    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= (size_t)P * row16)
+    // one CTA a pair: its token's row of row16 16-byte chunks
+    const int p = blockIdx.x;
+    if (p >= P)
         return;
-    const int p = (int)(i / row16), c = (int)(i % row16);
-    dst[i] = src[(size_t)pair_tok[p] * row16 + c];
+    const uint4 *s = src + (size_t)pair_tok[p] * row16;
+    uint4 *d = dst + (size_t)p * row16;
+    for (int c = threadIdx.x; c < row16; c += blockDim.x)
+        d[c] = s[c];
 }
 
 // h = SwiGLU(g, u) per pair, its q8_1 (f32 decisions, f16 scale), and the
 // dequantised fp16 h_hat for the down GEMM. One warp per 32-block.
 __global__ void moe_prefill_swiglu_kernel(const float *g, const float *u, int nblk, float limit, __half *hhat)
 {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    if (warp >= nblk)
+    // four lanes a 32-block, eight consecutive values a lane (the block's
+    // four lanes are all in range or all out, so the group's shuffles are safe)
+    const size_t it = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (it >= (size_t)nblk * 4)
         return;
-    const size_t i = (size_t)warp * 32 + lane;
-    const Q8Block b = q8_quant_warp(swiglu_f32(g[i], u[i], limit));
-    hhat[i] = __float2half_rn(__fmul_rn(b.d8, (float)b.q));
+    const unsigned gmask = 0xFu << (threadIdx.x & 28);
+    const size_t e0 = it * 8;
+    const float4 g0 = *reinterpret_cast<const float4 *>(g + e0), g1 = *reinterpret_cast<const float4 *>(g + e0 + 4);
+    const float4 u0 = *reinterpret_cast<const float4 *>(u + e0), u1 = *reinterpret_cast<const float4 *>(u + e0 + 4);
+    const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    float h[8], amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        h[j] = swiglu_f32(gv[j], uv[j], limit);
+        amax = fmaxf(amax, fabsf(h[j]));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 2));
+    // q8_1 of the block as q8_quant_warp takes it: d = amax / 127, the codes,
+    // d8 = f16(d); the dequantised values d8 * q as fp16
+    const float d = __fdiv_rn(amax, 127.0f), id = __frcp_rn(d), d8 = __half2float(__float2half_rn(d));
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int q0 = amax == 0.0f ? 0 : q8_code(h[2 * j], d, id);
+        const int q1 = amax == 0.0f ? 0 : q8_code(h[2 * j + 1], d, id);
+        const __half2 hh = __halves2half2(__float2half_rn(__fmul_rn(d8, (float)q0)),
+                                          __float2half_rn(__fmul_rn(d8, (float)q1)));
+        o[j] = *reinterpret_cast<const uint32_t *>(&hh);
+    }
+    *reinterpret_cast<uint4 *>(hhat + e0) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // the bf16 shared expert's hs = bf16(SwiGLU(gs, us))
