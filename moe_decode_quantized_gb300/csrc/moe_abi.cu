@@ -1407,12 +1407,17 @@ static int prefill_step(const moe_cfg *cfg, const moe_layer *layer, const moe_ar
     CUDA_OK(cudaGetLastError());
     CUDA_OK(mark(2));
     // q8_1 of x, dequantised to fp16, gathered into pair order
-    const int nbx = m * dim / 32;
-    moe_prefill_xhat_kernel<<<(nbx + 7) / 8, 256, 0, s>>>(static_cast<const uint16_t *>(x), nbx, xhat, xhat_lo);
-    moe_prefill_gather_kernel<<<(unsigned)P, 128, 0, s>>>(
-        reinterpret_cast<const uint4 *>(xhat), pair_tok, P, dim / 8, reinterpret_cast<uint4 *>(xg));
-    moe_prefill_gather_kernel<<<(unsigned)P, 128, 0, s>>>(
-        reinterpret_cast<const uint4 *>(xhat_lo), pair_tok, P, dim / 8, reinterpret_cast<uint4 *>(xg_lo));
+    if ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) {  // 16-byte reads of x: straight into pair order
+        moe_prefill_xhat_gather_kernel<<<(unsigned)P, 256, 0, s>>>(static_cast<const uint16_t *>(x), pair_tok, P, dim,
+                                                                   xg, xg_lo);
+    } else {
+        const int nbx = m * dim / 32;
+        moe_prefill_xhat_kernel<<<(nbx + 7) / 8, 256, 0, s>>>(static_cast<const uint16_t *>(x), nbx, xhat, xhat_lo);
+        moe_prefill_gather_kernel<<<(unsigned)P, 128, 0, s>>>(
+            reinterpret_cast<const uint4 *>(xhat), pair_tok, P, dim / 8, reinterpret_cast<uint4 *>(xg));
+        moe_prefill_gather_kernel<<<(unsigned)P, 128, 0, s>>>(
+            reinterpret_cast<const uint4 *>(xhat_lo), pair_tok, P, dim / 8, reinterpret_cast<uint4 *>(xg_lo));
+    }
     CUDA_OK(cudaGetLastError());
     CUDA_OK(mark(3));
     // routed gate and up: Q2_K rows (4 super-blocks a raw stage) x the groups' rows

@@ -788,6 +788,50 @@ __global__ void moe_prefill_xhat_kernel(const uint16_t *x, int nblk, __half *xha
     xhat_lo[(size_t)warp * 32 + lane] = __float2half_rn(__fsub_rn(xh, __half2float(hi)));
 }
 
+// q8_1 of x, dequantised to fp16 hi + lo (as moe_prefill_xhat_kernel), written
+// straight into pair order: CTA p takes its token's row, eight values a lane,
+// four lanes a 32-block (a group's lanes run the same iterations)
+__global__ void moe_prefill_xhat_gather_kernel(const uint16_t *x, const int32_t *pair_tok, int P, int dim, __half *xg,
+                                               __half *xg_lo)
+{
+    const int p = blockIdx.x;
+    if (p >= P)
+        return;
+    const uint16_t *xr = x + (size_t)pair_tok[p] * dim;
+    const unsigned gmask = 0xFu << (threadIdx.x & 28);
+    for (int it = threadIdx.x; it < dim / 8; it += blockDim.x) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(xr + (size_t)it * 8);
+        const float v[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                            bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            amax = fmaxf(amax, fabsf(v[j]));
+        amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 2));
+        const float d = __fdiv_rn(amax, 127.0f), id = __frcp_rn(d), d8 = __half2float(__float2half_rn(d));
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float xh[2];
+            __half h[2], l[2];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int q = amax == 0.0f ? 0 : q8_code(v[2 * j + c], d, id);
+                xh[c] = __fmul_rn(d8, (float)q);
+                h[c] = __float2half_rn(xh[c]);
+                l[c] = __float2half_rn(__fsub_rn(xh[c], __half2float(h[c])));
+            }
+            const __half2 hh = __halves2half2(h[0], h[1]), ll = __halves2half2(l[0], l[1]);
+            hi[j] = *reinterpret_cast<const uint32_t *>(&hh);
+            lo[j] = *reinterpret_cast<const uint32_t *>(&ll);
+        }
+        const size_t o = (size_t)p * dim + (size_t)it * 8;
+        *reinterpret_cast<uint4 *>(xg + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(xg_lo + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+}
+
 __global__ void moe_prefill_gather_kernel(const uint4 *src, const int32_t *pair_tok, int P, int row16, uint4 *dst)
 {
     // one CTA a pair: its token's row of row16 16-byte chunks
