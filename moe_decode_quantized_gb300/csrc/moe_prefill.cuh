@@ -30,10 +30,11 @@
 // M = 128 MMA takes as long for 16 columns as for 128. down (AK = 2) takes single
 // fp16 parts (about 2^-12 relative per operand): its output is only summed.
 // The tensor cores' f32 accumulation is coarser than a sequential f32 sum
-// (about 2e-5 relative over K = 4096), so K is split over up to four
-// accumulators in TMEM (4 x 128 columns) whose results the epilogue adds in
-// f32, in order; over K = 4096 that keeps the router logits within 1e-5.
-// One warp issues the MMAs; the eight worker warps (two a scheduler: the
+// (about 2e-5 relative over K = 4096), so the K-chunks are dealt round-robin
+// over up to four accumulators in TMEM (4 x 128 columns), each taking its
+// chunks in order, whose results the epilogue adds in f32, in order; over
+// K = 4096 that keeps the router logits within 1e-5.
+// Two warps issue the MMAs (alternate K-chunks); the eight worker warps (two a scheduler: the
 // dequantisation is a chain of dependent integer and float steps) are also
 // the epilogue (TMEM -> registers -> global).
 #pragma once
@@ -46,7 +47,7 @@ namespace moe {
 #define TC_NT 128       // columns (tokens) of a tile, at most
 #define TC_KC 64        // K per stage (one 128-byte swizzle atom of 16-bit elements)
 #define TC_WORKERS 8    // worker warps: two threads a tile row (one 32-weight group each)
-#define TC_THREADS ((TC_WORKERS + 3) * 32)  // warps 0-7 workers / epilogue, 8 and 9 producers, 10 MMA
+#define TC_THREADS ((TC_WORKERS + 4) * 32)  // warps 0-7 workers / epilogue, 8 and 9 producers, 10 and 11 MMA
 #define TC_BROWS 16     // rows of a B TMA box
 #define TC_TMEM_COLS 512  // TMEM columns a CTA holds: up to 4 accumulators of TC_NT columns (dense),
                           // or 2 accumulators and the A stages from column 256 (K-quant)
@@ -330,7 +331,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // seen chunk j - D done (it waited for it, or for a later one, before
     // filling the stage now being refilled) and no MMA of chunk j + D can run
     // before the waiter's own next stage, so parity j / D is unambiguous.
-    const int D = max(S, SB);  // S <= TC_SB_MAX
+    // Even, so that chunks j and j + D are issued by the same MMA thread and
+    // their commits reach barrier j % D in order (S <= 8, SB <= TC_SB_MAX).
+    const int D = (max(S, SB) + 1) & ~1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s)
@@ -343,7 +346,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mbar_init(&raw_full[r], 1);
             mbar_init(&raw_empty[r], TC_WORKERS);
         }
-        mbar_init(done, 1);
+        mbar_init(done, 2);  // one commit from each MMA thread
         fence_barrier_init();
     }
     if (warp == 0)
@@ -406,19 +409,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
             }
         }
-    } else if (warp == TC_WORKERS + 2) {
-        // ---------------- MMA issuer
+    } else if (warp == TC_WORKERS + 2 || warp == TC_WORKERS + 3) {
+        // ---------------- MMA issuers: two threads (one a warp), thread h the
+        // K-chunks h, h + 2, ..., so that one's waits and commits overlap the
+        // other's MMAs (an MMA costs about the same for any N <= 128, and
+        // the issuing thread's per-chunk waits, commit and stepping would
+        // otherwise leave the tensor pipe idle); chunk kc accumulates into
+        // accumulator kc % ksplit, so each accumulator takes its chunks in
+        // order from one thread (ksplit 1: thread 0 alone)
         if (lane == 0) {
-            const int kper = KC / a.ksplit;  // K-chunks an accumulator takes
-            RingPos pa, pb, pd;               // A stage, B stage, completion barrier
-            int acc_i = 0, kin = 0;           // accumulator, chunk within it
-            for (int kc = 0; kc < KC; ++kc) {
+            const int h = warp - (TC_WORKERS + 2), step = a.ksplit > 1 ? 2 : 1;
+            RingPos pa, pb, pd;  // A stage, B stage, completion barrier of chunk kc
+            if (h == 1) {
+                pa.next(S);
+                pb.next(SB);
+                pd.next(D);
+            }
+            for (int kc = h; kc < KC && (h == 0 || step == 2); kc += step) {
                 const int s = pa.slot, t = pb.slot;
                 tc_wait(&full_a[s], pa.phase, a, dead);
                 tc_wait(&full_b[t], pb.phase, a, dead);
                 tc_fence_after();
-                const uint32_t acc = tmem + (uint32_t)acc_i * TC_NT;
-                const bool first = kin == 0;
+                const uint32_t acc = tmem + (uint32_t)(kc & (a.ksplit - 1)) * TC_NT;
+                const bool first = kc < a.ksplit;
                 const uint64_t bd = sw128_desc(sb + (size_t)t * bstage);
                 if constexpr (AK == 0) {
                     const uint64_t ad = sw128_desc(sa + (size_t)s * 16384);
@@ -446,12 +459,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                 }
                 mma_commit(&mdone[pd.slot]);  // frees A stage s and B stage t
-                pa.next(S);
-                pb.next(SB);
-                pd.next(D);
-                if (++kin == kper) {
-                    kin = 0;
-                    ++acc_i;
+                for (int i = 0; i < step; ++i) {
+                    pa.next(S);
+                    pb.next(SB);
+                    pd.next(D);
                 }
             }
             mma_commit(done);
