@@ -212,12 +212,19 @@ __device__ __forceinline__ void dq_q3k_group(const uint32_t (&w)[28], int gi, ui
     for (int wi = 0; wi < 8; ++wi) {
         const uint32_t v = ((w[8 + 8 * half + wi] >> (2 * g)) & 0x03030303u) | (((w[wi] >> hsh) & 0x01010101u) << 2);
         const int u = wi >> 2;
-        float f[4];
-#pragma unroll
-        for (int b = 0; b < 4; ++b)  // 2^23 + v exactly, then v - 4
-            f[b] = __uint_as_float(__byte_perm(v, 0x4B000000u, b | 0x7440)) - 8388612.0f;
-        const __half2 h01 = __floats2half2_rn(f[0] * ds[u], f[1] * ds[u]);
-        const __half2 h23 = __floats2half2_rn(f[2] * ds[u], f[3] * ds[u]);
+        // 2^23 + v exactly, then v - 4 and its product with ds, two lanes an
+        // instruction (packed f32, each lane rounded to nearest as alone)
+        const float2 m4 = make_float2(-8388612.0f, -8388612.0f), d2 = make_float2(ds[u], ds[u]);
+        const float2 f01 = __fmul2_rn(__fadd2_rn(make_float2(__uint_as_float(__byte_perm(v, 0x4B000000u, 0x7440)),
+                                                             __uint_as_float(__byte_perm(v, 0x4B000000u, 0x7441))),
+                                                 m4),
+                                      d2);
+        const float2 f23 = __fmul2_rn(__fadd2_rn(make_float2(__uint_as_float(__byte_perm(v, 0x4B000000u, 0x7442)),
+                                                             __uint_as_float(__byte_perm(v, 0x4B000000u, 0x7443))),
+                                                 m4),
+                                      d2);
+        const __half2 h01 = __float22half2_rn(f01);
+        const __half2 h23 = __float22half2_rn(f23);
         o[2 * wi] = *reinterpret_cast<const uint32_t *>(&h01);
         o[2 * wi + 1] = *reinterpret_cast<const uint32_t *>(&h23);
     }
