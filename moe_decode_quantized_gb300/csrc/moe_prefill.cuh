@@ -618,10 +618,12 @@ __global__ void __launch_bounds__(256) moe_prefill_topk_kernel(PTopArgs a)
 // ------------------------------------------------------------------ grouping by expert
 
 // One CTA of 1024 threads. The pairs (token, pick) grouped by expert in
-// ascending id, tokens ascending within an expert (deterministic): count,
-// exclusive scan, then per expert a warp walks the tokens in order and
-// places its pairs with ballots. Also the column tasks of the routed GEMMs
-// (ceil(count / TC_NT) per expert) and each pick's pair index.
+// ascending id, tokens ascending within an expert (deterministic): each
+// warp counts its contiguous range of picks per expert, an exclusive scan
+// gives the expert offsets and each warp's first place in every group, and
+// each warp places its picks in order (match_any ranks). Also the column
+// tasks of the routed GEMMs (ceil(count / TC_NT) per expert) and each pick's
+// pair index.
 struct PPlanArgs {
     const int32_t *picks;
     const float *weights;
