@@ -380,8 +380,9 @@ int moe_gemm_bf16(const void *a_dev, const void *b_dev, float *d_dev, int M, int
  * the Q2_K / Q3_K blocks must be multiples of 16 bytes for TMA), the shared
  * expert bf16 or absent, 0 <= m <= 65536 (cfg->max_tokens is not used).
  * arena_slots: slots in the arena (the tensor maps cover that many). x_dev
- * bf16 [m, dim]; residual_dev f32 [m, dim] (in/out); x_next_dev bf16
- * [m, dim]; picks_dev i32 [m, topk], weights_dev f32 [m, topk] (pick
+ * bf16 [m, dim], 16-byte aligned (a TMA operand; otherwise MOE_EINVAL before
+ * any launch); residual_dev f32 [m, dim] (in/out); x_next_dev bf16 [m, dim]
+ * (16- and 8-byte alignment of these take the wider accesses); picks_dev i32 [m, topk], weights_dev f32 [m, topk] (pick
  * order); ws_dev: moe_prefill_workspace_bytes bytes (no initialisation
  * needed). Errors: MOE_EUNSUPPORTED for the shapes above; a picked expert
  * whose slot is -1 uses slot 0 and sets MOE_WS_PLAN (moe_prefill_status). */

@@ -552,8 +552,8 @@ int map_arena(CUtensorMap *m, const void *base, uint64_t row_bytes, uint64_t row
 // ------------------------------------------------------------------ prefill
 
 struct PfLayout {
-    size_t logits, scores, flags, cnt, off, pair_tok, pair_w, pick_pair, tasks, ntasks, status, xhat, xhat_lo, xg,
-        xg_lo, g, u, hh, dw, gs, us, hs, sd, acc, total;
+    size_t logits, scores, flags, cnt, off, pair_tok, pair_w, pick_pair, tasks, ntasks, status, xg, xg_lo, g, u, hh,
+        dw, gs, us, hs, sd, acc, total;
     int P, max_tasks;
 };
 
@@ -576,8 +576,6 @@ PfLayout pf_layout(const moe_cfg &c, int m)
     L.tasks = take(sizeof(TcTask) * (size_t)L.max_tasks);
     L.ntasks = take(4);
     L.status = take(4);
-    L.xhat = take(2 * M * c.dim);
-    L.xhat_lo = take(2 * M * c.dim);
     L.xg = take(2 * P * c.dim);
     L.xg_lo = take(2 * P * c.dim);
     L.g = take(4 * P * c.inter);
@@ -1373,8 +1371,7 @@ static int prefill_step(const moe_cfg *cfg, const moe_layer *layer, const moe_ar
     TcTask *tasks = reinterpret_cast<TcTask *>(w + L.tasks);
     int32_t *ntasks = reinterpret_cast<int32_t *>(w + L.ntasks);
     uint32_t *status = reinterpret_cast<uint32_t *>(w + L.status);
-    __half *xhat = reinterpret_cast<__half *>(w + L.xhat), *xg = reinterpret_cast<__half *>(w + L.xg);
-    __half *xhat_lo = reinterpret_cast<__half *>(w + L.xhat_lo), *xg_lo = reinterpret_cast<__half *>(w + L.xg_lo);
+    __half *xg = reinterpret_cast<__half *>(w + L.xg), *xg_lo = reinterpret_cast<__half *>(w + L.xg_lo);
     __half *hh = reinterpret_cast<__half *>(w + L.hh);
     float *g = reinterpret_cast<float *>(w + L.g), *u = reinterpret_cast<float *>(w + L.u);
     float *dw = reinterpret_cast<float *>(w + L.dw), *gs = reinterpret_cast<float *>(w + L.gs);
@@ -1407,17 +1404,9 @@ static int prefill_step(const moe_cfg *cfg, const moe_layer *layer, const moe_ar
     CUDA_OK(cudaGetLastError());
     CUDA_OK(mark(2));
     // q8_1 of x, dequantised to fp16, gathered into pair order
-    if ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) {  // 16-byte reads of x: straight into pair order
-        moe_prefill_xhat_gather_kernel<<<(unsigned)P, 256, 0, s>>>(static_cast<const uint16_t *>(x), pair_tok, P, dim,
-                                                                   xg, xg_lo);
-    } else {
-        const int nbx = m * dim / 32;
-        moe_prefill_xhat_kernel<<<(nbx + 7) / 8, 256, 0, s>>>(static_cast<const uint16_t *>(x), nbx, xhat, xhat_lo);
-        moe_prefill_gather_kernel<<<(unsigned)P, 128, 0, s>>>(
-            reinterpret_cast<const uint4 *>(xhat), pair_tok, P, dim / 8, reinterpret_cast<uint4 *>(xg));
-        moe_prefill_gather_kernel<<<(unsigned)P, 128, 0, s>>>(
-            reinterpret_cast<const uint4 *>(xhat_lo), pair_tok, P, dim / 8, reinterpret_cast<uint4 *>(xg_lo));
-    }
+    // (x is 16-byte aligned: checked above, the router GEMM's tensor map needs it)
+    moe_prefill_xhat_gather_kernel<<<(unsigned)P, 256, 0, s>>>(static_cast<const uint16_t *>(x), pair_tok, P, dim, xg,
+                                                               xg_lo);
     CUDA_OK(cudaGetLastError());
     CUDA_OK(mark(3));
     // routed gate and up: Q2_K rows (4 super-blocks a raw stage) x the groups' rows

@@ -792,25 +792,10 @@ __global__ void __launch_bounds__(1024) moe_prefill_plan_kernel(PPlanArgs a)
 
 // ------------------------------------------------------------------ activations
 
-// x_hat = the dequantised q8_1 of each token's x (f16(d) * q, exact in f32)
-// as fp16 hi + lo (exactly: 18 significant bits), then gathered into pair
-// order: Xg[p] = x_hat[pair_tok[p]]. One warp per 32-block.
-__global__ void moe_prefill_xhat_kernel(const uint16_t *x, int nblk, __half *xhat, __half *xhat_lo)
-{
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    if (warp >= nblk)
-        return;
-    const float v = bf16_to_f32(x[(size_t)warp * 32 + lane]);
-    const Q8Block b = q8_quant_warp(v);
-    const float xh = __fmul_rn(b.d8, (float)b.q);
-    const __half hi = __float2half_rn(xh);
-    xhat[(size_t)warp * 32 + lane] = hi;
-    xhat_lo[(size_t)warp * 32 + lane] = __float2half_rn(__fsub_rn(xh, __half2float(hi)));
-}
-
-// q8_1 of x, dequantised to fp16 hi + lo (as moe_prefill_xhat_kernel), written
-// straight into pair order: CTA p takes its token's row, eight values a lane,
-// four lanes a 32-block (a group's lanes run the same iterations)
+// q8_1 of x (f16(d) * q, exact in f32) as fp16 hi + lo (exactly: 18
+// significant bits), written straight into pair order: CTA p takes its
+// token's row, eight values a lane, four lanes a 32-block (a group's lanes
+// run the same iterations); x is 16-byte aligned
 __global__ void moe_prefill_xhat_gather_kernel(const uint16_t *x, const int32_t *pair_tok, int P, int dim, __half *xg,
                                                __half *xg_lo)
 {
@@ -850,18 +835,6 @@ __global__ void moe_prefill_xhat_gather_kernel(const uint16_t *x, const int32_t 
         *reinterpret_cast<uint4 *>(xg + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4 *>(xg_lo + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
-}
-
-__global__ void moe_prefill_gather_kernel(const uint4 *src, const int32_t *pair_tok, int P, int row16, uint4 *dst)
-{
-    // one CTA a pair: its token's row of row16 16-byte chunks
-    const int p = blockIdx.x;
-    if (p >= P)
-        return;
-    const uint4 *s = src + (size_t)pair_tok[p] * row16;
-    uint4 *d = dst + (size_t)p * row16;
-    for (int c = threadIdx.x; c < row16; c += blockDim.x)
-        d[c] = s[c];
 }
 
 // h = SwiGLU(g, u) per pair, its q8_1 (f32 decisions, f16 scale), and the

@@ -135,3 +135,47 @@ def test_prefill_decode_layer_512_tokens():
     assert (counts == 0).sum() > cfg.n_routed // 2 and counts.max() > 3 * counts.mean()  # skewed groups
     del wl
     torch.cuda.empty_cache()
+
+
+def _prefill_once(wl, cfg, x, res, xn, m):
+    picks = torch.zeros((m, cfg.topk), dtype=torch.int32, device="cuda")
+    weights = torch.zeros((m, cfg.topk), dtype=torch.float32, device="cuda")
+    ws = torch.empty(moe.prefill_workspace_bytes(cfg, m), dtype=torch.uint8, device="cuda")
+    moe.prefill_step(cfg, wl.layer(0), wl.arena, cfg.n_routed, x, res, xn, picks, weights, m, ws)
+    torch.cuda.synchronize()
+    assert moe.prefill_status(cfg, m, ws) == 0
+
+
+def test_prefill_unaligned_residual_and_x_next_give_the_same_bits():
+    """residual only 4-byte and x_next only 2-byte aligned: the finish takes
+    one element a thread instead of four; the outputs are the aligned run's,
+    bit for bit (the same sums in the same order)."""
+    cfg = moe.Config(dim=1024, inter=2048, n_routed=32, topk=4, max_tokens=1)
+    wl = Workload(cfg, n_layers=1, seed=87, shared=True, bias_range=(-1.0, 1.0))
+    m = 20
+    x = bf16_tensor(synth.x_bf16(87, 0, m, cfg.dim), "cuda")
+    res0 = torch.full((m, cfg.dim), 0.25, dtype=torch.float32, device="cuda")
+    xn0 = torch.empty_like(x)
+    _prefill_once(wl, cfg, x, res0, xn0, m)
+    rbuf = torch.full((m * cfg.dim + 1,), 0.25, dtype=torch.float32, device="cuda")
+    xbuf = torch.zeros((m * cfg.dim + 1,), dtype=x.dtype, device="cuda")
+    res1, xn1 = rbuf[1:].view(m, cfg.dim), xbuf[1:].view(m, cfg.dim)
+    assert res1.data_ptr() % 16 == 4 and xn1.data_ptr() % 8 == 2
+    _prefill_once(wl, cfg, x, res1, xn1, m)
+    assert torch.equal(res0, res1) and torch.equal(xn0, xn1)
+
+
+def test_prefill_rejects_an_unaligned_x_before_any_launch():
+    """x must be 16-byte aligned (the router GEMM reads it through a tensor
+    map): an offset view is refused on the host, and the next step runs."""
+    cfg = moe.Config(dim=1024, inter=2048, n_routed=32, topk=4, max_tokens=1)
+    wl = Workload(cfg, n_layers=1, seed=88, shared=True, bias_range=(-1.0, 1.0))
+    m = 4
+    xbuf = bf16_tensor(synth.x_bf16(88, 0, m * cfg.dim + 8, 1).reshape(-1), "cuda")
+    x_bad = xbuf[1:1 + m * cfg.dim].view(m, cfg.dim)
+    assert x_bad.data_ptr() % 16 == 2
+    res = torch.zeros((m, cfg.dim), dtype=torch.float32, device="cuda")
+    xn = torch.empty((m, cfg.dim), dtype=x_bad.dtype, device="cuda")
+    with pytest.raises(moe.MoeError):
+        _prefill_once(wl, cfg, x_bad, res, xn, m)
+    _prefill_once(wl, cfg, xbuf[8:8 + m * cfg.dim].view(m, cfg.dim), res, xn, m)
