@@ -179,3 +179,15 @@ def test_prefill_rejects_an_unaligned_x_before_any_launch():
     with pytest.raises(moe.MoeError):
         _prefill_once(wl, cfg, x_bad, res, xn, m)
     _prefill_once(wl, cfg, xbuf[8:8 + m * cfg.dim].view(m, cfg.dim), res, xn, m)
+
+
+def test_prefill_plan_beyond_its_shared_memory_tables():
+    """1000 tokens x top 6 = 6000 picks, more than the plan kernel builds in
+    shared memory: the pair tables are written straight to global memory;
+    a sample of the tokens checked against the oracle."""
+    cfg = moe.Config(dim=1024, inter=2048, n_routed=32, topk=6, max_tokens=1)
+    wl = Workload(cfg, n_layers=1, seed=89, shared=True, bias_range=(-1.0, 1.0))
+    m = 1000
+    x_bits = synth.x_bf16(89, 0, m, cfg.dim)
+    picks = _compare(wl, cfg, x_bits, m, list(range(0, m, 41)) + [m - 1])
+    assert m * cfg.topk > 5120 and (picks >= 0).all()
