@@ -437,7 +437,7 @@ __device__ __forceinline__ bool ring_acquire(const Ring &r, int j, uint32_t *sta
     if (*seq != j) {
         const uint64_t t0 = globaltimer();
         while (*seq != j) {
-            __nanosleep(64);
+            __nanosleep(16);
             if (globaltimer() - t0 > r.wait_ns) {
                 atomicOr(status, (uint32_t)MOE_WS_TIMEOUT);
                 return false;
@@ -578,7 +578,7 @@ __device__ bool g_load_hs(const GArgs &a, const Ring &ring, uint16_t *hs_s, int 
     if (ld_acquire_gpu(a.gctr + 4) < target) {
         const uint64_t t0 = globaltimer();
         while (ld_acquire_gpu(a.gctr + 4) < target) {
-            __nanosleep(128);
+            __nanosleep(16);
             if (globaltimer() - t0 > a.wait_ns) {
                 atomicOr(a.status, (uint32_t)MOE_WS_TIMEOUT);
                 ok = false;
@@ -752,7 +752,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
                         have_hs = true;
                         break;
                     }
-                    __nanosleep(256);
+                    __nanosleep(16);
                 }
             }
             if (have_hs) {
@@ -790,7 +790,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
             if (ld_acquire_gpu(a.gctr + 5) == 0u) {
                 const uint64_t t0 = globaltimer();
                 while (ld_acquire_gpu(a.gctr + 5) == 0u) {
-                    __nanosleep(64);
+                    __nanosleep(16);
                     if (globaltimer() - t0 > a.wait_ns) {
                         if (lane == 0)
                             atomicOr(a.status, (uint32_t)MOE_WS_TIMEOUT);
@@ -1057,7 +1057,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
                     if (*f == 0) {
                         const uint64_t t0 = globaltimer();
                         while (*f == 0) {
-                            __nanosleep(64);
+                            __nanosleep(16);
                             if (globaltimer() - t0 > a.wait_ns) {
                                 atomicOr(a.status, (uint32_t)MOE_WS_TIMEOUT);
                                 break;
