@@ -614,6 +614,10 @@ int launch_tc(const CUtensorMap &am, const CUtensorMap &bm, const CUtensorMap &b
 {
     if (grid.x == 0 || grid.y == 0)
         return MOE_OK;
+    // the MMA-completion ring has max(S, SB) barriers, rounded up to even,
+    // in room for TC_SB_MAX (an even number)
+    if (a.S < 1 || a.S > TC_SB_MAX)
+        return fail(MOE_EUNSUPPORTED, "prefill GEMM: %d operand stages (at most %d)", a.S, TC_SB_MAX);
     const size_t fixed = tc_smem_bytes(AK, a.S, a.SR, a.raw_bytes, 0);
     const size_t full = (size_t)TC_SB_MAX * tc_parts(AK) * TC_NT * 128;
     if ((size_t)smem_optin < fixed + 2 * tc_parts(AK) * TC_NT * 128)

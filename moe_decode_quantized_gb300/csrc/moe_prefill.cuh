@@ -52,7 +52,7 @@ namespace moe {
 #define TC_TMEM_COLS 512  // TMEM columns a CTA holds: up to 4 accumulators of TC_NT columns (dense),
                           // or 2 accumulators and the A stages from column 256 (K-quant)
 #define TC_TA0 256        // first TMEM column of the K-quant A stages
-#define TC_SB_MAX 16      // stages of the B ring, at most
+#define TC_SB_MAX 8       // stages of the B ring, at most (and of the completion ring: S <= TC_SB_MAX)
 
 // a column task of the routed GEMMs: the expert's slot, its first pair and
 // the number of its pairs in this tile
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // filling the stage now being refilled) and no MMA of chunk j + D can run
     // before the waiter's own next stage, so parity j / D is unambiguous.
     // Even, so that chunks j and j + D are issued by the same MMA thread and
-    // their commits reach barrier j % D in order (S <= 8, SB <= TC_SB_MAX).
+    // their commits reach barrier j % D in order (S, SB <= TC_SB_MAX, even).
     const int D = (max(S, SB) + 1) & ~1;
 
     if (threadIdx.x == 0) {
