@@ -14,8 +14,9 @@ the picks change from step to step. value = token-layer steps per second over
 all ranks.
 
 Other workloads (--workload): batch8 (the same layers at m = 8 tokens),
-chain40 (40 stacked layers, one token, one replay = one 40-layer decode step;
-tokens/s), prefill (512 tokens through one layer on the tensor-core arm,
+decode_kq (the default workload with a K-quant shared expert: Q2_K w1/w3,
+Q3_K w2), chain40 (40 stacked layers, one token, one replay = one 40-layer
+decode step; tokens/s), prefill (512 tokens through one layer on the tensor-core arm,
 correction bias ~U(-1, 1); tokens/s).
 
 --impl reference times the CPU oracle (oracle/, plain C, f64) on the same
@@ -47,6 +48,7 @@ WORKLOADS = {
     # name: (m, layers per step, metric, unit)
     "decode": (1, 8, "decode tokens/s per MoE layer step (1 GB300)", "token-layer steps/s"),
     "batch8": (8, 8, "decode tokens/s per MoE layer step (1 GB300), m=8", "token-layer steps/s"),
+    "decode_kq": (1, 8, "decode tokens/s per MoE layer step (1 GB300), K-quant shared expert", "token-layer steps/s"),
     "chain40": (1, 40, "decode tokens/s, 40-layer MoE decode step (1 GB300)", "tokens/s"),
     # the batched (prefill) arm: 512 tokens through one layer, expert load
     # skewed by a correction bias ~U(-1, 1)
@@ -133,16 +135,18 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ bytes (algorithmic)
 
-def algorithmic_bytes(cfg, m, ne):
+def algorithmic_bytes(cfg, m, ne, shared_kquant=False):
     """Bytes one layer step must move, per kernel (router, gate/up, down)."""
     dim, inter, n, k = cfg.dim, cfg.inter, cfg.n_routed, cfg.topk
     q2 = inter * (dim // 256) * 84
     q3 = dim * (inter // 256) * 110
     router = n * dim * 2 + m * dim * 2 + m * n * 4
-    # gate/up: routed Q2_K gate+up, the whole bf16 shared expert (W1, W3, W2),
-    # x; writes g, u, h, gs, us, hs and sd
-    gateup = 2 * ne * q2 + 3 * inter * dim * 2 + m * dim * 2 + 3 * m * k * inter * 4 \
-        + m * inter * (4 + 4 + 2) + m * dim * 4
+    # gate/up: routed Q2_K gate+up, the whole shared expert (bf16 W1, W3, W2,
+    # or Q2_K W1, W3 and Q3_K W2), x; writes g, u, h, gs, us, hs (bf16, or f32
+    # to be quantised to q8_1 for the Q3_K W2) and sd
+    shared = 2 * q2 + q3 if shared_kquant else 3 * inter * dim * 2
+    gateup = 2 * ne * q2 + shared + m * dim * 2 + 3 * m * k * inter * 4 \
+        + m * inter * (4 + 4 + (4 if shared_kquant else 2)) + m * dim * 4
     # down: routed Q3_K down, h of the plan; writes down rows; reads sd and the
     # residual, writes acc, the residual and x_next
     down = ne * q3 + m * k * inter * 4 + m * k * dim * 4 + m * dim * (4 + 4 + 4 + 4 + 2)
@@ -184,7 +188,8 @@ def hbm_peak():
 
 # ------------------------------------------------------------------ CPU oracle (baseline leg)
 
-def oracle_sample(cfg, m, budget_s, seed=1000, max_steps=10 ** 9, warmup=0, bias_range=(-0.1, 0.1)):
+def oracle_sample(cfg, m, budget_s, seed=1000, max_steps=10 ** 9, warmup=0, bias_range=(-0.1, 0.1),
+                  shared_kquant=False):
     """The oracle as it stands, on host cores: one layer step per iteration over
     the same synthetic decode layer. Returns (steps, seconds, threads, sample text)."""
     import numpy as np
@@ -197,7 +202,12 @@ def oracle_sample(cfg, m, budget_s, seed=1000, max_steps=10 ** 9, warmup=0, bias
                     cfg.route_scale, cfg.swiglu_limit)
     router = synth.router_bf16(seed, 0, cfg.n_routed, cfg.dim)
     bias = synth.bias_f32(seed, 0, cfg.n_routed, *bias_range)
-    shared = synth.shared_bf16(seed, 0, cfg.dim, cfg.inter)
+    if shared_kquant:
+        img = np.frombuffer(synth.expert_bytes(seed, 0, synth.SHARED_KQ_INDEX, shp), np.uint8)
+        shared = (img[shp.gate_off:shp.gate_off + shp.gate_bytes], img[shp.up_off:shp.up_off + shp.up_bytes],
+                  img[shp.down_off:shp.down_off + shp.down_bytes])
+    else:
+        shared = synth.shared_bf16(seed, 0, cfg.dim, cfg.inter)
     cache = {}
     done, spent, i = 0, 0.0, 0
     while done < max_steps and (spent < budget_s or done == 0):
@@ -213,7 +223,7 @@ def oracle_sample(cfg, m, budget_s, seed=1000, max_steps=10 ** 9, warmup=0, bias
             experts[e] = cache[e]
         t0 = time.perf_counter()
         oracle.layer(oc, x, router, bias, experts, (shp.gate_off, shp.up_off, shp.down_off), shared,
-                     threads=threads)
+                     threads=threads, shared_kquant=shared_kquant)
         dt = time.perf_counter() - t0
         i += 1
         if i <= warmup:
@@ -221,7 +231,8 @@ def oracle_sample(cfg, m, budget_s, seed=1000, max_steps=10 ** 9, warmup=0, bias
         spent += dt
         done += 1
     sample = (f"{done} layer steps of {m} tokens through the decode layer (dim {cfg.dim}, inter {cfg.inter}, "
-              f"{cfg.n_routed}x{cfg.topk}, shared expert, bias U{bias_range}), oracle.layer timed, {threads} threads")
+              f"{cfg.n_routed}x{cfg.topk}, {'K-quant' if shared_kquant else 'bf16'} shared expert, bias U{bias_range}), "
+              f"oracle.layer timed, {threads} threads")
     return done, spent, threads, sample
 
 
@@ -245,7 +256,8 @@ def run_ours(args):
     if args.layers:
         L = args.layers
     cfg = decode_cfg(m, args.experts)
-    wl = Workload(cfg, n_layers=L, seed=rank, shared=True)
+    kq = args.workload == "decode_kq"
+    wl = Workload(cfg, n_layers=L, seed=rank, shared=True, shared_kquant=kq)
     layers = [wl.layer(l) for l in range(L)]
     x_a = x_tensor(rank, 0, m, cfg.dim)
     x_b = torch.empty_like(x_a)
@@ -346,7 +358,7 @@ def run_ours(args):
                 kms.append(t)
     kms = np.array(kms, np.float64)
     k_ms = kms.mean(axis=0)
-    b_router, b_gateup, b_down = algorithmic_bytes(cfg, m, ne)
+    b_router, b_gateup, b_down = algorithmic_bytes(cfg, m, ne, kq)
     peak, peak_kind = hbm_peak()
     # the roofline of the kernel with the largest measured time
     names = ["router", "gateup", "down"]
@@ -357,7 +369,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        n, spent, thr, sample = oracle_sample(cfg, m, args.cpu_budget)
+        n, spent, thr, sample = oracle_sample(cfg, m, args.cpu_budget, shared_kquant=kq)
         cu = n * m / spent
         if args.workload == "chain40":
             cu = cu / L
@@ -365,15 +377,17 @@ def run_ours(args):
 
     if rank == 0:
         layer_bytes = b_router + b_gateup + b_down
+        sh_text = "Q2_K/Q3_K shared expert" if kq else "bf16 shared expert"
         out = {
             "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
             "dtype": "q2_k/q3_k x q8_1 int8 dot (dp4a) + bf16, f32 accumulate",
-            "data": "synthetic (seeded SplitMix64: random Q2_K/Q3_K blocks, bf16 ~N(0,0.02) router and shared expert, x ~N(0,1))",
+            "data": "synthetic (seeded SplitMix64: random Q2_K/Q3_K blocks, bf16 ~N(0,0.02) router"
+                    + (", random Q2_K/Q3_K shared expert" if kq else " and shared expert") + ", x ~N(0,1))",
             "config": {
                 "workload": f"{args.workload}: MoE decode layer dim 4096, inter 2048, {cfg.n_routed} routed experts top 6 "
-                            f"(Q2_K gate/up, Q3_K down), bf16 router + bf16 shared expert, m={m}",
+                            f"(Q2_K gate/up, Q3_K down), bf16 router + {sh_text}, m={m}",
                 "layers_per_step": L, "tokens_per_layer_step": m, "graph": "CUDA graph, PDL-chained kernels",
                 "token": f"{NX} distinct tokens in turn: step i copies token i % {NX} (resident on the device) "
                          "into the graph's input and zeroes the residual inside the timed region (two copies a step)",
@@ -387,7 +401,9 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "kernel": f"moe_{names[dom]}_kernel", "achieved": achieved, "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                          # the committed DRAM counts are per launch of the one-token step
-                         "traffic": measured_traffic(names[dom]) if m == 1 else None, "algorithmic_bytes": b_dom,
+                         # with the bf16 shared expert
+                         "traffic": measured_traffic(names[dom]) if m == 1 and not kq else None,
+                         "algorithmic_bytes": b_dom,
                          "avg_launch_us": k_ms[dom] * 1e3,
                          "timing": "per-kernel CUDA events on the launching stream, kernels launched one at a "
                                    "time over the workload's layers after the timed region"},
@@ -560,6 +576,8 @@ def run_prefill(args):
 
 # ------------------------------------------------------------------ reference arm (the oracle)
 
+REF_CAP_S = 120.0  # seconds of oracle time at most (the timed steps stop there)
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -569,14 +587,17 @@ def run_reference(args):
     bias = (-0.1, 0.1)
     if args.workload == "prefill":  # each step a bounded sample: 4 of the 512 tokens
         m, bias = 4, PREFILL_BIAS
-    n, spent, thr, sample = oracle_sample(cfg, m, budget_s=0.0, max_steps=args.steps,
-                                          warmup=args.warmup, bias_range=bias)
+    # K steps after W warm-up steps, unless the oracle's time passes REF_CAP_S
+    # first: "steps" is the number timed
+    n, spent, thr, sample = oracle_sample(cfg, m, budget_s=REF_CAP_S, max_steps=args.steps,
+                                          warmup=args.warmup, bias_range=bias,
+                                          shared_kquant=args.workload == "decode_kq")
     value = n * m / spent
     if args.workload == "chain40":
         value = value / (args.layers or L)
     out = {
         "impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": spent * 1e3 / max(1, n),
+        "steps": n, "steps_requested": args.steps, "warmup": args.warmup, "ms_per_step": spent * 1e3 / max(1, n),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (same seeded generator as the GPU arm)",
         "config": {"workload": f"{args.workload}: the CPU oracle, one layer step per step, m={m}",

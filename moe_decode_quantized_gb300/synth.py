@@ -51,6 +51,7 @@ T_GATE = 7
 T_UP = 8
 T_DOWN = 9
 T_F32 = 10        # plain approx-normal f32 (inputs to the oracle's quantiser)
+SHARED_KQ_INDEX = 4095  # expert index in the generator's keys of a K-quant shared expert
 T_LOGITS = 11     # synthetic logits fed straight to the selection
 
 # the Irwin-Hall (n=4) standard deviation of a sum of four u16 fields

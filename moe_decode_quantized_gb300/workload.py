@@ -17,7 +17,7 @@ import torch
 from . import (MOE_SHARED_BF16, MOE_SHARED_KQUANT, Arena, Config, Layer, SLOT_TABLE_LAYERS, synth, synth_gpu,
                workspace_bytes, workspace_init)
 
-SHARED_KQ_INDEX = 4095  # expert index in the generator's keys of a K-quant shared expert
+SHARED_KQ_INDEX = synth.SHARED_KQ_INDEX  # the K-quant shared expert's blocks: this expert index
 
 
 def bf16_tensor(bits: np.ndarray, device) -> torch.Tensor:
