@@ -366,6 +366,7 @@ int launch_experts(const moe_cfg &c, int m, const Geo &G, const Bufs &B, const u
     da.x_next = x_next;
     da.rgcnt = B.rgcnt;
     da.status = B.ctrl + MOE_CTRL_STATUS;
+    da.gctr = B.ctrl + MOE_CTRL_GATEUP;
     da.limit = c.swiglu_limit;
     da.wait_ns = g_wait_ns.load();
     da.dim = c.dim;

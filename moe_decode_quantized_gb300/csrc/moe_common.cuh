@@ -85,7 +85,7 @@ inline WsLayout ws_layout(const moe_cfg &c)
 // control words at ws + ctrl
 #define MOE_CTRL_TICKET 0
 #define MOE_CTRL_STATUS 1
-#define MOE_CTRL_GATEUP 2  // 6 words: gate/up task counters, exit ticket, shared rows done, plan hint
+#define MOE_CTRL_GATEUP 2  // 6 words: gate/up task counters (one unused), shared rows done, plan hint
 
 inline int header_words(int m, int k) { return m * (1 + 3 * k) + 2 + 2 * m * k; }
 
@@ -216,6 +216,15 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const uint32_t *p)
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+
+// A plain store at GPU scope (to L2) with nothing to wait for: resets a
+// counter that no one else touches until a later kernel, which the kernel
+// boundary orders after it (an atomic exchange would return a value the
+// thread then waits for).
+__device__ __forceinline__ void st_relaxed_gpu(uint32_t *p, unsigned v)
+{
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // Programmatic dependent launch. wait: block until the preceding kernel in

@@ -509,9 +509,10 @@ struct GArgs {
     float *hsf;                        // [m, inter] SwiGLU(gs, us) (K-quant shared expert)
     float *sd;                         // [m, dim] W2 hs
     uint32_t *status;
-    // [0] shared row-task counter, [1] routed-task counter, [2] exit ticket,
+    // [0] shared row-task counter, [1] routed-task counter, [2] unused,
     // [3] W2 task counter, [4] shared rows done (hs[i] written), [5] the
-    // selection's plan-ready hint
+    // selection's plan-ready hint; all 0 at the start (the down kernel after
+    // this one resets them)
     uint32_t *gctr;
     float limit;
     unsigned long long wait_ns;  // bound on each wait
@@ -1132,17 +1133,8 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
             });
         }
     }
-    // the last CTA out resets the grid-wide counters: by then every producer
-    // has stopped taking tasks and every consumer has counted its hs rows
-    consumers_sync();
-    if (threadIdx.x == 0 && atomicAdd(a.gctr + 2, 1u) == gridDim.x - 1) {
-        atomicExch(a.gctr + 0, 0u);
-        atomicExch(a.gctr + 1, 0u);
-        atomicExch(a.gctr + 3, 0u);
-        atomicExch(a.gctr + 4, 0u);
-        atomicExch(a.gctr + 5, 0u);
-        atomicExch(a.gctr + 2, 0u);
-    }
+    // the grid-wide counters are reset by the down kernel launched next, once
+    // this grid has completed: no CTA waits on an exit ticket here
 }
 
 // ------------------------------------------------------------------ down kernel
@@ -1159,6 +1151,7 @@ struct DArgs {
     float *residual;              // [m, dim] or NULL
     uint16_t *x_next;             // [m, dim] or NULL
     uint32_t *rgcnt, *status;
+    uint32_t *gctr;  // the gate/up kernel's six counters: reset here once that grid has completed
     float limit;
     unsigned long long wait_ns;  // bound on each wait
     int has_shared;  // add sd to the routed sum
@@ -1363,6 +1356,11 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
     // ---------------- consumers: wait for h; build the activations
     pdl_launch_dependents();
     pdl_wait();
+    // the gate/up grid has completed (this wait, or the stream's order): its
+    // six counters are free for the next launch, which the kernel boundaries
+    // order after these stores (one a thread, in the last CTA)
+    if (blockIdx.x == gridDim.x - 1 && threadIdx.x < 6)
+        st_relaxed_gpu(a.gctr + threadIdx.x, 0u);
     const int npairs = a.m * a.k;
     for (int q = threadIdx.x; q < npairs; q += MOE_CONSUMER_WARPS * 32) {
         s_rows[q] = __ldcg(a.plan_rows + q);

@@ -878,11 +878,13 @@ __global__ void __launch_bounds__(256) moe_router_kernel(RouteArgs a)
     select_and_plan<true>(a, a.logits, a.scores, a.keys, s_slot, reinterpret_cast<uint8_t *>(sw));
     __syncthreads();
     if (tid == 0) {
-        atomicExch(a.ctrl + MOE_CTRL_TICKET, 0u);
         // the plan is written: released to the gate/up kernel's producers,
         // which read it without waiting for this grid to finish (release:
         // this CTA's stores, ordered before by the barrier)
         asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a.ctrl + MOE_CTRL_GATEUP + 5), "r"(1u) : "memory");
+        // the ticket, for the next launch (every CTA has taken its own):
+        // after the release, which so does not wait for it
+        st_relaxed_gpu(a.ctrl + MOE_CTRL_TICKET, 0u);
     }
 }
 
