@@ -567,6 +567,24 @@ __host__ __device__ inline size_t g_smem_bytes(int S, int m, int dim, int inter,
     return g_stage_off(S, m, dim, inter, sk, stage) + (size_t)S * stage_bytes + 16;
 }
 
+// q8_1(hs) of a K-quant shared expert into shared memory (the producer warp,
+// once hs is complete grid-wide): m * inter / 8 lane items, a multiple of 32,
+// so the whole warp calls q8_block_quad together. Out of line: inlined into
+// the producer, this loop made the bf16 layer step 0.3 us slower, although
+// that step never runs it.
+__device__ __noinline__ void q8_hs_build(const float *hsf, uint8_t *hact, int m, int inter, int lane)
+{
+    const int nbi = inter / MOE_QK, bpr = inter / 32;
+    const size_t arow = act_row_bytes(inter);
+    for (int i = lane; i < m * inter / 8; i += 32) {
+        const int b = i >> 2, sub = i & 3, t = b / bpr, bi = b - t * bpr;
+        const float4 *h4 = reinterpret_cast<const float4 *>(hsf + (size_t)t * inter + bi * 32 + 8 * sub);
+        const float4 p = __ldcg(h4), q = __ldcg(h4 + 1);
+        const float v[8] = {p.x, p.y, p.z, p.w, q.x, q.y, q.z, q.w};
+        q8_block_quad(v, sub, hact + t * arow, nbi, bi, false);
+    }
+}
+
 // The producer warp: waits (bounded) until every hs row of the shared
 // expert is done grid-wide, copies hs into shared memory (bf16) or builds
 // q8_1(hs) there (K-quant: four lanes a block, as the activation of the
@@ -589,20 +607,8 @@ __device__ bool g_load_hs(const GArgs &a, const Ring &ring, uint16_t *hs_s, int 
     }
     // every lane polled itself: its loads below come after its own acquire
     // (unstaged, the consumers read hs from L2 once the flag is up)
-    if (a.sk == 2) {
-        // m * inter / 8 lane items (a multiple of 32): the whole warp calls
-        // q8_block_quad together
-        uint8_t *hact = reinterpret_cast<uint8_t *>(hs_s);
-        const int nbi = a.inter / MOE_QK, bpr = a.inter / 32;
-        const size_t arow = act_row_bytes(a.inter);
-        for (int i = lane; i < a.m * a.inter / 8; i += 32) {
-            const int b = i >> 2, sub = i & 3, t = b / bpr, bi = b - t * bpr;
-            const float4 *h4 = reinterpret_cast<const float4 *>(a.hsf + (size_t)t * a.inter + bi * 32 + 8 * sub);
-            const float4 p = __ldcg(h4), q = __ldcg(h4 + 1);
-            const float v[8] = {p.x, p.y, p.z, p.w, q.x, q.y, q.z, q.w};
-            q8_block_quad(v, sub, hact + t * arow, nbi, bi, false);
-        }
-    }
+    if (a.sk == 2)
+        q8_hs_build(a.hsf, reinterpret_cast<uint8_t *>(hs_s), a.m, a.inter, lane);
     const int n16 = a.stage_x && a.sk == 1 ? a.m * a.inter / 8 : 0;
     const uint4 *src = reinterpret_cast<const uint4 *>(a.hs);
     uint4 *dst = reinterpret_cast<uint4 *>(hs_s);
