@@ -106,9 +106,13 @@ int dev_info(DevInfo **out)
     if (!I.attrs) {
         CUDA_OK(cudaDeviceGetAttribute(&I.sms, cudaDevAttrMultiProcessorCount, d));
         CUDA_OK(cudaDeviceGetAttribute(&I.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d));
-        CUDA_OK(cudaFuncSetAttribute(moe_router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
+        CUDA_OK(cudaFuncSetAttribute(moe_router_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
+        CUDA_OK(cudaFuncSetAttribute(moe_router_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
+        CUDA_OK(cudaFuncSetAttribute(moe_router_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
         CUDA_OK(cudaFuncSetAttribute(moe_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
-        CUDA_OK(cudaFuncSetAttribute(moe_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
+        CUDA_OK(cudaFuncSetAttribute(moe_gateup_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
+        CUDA_OK(cudaFuncSetAttribute(moe_gateup_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
+        CUDA_OK(cudaFuncSetAttribute(moe_gateup_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
         CUDA_OK(cudaFuncSetAttribute(moe_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
         CUDA_OK(cudaFuncSetAttribute(moe_prefill_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      I.smem_optin - 16384));  // beside its static tables
@@ -272,6 +276,17 @@ Bufs ws_bufs(const moe_cfg &c, void *ws)
     return B;
 }
 
+// the router and gate/up kernels built for one token and for eight (each
+// holds that count's code alone), else for any count
+void (*router_kernel_for(int m))(RouteArgs)
+{
+    return m == 1 ? moe_router_kernel<1> : m == 8 ? moe_router_kernel<8> : moe_router_kernel<0>;
+}
+void (*gateup_kernel_for(int m))(GArgs)
+{
+    return m == 1 ? moe_gateup_kernel<1> : m == 8 ? moe_gateup_kernel<8> : moe_gateup_kernel<0>;
+}
+
 RouteArgs route_args(const moe_cfg &c, int m)
 {
     RouteArgs a{};
@@ -347,7 +362,7 @@ int launch_experts(const moe_cfg &c, int m, const Geo &G, const Bufs &B, const u
     ga.plan_off = m * (1 + 3 * k);
     ga.S = G.g_S;
     ga.stage_bytes = G.g_stage;
-    int rc = launch(moe_gateup_kernel, dim3(G.grid), dim3(MOE_THREADS), G.g_smem, s, pdl_gateup, ga);
+    int rc = launch(gateup_kernel_for(m), dim3(G.grid), dim3(MOE_THREADS), G.g_smem, s, pdl_gateup, ga);
     if (rc)
         return rc;
     if (ev)
@@ -417,7 +432,7 @@ int layer_step(const moe_cfg &c, const moe_layer &ly, const moe_arena &ar, const
     const bool pdl = ev == nullptr;
     if (ev)
         CUDA_OK(cudaEventRecord(ev[0], s));
-    if ((rc = launch(moe_router_kernel, dim3(G.r_grid), dim3(256), G.r_smem, s, pdl, ra)))
+    if ((rc = launch(router_kernel_for(m), dim3(G.r_grid), dim3(256), G.r_smem, s, pdl, ra)))
         return rc;
     if (ev)
         CUDA_OK(cudaEventRecord(ev[1], s));
@@ -901,7 +916,7 @@ int moe_router_logits(const moe_cfg *cfg, const void *x, const void *w, float *l
     a.logits = logits;
     a.rows_per_cta = G.r_rows;
     a.do_select = 0;
-    return launch(moe_router_kernel, dim3(G.r_grid), dim3(256), G.r_smem, (cudaStream_t)stream, false, a);
+    return launch(router_kernel_for(m), dim3(G.r_grid), dim3(256), G.r_smem, (cudaStream_t)stream, false, a);
 }
 
 int moe_quantize_q8_1(const moe_cfg *cfg, const void *x, int m, void *out, moe_stream_t stream)

@@ -280,6 +280,18 @@ __device__ __forceinline__ void with_m(int m, F &&f)
     }
 }
 
+// with_m in a kernel built for one token count: KM > 0 instantiates f for
+// that count alone (the kernel's code holds one copy of it), KM = 0 for
+// every count
+template <int KM, typename F>
+__device__ __forceinline__ void with_m_k(int m, F &&f)
+{
+    if constexpr (KM > 0)
+        f(IntC<KM>{});
+    else
+        with_m(m, f);
+}
+
 // s += w . x over one 16-byte chunk of 8 bf16 each, in element order
 __device__ __forceinline__ float fma_bf16x8(const uint4 &w, const uint4 &x, float s)
 {

@@ -631,6 +631,9 @@ __device__ bool g_load_hs(const GArgs &a, const Ring &ring, uint16_t *hs_s, int 
     return ok;
 }
 
+// KM: the token count the kernel is built for (it holds that case's code
+// alone: 1 or 8), or 0 for any m
+template <int KM>
 __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -968,7 +971,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
             const int i = t.row;
             const bool up = t.p != 0;
             const uint4 *wr = reinterpret_cast<const uint4 *>(st);
-            with_m(a.m, [&](auto MC) {
+            with_m_k<KM>(a.m, [&](auto MC) {
                 constexpr int M = decltype(MC)::value;
                 float ac[M];
 #pragma unroll
@@ -1106,7 +1109,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gateup_kernel(GArgs a)
                     mbar_arrive(&ring.empty[slot]);
                 continue;
             }
-            with_m(a.m, [&](auto MC) {
+            with_m_k<KM>(a.m, [&](auto MC) {
                 constexpr int M = decltype(MC)::value;
                 for (int rr = 0; rr < a.w2r; ++rr) {
                     const uint4 *wr = reinterpret_cast<const uint4 *>(st) + (size_t)rr * (inter / 8);

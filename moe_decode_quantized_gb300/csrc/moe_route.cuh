@@ -746,6 +746,9 @@ __host__ __device__ inline size_t router_pre_bytes(int n, int rows) { return ali
 
 // smem: [0,128) barrier + flag; the staged constants; then the CTA's router
 // rows, x, logits; the last CTA reuses the rows area for the selection
+// KM: the token count the kernel is built for (it holds that case's code
+// alone: 1 or 8), or 0 for any m
+template <int KM>
 __global__ void __launch_bounds__(256) moe_router_kernel(RouteArgs a)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -800,7 +803,7 @@ __global__ void __launch_bounds__(256) moe_router_kernel(RouteArgs a)
     // chunks j + 32 i into four partial sums (i mod 4), added pairwise, then a
     // warp butterfly -- a fixed order per (token, row), whatever m is
     const int nch = dim / 8;
-    with_m(m, [&](auto MC) {
+    with_m_k<KM>(m, [&](auto MC) {
         constexpr int M = decltype(MC)::value;
         const uint4 *x4 = reinterpret_cast<const uint4 *>(sx);
         for (int r = warp; r < nrows; r += blockDim.x >> 5) {
