@@ -113,7 +113,8 @@ int dev_info(DevInfo **out)
         CUDA_OK(cudaFuncSetAttribute(moe_gateup_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
         CUDA_OK(cudaFuncSetAttribute(moe_gateup_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
         CUDA_OK(cudaFuncSetAttribute(moe_gateup_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
-        CUDA_OK(cudaFuncSetAttribute(moe_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
+        CUDA_OK(cudaFuncSetAttribute(moe_down_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
+        CUDA_OK(cudaFuncSetAttribute(moe_down_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, I.smem_optin));
         CUDA_OK(cudaFuncSetAttribute(moe_prefill_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      I.smem_optin - 16384));  // beside its static tables
         int rc = tc_attr<0>(I.smem_optin);
@@ -394,7 +395,8 @@ int launch_experts(const moe_cfg &c, int m, const Geo &G, const Bufs &B, const u
     da.pair_cap = G.d_pair_cap;
     da.own_rows = G.d_own_rows;
     da.stage_bytes = G.d_stage;
-    if ((rc = launch(moe_down_kernel, dim3(G.grid), dim3(MOE_THREADS), G.d_smem, s, ev == nullptr, da)))
+    if ((rc = launch(G.d_own_rows > 0 ? moe_down_kernel<1> : moe_down_kernel<0>, dim3(G.grid), dim3(MOE_THREADS),
+                     G.d_smem, s, ev == nullptr, da)))
         return rc;
     if (ev)
         CUDA_OK(cudaEventRecord(ev[1], s));

@@ -1224,7 +1224,9 @@ __device__ __forceinline__ void d_task(const DRange &R, int tix, int &p, int &gr
 }
 
 // ps: the plan's pair starts as cached by cache_plan (clamped, ne at
-// ps_ne), or NULL to read them from the header
+// ps_ne), or NULL to read them from the header. OWN: the kernel's path, 1 row
+// ownership, 0 tickets (the host launches the instance that matches own_rows)
+template <int OWN>
 __device__ __forceinline__ DRange d_range(const DArgs &a, const int *ps = nullptr, int ps_ne = 0)
 {
     auto start = [&](int i) {  // pair start of plan expert i (i <= ne)
@@ -1234,7 +1236,7 @@ __device__ __forceinline__ DRange d_range(const DArgs &a, const int *ps = nullpt
     r.ne = ps ? ps_ne : min(max(__ldcg(a.hdr + a.plan_off), 0), a.cap);
     r.tpr = a.dim / down_rows_per_task(a.inter);
     r.Tr = r.ne * r.tpr;
-    r.own = a.own_rows > 0;
+    r.own = OWN == 1;
     r.g_lo = r.ng = 0;
     if (r.own) {
         r.g_lo = (int)((long long)blockIdx.x * r.tpr / gridDim.x);
@@ -1291,6 +1293,9 @@ __device__ __forceinline__ void finish_row(const DArgs &a, int t, int r, bool sh
     }
 }
 
+// OWN: 1 for row ownership (own_rows > 0), 0 for row-group tickets; each
+// instance holds its own path's code alone
+template <int OWN>
 __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -1316,7 +1321,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
         pdl_launch_dependents();
         cache_plan(ring, a.hdr, a.plan_off, a.plan_rows, a.ptrs, a.cap, 2, 1);
         const PlanCache &pc = *ring.pc;
-        const DRange R = d_range(a, pc.pair_start, pc.ne);
+        const DRange R = d_range<OWN>(a, pc.pair_start, pc.ne);
         const uint64_t pol = policy_evict_first();
         const int P = min(MOE_PRODUCER_LANES, ring.S);
         const bool issuer = lane < P;
@@ -1360,7 +1365,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_down_kernel(DArgs a)
         }
         return;
     }
-    const DRange R = d_range(a);
+    const DRange R = d_range<OWN>(a);
 
     // ---------------- consumers: wait for h; build the activations
     pdl_launch_dependents();
