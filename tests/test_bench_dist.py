@@ -86,3 +86,34 @@ def test_kernel_hash_ignores_comments_only(tmp_path, monkeypatch):
     assert bench.kernel_hash() == h0
     f.write_text(text.replace("namespace moe {", "namespace moe {\nconstexpr int kNewCode = 1;", 1))
     assert bench.kernel_hash() != h0
+
+
+def test_reference_arm_times_the_requested_steps(capsys, monkeypatch):
+    """--impl reference times K oracle steps after W warm-up steps and says so
+    (a cap on the oracle's time only stops a much longer run early)."""
+    sys.path.insert(0, ROOT)
+    import json
+
+    import bench
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    bench.main(["--impl", "reference", "--steps", "2", "--warmup", "3"])
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert line["steps"] == 2 and line["steps_requested"] == 2 and line["warmup"] == 3
+    assert line["cpu_baseline"]["sample"].startswith("2 layer steps")
+    assert line["value"] > 0 and line["e2e"]["value"] == line["value"]
+
+
+def test_algorithmic_bytes_of_the_kquant_shared_expert():
+    """The shared expert as Q2_K W1/W3 (84 bytes a 256-weight block) and Q3_K W2
+    (110 bytes a block) instead of bf16 (2 bytes a weight); hs in f32."""
+    sys.path.insert(0, ROOT)
+    import bench
+    cfg = bench.decode_cfg(1)
+    r0, g0, d0 = bench.algorithmic_bytes(cfg, 1, 6)
+    r1, g1, d1 = bench.algorithmic_bytes(cfg, 1, 6, shared_kquant=True)
+    w = 2048 * 4096  # weights of each shared matrix
+    assert (r1, d1) == (r0, d0)
+    assert g0 - g1 == 3 * w * 2 - (2 * w // 256 * 84 + w // 256 * 110) - 2048 * 2
+    assert (r1 + g1 + d1) / 1e6 == pytest.approx(67.3, abs=0.1)
